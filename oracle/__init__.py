@@ -1,0 +1,193 @@
+"""CPU oracle for paged-KV attention (ctypes wrapper around pa_oracle.c).
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
+legs of ``bench.py`` may import this package.  The product library in
+``paged_kv_continuous_gb300`` never imports, links or executes anything here,
+and this package imports nothing from it.
+
+Each function returns float64 NumPy arrays computed by the plain definitions
+in ``pa_oracle.c`` (see the header there for the passages each follows and
+the readings taken where the pages are silent).  Inputs are bf16 bit patterns
+held in ``np.uint16`` arrays and int32 index arrays, all on the host.
+
+Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
+against brute force over contiguous K/V, closed forms and invariants; none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libpa_oracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile pa_oracle.c with gcc (C11, fp64, OpenMP, no fast-math)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC",
+           "-fopenmp", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # PA_ORACLE_LIB points the wrapper at another build of pa_oracle.c;
+            # the mutation tests use it to load deliberately broken copies.
+            lib = ctypes.CDLL(os.environ.get("PA_ORACLE_LIB") or build())
+            P = ctypes.c_void_p
+            i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+            lib.pa_oracle_store_kv.argtypes = [P, P, i64, i64, i64, i64, i64, P, P, i64,
+                                               i32, i32, i32, P]
+            lib.pa_oracle_prefill_varlen.argtypes = [P, P, P, P, i32, P, P, i64, P, i64, P,
+                                                     i32, i32, i32, i32, dbl, i32]
+            lib.pa_oracle_decode.argtypes = [P, P, P, P, P, i64, P, i64, P, i32, i32, i32,
+                                             i32, i32, dbl, i32]
+            lib.pa_oracle_decode_range.argtypes = [P, P, P, P, P, i64, P, i64, P, P, i32,
+                                                   i32, i32, i32, i32, dbl]
+            lib.pa_oracle_merge.argtypes = [P, P, P, i64, i32, i32]
+            lib.pa_oracle_merge.restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def max_threads() -> int:
+    return int(_load().pa_oracle_max_threads())
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        names = {1: "bad argument", 2: "index out of range", 3: "out of memory"}
+        raise ValueError(f"oracle {what}: {names.get(rc, rc)}")
+
+
+def store_kv(k, v, k_cache, v_cache, slot_mapping, block_size=16):
+    """Copy each token's K/V rows into the pool slots named by slot_mapping.
+
+    ``k``/``v`` are uint16 arrays of shape [T, Hkv, D] (any strides);
+    ``k_cache``/``v_cache`` are uint16 [num_blocks, block_size, Hkv, D] and are
+    updated in place.
+    """
+    lib = _load()
+    assert k.dtype == np.uint16 and v.dtype == np.uint16
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    T, Hkv, D = k.shape
+    isz = k.itemsize
+    slots = _c(slot_mapping, np.int32)
+    rc = lib.pa_oracle_store_kv(
+        _ptr(k), _ptr(v), T, k.strides[0] // isz, k.strides[1] // isz,
+        v.strides[0] // isz, v.strides[1] // isz, _ptr(k_cache), _ptr(v_cache),
+        k_cache.shape[0], block_size, Hkv, D, _ptr(slots))
+    assert k.strides[2] == isz and v.strides[2] == isz
+    _check(rc, "store_kv")
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale, num_threads=0,
+           with_lse=False):
+    """Paged GQA decode: one query per sequence over its context_lens keys.
+
+    q: uint16 [B, Hq, D]; caches uint16 [NB, bs, Hkv, D]; block_tables int32
+    [B, max_blocks]; context_lens int32 [B].  Returns float64 [B, Hq, D]
+    (and the natural-log sum-exp [B, Hq] when ``with_lse``).
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    assert D2 == D
+    bt = _c(block_tables, np.int32)
+    ctx = _c(context_lens, np.int32)
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = lib.pa_oracle_decode(_ptr(out), _ptr(lse), _ptr(q), _ptr(_c(k_cache, np.uint16)),
+                              _ptr(_c(v_cache, np.uint16)), NB, _ptr(bt), bt.shape[1],
+                              _ptr(ctx), B, Hq, Hkv, D, bs, float(scale), int(num_threads))
+    _check(rc, "decode")
+    return (out, lse) if with_lse else out
+
+
+def decode_range(q, k_cache, v_cache, block_tables, key_lo, key_hi, scale):
+    """Decode query of each sequence over keys [key_lo[b], key_hi[b]) only.
+
+    Returns (out float64 [B, Hq, D], lse float64 [B, Hq]).
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    bt = _c(block_tables, np.int32)
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = lib.pa_oracle_decode_range(_ptr(out), _ptr(lse), _ptr(q),
+                                    _ptr(_c(k_cache, np.uint16)), _ptr(_c(v_cache, np.uint16)),
+                                    NB, _ptr(bt), bt.shape[1], _ptr(_c(key_lo, np.int32)),
+                                    _ptr(_c(key_hi, np.int32)), B, Hq, Hkv, D, bs,
+                                    float(scale))
+    _check(rc, "decode_range")
+    return out, lse
+
+
+def prefill_varlen(q, cu_seqlens, k_cache, v_cache, block_tables, context_lens, scale,
+                   num_threads=0, with_lse=False):
+    """Varlen causal prefill over each sequence's paged keys.
+
+    q: uint16 [T, Hq, D] (rows of sequence s are cu_seqlens[s]..cu_seqlens[s+1]-1);
+    the chunk's own keys are read from the cache (they are stored before
+    attention).  Returns float64 [T, Hq, D] (and lse [T, Hq]).
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    T, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    cu = _c(cu_seqlens, np.int32)
+    bt = _c(block_tables, np.int32)
+    out = np.zeros((T, Hq, D), np.float64)
+    lse = np.zeros((T, Hq), np.float64)
+    rc = lib.pa_oracle_prefill_varlen(_ptr(out), _ptr(lse), _ptr(q), _ptr(cu), len(cu) - 1,
+                                      _ptr(_c(k_cache, np.uint16)),
+                                      _ptr(_c(v_cache, np.uint16)), NB, _ptr(bt),
+                                      bt.shape[1], _ptr(_c(context_lens, np.int32)), Hq, Hkv,
+                                      D, bs, float(scale), int(num_threads))
+    _check(rc, "prefill_varlen")
+    return (out, lse) if with_lse else out
+
+
+def merge(part_o, part_lse):
+    """Log-sum-exp merge of split partials.
+
+    part_o float64 [R, S, D], part_lse float64 [R, S] -> float64 [R, D].
+    """
+    lib = _load()
+    po = _c(part_o, np.float64)
+    pl = _c(part_lse, np.float64)
+    R, S, D = po.shape
+    out = np.zeros((R, D), np.float64)
+    lib.pa_oracle_merge(_ptr(out), _ptr(po), _ptr(pl), R, S, D)
+    return out

@@ -1,0 +1,48 @@
+"""Planted mistakes in copies of the oracle source must each fail the pins.
+
+Each mutant is a one-line change a real implementation could plausibly
+contain.  The copy is compiled on the CPU into a temporary directory and the
+pin suite is run against it in a subprocess; the test passes only when the
+pins reject the mutant.  The real oracle is never modified."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "pa_oracle.c")
+
+MUTANTS = {
+    "gqa_interleaved_head_map": ("g * group + hi;", "hi * num_kv_heads + g;"),
+    "causal_boundary_exclusive": ("prefix + i + 1,", "prefix + i,"),
+    "scale_dropped": ("double s = scale * dot;", "double s = dot;"),
+    "max_not_subtracted": ("double p = exp(scores[j - lo] - m);",
+                           "double p = exp(scores[j - lo]);"),
+    "normaliser_dropped": ("o[d] = acc / l;", "o[d] = acc;"),
+    "gather_row_off_by_one": ("int64_t row = j % block_size;",
+                              "int64_t row = (j + 1) % block_size;"),
+    "gather_logical_block": ("int64_t block = table_row[j / block_size];",
+                             "int64_t block = j / block_size;"),
+    "store_row_from_block": ("int64_t row = slot % block_size;",
+                             "int64_t row = (slot / block_size) % block_size;"),
+    "merge_unweighted": ("acc += exp(lse[s] - M) * part_o", "acc += part_o"),
+    "lse_natural_log_dropped": ("return m + log(l);", "return m + log2(l);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) >= 1, f"mutation site for {name} not found"
+    mutant = tmp_path / "pa_oracle_mutant.c"
+    mutant.write_text(text.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-fopenmp", "-shared", str(mutant),
+                    "-o", str(so), "-lm"], check=True)
+    env = dict(os.environ, PA_ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins accepted mutant {name}:\n{r.stdout[-2000:]}"
