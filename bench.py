@@ -1,0 +1,540 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV decode step on one GB300 (or N replicas).
+
+Workload: the continuous-batching mix -- 64 sequences with lognormal context
+lengths (median 1024, clipped to [1, 8192]), Qwen2.5-1.5B attention shapes
+(12 query heads, 2 KV heads, head_dim 128, 16-token blocks), a 40000-block
+shuffled pool per layer.  One step = pa_store_kv of the 64 new tokens, then
+pa_decode (balanced split-K + merge) over all sequences, for one layer.
+Steps cycle over L = 8 independent layer pools (same lengths and tables,
+different data), so every step reads its KV from HBM, not from L2 (8 x ~105
+MB of live KV >> the 126 MB L2).  Steps run as CUDA-graph replays (one graph
+= the L layers); external timing events inside the graphs give each
+kernel's duration on the launching stream.
+
+value  = algorithmic bytes of a step / device time of a step  (GB/s)
+e2e    = the same metric through the public Python API with the step's
+         inputs copied from pinned host memory and the output read back,
+         every step.
+--impl reference times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn effective KV GB/s (% of GB300 HBM peak) and seq-steps/s"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ["paged_kv_continuous_gb300/csrc/pa_decode_kernel.cuh",
+                  "paged_kv_continuous_gb300/csrc/pa_common.cuh",
+                  "paged_kv_continuous_gb300/csrc/pa_decode.cu"]
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (what the method must move; no padding, no partials)
+# ---------------------------------------------------------------------------
+
+def decode_alg_bytes(ctx, hq, hkv, d=128, bs=16):
+    ctx = np.asarray(ctx, np.int64)
+    kv = int(ctx.sum()) * hkv * d * 2 * 2            # K and V, bf16
+    qo = len(ctx) * hq * d * 2 * 2                   # q read + out written, bf16
+    tables = int(((ctx + bs - 1) // bs).sum()) * 4
+    return kv + qo + tables + len(ctx) * 4
+
+
+def store_alg_bytes(tokens, hkv, d=128):
+    return tokens * hkv * d * 2 * 2 * 2 + tokens * 4  # read + write K and V, slots
+
+
+def prefill_alg_flops(q_lens, ctx, hq, d=128):
+    tot = 0
+    for q, n in zip(q_lens, ctx):
+        p = n - q
+        tot += sum(p + i + 1 for i in range(q))
+    return 4 * d * hq * tot
+
+
+# ---------------------------------------------------------------------------
+# peaks, traffic record, clocks
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def sources_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's
+    sources are unchanged since the counters were taken."""
+    want = sources_hash(DECODE_SOURCES)
+    pat = re.compile(r"TRAFFIC kernel=(\S+) workload=(\S+) sha=(\w+) bytes_per_launch=(\d+)")
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*")):
+        try:
+            text = open(path).read()
+        except Exception:
+            continue
+        for m in pat.finditer(text):
+            if m.group(1) == kernel and m.group(2) == workload and m.group(3) == want:
+                return int(m.group(4))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples with host timestamps."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_id}", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.monotonic(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sel = [p for t, p in self.samples if t0 <= t <= t1]
+        note = "during timed region"
+        if not sel and self.samples:
+            # timed region shorter than the sampling period: nearest samples
+            sel = [min(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[1]]
+            note = "nearest sample (timed region shorter than 100 ms sampling)"
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in sel if num(p[0]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in sel:
+            for name, val in zip(names, p[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        pw = [num(p[2]) for p in sel if num(p[2]) is not None]
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": num(sel[0][1]), "reasons": sorted(reasons),
+                "power_w_max": max(pw) if pw else None, "samples": len(sel), "note": note}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas; rank 0 prints)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(units_per_rank, seconds_per_rank):
+    """Whole-job throughput of replicas: all units over the slowest rank."""
+    return float(sum(units_per_rank)) / max(seconds_per_rank)
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    import oracle
+    from paged_kv_continuous_gb300 import synth
+    w = synth.cb_decode_b64()
+    kc, vc = w.stored_caches()
+    threads = oracle.max_threads()
+    # size one step: a prefix of the sequences, so that W + K steps take ~2 min
+    t = time.perf_counter()
+    oracle.decode(w.q[:8], kc, vc, w.block_tables[:8], w.context_lens[:8], w.scale)
+    per_seq_token = (time.perf_counter() - t) / max(1, int(w.context_lens[:8].sum()))
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    nseq = 1
+    while nseq < w.batch and per_seq_token * w.context_lens[:nseq + 1].sum() < budget:
+        nseq += 1
+    sl = slice(0, nseq)
+
+    def step():
+        # the store rewrites the same slots with the same rows every step
+        oracle.store_kv(w.new_k[sl], w.new_v[sl], kc, vc, w.slot_mapping[sl])
+        oracle.decode(w.q[sl], kc, vc, w.block_tables[sl], w.context_lens[sl], w.scale)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    nbytes = decode_alg_bytes(w.context_lens[sl], w.num_q_heads, w.num_kv_heads) + \
+        store_alg_bytes(nseq, w.num_kv_heads)
+    value = nbytes / dt / 1e9
+    sample = (f"first {nseq} of 64 sequences of cb_decode_b64 "
+              f"({int(w.context_lens[sl].sum())} keys) per step; store + decode")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": "cb_decode_b64_lognormal1024", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def cpu_baseline_oracle(w, kc, vc, seconds=10.0):
+    import oracle
+    threads = oracle.max_threads()
+    n = 0
+    t0 = time.perf_counter()
+    ref = None
+    while n == 0 or time.perf_counter() - t0 < seconds:
+        ref = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    nbytes = decode_alg_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads)
+    return ref, {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+                 "sample": f"full cb_decode_b64 decode (64 sequences, "
+                           f"{int(w.context_lens.sum())} keys), {n} call(s), "
+                           f"{dt * 1e3:.1f} ms per call"}
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from paged_kv_continuous_gb300 import ops, synth
+
+    w = synth.cb_decode_b64(keep_seq=False)
+    L = args.layers
+    B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
+
+    def dev16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+
+    def dev32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    tables = dev32(w.block_tables)
+    ctx = dev32(w.context_lens)
+    slots = dev32(w.slot_mapping)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20260002 + 1000 * rank)
+    layers = []
+    for l in range(L):
+        if l == 0:
+            kc, vc = dev16(w.k_cache), dev16(w.v_cache)
+            q, nk, nv = dev16(w.q), dev16(w.new_k), dev16(w.new_v)
+        else:
+            shape = tuple(w.k_cache.shape)
+            kc = torch.randn(shape, generator=gen, device=dev, dtype=torch.bfloat16)
+            vc = torch.randn(shape, generator=gen, device=dev, dtype=torch.bfloat16)
+            q = torch.randn((B, Hq, D), generator=gen, device=dev, dtype=torch.bfloat16)
+            nk = torch.randn((B, Hkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
+            nv = torch.randn((B, Hkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+        layers.append(dict(kc=kc, vc=vc, q=q, nk=nk, nv=nv, out=out))
+    splits = ops.default_splits(local)
+    ws = ops.decode_workspace(Hq, splits, D, dev)
+
+    def step(l, timing=None):
+        x = layers[l]
+        if timing:
+            timing[0].record()
+        ops.store_kv(x["nk"], x["nv"], x["kc"], x["vc"], slots)
+        if timing:
+            timing[1].record()
+        ops.decode(x["q"], x["kc"], x["vc"], tables, ctx, w.scale, out=x["out"],
+                   num_splits=splits, workspace=ws)
+        if timing:
+            timing[2].record()
+
+    # first step of layer 0 checked against the oracle (bench-time parity)
+    step(0)
+    torch.cuda.synchronize()
+    got0 = layers[0]["out"].float().cpu().numpy().astype(np.float64)
+
+    # graphs: NC copies of "all L layers", each step bracketed by external events
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    NC = 8
+    graphs, events = [], []
+    ext_ok = True
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            for l in range(L):
+                step(l)
+    torch.cuda.synchronize()
+    for c in range(NC):
+        g = torch.cuda.CUDAGraph()
+        evs = []
+        for l in range(L):
+            try:
+                evs.append([torch.cuda.Event(enable_timing=True, external=True)
+                            for _ in range(3)])
+            except TypeError:
+                ext_ok = False
+                evs.append(None)
+        with torch.cuda.graph(g, stream=s):
+            for l in range(L):
+                step(l, evs[l])
+        graphs.append(g)
+        events.append(evs)
+    rem = args.steps % L
+    rem_graph = None
+    if rem:
+        rem_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(rem_graph, stream=s):
+            for l in range(rem):
+                step(l)
+    launches_per_step = 1 + 1 + (1 if splits > 1 else 0)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # warm-up steps (untimed)
+    for i in range(args.warmup):
+        step(i % L)
+    torch.cuda.synchronize()
+
+    gpu_id = str(local)
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        if getattr(props, "uuid", None):
+            gpu_id = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    full = args.steps // L
+    barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.monotonic()
+    with torch.cuda.stream(s):
+        start.record()
+        for i in range(full):
+            graphs[i % NC].replay()
+        if rem_graph is not None:
+            rem_graph.replay()
+        end.record()
+    torch.cuda.synchronize()
+    t_host1 = time.monotonic()
+    barrier()
+    sampler.stop()
+    elapsed_s = start.elapsed_time(end) / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_s = float(t.item())
+    err_word = ops.read_error_word(ws)
+
+    # per-kernel durations from the last replay of each graph copy
+    store_ms, decode_ms = [], []
+    if ext_ok and full >= 1:
+        for c in range(min(NC, full)):
+            for l in range(L):
+                e = events[c][l]
+                store_ms.append(e[0].elapsed_time(e[1]))
+                decode_ms.append(e[1].elapsed_time(e[2]))
+
+    ms_per_step = elapsed_s * 1e3 / args.steps
+    dec_bytes = decode_alg_bytes(w.context_lens, Hq, Hkv, D)
+    st_bytes = store_alg_bytes(B, Hkv, D)
+    step_bytes = dec_bytes + st_bytes
+    value = aggregate([step_bytes * args.steps] * world, [elapsed_s] * world) / 1e9
+
+    # e2e: public API, inputs from pinned host memory, output read back, per step
+    h_q = [layers[l]["q"].cpu().pin_memory() for l in range(L)]
+    h_nk = [layers[l]["nk"].cpu().pin_memory() for l in range(L)]
+    h_nv = [layers[l]["nv"].cpu().pin_memory() for l in range(L)]
+    h_tab = torch.from_numpy(w.block_tables).pin_memory()
+    h_ctx = torch.from_numpy(w.context_lens).pin_memory()
+    h_slot = torch.from_numpy(w.slot_mapping).pin_memory()
+    h_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    d_q = torch.empty_like(layers[0]["q"])
+    d_nk = torch.empty_like(layers[0]["nk"])
+    d_nv = torch.empty_like(layers[0]["nv"])
+    e2e_steps = min(args.steps, 2000)
+    h2d = (d_q.numel() + d_nk.numel() + d_nv.numel()) * 2 + h_tab.numel() * 4 + \
+        h_ctx.numel() * 4 + h_slot.numel() * 4
+    d2h = h_out.numel() * 2
+
+    def e2e_step(l):
+        x = layers[l]
+        d_q.copy_(h_q[l], non_blocking=True)
+        d_nk.copy_(h_nk[l], non_blocking=True)
+        d_nv.copy_(h_nv[l], non_blocking=True)
+        tables.copy_(h_tab, non_blocking=True)
+        ctx.copy_(h_ctx, non_blocking=True)
+        slots.copy_(h_slot, non_blocking=True)
+        ops.store_kv(d_nk, d_nv, x["kc"], x["vc"], slots)
+        ops.decode(d_q, x["kc"], x["vc"], tables, ctx, w.scale, out=x["out"],
+                   num_splits=splits, workspace=ws)
+        h_out.copy_(x["out"], non_blocking=True)
+
+    for i in range(min(args.warmup, 50)):
+        e2e_step(i % L)
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e2e_steps):
+        e2e_step(i % L)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = aggregate([step_bytes * e2e_steps] * world, [e2e_s] * world) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    # parity of the bench's own first step, and the CPU baseline (oracle)
+    import oracle  # bench's cpu_baseline leg
+    kc_ref, vc_ref = w.stored_caches()
+    ref, cpu = cpu_baseline_oracle(w, kc_ref, vc_ref, seconds=args.cpu_seconds)
+    abs_err = np.abs(got0 - ref)
+    parity_ok = bool(np.all(abs_err <= 2e-3 + 1e-2 * np.abs(ref)))
+
+    peak, peak_kind = hbm_peak()
+    dec_s = float(np.mean(decode_ms)) / 1e3 if decode_ms else None
+    achieved = dec_bytes / dec_s / 1e9 if dec_s else None
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak if achieved else None,
+                "traffic": recorded_traffic("decode_kernel", w.name),
+                "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS if achieved else None,
+                "kernel": "pa_decode (decode_kernel<6,2> + merge_kernel)",
+                "alg_bytes_per_launch": dec_bytes,
+                "launch_ms_mean": dec_s * 1e3 if dec_s else None,
+                "launch_samples": len(decode_ms)}
+    clocks = sampler.summary(t_host0, t_host1)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": B, "num_q_heads": Hq, "num_kv_heads": Hkv,
+                   "head_dim": D, "block_size": w.block_size, "layers": L,
+                   "total_context": int(w.context_lens.sum()),
+                   "context_median": float(np.median(w.context_lens)),
+                   "context_max": int(w.context_lens.max()), "num_splits": splits,
+                   "l2": f"inputs larger than L2: {L} layer pools cycled "
+                         f"(~{dec_bytes * L / 1e6:.0f} MB of live KV)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "step": "pa_store_kv(64 tokens) + pa_decode(+merge), one layer"},
+        "seq_steps_per_s": world * B * args.steps / elapsed_s,
+        "store_ms_mean": float(np.mean(store_ms)) if store_ms else None,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": e2e_steps,
+                "ms_per_step": e2e_s * 1e3 / e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "parity": {"ok": parity_ok, "max_abs_err": float(abs_err.max()),
+                   "checked": "first step of layer 0 vs oracle, all 64x12x128 outputs"},
+        "device_error_word": err_word,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=8)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        world, rank, _ = dist_env()
+        if rank != 0:
+            return
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,245 @@
+/*
+ * pa.h -- C ABI of the GB300 paged-KV attention library (libpa_gb300.so).
+ *
+ * Four operations over a block-paged KV cache, each a hand-written sm_103a
+ * CUDA kernel enqueued on the caller's stream:
+ *
+ *   pa_store_kv        write each new token's K/V rows into the pool slot
+ *                      named by slot_mapping;
+ *   pa_decode          paged GQA decode attention (one query per sequence),
+ *                      split across CTAs with log-sum-exp partials;
+ *   pa_decode_merge    combine those partials into the final rows;
+ *   pa_prefill_varlen  causal varlen attention of cu_seqlens-packed query
+ *                      chunks over each sequence's paged keys.
+ *
+ * Sources (web pages that describe the method):
+ *   [EAS] koas-w, "errors and solutions" (Qwen2.5-1.5B inference from
+ *         scratch): sections "KV Cache 管理" (global pool of 16-token
+ *         blocks, logical->physical block_table), "自写 Triton Kernel"
+ *         (store_kvcache_kernel; Decode_Paged_GQAAttention_Kernel), "CUDA
+ *         Graph" (static slot_mapping / block_table / context_lens buffers)
+ *         and "开发过程遇到的错误汇总" types 1, 2 and 5.
+ *   [MVT] mini-vllm tutorial, "step14_7 -- Batched Forward": sections
+ *         "解决方案：变长 batch（varlen）" and "cu_seqlens 只在 Attention 里才需要".
+ *   [CEB] PocketLLM, "cpp_engine Batching Implementation (Phase 3.1)",
+ *         section "当前 KV cache 结构" (one token row is [kv_heads, head_dim]).
+ *
+ * Conventions shared by every entry point
+ *   - All array arguments are DEVICE pointers into caller-owned memory; the
+ *     library allocates nothing and keeps no state between calls.  Scalars
+ *     are passed by value.  `stream` is a cudaStream_t (NULL = legacy default
+ *     stream); all work is enqueued there and the call returns without
+ *     synchronising.  PA_OK means "validated and launched", not "finished".
+ *   - Element type of q, k, v and the pools is bf16.  Outputs are bf16
+ *     (out_dtype = PA_DTYPE_BF16, round to nearest even) or fp32
+ *     (PA_DTYPE_F32).  Arithmetic is fp32.
+ *   - KV pool layout: k_cache and v_cache are contiguous
+ *     [num_blocks][block_size][num_kv_heads][head_dim]; slot s is physical
+ *     block s / block_size, row s % block_size ([EAS] "KV Cache 管理";
+ *     token row as in [CEB]).
+ *   - block_tables is int32 [batch][block_table_stride] (row-major, row
+ *     stride in elements); entry j of row b is the physical block holding
+ *     positions 16j .. 16j+15 of sequence b.  Only entries
+ *     j < ceil(context_lens[b] / block_size) are read; the rest may hold
+ *     anything.
+ *   - context_lens[b] is the number of keys sequence b attends to, INCLUDING
+ *     tokens stored in the same step ([EAS] error type 1).
+ *   - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *   - Supported shapes: head_dim = 128, block_size = 16, num_kv_heads in
+ *     {1, 2, 4, 8}, num_q_heads / num_kv_heads in 1..8.  Other shapes return
+ *     PA_ERR_UNSUPPORTED without launching.
+ *   - Errors: host-side checks return a status and launch nothing.  Device-
+ *     side checks (a block-table entry outside [0, num_blocks), a slot past
+ *     the pool, a prefix shorter than zero, a pipeline wait that gave up)
+ *     never fault: the kernel skips the access, ORs a PA_DEVERR_* bit into
+ *     the caller's error word and leaves the affected output rows
+ *     unspecified.
+ */
+#ifndef PA_GB300_H
+#define PA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+typedef int32_t pa_status;
+#define PA_OK 0
+#define PA_ERR_INVALID_ARG 1   /* null pointer, negative size, bad stride, ... */
+#define PA_ERR_UNSUPPORTED 2   /* shape outside the supported set */
+#define PA_ERR_WORKSPACE 3     /* workspace missing or too small */
+#define PA_ERR_LAUNCH 4        /* the CUDA runtime rejected the launch */
+#define PA_ERR_DEVICE 5        /* a device query or copy failed */
+
+#define PA_DTYPE_BF16 0
+#define PA_DTYPE_F32 1
+
+/* Bits a kernel ORs into the caller's int32 error word. */
+#define PA_DEVERR_BLOCK_INDEX 1   /* block table entry outside [0, num_blocks) */
+#define PA_DEVERR_SLOT_INDEX 2    /* slot_mapping entry outside the pool */
+#define PA_DEVERR_WAIT_TIMEOUT 4  /* a pipeline wait gave up after ~2 s */
+#define PA_DEVERR_SHAPE 8         /* context_lens / cu_seqlens inconsistent */
+
+/* ABI version of the loaded library (PA_ABI_VERSION it was built with). */
+PA_API int32_t pa_abi_version(void);
+
+/* Static, human-readable name of a pa_status value. */
+PA_API const char *pa_status_string(pa_status status);
+
+/*
+ * pa_store_kv -- slot_mapping store ([EAS] "自写 Triton Kernel",
+ * store_kvcache_kernel; strides as in [EAS] error type 2).
+ *
+ * For every token t < num_tokens with slot = slot_mapping[t] >= 0, copies
+ * k[t][h][0..head_dim) and v[t][h][0..head_dim) for every kv head h into
+ * k_cache / v_cache at physical block slot / block_size, row
+ * slot % block_size.  Tokens with slot < 0 are padding and are skipped.
+ * The copy is bit-exact.  Two tokens naming the same slot is a caller error
+ * (one of them wins, unspecified which).
+ *
+ *   k, v           bf16 source rows; element (t, h, d) lives at
+ *                  k + t * k_tok_stride + h * k_head_stride + d (strides in
+ *                  elements, d contiguous), same for v.
+ *   k_cache,
+ *   v_cache        pools, [num_blocks][block_size][num_kv_heads][head_dim].
+ *   slot_mapping   int32 [num_tokens].
+ *   error_flags    optional int32 word (may be NULL); a slot >= num_blocks *
+ *                  block_size sets PA_DEVERR_SLOT_INDEX and that token is
+ *                  skipped.
+ */
+PA_API pa_status pa_store_kv(const void *k, const void *v, int64_t num_tokens,
+                      int64_t k_tok_stride, int64_t k_head_stride,
+                      int64_t v_tok_stride, int64_t v_head_stride,
+                      void *k_cache, void *v_cache, int64_t num_blocks,
+                      int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                      const int32_t *slot_mapping, int32_t *error_flags,
+                      void *stream);
+
+/*
+ * Decode split partition.  The decode work is the list of all KV blocks of
+ * all sequences, sequence after sequence: sequence b owns
+ * n_b = ceil(context_lens[b] / block_size) blocks, the global block index of
+ * its block j is P_b + j with P_b = n_0 + ... + n_{b-1}, and
+ * N = n_0 + ... + n_{batch-1}.  With S = num_splits, split c in [0, S)
+ * processes global blocks [floor(c N / S), floor((c + 1) N / S)).  Every
+ * split therefore moves the same number of KV bytes (+-1 block), however
+ * skewed the lengths are.
+ *
+ * A sequence whose blocks all fall in one split is finished by that split,
+ * which writes its output rows directly.  A sequence spread over splits
+ * c0 < c1 leaves a partial result in every split it touches: split c0 in
+ * slot (c0, 1) and every non-empty split c in (c0, c1] in slot (c, 0).  A
+ * partial is the attention output over that split's keys only, normalised
+ * over those keys, plus the natural-log sum-exp of its scaled scores.
+ *
+ * Workspace layout (bytes, from the workspace pointer, 256-byte aligned):
+ *   [0, 4)        int32 error word (PA_DEVERR_* bits; never cleared by the
+ *                 library -- zero it once when allocating);
+ *   [256, ...)    float partial_o[S][2][num_q_heads][head_dim];
+ *   then          float partial_lse[S][2][num_q_heads].
+ */
+PA_API size_t pa_decode_workspace_size(int32_t num_splits, int32_t num_q_heads, int32_t head_dim);
+
+/* num_splits used when pa_decode is given 0: one split per resident CTA of
+ * `device` (its SM count for the shipped kernel).  Returns <= 0 on error. */
+PA_API int32_t pa_decode_default_splits(int32_t device);
+
+/*
+ * pa_decode -- paged GQA decode attention ([EAS] "自写 Triton Kernel",
+ * Decode_Paged_GQAAttention_Kernel; flash-decoding split-K with a balanced
+ * block partition).
+ *
+ * For each sequence b and query head h, with g = h / (num_q_heads /
+ * num_kv_heads) and n = context_lens[b]:
+ *   out[b][h] = sum_{j<n} softmax_j(scale * q[b][h] . K_b[j][g]) V_b[j][g]
+ * where K_b[j] is row j % block_size of physical block
+ * block_tables[b][j / block_size].  The kernel walks the block table and
+ * streams pages through shared memory; nothing is gathered into contiguous
+ * memory.  Sequences with context 0 get a zero row.  If any sequence is
+ * spread over splits (see the partition above), pa_decode also enqueues
+ * pa_decode_merge on the same stream, so `out` is complete when the stream
+ * reaches the end of the call.
+ *
+ *   out            [batch][num_q_heads][head_dim], out_dtype.
+ *   q              bf16 [batch][num_q_heads][head_dim], contiguous.
+ *   k_cache,
+ *   v_cache        bf16 pools (layout above), num_blocks blocks each.
+ *   block_tables   int32 [batch][block_table_stride].
+ *   context_lens   int32 [batch]; negative values are treated as 0.
+ *   scale          softmax scale applied to q . k (e.g. 1/sqrt(head_dim)).
+ *   num_splits     S of the partition; 0 = pa_decode_default_splits.
+ *   workspace      device buffer of workspace_bytes >=
+ *                  pa_decode_workspace_size(S, num_q_heads, head_dim).
+ * Results do not depend on how sequences are laid out in the pool; with a
+ * fixed num_splits they are deterministic run to run.
+ */
+PA_API pa_status pa_decode(void *out, int32_t out_dtype, const void *q, const void *k_cache,
+                    const void *v_cache, int64_t num_blocks, const int32_t *block_tables,
+                    int32_t block_table_stride, const int32_t *context_lens, int32_t batch,
+                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t block_size, float scale, int32_t num_splits, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/*
+ * pa_decode_merge -- log-sum-exp merge of decode partials (flash-decoding).
+ *
+ * For every sequence spread over splits c0 < c1 (partition above, from
+ * context_lens, block_size and num_splits) and every query head, with
+ * partials (o_i, lse_i) read from the workspace slots listed above:
+ *   M = max_i lse_i,  w_i = exp(lse_i - M),  out = sum_i w_i o_i / sum_i w_i.
+ * Rows of sequences held by a single split are not touched.  pa_decode
+ * calls this itself; it is exported so that the merge can be run and timed
+ * on its own.
+ */
+PA_API pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *workspace,
+                          size_t workspace_bytes, const int32_t *context_lens,
+                          int32_t batch, int32_t num_q_heads, int32_t head_dim,
+                          int32_t block_size, int32_t num_splits, void *stream);
+
+/*
+ * pa_prefill_varlen -- causal varlen attention over a paged prefix ([MVT]
+ * "解决方案：变长 batch（varlen）", "cu_seqlens 只在 Attention 里才需要"; the
+ * per-sequence loop there is the one this kernel removes).
+ *
+ * Query rows of sequence s are rows cu_seqlens[s] .. cu_seqlens[s+1]-1 of q
+ * (q_len_s of them).  The sequence has n_s = context_lens[s] keys in the
+ * pool, its chunk's own keys included: store the chunk with pa_store_kv
+ * first.  Query i of the chunk sits at absolute position P_s + i with
+ * P_s = n_s - q_len_s (the paged prefix, [MVT] start_positions) and attends
+ * keys 0 .. P_s + i inclusive of its own sequence only.
+ *
+ *   out            [total_tokens][num_q_heads][head_dim], out_dtype.
+ *   q              bf16 [total_tokens][num_q_heads][head_dim], contiguous.
+ *   cu_seqlens     int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
+ *                  cu_seqlens[num_seqs] = total_tokens.
+ *   max_q_len      upper bound of every q_len_s (sizes the launch grid).
+ *   context_lens   int32 [num_seqs]; q_len_s > n_s sets PA_DEVERR_SHAPE and
+ *                  that sequence's rows are left unspecified.
+ *   error_flags    optional int32 word (may be NULL).
+ * Rows of different sequences never attend to each other, so a sequence's
+ * rows equal what the same call gives for that sequence alone.
+ */
+PA_API pa_status pa_prefill_varlen(void *out, int32_t out_dtype, const void *q,
+                            const int32_t *cu_seqlens, int32_t num_seqs,
+                            int32_t total_tokens, int32_t max_q_len, const void *k_cache,
+                            const void *v_cache, int64_t num_blocks,
+                            const int32_t *block_tables, int32_t block_table_stride,
+                            const int32_t *context_lens, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            float scale, int32_t *error_flags, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_GB300_H */

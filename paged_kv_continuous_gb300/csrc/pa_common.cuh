@@ -1,0 +1,151 @@
+// Device-side building blocks shared by the kernels of libpa_gb300.so:
+// mbarrier and bulk-copy (TMA) wrappers in inline PTX for sm_103a, bounded
+// pipeline waits, bf16 unpacking and the device error word.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlockSize = 16;
+// A pipeline wait gives up after this long, ORs PA_DEVERR_WAIT_TIMEOUT into
+// the error word and lets the kernel run out without touching memory again.
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void report(int32_t *err, int bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// ---- mbarrier ------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for phase `parity` of the barrier.  Gives up when *abort is set (by
+// another warp that already gave up) or after kWaitTimeoutNs; in the latter
+// case it sets *abort and reports PA_DEVERR_WAIT_TIMEOUT.  Returns true when
+// the phase completed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          int32_t *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+    if (*abort) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      *abort = 1;
+      report(err, PA_DEVERR_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ---- bulk copies (TMA, non-tensor) ---------------------------------------
+
+// Global -> shared bulk copy completing on an mbarrier.  dst, src and bytes
+// must be multiples of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// L2 policies for bulk loads: KV pages are streamed once per step, the small
+// per-sequence rows (q) are kept.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ---- named barrier among a subset of warps --------------------------------
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---- bf16 helpers --------------------------------------------------------
+
+// Two bf16 values packed in a 32-bit word (element 0 in the low half) to
+// fp32: a bf16 is the high half of an fp32, so both widenings are exact.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// fp32 -> bf16 with round to nearest even (finite inputs; NaN stays NaN).
+__device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ int ceil_div_blocks(int n) { return (n + kBlockSize - 1) / kBlockSize; }
+
+// Split c of S over N global blocks starts at floor(c N / S).
+__device__ __forceinline__ long long split_begin(long long c, long long S, long long N) {
+  return c * N / S;
+}
+// The split holding global block x: the largest c with split_begin(c) <= x.
+__device__ __forceinline__ long long split_of_block(long long x, long long S, long long N) {
+  return ((x + 1) * S - 1) / N;
+}
+
+}  // namespace pa

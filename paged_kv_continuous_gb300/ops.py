@@ -1,0 +1,197 @@
+"""Thin Python binding over libpa_gb300.so (the C ABI in include/pa.h).
+
+Argument marshalling only: every function takes torch tensors that already
+live on the GPU, checks shapes and dtypes, and passes raw device pointers,
+element strides and the current CUDA stream to the C entry point of the same
+name.  All arithmetic runs in the library's sm_103a kernels; there is no
+fallback path.  Importing this module loads the library and raises if it has
+not been built (``python -m paged_kv_continuous_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libpa_gb300.so")
+
+PA_OK = 0
+PA_DTYPE_BF16 = 0
+PA_DTYPE_F32 = 1
+DEVERR_BLOCK_INDEX = 1
+DEVERR_SLOT_INDEX = 2
+DEVERR_WAIT_TIMEOUT = 4
+DEVERR_SHAPE = 8
+
+EXPORTED = (
+    "pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
+    "pa_decode_default_splits", "pa_decode", "pa_decode_merge", "pa_prefill_varlen",
+)
+
+
+class PagedAttentionError(RuntimeError):
+    pass
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise PagedAttentionError(
+            f"{path} is missing: build it with `python -m paged_kv_continuous_gb300.build`")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    lib.pa_abi_version.restype = i32
+    lib.pa_abi_version.argtypes = []
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_status_string.argtypes = [i32]
+    lib.pa_store_kv.restype = i32
+    lib.pa_store_kv.argtypes = [P, P, i64, i64, i64, i64, i64, P, P, i64, i32, i32, i32, P, P, P]
+    lib.pa_decode_workspace_size.restype = sz
+    lib.pa_decode_workspace_size.argtypes = [i32, i32, i32]
+    lib.pa_decode_default_splits.restype = i32
+    lib.pa_decode_default_splits.argtypes = [i32]
+    lib.pa_decode.restype = i32
+    lib.pa_decode.argtypes = [P, i32, P, P, P, i64, P, i32, P, i32, i32, i32, i32, i32, f32,
+                              i32, P, sz, P]
+    lib.pa_decode_merge.restype = i32
+    lib.pa_decode_merge.argtypes = [P, i32, P, sz, P, i32, i32, i32, i32, i32, P]
+    lib.pa_prefill_varlen.restype = i32
+    lib.pa_prefill_varlen.argtypes = [P, i32, P, P, i32, i32, i32, P, P, i64, P, i32, P, i32,
+                                      i32, i32, i32, f32, P, P]
+    return lib
+
+
+lib = load_library()
+
+
+def _check(status: int, what: str):
+    if status != PA_OK:
+        raise PagedAttentionError(f"{what}: {lib.pa_status_string(status).decode()} ({status})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, name, dims=None):
+    if not t.is_cuda:
+        raise PagedAttentionError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise PagedAttentionError(f"{name} must be {dtype}, got {t.dtype}")
+    if dims is not None and t.dim() != dims:
+        raise PagedAttentionError(f"{name} must have {dims} dims, got {tuple(t.shape)}")
+
+
+def _out_code(dtype):
+    if dtype == torch.bfloat16:
+        return PA_DTYPE_BF16
+    if dtype == torch.float32:
+        return PA_DTYPE_F32
+    raise PagedAttentionError(f"unsupported output dtype {dtype}")
+
+
+def store_kv(k, v, k_cache, v_cache, slot_mapping, error_flags=None, stream=None):
+    """pa_store_kv: k/v bf16 [T, Hkv, D] (any token/head strides, unit dim
+    stride) into the pools at slot_mapping (int32 [T])."""
+    _need(k, torch.bfloat16, "k", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    _need(k_cache, torch.bfloat16, "k_cache", 4)
+    _need(v_cache, torch.bfloat16, "v_cache", 4)
+    _need(slot_mapping, torch.int32, "slot_mapping", 1)
+    if k.stride(2) != 1 or v.stride(2) != 1:
+        raise PagedAttentionError("k/v need a unit stride along head_dim")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise PagedAttentionError("pools must be contiguous")
+    T, Hkv, D = k.shape
+    NB, bs, Hkv2, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or v.shape != k.shape or v_cache.shape != k_cache.shape:
+        raise PagedAttentionError("shape mismatch between k/v and the pools")
+    if slot_mapping.shape[0] != T:
+        raise PagedAttentionError("slot_mapping must have one entry per token")
+    _check(lib.pa_store_kv(_ptr(k), _ptr(v), T, k.stride(0), k.stride(1), v.stride(0),
+                           v.stride(1), _ptr(k_cache), _ptr(v_cache), NB, bs, Hkv, D,
+                           _ptr(slot_mapping), _ptr(error_flags), _stream(stream)),
+           "pa_store_kv")
+
+
+def default_splits(device=None) -> int:
+    d = torch.cuda.current_device() if device is None else device
+    return int(lib.pa_decode_default_splits(d))
+
+
+def decode_workspace(num_q_heads: int, num_splits: int = 0, head_dim: int = 128, device=None):
+    """A zeroed workspace for pa_decode (the error word must start at zero)."""
+    s = num_splits if num_splits > 0 else default_splits(device)
+    n = int(lib.pa_decode_workspace_size(s, num_q_heads, head_dim))
+    if n == 0:
+        raise PagedAttentionError("bad workspace request")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+           out_dtype=torch.bfloat16, num_splits=0, workspace=None, stream=None):
+    """pa_decode: q bf16 [B, Hq, D] over the paged pools; returns out [B, Hq, D]."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k_cache, torch.bfloat16, "k_cache", 4)
+    _need(v_cache, torch.bfloat16, "v_cache", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    if not q.is_contiguous():
+        raise PagedAttentionError("q must be contiguous")
+    if block_tables.stride(1) != 1:
+        raise PagedAttentionError("block_tables rows must be contiguous")
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(Hq, num_splits, D, q.device)
+    _check(lib.pa_decode(_ptr(out), _out_code(out.dtype), _ptr(q), _ptr(k_cache),
+                         _ptr(v_cache), NB, _ptr(block_tables), block_tables.stride(0),
+                         _ptr(context_lens), B, Hq, Hkv, D, bs, float(scale), int(num_splits),
+                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                         _stream(stream)), "pa_decode")
+    return out
+
+
+def decode_merge(out, workspace, context_lens, num_splits, block_size=16, stream=None):
+    """pa_decode_merge over a workspace filled by pa_decode (or by hand)."""
+    B, Hq, D = out.shape
+    _check(lib.pa_decode_merge(_ptr(out), _out_code(out.dtype), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(),
+                               _ptr(context_lens), B, Hq, D, block_size, int(num_splits),
+                               _stream(stream)), "pa_decode_merge")
+    return out
+
+
+def prefill_varlen(q, cu_seqlens, k_cache, v_cache, block_tables, context_lens, scale,
+                   max_q_len, out=None, out_dtype=torch.bfloat16, error_flags=None,
+                   stream=None):
+    """pa_prefill_varlen: q bf16 [T, Hq, D] packed by cu_seqlens (int32 [N+1])."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(cu_seqlens, torch.int32, "cu_seqlens", 1)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    T, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=out_dtype, device=q.device)
+    _check(lib.pa_prefill_varlen(_ptr(out), _out_code(out.dtype), _ptr(q), _ptr(cu_seqlens),
+                                 cu_seqlens.shape[0] - 1, T, int(max_q_len), _ptr(k_cache),
+                                 _ptr(v_cache), NB, _ptr(block_tables), block_tables.stride(0),
+                                 _ptr(context_lens), Hq, Hkv, D, bs, float(scale),
+                                 _ptr(error_flags), _stream(stream)), "pa_prefill_varlen")
+    return out
+
+
+def read_error_word(buf) -> int:
+    """Host copy of an int32 error word (first 4 bytes of ``buf``); syncs."""
+    return int(buf[:4].view(torch.int32).item()) if buf.dtype == torch.uint8 else int(
+        buf.reshape(-1)[0].item())

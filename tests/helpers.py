@@ -53,3 +53,65 @@ def normal_bits(rng, shape):
 
 def const_bits(value, shape):
     return bf16_bits(np.full(shape, value, np.float32))
+
+
+# ---------------------------------------------------------------------------
+# GPU-side helpers (torch imported lazily so CPU tests never need CUDA)
+# ---------------------------------------------------------------------------
+
+def to_dev_bf16(bits):
+    """uint16 bf16 bit patterns (numpy) -> torch.bfloat16 CUDA tensor."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+        torch.bfloat16).cuda()
+
+
+def to_dev_i32(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+def bf16_dev_to_bits(t):
+    """torch.bfloat16 CUDA tensor -> numpy uint16 bit patterns."""
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def dev_to_f64(t):
+    """GPU output (bf16 or fp32) -> float64 numpy, exactly."""
+    import torch
+    if t.dtype == torch.bfloat16:
+        return bf16_to_f64(bf16_dev_to_bits(t))
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+ATOL = 2e-3
+RTOL = 1e-2
+
+
+def assert_attention_close(got, ref, what="", strict=False):
+    """The attention tolerance (bf16 inputs, fp32 accumulation): every element
+    within 2e-3 + 1e-2 |ref|.  With ``strict`` (fp32 outputs, where no output
+    rounding is involved) also max-abs <= 2e-3 and max-rel <= 1e-2, the
+    relative denominator floored at 1e-3."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    if np.any(bad):
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance; worst at {i}: "
+                             f"got {got[i]!r} ref {ref[i]!r} err {err[i]:.3e}")
+    if strict:
+        mabs, mrel = max_errors(got, ref)
+        assert mabs <= ATOL, f"{what}: max abs error {mabs:.3e} > {ATOL}"
+        assert mrel <= RTOL, f"{what}: max rel error {mrel:.3e} > {RTOL}"
+
+
+def max_errors(got, ref):
+    err = np.abs(np.asarray(got, np.float64) - ref)
+    rel = err / np.maximum(np.abs(ref), 1e-3)
+    return float(err.max(initial=0.0)), float(rel.max(initial=0.0))

@@ -1,0 +1,99 @@
+"""The C-ABI library loads without a GPU and exports every entry point that
+include/pa.h declares; argument checks that run before any CUDA call
+return the documented statuses.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_continuous_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_four_operations():
+    names = declared_functions()
+    for op in ("pa_store_kv", "pa_decode", "pa_decode_merge", "pa_prefill_varlen"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in pa.h but not exported"
+
+
+def test_binding_names_match_header():
+    from paged_kv_continuous_gb300 import build
+    build.build()
+    from paged_kv_continuous_gb300 import ops
+    assert sorted(ops.EXPORTED) == declared_functions()
+
+
+def test_version_and_status_strings(lib):
+    lib.pa_abi_version.restype = ctypes.c_int32
+    assert lib.pa_abi_version() == 1
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_status_string.argtypes = [ctypes.c_int32]
+    assert lib.pa_status_string(0) == b"ok"
+    assert b"workspace" in lib.pa_status_string(3)
+    assert lib.pa_status_string(99) == b"unknown status"
+
+
+def test_workspace_size_formula(lib):
+    f = lib.pa_decode_workspace_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int32] * 3
+
+    def up(x):
+        return (x + 255) // 256 * 256
+    for S, H in [(1, 12), (152, 12), (152, 32), (7, 5)]:
+        assert f(S, H, 128) == 256 + up(S * 2 * H * 128 * 4) + up(S * 2 * H * 4)
+    assert f(0, 12, 128) == 0 and f(4, 12, 64) == 0
+
+
+def test_argument_checks_before_any_launch():
+    """Shapes outside the supported set and malformed arguments are rejected
+    on the host, before the library touches the device."""
+    from paged_kv_continuous_gb300 import build
+    build.build()
+    from paged_kv_continuous_gb300 import ops
+    L = ops.lib
+    nul = None
+    # unsupported head_dim / block size / group size
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 64, 16, 0.1, 0, nul, 0,
+                       nul) == 2
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 32, 0.1, 0, nul,
+                       0, nul) == 2
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 18, 2, 128, 16, 0.1, 0, nul,
+                       0, nul) == 2          # group of 9
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 3, 128, 16, 0.1, 0, nul,
+                       0, nul) == 2          # 3 kv heads
+    # bad dtype / negative batch / NaN scale / null pointers
+    assert L.pa_decode(nul, 7, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 16, 0.1, 0, nul, 0,
+                       nul) == 1
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, -1, 12, 2, 128, 16, 0.1, 0, nul,
+                       0, nul) == 1
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 16, float("nan"),
+                       0, nul, 0, nul) == 1
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 16, 0.1, 0, nul, 0,
+                       nul) == 1
+    # empty batch is a no-op
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 0, 12, 2, 128, 16, 0.1, 0, nul, 0,
+                       nul) == 0
+    assert L.pa_store_kv(nul, nul, 0, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, nul) == 0
+    assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, nul) == 1
+    assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 96, nul, nul, nul) == 2
+    assert L.pa_decode_merge(nul, 0, nul, 0, nul, 1, 12, 128, 16, 0, nul) == 1
+    assert L.pa_decode_merge(nul, 0, nul, 0, nul, 1, 12, 128, 16, 4, nul) == 1
