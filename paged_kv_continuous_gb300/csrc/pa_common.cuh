@@ -110,8 +110,9 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 
 // ---- named barrier among a subset of warps --------------------------------
 
+// Non-aligned form: lanes of a warp may arrive from divergent paths.
 __device__ __forceinline__ void named_barrier(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // ---- bf16 helpers --------------------------------------------------------
@@ -133,7 +134,8 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
+               : "r"(addr)
+               : "memory");
   return v;
 }
 

@@ -287,7 +287,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
     const bool piece_last = (gb == hi - 1) || (j == n - 1);
     const int sidx = (int)(it % S::NST);
     const uint32_t sbase = stage0 + sidx * S::STAGE_BYTES;
-    const bool have = mbar_wait(full0 + 8 * sidx, (int)((it / S::NST) & 1), abort_flag, p.err);
+    // warp-uniform: the shuffles below need every lane of the warp
+    const bool have = __all_sync(
+        0xffffffffu, mbar_wait(full0 + 8 * sidx, (int)((it / S::NST) & 1), abort_flag, p.err));
     if (piece_first) {
       piece_j0 = j;
       st.reset();
@@ -305,7 +307,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
       }
     }
     const int valid = min(kBlockSize, ctx - j * kBlockSize);  // keys of this block
-    if (have && sub < valid) {
+    // Both half-warps enter together whenever the warp's first token is a key
+    // (the shuffles need all 32 lanes); tokens past `valid` are masked.
+    if (have && (cw / HKV) * 2 < valid) {
       // scores of this unit's tokens, all G heads, partial over 8 dims
       float s[HKV][G];
 #pragma unroll
@@ -338,7 +342,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
         for (int t = 0; t < HKV; ++t)
           if (sub + t * SUBS < valid) mx = fmaxf(mx, s[t][h]);
         const float m_new = fmaxf(st.m[h], mx);
-        const float alpha = exp2f(st.m[h] - m_new);
+        // no key seen yet by this unit (all masked so far): state stays empty
+        const float alpha = m_new == -INFINITY ? 1.f : exp2f(st.m[h] - m_new);
         st.m[h] = m_new;
         float lsum = st.l[h] * alpha;
 #pragma unroll
