@@ -121,9 +121,18 @@ def store_kv(k, v, k_cache, v_cache, slot_mapping, error_flags=None, stream=None
            "pa_store_kv")
 
 
+def _device_index(device=None) -> int:
+    if device is None:
+        return torch.cuda.current_device()
+    if isinstance(device, torch.device):
+        return device.index if device.index is not None else torch.cuda.current_device()
+    if isinstance(device, str):
+        return _device_index(torch.device(device))
+    return int(device)
+
+
 def default_splits(device=None) -> int:
-    d = torch.cuda.current_device() if device is None else device
-    return int(lib.pa_decode_default_splits(d))
+    return int(lib.pa_decode_default_splits(_device_index(device)))
 
 
 def decode_workspace(num_q_heads: int, num_splits: int = 0, head_dim: int = 128, device=None):
