@@ -207,6 +207,36 @@ PA_API pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *works
                           int32_t block_size, int32_t num_splits, void *stream);
 
 /*
+ * pa_decode_noalloc -- pa_decode without a workspace argument, for callers
+ * that cannot allocate device memory: an engine that gives nearly all free
+ * memory to its KV block pool at start-up and must not allocate on the
+ * decode path, a caller that only receives device pointers from a framework
+ * owning the allocator, or a decode loop that cannot take the device-wide
+ * synchronisation an allocation may cause.  The pages describe no such
+ * entry point; it has no counterpart there.
+ *
+ * Same arguments and result as pa_decode, except: the split partials live
+ * in a fixed 8 MiB array inside the library (a file-scope __device__ array,
+ * held by every GPU that loads the library until the process exits);
+ * device-side error bits go to `error_flags` (optional int32 word, may be
+ * NULL).  Returns PA_ERR_WORKSPACE, launching nothing, when
+ * pa_decode_workspace_size(S, num_q_heads, head_dim) exceeds 8 MiB for the
+ * split count S in use (S <= 677 at 12 query heads, S <= 254 at 32).  The
+ * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  The first call on a device, with that device current, looks up
+ * the array's device address and caches it; make that first call before
+ * any stream capture.  All calls on a device share the array: calls that
+ * overlap on the GPU race on it.  Nothing in it needs to start at zero.
+ */
+PA_API pa_status pa_decode_noalloc(void *out, int32_t out_dtype, const void *q,
+                                   const void *k_cache, const void *v_cache,
+                                   int64_t num_blocks, const int32_t *block_tables,
+                                   int32_t block_table_stride, const int32_t *context_lens,
+                                   int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size, float scale,
+                                   int32_t num_splits, int32_t *error_flags, void *stream);
+
+/*
  * pa_prefill_varlen -- causal varlen attention over a paged prefix ([MVT]
  * "解决方案：变长 batch（varlen）", "cu_seqlens 只在 Attention 里才需要"; the
  * per-sequence loop there is the one this kernel removes).

@@ -28,6 +28,7 @@ DEVERR_SHAPE = 8
 EXPORTED = (
     "pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
     "pa_decode_default_splits", "pa_decode", "pa_decode_merge", "pa_prefill_varlen",
+    "pa_decode_noalloc",
 )
 
 
@@ -57,6 +58,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                               i32, P, sz, P]
     lib.pa_decode_merge.restype = i32
     lib.pa_decode_merge.argtypes = [P, i32, P, sz, P, i32, i32, i32, i32, i32, P]
+    lib.pa_decode_noalloc.restype = i32
+    lib.pa_decode_noalloc.argtypes = [P, i32, P, P, P, i64, P, i32, P, i32, i32, i32, i32, i32,
+                                      f32, i32, P, P]
     lib.pa_prefill_varlen.restype = i32
     lib.pa_prefill_varlen.argtypes = [P, i32, P, P, i32, i32, i32, P, P, i64, P, i32, P, i32,
                                       i32, i32, i32, f32, P, P]
