@@ -140,13 +140,22 @@ PA_API pa_status pa_store_kv(const void *k, const void *v, int64_t num_tokens,
  * c0 < c1 leaves a partial result in every split it touches: split c0 in
  * slot (c0, 1) and every non-empty split c in (c0, c1] in slot (c, 0).  A
  * partial is the attention output over that split's keys only, normalised
- * over those keys, plus the natural-log sum-exp of its scaled scores.
+ * over those keys, plus the natural-log sum-exp of its scaled scores.  The
+ * split that completes a sequence's set of partials (counted in
+ * counters[c1]) merges them into the output rows and sets the counter back
+ * to zero, all inside the decode kernel.
  *
- * Workspace layout (bytes, from the workspace pointer, 256-byte aligned):
- *   [0, 4)        int32 error word (PA_DEVERR_* bits; never cleared by the
- *                 library -- zero it once when allocating);
- *   [256, ...)    float partial_o[S][2][num_q_heads][head_dim];
- *   then          float partial_lse[S][2][num_q_heads].
+ * Workspace layout (bytes from the workspace pointer; R(x) rounds x up to
+ * a multiple of 256; H = num_q_heads, D = head_dim):
+ *   [0, 4)              int32 error word (PA_DEVERR_* bits; the library
+ *                       only ORs bits in);
+ *   [256, ...)          float partial_o[S][2][H][D];
+ *   256 + R(8SHD)       float partial_lse[S][2][H];
+ *   then + R(8SH)       int32 counters[S] (zero between calls).
+ * Zero the whole workspace once when allocating it; every completed call
+ * leaves the counters at zero again.  After a call that reported
+ * PA_DEVERR_WAIT_TIMEOUT, zero it again.  One workspace serves one call in
+ * flight at a time.
  */
 PA_API size_t pa_decode_workspace_size(int32_t num_splits, int32_t num_q_heads, int32_t head_dim);
 
@@ -165,10 +174,9 @@ PA_API int32_t pa_decode_default_splits(int32_t device);
  * where K_b[j] is row j % block_size of physical block
  * block_tables[b][j / block_size].  The kernel walks the block table and
  * streams pages through shared memory; nothing is gathered into contiguous
- * memory.  Sequences with context 0 get a zero row.  If any sequence is
- * spread over splits (see the partition above), pa_decode also enqueues
- * pa_decode_merge on the same stream, so `out` is complete when the stream
- * reaches the end of the call.
+ * memory.  Sequences with context 0 get a zero row.  Sequences spread over
+ * splits (see the partition above) are merged inside the same kernel, so
+ * `out` is complete when the stream reaches the end of the call.
  *
  *   out            [batch][num_q_heads][head_dim], out_dtype.
  *   q              bf16 [batch][num_q_heads][head_dim], contiguous.
@@ -198,8 +206,10 @@ PA_API pa_status pa_decode(void *out, int32_t out_dtype, const void *q, const vo
  * partials (o_i, lse_i) read from the workspace slots listed above:
  *   M = max_i lse_i,  w_i = exp(lse_i - M),  out = sum_i w_i o_i / sum_i w_i.
  * Rows of sequences held by a single split are not touched.  pa_decode
- * calls this itself; it is exported so that the merge can be run and timed
- * on its own.
+ * performs the same merge inside its own kernel; this standalone kernel
+ * combines partials that are already in a workspace (e.g. written by
+ * another producer, or kept for inspection) and lets the merge be tested
+ * and timed on its own.  Counters are neither read nor written.
  */
 PA_API pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *workspace,
                           size_t workspace_bytes, const int32_t *context_lens,
@@ -221,12 +231,14 @@ PA_API pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *works
  * device-side error bits go to `error_flags` (optional int32 word, may be
  * NULL).  Returns PA_ERR_WORKSPACE, launching nothing, when
  * pa_decode_workspace_size(S, num_q_heads, head_dim) exceeds 8 MiB for the
- * split count S in use (S <= 677 at 12 query heads, S <= 254 at 32).  The
+ * split count S in use (S <= 677 at 12 query heads, S <= 253 at 32).  The
  * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  * routine.  The first call on a device, with that device current, looks up
  * the array's device address and caches it; make that first call before
  * any stream capture.  All calls on a device share the array: calls that
- * overlap on the GPU race on it.  Nothing in it needs to start at zero.
+ * overlap on the GPU race on it.  Each call clears the split arrival
+ * counters in the array (an asynchronous memset on `stream`) before its
+ * kernel; nothing else in it needs to start at zero.
  */
 PA_API pa_status pa_decode_noalloc(void *out, int32_t out_dtype, const void *q,
                                    const void *k_cache, const void *v_cache,

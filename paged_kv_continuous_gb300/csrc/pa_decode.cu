@@ -1,8 +1,15 @@
 // Host side of pa_decode / pa_decode_merge: argument checks, the workspace
-// layout, the split count and the launches.  The kernels are in
-// pa_decode_kernel.cuh (instantiated in pa_decode_h*.cu).
+// layout, the split count, the TMA tensor maps of the two pools and the
+// launches.  The decode kernel is in pa_decode_kernel.cuh (instantiated in
+// pa_decode_h*.cu); the standalone merge kernel is below.
+#include <climits>
+#include <cstring>
 #include <cmath>
+#include <mutex>
 
+#include <cudaTypedefs.h>
+
+#include "pa_decode_internal.h"
 #include "pa_decode_kernel.cuh"
 
 namespace pa {
@@ -97,45 +104,38 @@ __global__ void __launch_bounds__(32 * kMergeSeqPerCta) merge_kernel(const Merge
 
 namespace {
 
-constexpr size_t kWsHeader = 256;
-
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-
-size_t part_o_bytes(long long splits, int hq) {
-  return align256((size_t)splits * 2 * hq * kHeadDim * sizeof(float));
-}
-size_t part_lse_bytes(long long splits, int hq) {
-  return align256((size_t)splits * 2 * hq * sizeof(float));
-}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-pa_status check_heads(int32_t hq, int32_t hkv, int32_t head_dim, int32_t block_size) {
-  if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
-  if (!(hkv == 1 || hkv == 2 || hkv == 4 || hkv == 8)) return PA_ERR_UNSUPPORTED;
-  if (hq < hkv || hq % hkv != 0 || hq / hkv > 8) return PA_ERR_UNSUPPORTED;
-  return PA_OK;
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
 }
 
-int current_device() {
-  int d = -1;
-  return cudaGetDevice(&d) == cudaSuccess ? d : -1;
-}
-
-MergeParams merge_params(void *out, int32_t out_dtype, const void *workspace,
-                         const int32_t *context_lens, int32_t batch, int32_t hq,
-                         int32_t splits) {
-  const char *ws = static_cast<const char *>(workspace);
-  MergeParams m;
-  m.out = out;
-  m.out_f32 = out_dtype == PA_DTYPE_F32;
-  m.part_o = reinterpret_cast<const float *>(ws + kWsHeader);
-  m.part_lse = reinterpret_cast<const float *>(ws + kWsHeader + part_o_bytes(splits, hq));
-  m.context_lens = context_lens;
-  m.batch = batch;
-  m.num_q_heads = hq;
-  m.num_splits = splits;
-  return m;
+// 2-D view of a pool: rows = token slots (num_blocks * 16), columns = the
+// Hkv * 128 elements of a slot; one TMA tile = 16 slots x 64 columns with
+// the 128-byte swizzle.
+bool encode_pool_map(CUtensorMap *map, const void *pool, long long num_blocks, int hkv) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)hkv * kHeadDim, (cuuint64_t)num_blocks * kBlockSize};
+  cuuint64_t strides[1] = {(cuuint64_t)hkv * kHeadDim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t launch_merge(const MergeParams &m, cudaStream_t s) {
@@ -145,21 +145,95 @@ cudaError_t launch_merge(const MergeParams &m, cudaStream_t s) {
 }
 
 }  // namespace
+
+WorkspaceLayout workspace_layout(long long splits, int hq) {
+  WorkspaceLayout w;
+  w.part_o = kWorkspaceHeader;
+  w.part_lse = w.part_o + align256((size_t)splits * 2 * hq * kHeadDim * sizeof(float));
+  w.counters = w.part_lse + align256((size_t)splits * 2 * hq * sizeof(float));
+  w.total = w.counters + align256((size_t)splits * sizeof(int32_t));
+  return w;
+}
+
+pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int device,
+                     bool clear_counters) {
+  const WorkspaceLayout L = workspace_layout(r.splits, r.num_q_heads);
+  char *ws = static_cast<char *>(workspace);
+  CUtensorMap tk, tv;
+  memset(&tk, 0, sizeof tk);
+  memset(&tv, 0, sizeof tv);
+  if (r.num_blocks > 0) {
+    if (!encode_pool_map(&tk, r.k_cache, r.num_blocks, r.num_kv_heads) ||
+        !encode_pool_map(&tv, r.v_cache, r.num_blocks, r.num_kv_heads))
+      return PA_ERR_DEVICE;
+  }
+  DecodeParams p;
+  p.out = r.out;
+  p.out_f32 = r.out_dtype == PA_DTYPE_F32;
+  p.q = static_cast<const uint16_t *>(r.q);
+  p.num_blocks = r.num_blocks;
+  p.block_tables = r.block_tables;
+  p.bt_stride = r.block_table_stride;
+  p.context_lens = r.context_lens;
+  p.batch = r.batch;
+  p.qk_scale_log2 = r.scale * 1.4426950408889634f;
+  p.num_splits = r.splits;
+  p.part_o = reinterpret_cast<float *>(ws + L.part_o);
+  p.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
+  p.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+  p.err = err;
+  cudaStream_t s = static_cast<cudaStream_t>(r.stream);
+  if (clear_counters &&
+      cudaMemsetAsync(p.counters, 0, (size_t)r.splits * sizeof(int32_t), s) != cudaSuccess)
+    return PA_ERR_LAUNCH;
+  const int G = r.num_q_heads / r.num_kv_heads;
+  cudaError_t e;
+  switch (r.num_kv_heads) {
+    case 1: e = launch_decode<1>(G, tk, tv, p, s, device); break;
+    case 2: e = launch_decode<2>(G, tk, tv, p, s, device); break;
+    case 4: e = launch_decode<4>(G, tk, tv, p, s, device); break;
+    default: e = launch_decode<8>(G, tk, tv, p, s, device); break;
+  }
+  return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+}
+
+pa_status check_decode_request(DecodeRequest &r, int *device_out) {
+  if (r.batch < 0 || r.num_blocks < 0 || r.num_splits < 0) return PA_ERR_INVALID_ARG;
+  if (r.out_dtype != PA_DTYPE_BF16 && r.out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
+  if (r.head_dim != kHeadDim || r.block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  const int hkv = r.num_kv_heads, hq = r.num_q_heads;
+  if (!(hkv == 1 || hkv == 2 || hkv == 4 || hkv == 8)) return PA_ERR_UNSUPPORTED;
+  if (hq < hkv || hq % hkv != 0 || hq / hkv > 8) return PA_ERR_UNSUPPORTED;
+  if (!std::isfinite(r.scale)) return PA_ERR_INVALID_ARG;
+  if (r.num_blocks > (long long)(INT_MAX / kBlockSize)) return PA_ERR_UNSUPPORTED;
+  if (r.batch == 0) return PA_OK;
+  if (!r.out || !r.q || !r.k_cache || !r.v_cache || !r.block_tables || !r.context_lens)
+    return PA_ERR_INVALID_ARG;
+  if (r.block_table_stride < 1) return PA_ERR_INVALID_ARG;
+  if (!aligned16(r.out) || !aligned16(r.q) || !aligned16(r.k_cache) || !aligned16(r.v_cache))
+    return PA_ERR_INVALID_ARG;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0) return PA_ERR_DEVICE;
+  r.splits = r.num_splits > 0 ? r.num_splits : pa_decode_default_splits(device);
+  if (r.splits < 1) return PA_ERR_DEVICE;
+  *device_out = device;
+  return PA_OK;
+}
+
 }  // namespace pa
 
 extern "C" size_t pa_decode_workspace_size(int32_t num_splits, int32_t num_q_heads,
                                            int32_t head_dim) {
   using namespace pa;
   if (num_splits < 1 || num_q_heads < 1 || head_dim != kHeadDim) return 0;
-  return kWsHeader + part_o_bytes(num_splits, num_q_heads) +
-         part_lse_bytes(num_splits, num_q_heads);
+  return workspace_layout(num_splits, num_q_heads).total;
 }
 
 extern "C" int32_t pa_decode_default_splits(int32_t device) {
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return -1;
-  return sms;  // one 1-CTA-per-SM split per SM
+  return sms;  // the decode kernel runs one CTA per SM
 }
 
 extern "C" pa_status pa_decode(void *out, int32_t out_dtype, const void *q, const void *k_cache,
@@ -170,60 +244,16 @@ extern "C" pa_status pa_decode(void *out, int32_t out_dtype, const void *q, cons
                                float scale, int32_t num_splits, void *workspace,
                                size_t workspace_bytes, void *stream) {
   using namespace pa;
-  if (batch < 0 || num_blocks < 0 || num_splits < 0) return PA_ERR_INVALID_ARG;
-  if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
-  const pa_status hs = check_heads(num_q_heads, num_kv_heads, head_dim, block_size);
-  if (hs != PA_OK) return hs;
-  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
-  if (batch == 0) return PA_OK;
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
-    return PA_ERR_INVALID_ARG;
-  if (block_table_stride < 1) return PA_ERR_INVALID_ARG;
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-    return PA_ERR_INVALID_ARG;
-  const int device = current_device();
-  if (device < 0) return PA_ERR_DEVICE;
-  const int32_t splits = num_splits > 0 ? num_splits : pa_decode_default_splits(device);
-  if (splits < 1) return PA_ERR_DEVICE;
+  DecodeRequest r{out, out_dtype, q, k_cache, v_cache, num_blocks, block_tables,
+                  block_table_stride, context_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                  block_size, scale, num_splits, 0, stream};
+  int device = -1;
+  const pa_status st = check_decode_request(r, &device);
+  if (st != PA_OK || batch == 0) return st;
   if (!workspace || !aligned16(workspace) ||
-      workspace_bytes < pa_decode_workspace_size(splits, num_q_heads, head_dim))
+      workspace_bytes < pa_decode_workspace_size(r.splits, num_q_heads, head_dim))
     return PA_ERR_WORKSPACE;
-
-  char *ws = static_cast<char *>(workspace);
-  DecodeParams p;
-  p.out = out;
-  p.out_f32 = out_dtype == PA_DTYPE_F32;
-  p.q = static_cast<const uint16_t *>(q);
-  p.k_cache = static_cast<const uint16_t *>(k_cache);
-  p.v_cache = static_cast<const uint16_t *>(v_cache);
-  p.num_blocks = num_blocks;
-  p.block_tables = block_tables;
-  p.bt_stride = block_table_stride;
-  p.context_lens = context_lens;
-  p.batch = batch;
-  p.qk_scale_log2 = scale * 1.4426950408889634f;
-  p.num_splits = splits;
-  p.part_o = reinterpret_cast<float *>(ws + kWsHeader);
-  p.part_lse = reinterpret_cast<float *>(ws + kWsHeader + part_o_bytes(splits, num_q_heads));
-  p.err = reinterpret_cast<int32_t *>(ws);
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int G = num_q_heads / num_kv_heads;
-  cudaError_t e;
-  switch (num_kv_heads) {
-    case 1: e = launch_decode<1>(G, p, s, device); break;
-    case 2: e = launch_decode<2>(G, p, s, device); break;
-    case 4: e = launch_decode<4>(G, p, s, device); break;
-    default: e = launch_decode<8>(G, p, s, device); break;
-  }
-  if (e != cudaSuccess) return PA_ERR_LAUNCH;
-  if (splits > 1) {
-    e = launch_merge(merge_params(out, out_dtype, workspace, context_lens, batch, num_q_heads,
-                                  splits),
-                     s);
-    if (e != cudaSuccess) return PA_ERR_LAUNCH;
-  }
-  return PA_OK;
+  return run_decode(r, workspace, static_cast<int32_t *>(workspace), device, false);
 }
 
 extern "C" pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *workspace,
@@ -240,8 +270,17 @@ extern "C" pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *w
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < pa_decode_workspace_size(num_splits, num_q_heads, head_dim))
     return PA_ERR_WORKSPACE;
-  const cudaError_t e = launch_merge(
-      merge_params(out, out_dtype, workspace, context_lens, batch, num_q_heads, num_splits),
-      static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+  const WorkspaceLayout L = workspace_layout(num_splits, num_q_heads);
+  const char *ws = static_cast<const char *>(workspace);
+  MergeParams m;
+  m.out = out;
+  m.out_f32 = out_dtype == PA_DTYPE_F32;
+  m.part_o = reinterpret_cast<const float *>(ws + L.part_o);
+  m.part_lse = reinterpret_cast<const float *>(ws + L.part_lse);
+  m.context_lens = context_lens;
+  m.batch = batch;
+  m.num_q_heads = num_q_heads;
+  m.num_splits = num_splits;
+  return launch_merge(m, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
+                                                                           : PA_ERR_LAUNCH;
 }

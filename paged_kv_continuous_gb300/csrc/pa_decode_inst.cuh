@@ -11,7 +11,8 @@ namespace pa {
 
 namespace {
 template <int G>
-cudaError_t launch_g(const DecodeParams &p, cudaStream_t s, int device) {
+cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
+                     cudaStream_t s, int device) {
   using Sh = DecodeShape<G, PA_HKV>;
   static bool configured[64] = {};
   if (device < 0 || device >= 64 || !configured[device]) {
@@ -20,38 +21,24 @@ cudaError_t launch_g(const DecodeParams &p, cudaStream_t s, int device) {
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < 64) configured[device] = true;
   }
-  decode_kernel<G, PA_HKV><<<p.num_splits, kDecodeThreads, Sh::SMEM, s>>>(p);
+  decode_kernel<G, PA_HKV><<<p.num_splits, kDecodeThreads, Sh::SMEM, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 }  // namespace
 
 template <>
-cudaError_t launch_decode<PA_HKV>(int G, const DecodeParams &p, cudaStream_t s, int device) {
+cudaError_t launch_decode<PA_HKV>(int G, const CUtensorMap &tk, const CUtensorMap &tv,
+                                  const DecodeParams &p, cudaStream_t s, int device) {
   switch (G) {
-    case 1: return launch_g<1>(p, s, device);
-    case 2: return launch_g<2>(p, s, device);
-    case 3: return launch_g<3>(p, s, device);
-    case 4: return launch_g<4>(p, s, device);
-    case 5: return launch_g<5>(p, s, device);
-    case 6: return launch_g<6>(p, s, device);
-    case 7: return launch_g<7>(p, s, device);
-    case 8: return launch_g<8>(p, s, device);
+    case 1: return launch_g<1>(tk, tv, p, s, device);
+    case 2: return launch_g<2>(tk, tv, p, s, device);
+    case 3: return launch_g<3>(tk, tv, p, s, device);
+    case 4: return launch_g<4>(tk, tv, p, s, device);
+    case 5: return launch_g<5>(tk, tv, p, s, device);
+    case 6: return launch_g<6>(tk, tv, p, s, device);
+    case 7: return launch_g<7>(tk, tv, p, s, device);
+    case 8: return launch_g<8>(tk, tv, p, s, device);
     default: return cudaErrorInvalidValue;
-  }
-}
-
-template <>
-int decode_smem_bytes<PA_HKV>(int G) {
-  switch (G) {
-    case 1: return DecodeShape<1, PA_HKV>::SMEM;
-    case 2: return DecodeShape<2, PA_HKV>::SMEM;
-    case 3: return DecodeShape<3, PA_HKV>::SMEM;
-    case 4: return DecodeShape<4, PA_HKV>::SMEM;
-    case 5: return DecodeShape<5, PA_HKV>::SMEM;
-    case 6: return DecodeShape<6, PA_HKV>::SMEM;
-    case 7: return DecodeShape<7, PA_HKV>::SMEM;
-    case 8: return DecodeShape<8, PA_HKV>::SMEM;
-    default: return 0;
   }
 }
 

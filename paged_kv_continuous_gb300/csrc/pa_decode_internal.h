@@ -1,0 +1,47 @@
+// Host-side pieces shared by pa_decode.cu and pa_decode_noalloc.cu (not part
+// of the public ABI).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+constexpr size_t kWorkspaceHeader = 256;  // int32 error word + reserved
+
+// Byte offsets inside a decode workspace for `splits` splits.
+struct WorkspaceLayout {
+  size_t part_o;    // float [splits][2][hq][128]
+  size_t part_lse;  // float [splits][2][hq]
+  size_t counters;  // int32 [splits], zero between calls
+  size_t total;
+};
+WorkspaceLayout workspace_layout(long long splits, int hq);
+
+struct DecodeRequest {
+  void *out;
+  int32_t out_dtype;
+  const void *q, *k_cache, *v_cache;
+  int64_t num_blocks;
+  const int32_t *block_tables;
+  int32_t block_table_stride;
+  const int32_t *context_lens;
+  int32_t batch, num_q_heads, num_kv_heads, head_dim, block_size;
+  float scale;
+  int32_t num_splits;  // as given (0 = default)
+  int32_t splits;      // resolved by check_decode_request
+  void *stream;
+};
+
+// Host checks shared by both decode entry points; resolves r.splits.
+pa_status check_decode_request(DecodeRequest &r, int *device);
+
+// Encodes the pool tensor maps and launches the decode kernel (which merges
+// cut sequences itself).  `clear_counters` enqueues a memset of the arrival
+// counters first.
+pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int device,
+                     bool clear_counters);
+
+}  // namespace pa

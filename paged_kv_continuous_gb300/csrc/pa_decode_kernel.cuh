@@ -2,28 +2,41 @@
 // "自写 Triton Kernel", Decode_Paged_GQAAttention_Kernel: the kernel walks the
 // block_table itself, keeps an online softmax and serves all query heads of
 // a GQA group from one K/V read; no gather into contiguous memory) with
-// flash-decoding split-K partials.
+// flash-decoding split-K partials merged inside the kernel.
 //
 // Work partition.  The blocks of all sequences, in order, form one list of
 // N blocks; CTA c of S takes blocks [floor(cN/S), floor((c+1)N/S)).  Every
 // CTA moves the same number of bytes however skewed the lengths are, and
 // consecutive sequences flow through one CTA's pipeline without draining it.
 // A "piece" is the run of one sequence's blocks inside one CTA.  A piece
-// that is the whole sequence writes the output rows; a cut piece writes a
+// that is the whole sequence writes the output rows.  A cut piece writes a
 // partial (o normalised over its keys, natural-log sum-exp) to the
-// workspace for the merge kernel.
+// workspace and bumps the sequence's arrival counter; the CTA that brings
+// the counter to the piece count merges all partials of that sequence
+// (log-sum-exp) and writes its rows, then resets the counter to zero.
 //
 // CTA layout (288 threads).  Warp 0, lane 0 is the producer: it walks the
-// CTA's block list and bulk-copies (TMA, cp.async.bulk) each physical block
-// of K and V -- one contiguous [16][Hkv][128] bf16 page each -- plus the
-// sequence's q row at the start of a piece, into a ring of NST stages
-// guarded by full/empty mbarriers.  Warps 1..8 consume every stage; a
-// half-warp unit owns one kv head g and a fixed subset of the block's 16
-// tokens, lane l owns dims 8l..8l+7.  Scores are dot products in packed fp32
-// (FFMA2) reduced with warp shuffles; each unit keeps a running max, sum and
-// output for the G query heads of its kv head; units of the same kv head are
-// merged through shared memory at the end of each piece.
+// CTA's block list and issues, per physical block and kv head, two TMA tile
+// loads of K and two of V (16 tokens x 64 dims each, 128-byte swizzle), plus
+// a bulk copy of the sequence's q row at the start of a piece, into a ring
+// of NST stages guarded by full/empty mbarriers.  Warps 1..8 consume: warp
+// (g, ph) handles kv head g of every stage whose index is ph modulo
+// 8 / Hkv.
+//
+// Arithmetic per (block, kv head) on the tensor cores (mma.sync m16n8k16,
+// bf16 in, fp32 accumulate), with the G query heads of the group as the
+// N = 8 dimension:
+//   S^T[16 tokens][8 heads] = K[16 x 128] . Q^T[128 x 8]      (8 MMAs)
+//   online softmax over the 16 tokens per head column (fp32, base 2)
+//   O^T[128][8]  += V^T[128 x 16] . P^T[16 x 8]                (8 MMAs x 2)
+// P is split into bf16 hi + lo parts (two MMAs per tile) so the product
+// keeps ~16 bits of the fp32 weights.  K fragments come from ldmatrix on the
+// swizzled tiles, V fragments from ldmatrix.trans, P^T from movmatrix.trans
+// of the score fragment.
 #pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
 
 #include "pa_common.cuh"
 
@@ -32,45 +45,47 @@ namespace pa {
 struct DecodeParams {
   void *out;
   int out_f32;
-  const uint16_t *q;        // [B][HQ][128]
-  const uint16_t *k_cache;  // [num_blocks][16][HKV][128]
-  const uint16_t *v_cache;
+  const uint16_t *q;  // [B][HQ][128]
   long long num_blocks;
   const int32_t *block_tables;
   long long bt_stride;
   const int32_t *context_lens;
   int batch;
-  float qk_scale_log2;  // softmax scale * log2(e): scores are kept in base 2
+  float qk_scale_log2;  // softmax scale * log2(e): exponentials are base 2
   int num_splits;
-  float *part_o;    // [S][2][HQ][128]
-  float *part_lse;  // [S][2][HQ], natural log
+  float *part_o;      // [S][2][HQ][128]
+  float *part_lse;    // [S][2][HQ], natural log
+  int32_t *counters;  // [S] arrival counters, zero between calls
   int32_t *err;
 };
 
 constexpr int kDecodeConsumerWarps = 8;
 constexpr int kDecodeThreads = 32 * (1 + kDecodeConsumerWarps);
 constexpr int kDecodeSmemBudget = 227 * 1024;
+constexpr int kTileBytes = kBlockSize * 64 * 2;  // 16 tokens x 64 dims bf16 = 2 KB
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 template <int G, int HKV>
 struct DecodeShape {
   static constexpr int HQ = G * HKV;
-  static constexpr int KV_BYTES = kBlockSize * HKV * kHeadDim * 2;  // one page of K (or V)
+  static constexpr int NPH = kDecodeConsumerWarps / HKV;  // stage phases = warps per kv head
+  static constexpr int KV_BYTES = HKV * 2 * kTileBytes;     // one block of K (or V), all heads
   static constexpr int Q_BYTES = HQ * kHeadDim * 2;
-  static constexpr int STAGE_BYTES = align_up(2 * KV_BYTES + Q_BYTES, 128);
-  static constexpr int WARPS_PER_HEAD = kDecodeConsumerWarps / HKV;
-  // per consumer warp: m, l and o[128] for each of its G heads
+  static constexpr int STAGE_BYTES = align_up(2 * KV_BYTES + Q_BYTES, 1024);
+  // per consumer warp and query head of its group: m, l, o[128]
   static constexpr int RED_FLOATS_PER_HEAD = kHeadDim + 2;
   static constexpr int RED_BYTES =
-      WARPS_PER_HEAD > 1 ? kDecodeConsumerWarps * G * RED_FLOATS_PER_HEAD * 4 : 0;
+      NPH > 1 ? align_up(kDecodeConsumerWarps * G * RED_FLOATS_PER_HEAD * 4, 1024) : 0;
   static constexpr int CTL_BYTES = 256;
-  static constexpr int NST_FIT = (kDecodeSmemBudget - RED_BYTES - CTL_BYTES) /
-                                 (STAGE_BYTES + 16);
-  static constexpr int NST = NST_FIT > 16 ? 16 : NST_FIT;
-  static constexpr int SMEM = NST * STAGE_BYTES + RED_BYTES + NST * 16 + CTL_BYTES;
+  static constexpr int NST_FIT =
+      (kDecodeSmemBudget - 1024 - RED_BYTES - CTL_BYTES) / (STAGE_BYTES + 16);
+  static constexpr int NST = NST_FIT > 12 ? 12 : NST_FIT;
+  // +1024: the dynamic smem base is realigned to 1024 bytes for the swizzle
+  static constexpr int SMEM = 1024 + NST * STAGE_BYTES + RED_BYTES + NST * 16 + CTL_BYTES;
   static_assert(NST >= 2, "stage does not fit twice in shared memory");
-  static_assert(16 % HKV == 0 && kDecodeConsumerWarps % HKV == 0, "unsupported kv heads");
+  static_assert(kDecodeConsumerWarps % HKV == 0, "unsupported kv head count");
+  static_assert(G >= 1 && G <= 8, "group size must fit the N = 8 MMA dimension");
 };
 
 struct DecodeCtl {
@@ -78,6 +93,7 @@ struct DecodeCtl {
   long long first_prefix;    // global index of block 0 of first_b
   int first_b;               // sequence holding this CTA's first block
   int abort;                 // set by a wait that gave up
+  int last;                  // this CTA merges the current cut sequence
 };
 
 __device__ __forceinline__ int seq_blocks(const int32_t *ctx, int b) {
@@ -85,28 +101,125 @@ __device__ __forceinline__ int seq_blocks(const int32_t *ctx, int b) {
   return n > 0 ? ceil_div_blocks(n) : 0;
 }
 
-// Online-softmax state of one half-warp unit for its G heads; lane l holds
-// output dims 8l..8l+7 as four packed pairs.
-template <int G>
-struct UnitState {
-  float2 o[G][4];
-  float m[G];
-  float l[G];
-  __device__ __forceinline__ void reset() {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[h][i] = make_float2(0.f, 0.f);
-    }
+// ---- tensor-core and TMA helpers -------------------------------------------
+
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                              uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                          uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// d += A(16x16, row) . B(16x8, col), bf16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Byte offset of (row, 16-byte chunk) in a tile written by TMA with the
+// 128-byte swizzle: the chunk index is XORed with the row index mod 8.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+// ---- output writers ---------------------------------------------------------
+
+__device__ __forceinline__ void store_out1(void *out, int out_f32, long long idx, float a) {
+  if (out_f32)
+    static_cast<float *>(out)[idx] = a;
+  else
+    static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(a);
+}
+
+__device__ __forceinline__ void store_out2(void *out, int out_f32, long long idx, float a,
+                                           float b) {
+  if (out_f32)
+    *reinterpret_cast<float2 *>(static_cast<float *>(out) + idx) = make_float2(a, b);
+  else
+    *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(out) + idx) = float2_to_bf16x2(a, b);
+}
+
+__device__ __forceinline__ void store_out4(void *out, int out_f32, long long idx, float4 v) {
+  if (out_f32) {
+    *reinterpret_cast<float4 *>(static_cast<float *>(out) + idx) = v;
+  } else {
+    uint2 w;
+    w.x = float2_to_bf16x2(v.x, v.y);
+    w.y = float2_to_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + idx) = w;
   }
-};
+}
+
+// Log-sum-exp merge of all partials of sequence b (split-K pieces c0..c1),
+// done by the consumer threads of the CTA that completed the set.
+template <int HQ>
+__device__ void merge_sequence(const DecodeParams &p, int b, long long c0, long long c1,
+                               long long S, long long N, int ct, int nthreads) {
+  for (int item = ct; item < HQ * (kHeadDim / 4); item += nthreads) {
+    const int h = item / (kHeadDim / 4);
+    const int d = (item % (kHeadDim / 4)) * 4;
+    float M = -INFINITY;
+    for (long long cc = c0; cc <= c1; ++cc) {
+      if (cc != c0 && split_begin(cc, S, N) == split_begin(cc + 1, S, N)) continue;
+      const long long row = (cc * 2 + (cc == c0 ? 1 : 0)) * HQ + h;
+      M = fmaxf(M, __ldcg(p.part_lse + row));
+    }
+    float W = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long long cc = c0; cc <= c1; ++cc) {
+      if (cc != c0 && split_begin(cc, S, N) == split_begin(cc + 1, S, N)) continue;
+      const long long row = (cc * 2 + (cc == c0 ? 1 : 0)) * HQ + h;
+      const float lse = __ldcg(p.part_lse + row);
+      const float w = lse == -INFINITY ? 0.f : __expf(lse - M);
+      const float4 o = __ldcg(reinterpret_cast<const float4 *>(p.part_o + row * kHeadDim + d));
+      W += w;
+      acc.x += w * o.x;
+      acc.y += w * o.y;
+      acc.z += w * o.z;
+      acc.w += w * o.w;
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d,
+               make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+  }
+}
 
 template <int G, int HKV>
-__global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
   using S = DecodeShape<G, HKV>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  // realign to 1024 bytes: the 128-byte swizzle pattern repeats every 1 KB
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float *red = reinterpret_cast<float *>(smem + S::NST * S::STAGE_BYTES);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::NST * S::STAGE_BYTES + S::RED_BYTES);
   uint64_t *empty = full + S::NST;
@@ -125,6 +238,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
     ctl->first_b = -1;
     ctl->first_prefix = 0;
     ctl->abort = 0;
+    ctl->last = 0;
   }
   __syncthreads();
   {
@@ -169,20 +283,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
             n == 0 && ((lo <= prefix && prefix < hi) || (prefix >= N && c == nsplit - 1));
         if (owns_empty) {
           const long long row0 = (long long)b * S::HQ * kHeadDim;
-          if (p.out_f32) {
-            float *o = static_cast<float *>(p.out) + row0;
-            for (int i = 0; i < S::HQ * kHeadDim; ++i) o[i] = 0.f;
-          } else {
-            uint16_t *o = static_cast<uint16_t *>(p.out) + row0;
-            for (int i = 0; i < S::HQ * kHeadDim; ++i) o[i] = 0;
-          }
+          for (int i = 0; i < S::HQ * kHeadDim; i += 2)
+            store_out2(p.out, p.out_f32, row0 + i, 0.f, 0.f);
         }
       }
       running += chunk_total;
       __syncthreads();
     }
   }
-  if (lo >= hi) return;  // no block for this CTA (N < S)
+  if (lo >= hi) return;    // no block for this CTA (N < S)
   if (ctl->first_b < 0) {  // cannot happen for consistent inputs; never walk from b = -1
     if (tid == 0) report(p.err, PA_DEVERR_SHAPE);
     return;
@@ -206,6 +315,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
   if (warp == 0) {
     // ---- 4. producer ---------------------------------------------------------
     if (lane != 0) return;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
+                 : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v))
+                 : "memory");
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
     int b = first_b;
@@ -227,16 +340,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
       // a row holds bt_stride entries: a context longer than the row is a
       // caller error, reported and not read
       const bool in_row = j < p.bt_stride;
-      const long long phys = in_row ? __ldg(p.block_tables + (long long)b * p.bt_stride + j) : -1;
+      const long long phys =
+          in_row ? __ldg(p.block_tables + (long long)b * p.bt_stride + j) : -1;
       const bool ok = phys >= 0 && phys < p.num_blocks;
       const uint32_t bytes = (ok ? 2u * S::KV_BYTES : 0u) + (piece_first ? S::Q_BYTES : 0u);
       const uint32_t dst = stage0 + st * S::STAGE_BYTES;
       const uint32_t bar = full0 + 8 * st;
       mbar_arrive_expect_tx(bar, bytes);
       if (ok) {
-        const long long off = phys * (long long)(kBlockSize * HKV * kHeadDim);
-        bulk_load(dst, p.k_cache + off, S::KV_BYTES, bar, pol_kv);
-        bulk_load(dst + S::KV_BYTES, p.v_cache + off, S::KV_BYTES, bar, pol_kv);
+        const int y = (int)(phys * kBlockSize);
+#pragma unroll
+        for (int g = 0; g < HKV; ++g) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_load_tile(dst + (g * 2 + h) * kTileBytes, &tmap_k, g * kHeadDim + h * 64, y, bar,
+                          pol_kv);
+            tma_load_tile(dst + S::KV_BYTES + (g * 2 + h) * kTileBytes, &tmap_v,
+                          g * kHeadDim + h * 64, y, bar, pol_kv);
+          }
+        }
       } else {
         report(p.err, in_row ? PA_DEVERR_BLOCK_INDEX : PA_DEVERR_SHAPE);
       }
@@ -256,21 +378,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
   }
 
   // ---- 5. consumers -----------------------------------------------------------
-  const int cw = warp - 1;                   // consumer warp 0..7
-  const int hw = lane >> 4;                  // half-warp
-  const int l = lane & 15;                   // dims 8l..8l+7
-  const int g = cw % HKV;                    // kv head of this warp
-  constexpr int SUBS = kBlockSize / HKV;     // units per kv head = token stride
-  const int sub = (cw / HKV) * 2 + hw;       // tokens sub, sub + SUBS, ...
-  const int row_off = g * kHeadDim * 2 + l * 16;  // byte offset of (g, 8l) in a token row
+  const int cw = warp - 1;    // consumer warp 0..7
+  const int g = cw % HKV;     // kv head of this warp
+  const int ph = cw / HKV;    // stage phase of this warp
+  const int gid = lane >> 2;  // fragment row group
+  const int qd = lane & 3;    // fragment column pair
+  const int ct = tid - 32;    // consumer thread index 0..255
+  const float cl2 = p.qk_scale_log2;
 
-  UnitState<G> st;
-  st.reset();
-  float2 qf[G][4];
+  uint32_t qf[8][2];  // Q^T fragments of the group, per 16-dim k-step
+  float o[8][4];      // O^T rows 16 mt + {gid, gid + 8}, head columns 2 qd, 2 qd + 1
+  float m0 = -INFINITY, m1 = -INFINITY;  // running max (raw score units), heads 2qd, 2qd+1
+  float l0 = 0.f, l1 = 0.f;              // running sum over this lane's tokens
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) qf[ks][0] = qf[ks][1] = 0u;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
 
   int b = first_b;
-  int n = seq_blocks(p.context_lens, b);
   int ctx = __ldg(p.context_lens + b);
+  int n = ctx > 0 ? ceil_div_blocks(ctx) : 0;
   int j = (int)(lo - first_prefix);
   int piece_j0 = j;
   long long it = 0;
@@ -287,178 +416,198 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
     const bool piece_last = (gb == hi - 1) || (j == n - 1);
     const int sidx = (int)(it % S::NST);
     const uint32_t sbase = stage0 + sidx * S::STAGE_BYTES;
-    // warp-uniform: the shuffles below need every lane of the warp
+    // warp-uniform: the collective instructions below need every lane
     const bool have = __all_sync(
         0xffffffffu, mbar_wait(full0 + 8 * sidx, (int)((it / S::NST) & 1), abort_flag, p.err));
     if (piece_first) {
       piece_j0 = j;
-      st.reset();
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
       if (have) {
+        const uint32_t qrow = sbase + 2 * S::KV_BYTES + (g * G + gid) * kHeadDim * 2;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const uint4 w = lds128(sbase + 2 * S::KV_BYTES + (g * G + h) * kHeadDim * 2 + l * 16);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f = bf16x2_to_float2(ws[i]);
-            qf[h][i] = make_float2(f.x * p.qk_scale_log2, f.y * p.qk_scale_log2);
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t x0 = 0, x1 = 0;
+          if (gid < G) {
+            asm volatile("ld.shared.u32 %0, [%1];"
+                         : "=r"(x0)
+                         : "r"(qrow + (16 * ks + 2 * qd) * 2)
+                         : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];"
+                         : "=r"(x1)
+                         : "r"(qrow + (16 * ks + 8 + 2 * qd) * 2)
+                         : "memory");
           }
+          qf[ks][0] = x0;
+          qf[ks][1] = x1;
         }
       }
     }
-    const int valid = min(kBlockSize, ctx - j * kBlockSize);  // keys of this block
-    // Both half-warps enter together whenever the warp's first token is a key
-    // (the shuffles need all 32 lanes); tokens past `valid` are masked.
-    if (have && (cw / HKV) * 2 < valid) {
-      // scores of this unit's tokens, all G heads, partial over 8 dims
-      float s[HKV][G];
+    const int valid = min(kBlockSize, ctx - j * kBlockSize);  // keys of this block (>= 1)
+    if (have && (int)(it % S::NPH) == ph) {
+      const uint32_t kb = sbase + g * 2 * kTileBytes;
+      const uint32_t vb = sbase + S::KV_BYTES + g * 2 * kTileBytes;
+      // S^T = K . Q^T, two accumulation chains over the eight 16-dim k-steps
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int mi = lane >> 3, r = lane & 7;
+        const int t = r + ((mi & 1) << 3);
 #pragma unroll
-      for (int t = 0; t < HKV; ++t) {
-        const int tok = sub + t * SUBS;
-        const uint4 w = lds128(sbase + tok * HKV * kHeadDim * 2 + row_off);
-        const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
-        const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float2 a = __fmul2_rn(qf[h][0], k0);
-          a = __ffma2_rn(qf[h][1], k1, a);
-          a = __ffma2_rn(qf[h][2], k2, a);
-          a = __ffma2_rn(qf[h][3], k3, a);
-          s[t][h] = a.x + a.y;
+        for (int ks = 0; ks < 8; ++ks) {
+          const int chunk = ((ks & 3) << 1) + (mi >> 1);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kb + (ks >> 2) * kTileBytes + swz(t, chunk), a0, a1, a2, a3);
+          if (ks & 1)
+            mma_bf16(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+          else
+            mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
         }
       }
+      // scores: [0] (token gid, head 2qd) [1] (gid, 2qd+1) [2] (gid+8, 2qd) [3] (gid+8, 2qd+1)
+      const bool v0 = gid < valid, v1 = gid + 8 < valid;
+      const float s0 = v0 ? sa[0] + sb[0] : -INFINITY;
+      const float s1 = v0 ? sa[1] + sb[1] : -INFINITY;
+      const float s2 = v1 ? sa[2] + sb[2] : -INFINITY;
+      const float s3 = v1 ? sa[3] + sb[3] : -INFINITY;
+      float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
 #pragma unroll
-      for (int t = 0; t < HKV; ++t)
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int off = 8; off > 0; off >>= 1)
-            s[t][h] += __shfl_xor_sync(0xffffffffu, s[t][h], off);
-      // online softmax update (base 2; q was pre-scaled by scale*log2 e)
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int t = 0; t < HKV; ++t)
-          if (sub + t * SUBS < valid) mx = fmaxf(mx, s[t][h]);
-        const float m_new = fmaxf(st.m[h], mx);
-        // no key seen yet by this unit (all masked so far): state stays empty
-        const float alpha = m_new == -INFINITY ? 1.f : exp2f(st.m[h] - m_new);
-        st.m[h] = m_new;
-        float lsum = st.l[h] * alpha;
-#pragma unroll
-        for (int t = 0; t < HKV; ++t) {
-          const float pt = (sub + t * SUBS < valid) ? exp2f(s[t][h] - m_new) : 0.f;
-          s[t][h] = pt;
-          lsum += pt;
-        }
-        st.l[h] = lsum;
-        const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) st.o[h][i] = __fmul2_rn(st.o[h][i], a2);
+      for (int off = 4; off < 32; off <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
       }
-      // o += p v
+      // token 0 of every block is a key, so x0, x1 are finite
+      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+      const float al0 = exp2f((m0 - n0) * cl2), al1 = exp2f((m1 - n1) * cl2);
+      m0 = n0;
+      m1 = n1;
+      const float c0 = n0 * cl2, c1 = n1 * cl2;
+      const float p0 = exp2f(fmaf(s0, cl2, -c0)), p1 = exp2f(fmaf(s1, cl2, -c1));
+      const float p2 = exp2f(fmaf(s2, cl2, -c0)), p3 = exp2f(fmaf(s3, cl2, -c1));
+      l0 = fmaf(l0, al0, p0 + p2);
+      l1 = fmaf(l1, al1, p1 + p3);
 #pragma unroll
-      for (int t = 0; t < HKV; ++t) {
-        const int tok = sub + t * SUBS;
-        if (tok < valid) {
-          const uint4 w = lds128(sbase + S::KV_BYTES + tok * HKV * kHeadDim * 2 + row_off);
-          const float2 v0 = bf16x2_to_float2(w.x), v1 = bf16x2_to_float2(w.y);
-          const float2 v2 = bf16x2_to_float2(w.z), v3 = bf16x2_to_float2(w.w);
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+      // P^T fragments, hi + lo bf16 split
+      const uint32_t hA = float2_to_bf16x2(p0, p1), hB = float2_to_bf16x2(p2, p3);
+      const float2 fA = bf16x2_to_float2(hA), fB = bf16x2_to_float2(hB);
+      const uint32_t lA = float2_to_bf16x2(p0 - fA.x, p1 - fA.y);
+      const uint32_t lB = float2_to_bf16x2(p2 - fB.x, p3 - fB.y);
+      const uint32_t bh0 = movm_t(hA), bh1 = movm_t(hB);
+      const uint32_t bl0 = movm_t(lA), bl1 = movm_t(lB);
+      if (valid < kBlockSize) {
+        // rows past the last key may hold anything (NaN): zero them so that
+        // 0-weight rows contribute exactly 0 to the MMA
+        for (int i = lane; i < (kBlockSize - valid) * 16; i += 32) {
+          const int t = valid + (i >> 4), ch = i & 15;
+          const uint32_t a = vb + (ch >> 3) * kTileBytes + swz(t, ch & 7);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+        }
+        __syncwarp();
+      }
+      // O^T += V^T . P^T
+      {
+        const int mi = lane >> 3, r = lane & 7;
+        const int t = r + ((mi >> 1) << 3);
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const float2 pp = make_float2(s[t][h], s[t][h]);
-            st.o[h][0] = __ffma2_rn(pp, v0, st.o[h][0]);
-            st.o[h][1] = __ffma2_rn(pp, v1, st.o[h][1]);
-            st.o[h][2] = __ffma2_rn(pp, v2, st.o[h][2]);
-            st.o[h][3] = __ffma2_rn(pp, v3, st.o[h][3]);
-          }
+        for (int mt = 0; mt < 8; ++mt) {
+          const int chunk = 2 * mt + (mi & 1);  // 8-dim chunk 0..15
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vb + (chunk >> 3) * kTileBytes + swz(t, chunk & 7), a0, a1, a2, a3);
+          mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+          mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
         }
       }
+      // generic-proxy writes above must be ordered before the TMA that
+      // reuses this stage
+      if (valid < kBlockSize) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * sidx);
 
     if (!piece_last) continue;
-    // ---- end of a piece: merge units, write output row or partial ----------
+
+    // ---- end of a piece: merge the warps of each kv head, write rows -------
     const bool head_cut = piece_j0 > 0;
     const bool tail_cut = j < n - 1;
     const bool whole = !head_cut && !tail_cut;
-    // merge the two half-warps (same kv head, disjoint tokens)
+    float L0 = l0, L1 = l1;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float mo = __shfl_xor_sync(0xffffffffu, st.m[h], 16);
-      const float lo_ = __shfl_xor_sync(0xffffffffu, st.l[h], 16);
-      const float M = fmaxf(st.m[h], mo);
-      const float wa = st.m[h] == -INFINITY ? 0.f : exp2f(st.m[h] - M);
-      const float wb = mo == -INFINITY ? 0.f : exp2f(mo - M);
-      st.l[h] = st.l[h] * wa + lo_ * wb;
-      st.m[h] = M;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float2 x = st.o[h][i];
-        float2 y;
-        y.x = __shfl_xor_sync(0xffffffffu, x.x, 16);
-        y.y = __shfl_xor_sync(0xffffffffu, x.y, 16);
-        st.o[h][i] = make_float2(x.x * wa + y.x * wb, x.y * wa + y.y * wb);
-      }
+    for (int off = 4; off < 32; off <<= 1) {
+      L0 += __shfl_xor_sync(0xffffffffu, L0, off);
+      L1 += __shfl_xor_sync(0xffffffffu, L1, off);
     }
     const long long slot_row = (c * 2 + (head_cut ? 0 : 1)) * S::HQ;
-    if constexpr (S::WARPS_PER_HEAD == 1) {
-      if (hw == 0) {
+    const int ha = 2 * qd, hb = 2 * qd + 1;  // heads of this lane's fragment columns
+    if constexpr (S::NPH == 1) {
+      // one warp per kv head: write straight from the fragments
+      const float ia = L0 > 0.f ? 1.f / L0 : 0.f, ib = L1 > 0.f ? 1.f / L1 : 0.f;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const int qh = g * G + h;
-          const float L = st.l[h];
-          const float inv = L > 0.f ? 1.f / L : 0.f;
-          float r[8];
+      for (int mt = 0; mt < 8; ++mt) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            r[2 * i] = st.o[h][i].x * inv;
-            r[2 * i + 1] = st.o[h][i].y * inv;
+        for (int half = 0; half < 2; ++half) {
+          const int d = 16 * mt + gid + 8 * half;
+          if (ha < G) {
+            const long long row = whole ? (long long)b * S::HQ + g * G + ha : slot_row + g * G + ha;
+            const float v = o[mt][2 * half] * ia;
+            if (whole)
+              store_out1(p.out, p.out_f32, row * kHeadDim + d, v);
+            else
+              p.part_o[row * kHeadDim + d] = v;
           }
-          if (whole) {
-            const long long base = ((long long)b * S::HQ + qh) * kHeadDim + l * 8;
-            if (p.out_f32) {
-              float4 *o4 = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + base);
-              o4[0] = make_float4(r[0], r[1], r[2], r[3]);
-              o4[1] = make_float4(r[4], r[5], r[6], r[7]);
-            } else {
-              uint4 w;
-              w.x = float2_to_bf16x2(r[0], r[1]);
-              w.y = float2_to_bf16x2(r[2], r[3]);
-              w.z = float2_to_bf16x2(r[4], r[5]);
-              w.w = float2_to_bf16x2(r[6], r[7]);
-              *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + base) = w;
-            }
-          } else {
-            float4 *o4 = reinterpret_cast<float4 *>(p.part_o + (slot_row + qh) * kHeadDim + l * 8);
-            o4[0] = make_float4(r[0], r[1], r[2], r[3]);
-            o4[1] = make_float4(r[4], r[5], r[6], r[7]);
-            if (l == 0)
-              p.part_lse[slot_row + qh] =
-                  L > 0.f ? (st.m[h] + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+          if (hb < G) {
+            const long long row = whole ? (long long)b * S::HQ + g * G + hb : slot_row + g * G + hb;
+            const float v = o[mt][2 * half + 1] * ib;
+            if (whole)
+              store_out1(p.out, p.out_f32, row * kHeadDim + d, v);
+            else
+              p.part_o[row * kHeadDim + d] = v;
           }
         }
       }
+      if (!whole && gid == 0) {
+        if (ha < G)
+          p.part_lse[slot_row + g * G + ha] =
+              L0 > 0.f ? (m0 * cl2 + __log2f(L0)) * 0.69314718055994531f : -INFINITY;
+        if (hb < G)
+          p.part_lse[slot_row + g * G + hb] =
+              L1 > 0.f ? (m1 * cl2 + __log2f(L1)) * 0.69314718055994531f : -INFINITY;
+      }
     } else {
-      // several warps hold the same kv head: combine through shared memory
-      if (hw == 0) {
+      // several warps share a kv head: combine through shared memory
+      if (ha < G) {
+        float *ra = red + (cw * G + ha) * S::RED_FLOATS_PER_HEAD;
+        if (gid == 0) {
+          ra[0] = m0 == -INFINITY ? -INFINITY : m0 * cl2;
+          ra[1] = L0;
+        }
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float *r = red + (cw * G + h) * S::RED_FLOATS_PER_HEAD;
-          if (l == 0) {
-            r[0] = st.m[h];
-            r[1] = st.l[h];
-          }
-          // r + 2 is 8-byte aligned (130 floats per head record): float2 stores
-          float2 *o2 = reinterpret_cast<float2 *>(r + 2 + l * 8);
+        for (int mt = 0; mt < 8; ++mt) {
+          ra[2 + 16 * mt + gid] = o[mt][0];
+          ra[2 + 16 * mt + gid + 8] = o[mt][2];
+        }
+      }
+      if (hb < G) {
+        float *rb = red + (cw * G + hb) * S::RED_FLOATS_PER_HEAD;
+        if (gid == 0) {
+          rb[0] = m1 == -INFINITY ? -INFINITY : m1 * cl2;
+          rb[1] = L1;
+        }
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o2[i] = st.o[h][i];
+        for (int mt = 0; mt < 8; ++mt) {
+          rb[2 + 16 * mt + gid] = o[mt][1];
+          rb[2 + 16 * mt + gid + 8] = o[mt][3];
         }
       }
       named_barrier(1, kDecodeConsumerWarps * 32);
-      const int ct = tid - 32;
       for (int e = ct * 2; e < S::HQ * kHeadDim; e += kDecodeConsumerWarps * 32 * 2) {
         const int qh = e / kHeadDim;
         const int d = e % kHeadDim;
@@ -466,34 +615,51 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
         const int h = qh % G;
         float M = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < S::WARPS_PER_HEAD; ++k)
+        for (int k = 0; k < S::NPH; ++k)
           M = fmaxf(M, red[((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD]);
-        float L = 0.f, o0 = 0.f, o1 = 0.f;
+        float L = 0.f, oa = 0.f, ob = 0.f;
 #pragma unroll
-        for (int k = 0; k < S::WARPS_PER_HEAD; ++k) {
+        for (int k = 0; k < S::NPH; ++k) {
           const float *r = red + ((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD;
           const float w = r[0] == -INFINITY ? 0.f : exp2f(r[0] - M);
           L += r[1] * w;
-          o0 += r[2 + d] * w;
-          o1 += r[3 + d] * w;
+          oa += r[2 + d] * w;
+          ob += r[3 + d] * w;
         }
         const float inv = L > 0.f ? 1.f / L : 0.f;
-        o0 *= inv;
-        o1 *= inv;
         if (whole) {
-          const long long base = ((long long)b * S::HQ + qh) * kHeadDim + d;
-          if (p.out_f32)
-            *reinterpret_cast<float2 *>(static_cast<float *>(p.out) + base) = make_float2(o0, o1);
-          else
-            *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(p.out) + base) =
-                float2_to_bf16x2(o0, o1);
+          store_out2(p.out, p.out_f32, ((long long)b * S::HQ + qh) * kHeadDim + d, oa * inv,
+                     ob * inv);
         } else {
           *reinterpret_cast<float2 *>(p.part_o + (slot_row + qh) * kHeadDim + d) =
-              make_float2(o0, o1);
+              make_float2(oa * inv, ob * inv);
           if (d == 0)
             p.part_lse[slot_row + qh] =
                 L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
         }
+      }
+      named_barrier(1, kDecodeConsumerWarps * 32);
+    }
+
+    if (!whole) {
+      // publish this partial; the CTA completing the sequence's set merges it
+      __threadfence();
+      named_barrier(1, kDecodeConsumerWarps * 32);
+      const long long P = gb - j;  // global index of block 0 of b
+      const long long cs0 = split_of_block(P, nsplit, N);
+      const long long cs1 = split_of_block(P + n - 1, nsplit, N);
+      if (ct == 0) {
+        int pieces = 1;
+        for (long long cc = cs0 + 1; cc <= cs1; ++cc)
+          pieces += split_begin(cc, nsplit, N) < split_begin(cc + 1, nsplit, N) ? 1 : 0;
+        const int prev = atomicAdd(p.counters + cs1, 1);
+        ctl->last = prev == pieces - 1;
+      }
+      named_barrier(1, kDecodeConsumerWarps * 32);
+      if (ctl->last) {
+        __threadfence();
+        merge_sequence<S::HQ>(p, b, cs0, cs1, nsplit, N, ct, kDecodeConsumerWarps * 32);
+        if (ct == 0) p.counters[cs1] = 0;
       }
       named_barrier(1, kDecodeConsumerWarps * 32);
     }
@@ -502,8 +668,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_kernel(const DecodeP
 
 // Launches decode_kernel<G, HKV> for one G (defined per HKV in pa_decode_h*.cu).
 template <int HKV>
-cudaError_t launch_decode(int G, const DecodeParams &p, cudaStream_t s, int device);
-template <int HKV>
-int decode_smem_bytes(int G);
+cudaError_t launch_decode(int G, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const DecodeParams &p, cudaStream_t s, int device);
 
 }  // namespace pa

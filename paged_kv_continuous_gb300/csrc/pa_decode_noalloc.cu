@@ -15,19 +15,21 @@
 // calls cudaMalloc, cudaFree or any allocating routine.
 //
 // Sharing: every call on a device uses the same array and leaves its
-// partials there.  Nothing in it has to start at zero -- each partial the
-// merge reads is written earlier in the same call -- but calls that overlap
-// on the GPU (two streams, or two threads) race on it and give wrong rows.
+// partials there.  The split-K arrival counters in it must start at zero:
+// each call clears them on its stream (a memset, not an allocation) before
+// the kernel; the partials need no clearing (each one the merge reads is
+// written earlier in the same call).  Calls that overlap on the GPU (two
+// streams, or two threads) race on the array and give wrong rows.
 #include <cmath>
 #include <mutex>
 
+#include "pa_decode_internal.h"
 #include "pa_decode_kernel.cuh"
 
 namespace pa {
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB per device
-constexpr size_t kWsHeader = 256;                          // same layout as pa_decode's
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
@@ -60,63 +62,17 @@ extern "C" pa_status pa_decode_noalloc(void *out, int32_t out_dtype, const void 
                                        int32_t head_dim, int32_t block_size, float scale,
                                        int32_t num_splits, int32_t *error_flags, void *stream) {
   using namespace pa;
-  if (batch < 0 || num_blocks < 0 || num_splits < 0) return PA_ERR_INVALID_ARG;
-  if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
-  if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
-  if (!(num_kv_heads == 1 || num_kv_heads == 2 || num_kv_heads == 4 || num_kv_heads == 8))
-    return PA_ERR_UNSUPPORTED;
-  if (num_q_heads < num_kv_heads || num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > 8)
-    return PA_ERR_UNSUPPORTED;
-  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
-  if (batch == 0) return PA_OK;
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
-    return PA_ERR_INVALID_ARG;
-  if (block_table_stride < 1) return PA_ERR_INVALID_ARG;
-  auto misaligned = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
-  if (misaligned(out) || misaligned(q) || misaligned(k_cache) || misaligned(v_cache))
-    return PA_ERR_INVALID_ARG;
+  DecodeRequest r{out, out_dtype, q, k_cache, v_cache, num_blocks, block_tables,
+                  block_table_stride, context_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                  block_size, scale, num_splits, 0, stream};
   int device = -1;
-  if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_DEVICE;
-  const int32_t splits = num_splits > 0 ? num_splits : pa_decode_default_splits(device);
-  if (splits < 1) return PA_ERR_DEVICE;
-  // the partials of `splits` splits must fit in the fixed array
-  const size_t need = pa_decode_workspace_size(splits, num_q_heads, head_dim);
+  const pa_status st = check_decode_request(r, &device);
+  if (st != PA_OK || batch == 0) return st;
+  // the partials and counters of `splits` splits must fit in the fixed array
+  const size_t need = pa_decode_workspace_size(r.splits, num_q_heads, head_dim);
   if (need == 0 || need > kStaticScratchBytes) return PA_ERR_WORKSPACE;
   void *scratch = nullptr;
   if (scratch_address(device, &scratch) != cudaSuccess) return PA_ERR_DEVICE;
-
-  char *ws = static_cast<char *>(scratch);
-  const size_t part_o_bytes =
-      ((size_t)splits * 2 * num_q_heads * kHeadDim * sizeof(float) + 255) / 256 * 256;
-  DecodeParams p;
-  p.out = out;
-  p.out_f32 = out_dtype == PA_DTYPE_F32;
-  p.q = static_cast<const uint16_t *>(q);
-  p.k_cache = static_cast<const uint16_t *>(k_cache);
-  p.v_cache = static_cast<const uint16_t *>(v_cache);
-  p.num_blocks = num_blocks;
-  p.block_tables = block_tables;
-  p.bt_stride = block_table_stride;
-  p.context_lens = context_lens;
-  p.batch = batch;
-  p.qk_scale_log2 = scale * 1.4426950408889634f;
-  p.num_splits = splits;
-  p.part_o = reinterpret_cast<float *>(ws + kWsHeader);
-  p.part_lse = reinterpret_cast<float *>(ws + kWsHeader + part_o_bytes);
-  p.err = error_flags;
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int G = num_q_heads / num_kv_heads;
-  cudaError_t e;
-  switch (num_kv_heads) {
-    case 1: e = launch_decode<1>(G, p, s, device); break;
-    case 2: e = launch_decode<2>(G, p, s, device); break;
-    case 4: e = launch_decode<4>(G, p, s, device); break;
-    default: e = launch_decode<8>(G, p, s, device); break;
-  }
-  if (e != cudaSuccess) return PA_ERR_LAUNCH;
-  if (splits > 1)
-    return pa_decode_merge(out, out_dtype, scratch, kStaticScratchBytes, context_lens, batch,
-                           num_q_heads, head_dim, block_size, splits, stream);
-  return PA_OK;
+  // the arrival counters must start at zero: clear them on the stream first
+  return run_decode(r, scratch, error_flags, device, /*clear_counters=*/true);
 }

@@ -252,3 +252,26 @@ def test_merge_entry_point_against_oracle_partials(ops):
     assert cut.sum() >= 4
     assert_attention_close(got[cut], ref[cut], "merge", strict=True)
     assert np.all(np.isnan(got[~cut]))          # rows of uncut sequences untouched
+
+
+def test_decode_reuses_one_workspace_across_calls(ops):
+    """The in-kernel merge leaves its arrival counters at zero: one workspace
+    serves many consecutive calls (different split counts, different
+    batches) and every call matches the oracle."""
+    ws = ops.decode_workspace(12, 500)
+    torch.cuda.synchronize()
+    for name, splits in [("cb_decode_b64", 500), ("qwen_decode_b8", 97), ("cb_decode_b64", 31),
+                         ("tiny_decode", 3), ("cb_decode_b64", 500)]:
+        w = synth.CONFIGS[name]()
+        d = Dev(ops, w, store_on_gpu=False)
+        out = ops.decode(d.q, d.kc, d.vc, d.tables, d.ctx, w.scale, out_dtype=torch.float32,
+                         num_splits=splits, workspace=ws)
+        torch.cuda.synchronize()
+        assert ops.read_error_word(ws) == 0
+        assert_attention_close(dev_to_f64(out), oracle_decode(w), f"{name} S={splits}",
+                               strict=True)
+    wsl = ws.view(torch.int32)
+    S, H = 500, 12
+    up = lambda x: (x + 255) // 256 * 256
+    off = (256 + up(S * 2 * H * 128 * 4) + up(S * 2 * H * 4)) // 4
+    assert int(wsl[off:off + S].abs().sum().item()) == 0
