@@ -81,6 +81,9 @@ typedef int32_t pa_status;
 #define PA_ERR_LAUNCH 4        /* the CUDA runtime rejected the launch */
 #define PA_ERR_DEVICE 5        /* a device query or copy failed */
 
+/* Largest split count pa_decode accepts. */
+#define PA_DECODE_MAX_SPLITS 4096
+
 #define PA_DTYPE_BF16 0
 #define PA_DTYPE_F32 1
 
@@ -146,16 +149,18 @@ PA_API pa_status pa_store_kv(const void *k, const void *v, int64_t num_tokens,
  * to zero, all inside the decode kernel.
  *
  * Workspace layout (bytes from the workspace pointer; R(x) rounds x up to
- * a multiple of 256; H = num_q_heads, D = head_dim):
+ * a multiple of 256; H = num_q_heads, D = head_dim, C = 256 + 4 *
+ * PA_DECODE_MAX_SPLITS):
  *   [0, 4)              int32 error word (PA_DEVERR_* bits; the library
  *                       only ORs bits in);
- *   [256, ...)          float partial_o[S][2][H][D];
- *   256 + R(8SHD)       float partial_lse[S][2][H];
- *   then + R(8SH)       int32 counters[S] (zero between calls).
+ *   [256, C)            int32 counters[PA_DECODE_MAX_SPLITS], zero between
+ *                       calls, at the same place for every S;
+ *   [C, ...)            float partial_o[S][2][H][D];
+ *   C + R(8SHD)         float partial_lse[S][2][H].
  * Zero the whole workspace once when allocating it; every completed call
- * leaves the counters at zero again.  After a call that reported
- * PA_DEVERR_WAIT_TIMEOUT, zero it again.  One workspace serves one call in
- * flight at a time.
+ * leaves the counters at zero again, so the workspace can be reused with
+ * any split count.  After a call that reported PA_DEVERR_WAIT_TIMEOUT,
+ * zero it again.  One workspace serves one call in flight at a time.
  */
 PA_API size_t pa_decode_workspace_size(int32_t num_splits, int32_t num_q_heads, int32_t head_dim);
 
@@ -185,7 +190,8 @@ PA_API int32_t pa_decode_default_splits(int32_t device);
  *   block_tables   int32 [batch][block_table_stride].
  *   context_lens   int32 [batch]; negative values are treated as 0.
  *   scale          softmax scale applied to q . k (e.g. 1/sqrt(head_dim)).
- *   num_splits     S of the partition; 0 = pa_decode_default_splits.
+ *   num_splits     S of the partition, at most PA_DECODE_MAX_SPLITS;
+ *                  0 = pa_decode_default_splits.
  *   workspace      device buffer of workspace_bytes >=
  *                  pa_decode_workspace_size(S, num_q_heads, head_dim).
  * Results do not depend on how sequences are laid out in the pool; with a
@@ -231,7 +237,7 @@ PA_API pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *works
  * device-side error bits go to `error_flags` (optional int32 word, may be
  * NULL).  Returns PA_ERR_WORKSPACE, launching nothing, when
  * pa_decode_workspace_size(S, num_q_heads, head_dim) exceeds 8 MiB for the
- * split count S in use (S <= 677 at 12 query heads, S <= 253 at 32).  The
+ * split count S in use (S <= 676 at 12 query heads, S <= 253 at 32).  The
  * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  * routine.  The first call on a device, with that device current, looks up
  * the array's device address and caches it; make that first call before

@@ -12,18 +12,13 @@ namespace pa {
 
 constexpr int kHeadDim = 128;
 constexpr int kBlockSize = 16;
-// A pipeline wait gives up after this long, ORs PA_DEVERR_WAIT_TIMEOUT into
-// the error word and lets the kernel run out without touching memory again.
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+// A pipeline wait gives up after this many SM clock cycles (about 2 s at
+// 2 GHz, longer at lower clocks), ORs PA_DEVERR_WAIT_TIMEOUT into the error
+// word and lets the kernel run out without touching memory again.
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_timer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
 }
 
 __device__ __forceinline__ void report(int32_t *err, int bits) {
@@ -64,17 +59,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of the barrier.  Gives up when *abort is set (by
-// another warp that already gave up) or after kWaitTimeoutNs; in the latter
-// case it sets *abort and reports PA_DEVERR_WAIT_TIMEOUT.  Returns true when
-// the phase completed.
+// another warp that already gave up) or after kWaitTimeoutCycles SM cycles;
+// in the latter case it sets *abort and reports PA_DEVERR_WAIT_TIMEOUT.
+// Returns true when the phase completed.  The time limit uses the SM cycle
+// counter (a register read); a few waits are tried before it is read at all.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           int32_t *err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  while (true) {
-    if (*abort) return false;
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i)
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitTimeoutCycles) {
       *abort = 1;
       report(err, PA_DEVERR_WAIT_TIMEOUT);
       return false;

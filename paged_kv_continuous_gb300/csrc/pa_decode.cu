@@ -64,41 +64,8 @@ __global__ void __launch_bounds__(32 * kMergeSeqPerCta) merge_kernel(const Merge
   const long long c0 = split_of_block(P, S, N);
   const long long c1 = split_of_block(P + n - 1, S, N);
   if (c0 == c1) return;
-  const int HQ = p.num_q_heads;
-  auto piece_row = [&](long long cc) -> long long {
-    return (cc * 2 + (cc == c0 ? 1 : 0)) * HQ + h;
-  };
-  auto nonempty = [&](long long cc) -> bool {
-    return split_begin(cc, S, N) < split_begin(cc + 1, S, N);
-  };
-  float M = -INFINITY;
-  for (long long cc = c0; cc <= c1; ++cc)
-    if (cc == c0 || nonempty(cc)) M = fmaxf(M, __ldg(p.part_lse + piece_row(cc)));
-  float W = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (long long cc = c0; cc <= c1; ++cc) {
-    if (cc != c0 && !nonempty(cc)) continue;
-    const long long r = piece_row(cc);
-    const float lse = __ldg(p.part_lse + r);
-    const float w = lse == -INFINITY ? 0.f : __expf(lse - M);
-    const float4 o = __ldg(reinterpret_cast<const float4 *>(p.part_o + r * kHeadDim) + lane);
-    W += w;
-    acc.x += w * o.x;
-    acc.y += w * o.y;
-    acc.z += w * o.z;
-    acc.w += w * o.w;
-  }
-  const float inv = W > 0.f ? 1.f / W : 0.f;
-  const long long base = ((long long)b * HQ + h) * kHeadDim + lane * 4;
-  if (p.out_f32) {
-    *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + base) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  } else {
-    uint2 w2;
-    w2.x = float2_to_bf16x2(acc.x * inv, acc.y * inv);
-    w2.y = float2_to_bf16x2(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.out) + base) = w2;
-  }
+  merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * p.num_q_heads + h,
+            p.num_q_heads, h, c0, c1, S, N, lane);
 }
 
 
@@ -122,17 +89,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D view of a pool: rows = token slots (num_blocks * 16), columns = the
-// Hkv * 128 elements of a slot; one TMA tile = 16 slots x 64 columns with
-// the 128-byte swizzle.
+// 3-D view of a pool: (dim 128, kv head Hkv, token slot num_blocks * 16).
+// One TMA box = 64 dims x min(Hkv, 2) heads x 16 slots (one page), with the
+// 128-byte swizzle.
 bool encode_pool_map(CUtensorMap *map, const void *pool, long long num_blocks, int hkv) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)hkv * kHeadDim, (cuuint64_t)num_blocks * kBlockSize};
-  cuuint64_t strides[1] = {(cuuint64_t)hkv * kHeadDim * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides,
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv,
+                        (cuuint64_t)num_blocks * kBlockSize};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hkv * kHeadDim * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)(hkv >= 2 ? 2 : 1), (cuuint32_t)kBlockSize};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -148,10 +116,10 @@ cudaError_t launch_merge(const MergeParams &m, cudaStream_t s) {
 
 WorkspaceLayout workspace_layout(long long splits, int hq) {
   WorkspaceLayout w;
-  w.part_o = kWorkspaceHeader;
+  w.counters = kCounterOffset;
+  w.part_o = kCounterOffset + kCounterBytes;
   w.part_lse = w.part_o + align256((size_t)splits * 2 * hq * kHeadDim * sizeof(float));
-  w.counters = w.part_lse + align256((size_t)splits * 2 * hq * sizeof(float));
-  w.total = w.counters + align256((size_t)splits * sizeof(int32_t));
+  w.total = w.part_lse + align256((size_t)splits * 2 * hq * sizeof(float));
   return w;
 }
 
@@ -199,6 +167,7 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
 
 pa_status check_decode_request(DecodeRequest &r, int *device_out) {
   if (r.batch < 0 || r.num_blocks < 0 || r.num_splits < 0) return PA_ERR_INVALID_ARG;
+  if (r.num_splits > PA_DECODE_MAX_SPLITS) return PA_ERR_UNSUPPORTED;
   if (r.out_dtype != PA_DTYPE_BF16 && r.out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
   if (r.head_dim != kHeadDim || r.block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
   const int hkv = r.num_kv_heads, hq = r.num_q_heads;
@@ -216,6 +185,7 @@ pa_status check_decode_request(DecodeRequest &r, int *device_out) {
   if (cudaGetDevice(&device) != cudaSuccess || device < 0) return PA_ERR_DEVICE;
   r.splits = r.num_splits > 0 ? r.num_splits : pa_decode_default_splits(device);
   if (r.splits < 1) return PA_ERR_DEVICE;
+  if (r.splits > PA_DECODE_MAX_SPLITS) r.splits = PA_DECODE_MAX_SPLITS;
   *device_out = device;
   return PA_OK;
 }
@@ -225,7 +195,9 @@ pa_status check_decode_request(DecodeRequest &r, int *device_out) {
 extern "C" size_t pa_decode_workspace_size(int32_t num_splits, int32_t num_q_heads,
                                            int32_t head_dim) {
   using namespace pa;
-  if (num_splits < 1 || num_q_heads < 1 || head_dim != kHeadDim) return 0;
+  if (num_splits < 1 || num_splits > PA_DECODE_MAX_SPLITS || num_q_heads < 1 ||
+      head_dim != kHeadDim)
+    return 0;
   return workspace_layout(num_splits, num_q_heads).total;
 }
 
@@ -264,7 +236,7 @@ extern "C" pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *w
   if (batch < 0 || num_splits < 1 || num_q_heads < 1) return PA_ERR_INVALID_ARG;
   if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
   if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
-  if (num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
+  if (num_q_heads > 65535 || num_splits > PA_DECODE_MAX_SPLITS) return PA_ERR_UNSUPPORTED;
   if (batch == 0) return PA_OK;
   if (!out || !context_lens || !aligned16(out)) return PA_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace) ||

@@ -10,12 +10,16 @@
 namespace pa {
 
 constexpr size_t kWorkspaceHeader = 256;  // int32 error word + reserved
+// The arrival counters sit at a fixed place for every split count, so a
+// workspace reused with another split count still finds them at zero.
+constexpr size_t kCounterOffset = kWorkspaceHeader;
+constexpr size_t kCounterBytes = size_t(PA_DECODE_MAX_SPLITS) * 4;
 
 // Byte offsets inside a decode workspace for `splits` splits.
 struct WorkspaceLayout {
+  size_t counters;  // int32 [PA_DECODE_MAX_SPLITS], zero between calls
   size_t part_o;    // float [splits][2][hq][128]
   size_t part_lse;  // float [splits][2][hq]
-  size_t counters;  // int32 [splits], zero between calls
   size_t total;
 };
 WorkspaceLayout workspace_layout(long long splits, int hq);

@@ -15,12 +15,13 @@
 // the counter to the piece count merges all partials of that sequence
 // (log-sum-exp) and writes its rows, then resets the counter to zero.
 //
-// CTA layout (288 threads).  Warp 0, lane 0 is the producer: it walks the
-// CTA's block list and issues, per physical block and kv head, two TMA tile
-// loads of K and two of V (16 tokens x 64 dims each, 128-byte swizzle), plus
-// a bulk copy of the sequence's q row at the start of a piece, into a ring
-// of NST stages guarded by full/empty mbarriers.  Warps 1..8 consume: warp
-// (g, ph) handles kv head g of every stage whose index is ph modulo
+// CTA layout (320 threads).  Warps 0 and 1 are producers, filling alternate
+// stages of a ring of NST stages guarded by full/empty mbarriers: per
+// physical block they issue TMA box loads of K and V (16 tokens x 2 kv heads
+// x 64 dims each, 128-byte swizzle; 4 boxes per block at Hkv <= 2) plus a
+// bulk copy of the sequence's q row at the start of a piece.  Two producers
+// overlap the per-stage issue latency of one thread.  Warps 2..9 consume:
+// warp (g, ph) handles kv head g of every stage whose index is ph modulo
 // 8 / Hkv.
 //
 // Arithmetic per (block, kv head) on the tensor cores (mma.sync m16n8k16,
@@ -59,10 +60,11 @@ struct DecodeParams {
   int32_t *err;
 };
 
+constexpr int kDecodeProducerWarps = 2;
 constexpr int kDecodeConsumerWarps = 8;
-constexpr int kDecodeThreads = 32 * (1 + kDecodeConsumerWarps);
+constexpr int kDecodeThreads = 32 * (kDecodeProducerWarps + kDecodeConsumerWarps);
 constexpr int kDecodeSmemBudget = 227 * 1024;
-constexpr int kTileBytes = kBlockSize * 64 * 2;  // 16 tokens x 64 dims bf16 = 2 KB
+constexpr int kTileBytes = kBlockSize * 64 * 2;  // 16 tokens x 64 dims bf16 = 2 KB per head
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -70,6 +72,11 @@ template <int G, int HKV>
 struct DecodeShape {
   static constexpr int HQ = G * HKV;
   static constexpr int NPH = kDecodeConsumerWarps / HKV;  // stage phases = warps per kv head
+  // one TMA box = 16 tokens x HB heads x 64 dims; a page of K (or V) takes
+  // NPAIR * 2 boxes (head groups x dim halves)
+  static constexpr int HB = HKV >= 2 ? 2 : 1;
+  static constexpr int NPAIR = HKV / HB;
+  static constexpr int BOX_BYTES = HB * kTileBytes;
   static constexpr int KV_BYTES = HKV * 2 * kTileBytes;     // one block of K (or V), all heads
   static constexpr int Q_BYTES = HQ * kHeadDim * 2;
   static constexpr int STAGE_BYTES = align_up(2 * KV_BYTES + Q_BYTES, 1024);
@@ -80,7 +87,9 @@ struct DecodeShape {
   static constexpr int CTL_BYTES = 256;
   static constexpr int NST_FIT =
       (kDecodeSmemBudget - 1024 - RED_BYTES - CTL_BYTES) / (STAGE_BYTES + 16);
-  static constexpr int NST = NST_FIT > 12 ? 12 : NST_FIT;
+  static constexpr int NST_CAP = NST_FIT > 12 ? 12 : NST_FIT;
+  // an even ring: each slot is always filled by the same producer warp
+  static constexpr int NST = NST_CAP >= 4 ? (NST_CAP & ~1) : NST_CAP;
   // +1024: the dynamic smem base is realigned to 1024 bytes for the swizzle
   static constexpr int SMEM = 1024 + NST * STAGE_BYTES + RED_BYTES + NST * 16 + CTL_BYTES;
   static_assert(NST >= 2, "stage does not fit twice in shared memory");
@@ -101,14 +110,73 @@ __device__ __forceinline__ int seq_blocks(const int32_t *ctx, int b) {
   return n > 0 ? ceil_div_blocks(n) : 0;
 }
 
+// Warp-cooperative walk over the CTA's block list.  The walk position is
+// (b, ctx, j): block j of sequence b, whose context length is ctx.  One call
+// describes the next `count` <= 32 blocks (count <= remaining): lane L gets
+// the sequence, block index and context length of block L of the chunk.
+// Context lengths of up to 32 following sequences are loaded in parallel
+// and placed with a warp scan, so a chunk costs one round of loads however
+// many sequences it crosses.  The position then moves past the chunk.  All
+// 32 lanes must call it with the same position (the result is uniform).
+__device__ __forceinline__ int walk_chunk(const int32_t *ctx_arr, int batch, int &b, int &ctx,
+                                          int &j, long long remaining, int lane, int &lb,
+                                          int &lj, int &lctx) {
+  while (j >= (ctx > 0 ? ceil_div_blocks(ctx) : 0)) {  // leave finished / empty sequences
+    if (b + 1 >= batch) return 0;  // inconsistent with the block count: stop the walk
+    ++b;
+    ctx = __ldg(ctx_arr + b);
+    j = 0;
+  }
+  const int rem = ceil_div_blocks(ctx) - j;  // blocks left in b (>= 1)
+  int count = remaining < 32 ? (int)remaining : 32;
+  int nctx = 0, nn = 0;
+  if (rem < count) {
+    const int bb = b + 1 + lane;
+    nctx = bb < batch ? __ldg(ctx_arr + bb) : 0;
+    nn = nctx > 0 ? ceil_div_blocks(nctx) : 0;
+  }
+  int incl = nn;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  // k = number of following sequences that end at or before this lane's block
+  int k = 0;
+#pragma unroll 4
+  for (int kk = 0; kk < 32; ++kk) k += (rem + __shfl_sync(0xffffffffu, incl, kk) <= lane) ? 1 : 0;
+  const int ks = k < 32 ? k : 31;
+  const int excl_k = __shfl_sync(0xffffffffu, incl - nn, ks);
+  const int ctx_k = __shfl_sync(0xffffffffu, nctx, ks);
+  bool resolved = true;
+  if (lane < rem) {
+    lb = b;
+    lj = j + lane;
+    lctx = ctx;
+  } else {
+    lb = b + 1 + k;
+    lj = lane - rem - excl_k;
+    lctx = ctx_k;
+    resolved = k < 32;  // beyond 32 following sequences: left for the next chunk
+  }
+  const unsigned unres = __ballot_sync(0xffffffffu, !resolved);
+  if (unres) count = min(count, __ffs(unres) - 1);
+  const int last = count - 1;
+  b = __shfl_sync(0xffffffffu, lb, last);
+  j = __shfl_sync(0xffffffffu, lj, last) + 1;
+  ctx = __shfl_sync(0xffffffffu, lctx, last);
+  return count;
+}
+
 // ---- tensor-core and TMA helpers -------------------------------------------
 
-__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                              uint32_t bar, uint64_t policy) {
+// 3-D tile load (dims: dim, kv head, token slot) completing on an mbarrier.
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                             int z, uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -177,38 +245,78 @@ __device__ __forceinline__ void store_out4(void *out, int out_f32, long long idx
   }
 }
 
-// Log-sum-exp merge of all partials of sequence b (split-K pieces c0..c1),
-// done by the consumer threads of the CTA that completed the set.
-template <int HQ>
-__device__ void merge_sequence(const DecodeParams &p, int b, long long c0, long long c1,
-                               long long S, long long N, int ct, int nthreads) {
-  for (int item = ct; item < HQ * (kHeadDim / 4); item += nthreads) {
-    const int h = item / (kHeadDim / 4);
-    const int d = (item % (kHeadDim / 4)) * 4;
-    float M = -INFINITY;
-    for (long long cc = c0; cc <= c1; ++cc) {
-      if (cc != c0 && split_begin(cc, S, N) == split_begin(cc + 1, S, N)) continue;
-      const long long row = (cc * 2 + (cc == c0 ? 1 : 0)) * HQ + h;
-      M = fmaxf(M, __ldcg(p.part_lse + row));
-    }
-    float W = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (long long cc = c0; cc <= c1; ++cc) {
-      if (cc != c0 && split_begin(cc, S, N) == split_begin(cc + 1, S, N)) continue;
-      const long long row = (cc * 2 + (cc == c0 ? 1 : 0)) * HQ + h;
-      const float lse = __ldcg(p.part_lse + row);
-      const float w = lse == -INFINITY ? 0.f : __expf(lse - M);
-      const float4 o = __ldcg(reinterpret_cast<const float4 *>(p.part_o + row * kHeadDim + d));
-      W += w;
-      acc.x += w * o.x;
-      acc.y += w * o.y;
-      acc.z += w * o.z;
-      acc.w += w * o.w;
-    }
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-    store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d,
-               make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+// Log-sum-exp merge of one output row (sequence b, query head h) from the
+// split-K partials of splits c0..c1 (slot 1 of c0, slot 0 of the others),
+// by one warp; lane l owns dims 4l..4l+3.  Partials are read through L2
+// (written by other CTAs).  When N >= S every split holds at least one
+// block, so no split can be empty and no division is needed.
+__device__ __forceinline__ void merge_row(const float *part_o, const float *part_lse, void *out,
+                                          int out_f32, long long out_row, int HQ, int h,
+                                          long long c0, long long c1, long long S, long long N,
+                                          int lane) {
+  const bool dense = N >= S;
+  auto piece = [&](long long cc) -> bool {
+    return cc <= c1 &&
+           (dense || cc == c0 || split_begin(cc, S, N) < split_begin(cc + 1, S, N));
+  };
+  auto row_of = [&](long long cc) -> long long { return (cc * 2 + (cc == c0 ? 1 : 0)) * HQ + h; };
+  float M = -INFINITY;
+  for (long long base = c0; base <= c1; base += 32) {
+    const long long cc = base + lane;
+    if (piece(cc)) M = fmaxf(M, __ldcg(part_lse + row_of(cc)));
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float W = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long base = c0; base <= c1; base += 32) {
+    const long long cc = base + lane;
+    float w = 0.f;
+    if (piece(cc)) {
+      const float lse = __ldcg(part_lse + row_of(cc));
+      w = lse == -INFINITY ? 0.f : __expf(lse - M);
+    }
+    W += w;
+    unsigned mask = __ballot_sync(0xffffffffu, w > 0.f);
+    while (mask) {
+      // up to four rows in flight per round
+      int idx[4];
+      int cnt = 0;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        idx[u] = mask ? __ffs(mask) - 1 : -1;
+        if (mask) {
+          mask &= mask - 1;
+          ++cnt;
+        }
+      }
+      float4 v[4];
+      float wv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int src = idx[u] < 0 ? 0 : idx[u];
+        wv[u] = __shfl_sync(0xffffffffu, w, src);
+        const long long ccu = base + src;
+        v[u] = u < cnt ? __ldcg(reinterpret_cast<const float4 *>(part_o + row_of(ccu) * kHeadDim) +
+                                lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (u < cnt) {
+          acc.x += wv[u] * v[u].x;
+          acc.y += wv[u] * v[u].y;
+          acc.z += wv[u] * v[u].z;
+          acc.w += wv[u] * v[u].w;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  store_out4(out, out_f32, out_row * kHeadDim + lane * 4,
+             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
 }
 
 template <int G, int HKV>
@@ -312,78 +420,99 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int first_b = ctl->first_b;
   const long long first_prefix = ctl->first_prefix;
 
-  if (warp == 0) {
-    // ---- 4. producer ---------------------------------------------------------
-    if (lane != 0) return;
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
-                 : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v))
-                 : "memory");
+  if (warp < kDecodeProducerWarps) {
+    // ---- 4. producer warps: block descriptors 32 at a time; warp pw issues
+    //         the stages with index = pw (mod 2), lane 0 of it issuing ----
+    const int pw = warp;
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
+                   : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v))
+                   : "memory");
+    }
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
     int b = first_b;
-    int n = seq_blocks(p.context_lens, b);
+    int ctx = __ldg(p.context_lens + b);
     int j = (int)(lo - first_prefix);
-    long long issued = 0;
-    for (long long gb = lo; gb < hi; ++gb, ++issued, ++j) {
-      if (j == n) {
-        do {
-          ++b;
-          n = seq_blocks(p.context_lens, b);
-        } while (n == 0);
-        j = 0;
+    long long gb = lo, issued = 0;
+    bool stop = false;
+    while (gb < hi && !stop) {
+      int lb, lj, lctx;
+      const int count = walk_chunk(p.context_lens, p.batch, b, ctx, j, hi - gb, lane, lb, lj, lctx);
+      if (count == 0) {
+        if (lane == 0) report(p.err, PA_DEVERR_SHAPE);
+        break;
       }
-      const int st = (int)(issued % S::NST);
-      const int round = (int)(issued / S::NST);
-      if (round > 0 && !mbar_wait(empty0 + 8 * st, (round - 1) & 1, abort_flag, p.err)) break;
-      const bool piece_first = (gb == lo) || (j == 0);
-      // a row holds bt_stride entries: a context longer than the row is a
-      // caller error, reported and not read
-      const bool in_row = j < p.bt_stride;
-      const long long phys =
-          in_row ? __ldg(p.block_tables + (long long)b * p.bt_stride + j) : -1;
-      const bool ok = phys >= 0 && phys < p.num_blocks;
-      const uint32_t bytes = (ok ? 2u * S::KV_BYTES : 0u) + (piece_first ? S::Q_BYTES : 0u);
-      const uint32_t dst = stage0 + st * S::STAGE_BYTES;
-      const uint32_t bar = full0 + 8 * st;
-      mbar_arrive_expect_tx(bar, bytes);
-      if (ok) {
-        const int y = (int)(phys * kBlockSize);
-#pragma unroll
-        for (int g = 0; g < HKV; ++g) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tma_load_tile(dst + (g * 2 + h) * kTileBytes, &tmap_k, g * kHeadDim + h * 64, y, bar,
-                          pol_kv);
-            tma_load_tile(dst + S::KV_BYTES + (g * 2 + h) * kTileBytes, &tmap_v,
-                          g * kHeadDim + h * 64, y, bar, pol_kv);
-          }
+      // all block-table entries of the chunk in one round of loads
+      const bool in_row = lane < count && lj < p.bt_stride;
+      const long long phys = in_row ? __ldg(p.block_tables + (long long)lb * p.bt_stride + lj) : -1;
+      const bool pfirst = (gb + lane == lo) || (lj == 0);
+      for (int i = 0; i < count; ++i, ++issued) {
+        if ((int)(issued % kDecodeProducerWarps) != pw) continue;
+        const int st = (int)(issued % S::NST);
+        const int round = (int)(issued / S::NST);
+        if (round > 0 &&
+            !__all_sync(0xffffffffu,
+                        mbar_wait(empty0 + 8 * st, (round - 1) & 1, abort_flag, p.err))) {
+          stop = true;
+          break;
         }
-      } else {
-        report(p.err, in_row ? PA_DEVERR_BLOCK_INDEX : PA_DEVERR_SHAPE);
+        const long long ph_i = __shfl_sync(0xffffffffu, phys, i);
+        const int b_i = __shfl_sync(0xffffffffu, lb, i);
+        const bool first_i = __shfl_sync(0xffffffffu, pfirst ? 1 : 0, i) != 0;
+        const bool row_i = __shfl_sync(0xffffffffu, in_row ? 1 : 0, i) != 0;
+        if (lane == 0) {
+          const bool ok = ph_i >= 0 && ph_i < p.num_blocks;
+          const uint32_t bytes = (ok ? 2u * S::KV_BYTES : 0u) + (first_i ? S::Q_BYTES : 0u);
+          const uint32_t dst = stage0 + st * S::STAGE_BYTES;
+          const uint32_t bar = full0 + 8 * st;
+          mbar_arrive_expect_tx(bar, bytes);
+          if (ok) {
+            const int z = (int)(ph_i * kBlockSize);
+#pragma unroll
+            for (int pr = 0; pr < S::NPAIR; ++pr) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t off = (pr * 2 + h) * S::BOX_BYTES;
+                tma_load_box(dst + off, &tmap_k, h * 64, pr * S::HB, z, bar, pol_kv);
+                tma_load_box(dst + S::KV_BYTES + off, &tmap_v, h * 64, pr * S::HB, z, bar, pol_kv);
+              }
+            }
+          } else {
+            // a context longer than the table row (caller error) or an entry
+            // outside the pool: reported, not read
+            report(p.err, row_i ? PA_DEVERR_BLOCK_INDEX : PA_DEVERR_SHAPE);
+          }
+          if (first_i)
+            bulk_load(dst + 2 * S::KV_BYTES, p.q + (long long)b_i * S::HQ * kHeadDim, S::Q_BYTES,
+                      bar, pol_q);
+        }
       }
-      if (piece_first)
-        bulk_load(dst + 2 * S::KV_BYTES, p.q + (long long)b * S::HQ * kHeadDim, S::Q_BYTES, bar,
-                  pol_q);
+      gb += count;
     }
-    if (*abort_flag) {
-      // Drain: copies still in flight must land before the CTA's shared
-      // memory is released.  Bounded, independent of the abort flag.
+    if (lane == 0 && *abort_flag) {
+      // Drain: copies this warp still has in flight must land before the
+      // CTA's shared memory is released.  Bounded, independent of the abort
+      // flag.
       volatile int never = 0;
       const long long from = issued > S::NST ? issued - S::NST : 0;
       for (long long i = from; i < issued; ++i)
-        mbar_wait(full0 + 8 * (int)(i % S::NST), (int)((i / S::NST) & 1), &never, nullptr);
+        if ((int)(i % kDecodeProducerWarps) == pw)
+          mbar_wait(full0 + 8 * (int)(i % S::NST), (int)((i / S::NST) & 1), &never, nullptr);
     }
     return;
   }
 
   // ---- 5. consumers -----------------------------------------------------------
-  const int cw = warp - 1;    // consumer warp 0..7
+  const int cw = warp - kDecodeProducerWarps;  // consumer warp 0..7
   const int g = cw % HKV;     // kv head of this warp
   const int ph = cw / HKV;    // stage phase of this warp
   const int gid = lane >> 2;  // fragment row group
   const int qd = lane & 3;    // fragment column pair
-  const int ct = tid - 32;    // consumer thread index 0..255
+  const int ct = tid - 32 * kDecodeProducerWarps;  // consumer thread index 0..255
+  // this warp's kv head inside the TMA boxes: box group, row offset
+  const int gpair = g / S::HB, gsub = g % S::HB;
   const float cl2 = p.qk_scale_log2;
 
   uint32_t qf[8][2];  // Q^T fragments of the group, per 16-dim k-step
@@ -397,21 +526,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
 
-  int b = first_b;
-  int ctx = __ldg(p.context_lens + b);
-  int n = ctx > 0 ? ceil_div_blocks(ctx) : 0;
-  int j = (int)(lo - first_prefix);
-  int piece_j0 = j;
+  int wb = first_b;
+  int wctx = __ldg(p.context_lens + wb);
+  int wj = (int)(lo - first_prefix);
+  int piece_j0 = wj;
   long long it = 0;
-  for (long long gb = lo; gb < hi; ++gb, ++it, ++j) {
-    if (j == n) {
-      do {
-        ++b;
-        ctx = __ldg(p.context_lens + b);
-        n = ctx > 0 ? ceil_div_blocks(ctx) : 0;
-      } while (n == 0);
-      j = 0;
+  int chunk_left = 0, chunk_pos = 0;
+  int lb = 0, lj = 0, lctx = 0;
+  for (long long gb = lo; gb < hi; ++gb, ++it) {
+    if (chunk_left == 0) {
+      chunk_left = walk_chunk(p.context_lens, p.batch, wb, wctx, wj, hi - gb, lane, lb, lj, lctx);
+      chunk_pos = 0;
+      if (chunk_left == 0) break;  // same decision in every consumer warp and the producer
     }
+    const int b = __shfl_sync(0xffffffffu, lb, chunk_pos);
+    const int j = __shfl_sync(0xffffffffu, lj, chunk_pos);
+    const int ctx = __shfl_sync(0xffffffffu, lctx, chunk_pos);
+    const int n = ceil_div_blocks(ctx);
+    ++chunk_pos;
+    --chunk_left;
     const bool piece_first = (gb == lo) || (j == 0);
     const bool piece_last = (gb == hi - 1) || (j == n - 1);
     const int sidx = (int)(it % S::NST);
@@ -449,18 +582,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     const int valid = min(kBlockSize, ctx - j * kBlockSize);  // keys of this block (>= 1)
     if (have && (int)(it % S::NPH) == ph) {
-      const uint32_t kb = sbase + g * 2 * kTileBytes;
-      const uint32_t vb = sbase + S::KV_BYTES + g * 2 * kTileBytes;
+      // boxes of this head group: K at kb (+BOX_BYTES for dims 64..127), V at vb
+      const uint32_t kb = sbase + gpair * 2 * S::BOX_BYTES;
+      const uint32_t vb = sbase + S::KV_BYTES + gpair * 2 * S::BOX_BYTES;
       // S^T = K . Q^T, two accumulation chains over the eight 16-dim k-steps
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
       {
         const int mi = lane >> 3, r = lane & 7;
         const int t = r + ((mi & 1) << 3);
+        const int row = t * S::HB + gsub;  // 128-byte row of token t, this head
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const int chunk = ((ks & 3) << 1) + (mi >> 1);
           uint32_t a0, a1, a2, a3;
-          ldsm_x4(kb + (ks >> 2) * kTileBytes + swz(t, chunk), a0, a1, a2, a3);
+          ldsm_x4(kb + (ks >> 2) * S::BOX_BYTES + swz(row, chunk), a0, a1, a2, a3);
           if (ks & 1)
             mma_bf16(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
           else
@@ -508,7 +643,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         // 0-weight rows contribute exactly 0 to the MMA
         for (int i = lane; i < (kBlockSize - valid) * 16; i += 32) {
           const int t = valid + (i >> 4), ch = i & 15;
-          const uint32_t a = vb + (ch >> 3) * kTileBytes + swz(t, ch & 7);
+          const uint32_t a = vb + (ch >> 3) * S::BOX_BYTES + swz(t * S::HB + gsub, ch & 7);
           asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
         }
         __syncwarp();
@@ -517,11 +652,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       {
         const int mi = lane >> 3, r = lane & 7;
         const int t = r + ((mi >> 1) << 3);
+        const int row = t * S::HB + gsub;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           const int chunk = 2 * mt + (mi & 1);  // 8-dim chunk 0..15
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vb + (chunk >> 3) * kTileBytes + swz(t, chunk & 7), a0, a1, a2, a3);
+          ldsm_x4_t(vb + (chunk >> 3) * S::BOX_BYTES + swz(row, chunk & 7), a0, a1, a2, a3);
           mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
           mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
         }
@@ -649,16 +785,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const long long cs0 = split_of_block(P, nsplit, N);
       const long long cs1 = split_of_block(P + n - 1, nsplit, N);
       if (ct == 0) {
-        int pieces = 1;
-        for (long long cc = cs0 + 1; cc <= cs1; ++cc)
-          pieces += split_begin(cc, nsplit, N) < split_begin(cc + 1, nsplit, N) ? 1 : 0;
+        // splits holding a piece of b (all of c0..c1 unless some split is empty)
+        long long pieces = cs1 - cs0 + 1;
+        if (N < nsplit) {
+          pieces = 1;
+          for (long long cc = cs0 + 1; cc <= cs1; ++cc)
+            pieces += split_begin(cc, nsplit, N) < split_begin(cc + 1, nsplit, N) ? 1 : 0;
+        }
         const int prev = atomicAdd(p.counters + cs1, 1);
-        ctl->last = prev == pieces - 1;
+        ctl->last = prev == (int)pieces - 1;
       }
       named_barrier(1, kDecodeConsumerWarps * 32);
       if (ctl->last) {
         __threadfence();
-        merge_sequence<S::HQ>(p, b, cs0, cs1, nsplit, N, ct, kDecodeConsumerWarps * 32);
+        for (int h = cw; h < S::HQ; h += kDecodeConsumerWarps)
+          merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * S::HQ + h, S::HQ, h,
+                    cs0, cs1, nsplit, N, lane);
         if (ct == 0) p.counters[cs1] = 0;
       }
       named_barrier(1, kDecodeConsumerWarps * 32);

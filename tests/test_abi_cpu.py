@@ -59,8 +59,8 @@ def test_workspace_size_formula(lib):
     def up(x):
         return (x + 255) // 256 * 256
     for S, H in [(1, 12), (152, 12), (152, 32), (7, 5)]:
-        assert f(S, H, 128) == 256 + up(S * 2 * H * 128 * 4) + up(S * 2 * H * 4) + up(S * 4)
-    assert f(0, 12, 128) == 0 and f(4, 12, 64) == 0
+        assert f(S, H, 128) == 256 + 4 * 4096 + up(S * 2 * H * 128 * 4) + up(S * 2 * H * 4)
+    assert f(0, 12, 128) == 0 and f(4, 12, 64) == 0 and f(4097, 12, 128) == 0
 
 
 def test_argument_checks_before_any_launch():
