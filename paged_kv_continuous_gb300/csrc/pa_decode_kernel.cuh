@@ -85,13 +85,18 @@ struct DecodeShape {
   static constexpr int RED_BYTES =
       NPH > 1 ? align_up(kDecodeConsumerWarps * G * RED_FLOATS_PER_HEAD * 4, 1024) : 0;
   static constexpr int CTL_BYTES = 256;
+  // merge scratch: one weight per (piece, query head), up to MERGE_MAX_PIECES
+  static constexpr int MERGE_FLOATS = 2048;
+  static constexpr int MERGE_MAX_PIECES = MERGE_FLOATS / HQ;
+  static constexpr int MERGE_BYTES = MERGE_FLOATS * 4;
   static constexpr int NST_FIT =
-      (kDecodeSmemBudget - 1024 - RED_BYTES - CTL_BYTES) / (STAGE_BYTES + 16);
+      (kDecodeSmemBudget - 1024 - RED_BYTES - MERGE_BYTES - CTL_BYTES) / (STAGE_BYTES + 16);
   static constexpr int NST_CAP = NST_FIT > 12 ? 12 : NST_FIT;
   // an even ring: each slot is always filled by the same producer warp
   static constexpr int NST = NST_CAP >= 4 ? (NST_CAP & ~1) : NST_CAP;
   // +1024: the dynamic smem base is realigned to 1024 bytes for the swizzle
-  static constexpr int SMEM = 1024 + NST * STAGE_BYTES + RED_BYTES + NST * 16 + CTL_BYTES;
+  static constexpr int SMEM =
+      1024 + NST * STAGE_BYTES + RED_BYTES + MERGE_BYTES + NST * 16 + CTL_BYTES;
   static_assert(NST >= 2, "stage does not fit twice in shared memory");
   static_assert(kDecodeConsumerWarps % HKV == 0, "unsupported kv head count");
   static_assert(G >= 1 && G <= 8, "group size must fit the N = 8 MMA dimension");
@@ -319,6 +324,68 @@ __device__ __forceinline__ void merge_row(const float *part_o, const float *part
              make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
 }
 
+// Log-sum-exp merge of all partials of sequence b by the 256 consumer
+// threads of one CTA, when the pieces are few enough for their weights to fit
+// in shared memory (k <= MAXP, every split of c0..c1 non-empty): one round of
+// loads brings every (piece, head) lse into `w`; each head's weights
+// exp(lse - M) / sum are formed there; then each (head, 4 dims) item loads
+// its k partial rows eight at a time.  Returns false (nothing done) when the
+// pieces do not fit; the caller then merges row by row with merge_row.
+template <int HQ, int MAXP>
+__device__ bool merge_sequence_block(const DecodeParams &p, int b, long long c0, long long c1,
+                                     long long S, long long N, float *w, int ct, int nthreads,
+                                     int bar_id) {
+  const long long k = c1 - c0 + 1;
+  if (N < S || k > MAXP) return false;
+  auto row_of = [&](long long i, int h) -> long long {
+    const long long cc = c0 + i;
+    return (cc * 2 + (i == 0 ? 1 : 0)) * HQ + h;
+  };
+  for (int e = ct; e < (int)k * HQ; e += nthreads)
+    w[e] = __ldcg(p.part_lse + row_of(e / HQ, e % HQ));
+  named_barrier(bar_id, nthreads);
+  for (int h = ct; h < HQ; h += nthreads) {
+    float M = -INFINITY;
+    for (int i = 0; i < (int)k; ++i) M = fmaxf(M, w[i * HQ + h]);
+    float W = 0.f;
+    for (int i = 0; i < (int)k; ++i) {
+      const float lse = w[i * HQ + h];
+      const float e = lse == -INFINITY ? 0.f : __expf(lse - M);
+      w[i * HQ + h] = e;
+      W += e;
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    for (int i = 0; i < (int)k; ++i) w[i * HQ + h] *= inv;
+  }
+  named_barrier(bar_id, nthreads);
+  for (int item = ct; item < HQ * (kHeadDim / 4); item += nthreads) {
+    const int h = item / (kHeadDim / 4);
+    const int d = (item % (kHeadDim / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = 0; i0 < (int)k; i0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = i0 + u < (int)k
+                   ? __ldcg(reinterpret_cast<const float4 *>(p.part_o + row_of(i0 + u, h) * kHeadDim +
+                                                             d))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (i0 + u < (int)k) {
+          const float wu = w[(i0 + u) * HQ + h];
+          acc.x += wu * v[u].x;
+          acc.y += wu * v[u].y;
+          acc.z += wu * v[u].z;
+          acc.w += wu * v[u].w;
+        }
+      }
+    }
+    store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d, acc);
+  }
+  return true;
+}
+
 template <int G, int HKV>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -329,7 +396,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float *red = reinterpret_cast<float *>(smem + S::NST * S::STAGE_BYTES);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::NST * S::STAGE_BYTES + S::RED_BYTES);
+  float *mw = reinterpret_cast<float *>(smem + S::NST * S::STAGE_BYTES + S::RED_BYTES);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S::NST * S::STAGE_BYTES + S::RED_BYTES +
+                                                S::MERGE_BYTES);
   uint64_t *empty = full + S::NST;
   DecodeCtl *ctl = reinterpret_cast<DecodeCtl *>(empty + S::NST);
   volatile int *abort_flag = &ctl->abort;
@@ -798,9 +867,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       named_barrier(1, kDecodeConsumerWarps * 32);
       if (ctl->last) {
         __threadfence();
-        for (int h = cw; h < S::HQ; h += kDecodeConsumerWarps)
-          merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * S::HQ + h, S::HQ, h,
-                    cs0, cs1, nsplit, N, lane);
+        if (!merge_sequence_block<S::HQ, S::MERGE_MAX_PIECES>(p, b, cs0, cs1, nsplit, N, mw, ct,
+                                                               kDecodeConsumerWarps * 32, 1))
+          for (int h = cw; h < S::HQ; h += kDecodeConsumerWarps)
+            merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * S::HQ + h, S::HQ, h,
+                      cs0, cs1, nsplit, N, lane);
         if (ct == 0) p.counters[cs1] = 0;
       }
       named_barrier(1, kDecodeConsumerWarps * 32);
