@@ -1,7 +1,533 @@
-// pa_prefill_varlen: causal varlen attention over a paged prefix.  The
-// tcgen05 tensor-core kernel is not built yet; the entry point validates its
-// arguments and reports PA_ERR_UNSUPPORTED.
+// pa_prefill_varlen: causal varlen attention of cu_seqlens-packed query
+// chunks over each sequence's paged keys (mini-vllm tutorial, "step14_7 --
+// Batched Forward", sections "解决方案：变长 batch（varlen）" and "cu_seqlens 只在
+// Attention 里才需要": tokens of all sequences are flattened and cu_seqlens
+// marks the boundaries; attention stays inside a sequence and is causal;
+// keys come from the sequence's pages through its block table).
+//
+// One CTA computes a 128-row tile of one (sequence, kv head): rows are the
+// (query position, query head) pairs of PT = 128 / G consecutive positions
+// times the G query heads of the kv head, so every K/V tile read from the
+// pool serves the whole GQA group.  Per 128-key tile j:
+//   S   = Q K_j^T      tcgen05.mma (M 128, N 128, K 128), fp32 in TMEM
+//   P   = exp2(S * c - m)  per row, with the causal and length masks (fp32)
+//   O  += P V_j        tcgen05.mma, O accumulated in TMEM; when a row's
+//                      running max grows, its O row is rescaled in TMEM.
+//                      P is split into bf16 hi + lo parts (two MMA passes)
+//                      so the product keeps ~16 bits of the fp32 weights.
+// Warp 0 issues TMA loads of the K/V pages (two stages), warp 1 issues the
+// MMAs (one thread) and owns the TMEM allocation, warps 2..5 (one TMEM lane
+// = one row per thread) run the softmax, write P to shared memory as the A
+// operand of the second MMA, and store the output.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "pa_common.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kPfThreads = 192;
+constexpr int kPfRows = 128;      // M
+constexpr int kPfKeys = 128;      // keys per KV tile (N of the first MMA)
+constexpr int kHalfBytes = 128 * 128;  // 128 rows x 64 dims (bf16) with the 128-byte swizzle
+constexpr int kTileBytes2 = 2 * kHalfBytes;  // one 128 x 128 bf16 operand tile = 32 KB
+// shared memory (offsets from a 1024-aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTileBytes2;        // 2 stages
+constexpr int kOffV = kOffK + 2 * kTileBytes2;    // 2 stages
+constexpr int kOffP = kOffV + 2 * kTileBytes2;   // P hi, then P lo
+constexpr int kOffBar = kOffP + 2 * kTileBytes2;
+constexpr int kPfSmem = 1024 + kOffBar + 256;
+constexpr int kTmemCols = 256;  // S: columns 0..127, O: 128..255
+
+struct PrefillParams {
+  void *out;
+  int out_f32;
+  const uint16_t *q;
+  const int32_t *cu_seqlens;
+  int num_seqs;
+  long long num_blocks;
+  const int32_t *block_tables;
+  long long bt_stride;
+  const int32_t *context_lens;
+  int hq, hkv;
+  float qk_scale_log2;
+  int32_t *err;
+};
+
+// ---- tcgen05 helpers ----------------------------------------------------------
+
+// Shared-memory matrix descriptor (K- or MN-major, 128-byte swizzle):
+// start address, leading / stride byte offsets (>> 4), version 1, layout 2.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = 128,
+// A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1).
+__host__ __device__ constexpr uint32_t umma_idesc(int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(kPfKeys >> 3) << 17) | ((uint32_t)(kPfRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Byte offset of (row, 16-byte chunk) inside a [128 rows][128 B] swizzled half.
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+  return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+  constexpr int PT = kPfRows / G;  // query positions per tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t base = smem_addr(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  // barrier slots
+  const uint32_t b_kv_full0 = smem_addr(bars + 0);   // + 8 * stage
+  const uint32_t b_kv_empty0 = smem_addr(bars + 2);  // + 8 * stage
+  const uint32_t b_q_ready = smem_addr(bars + 4);
+  const uint32_t b_s_full = smem_addr(bars + 5);
+  const uint32_t b_s_free = smem_addr(bars + 6);
+  const uint32_t b_p_full = smem_addr(bars + 7);
+  const uint32_t b_o_full = smem_addr(bars + 8);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 11);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int q0 = __ldg(p.cu_seqlens + s);
+  const int q_len = __ldg(p.cu_seqlens + s + 1) - q0;
+  const int pos0 = mt * PT;
+  if (pos0 >= q_len) return;  // whole CTA: this tile has no query
+  const int n = __ldg(p.context_lens + s);
+  const int prefix = n - q_len;
+  if (prefix < 0) {
+    if (tid == 0) report(p.err, PA_DEVERR_SHAPE);
+    return;
+  }
+  // a chunk longer than max_q_len has rows no CTA covers: reported
+  if (mt == (int)gridDim.x - 1 && pos0 + PT < q_len && threadIdx.x == 0)
+    report(p.err, PA_DEVERR_SHAPE);
+  const int npos = min(PT, q_len - pos0);
+  const int rows = npos * G;
+  const int kmax = prefix + pos0 + npos - 1;  // last key any row of the tile sees
+  const int nkv = kmax / kPfKeys + 1;
+  const float c = p.qk_scale_log2;
+
+  if (tid == 0) {
+    mbar_init(b_kv_full0, 1);
+    mbar_init(b_kv_full0 + 8, 1);
+    mbar_init(b_kv_empty0, 1);
+    mbar_init(b_kv_empty0 + 8, 1);
+    mbar_init(b_q_ready, 128);
+    mbar_init(b_s_full, 1);
+    mbar_init(b_s_free, 128);
+    mbar_init(b_p_full, 128);
+    mbar_init(b_o_full, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
+
+  if (warp == 0) {
+    // ---- TMA producer: K and V pages of tile j into stage j & 1 ------------
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
+                   : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v))
+                   : "memory");
+      const int32_t *row = p.block_tables + (long long)s * p.bt_stride;
+      int j = 0;
+      for (; j < nkv; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !mbar_wait(b_kv_empty0 + 8 * st, ((j >> 1) - 1) & 1, abort_flag, p.err))
+          break;
+        const uint32_t kdst = base + kOffK + st * kTileBytes2;
+        const uint32_t vdst = base + kOffV + st * kTileBytes2;
+        // pages of this tile that hold keys (the rest stays as it is: masked)
+        int nb = 0;
+        for (int blk = 0; blk < kPfKeys / kBlockSize; ++blk)
+          if (j * kPfKeys + blk * kBlockSize < n) ++nb;
+        uint32_t bytes = 0;
+        bool okall = true;
+        long long phys[kPfKeys / kBlockSize];
+        for (int blk = 0; blk < nb; ++blk) {
+          const int lb = j * (kPfKeys / kBlockSize) + blk;
+          const long long ph = lb < p.bt_stride ? __ldg(row + lb) : -1;
+          phys[blk] = (ph >= 0 && ph < p.num_blocks) ? ph : -1;
+          if (phys[blk] >= 0) bytes += 4 * kBlockSize * 64 * 2;
+          else okall = false;
+        }
+        if (!okall) report(p.err, PA_DEVERR_BLOCK_INDEX);
+        mbar_arrive_expect_tx(b_kv_full0 + 8 * st, bytes);
+        for (int blk = 0; blk < nb; ++blk) {
+          if (phys[blk] < 0) continue;
+          const int z = (int)(phys[blk] * kBlockSize);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t off = h * kHalfBytes + blk * kBlockSize * 128;
+            tma_load_3d(kdst + off, &tmap_k, h * 64, g, z, b_kv_full0 + 8 * st);
+            tma_load_3d(vdst + off, &tmap_v, h * 64, g, z, b_kv_full0 + 8 * st);
+          }
+        }
+      }
+      if (*abort_flag) {
+        volatile int never = 0;
+        for (int i = j > 2 ? j - 2 : 0; i < j; ++i)
+          mbar_wait(b_kv_full0 + 8 * (i & 1), (i >> 1) & 1, &never, nullptr);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer -------------------------------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = umma_idesc(0), idesc_pv = umma_idesc(1);
+      bool ok = mbar_wait(b_q_ready, 0, abort_flag, p.err);
+      tc_fence_after();
+      int j = 0;
+      for (; j < nkv && ok; ++j) {
+        const int st = j & 1;
+        if (!mbar_wait(b_kv_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.err)) break;
+        if (j > 0 && !mbar_wait(b_s_free, (j - 1) & 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        // S = Q K^T: 8 k-steps of 16 dims (4 per 64-dim swizzled half)
+        const uint32_t kb = base + kOffK + st * kTileBytes2;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+          umma_f16(tmem_s, umma_desc(base + kOffQ + off, 16, 1024), umma_desc(kb + off, 16, 1024),
+                   idesc_qk, ks > 0);
+        }
+        umma_commit(b_s_full);
+        // O += (P_hi + P_lo) V: 2 x 8 k-steps of 16 keys; V is MN-major (dims
+        // contiguous): LBO = distance between the two 64-dim halves, SBO = 8 keys
+        if (!mbar_wait(b_p_full, j & 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t vb = base + kOffV + st * kTileBytes2;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t pa =
+                base + kOffP + part * kTileBytes2 + (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+            umma_f16(tmem_o, umma_desc(pa, 16, 1024),
+                     umma_desc(vb + ks * 16 * 128, kHalfBytes, 1024), idesc_pv,
+                     (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(b_o_full);
+        umma_commit(b_kv_empty0 + 8 * st);
+      }
+      if (*abort_flag) {
+        // let issued MMAs finish before TMEM is released (bounded)
+        volatile int never = 0;
+        if (j > 0) mbar_wait(b_o_full, (j - 1) & 1, &never, nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- softmax / epilogue warps: thread = row r ---------------------------------
+    const int lb = 32 * (warp & 3);  // TMEM lanes this warp may access
+    const int r = lb + lane;         // row of the tile
+    const int rpos = r / G;          // query position in the tile
+    const int hs = r % G;            // query head in the group
+    const bool rvalid = r < rows;
+    const int limit = rvalid ? prefix + pos0 + rpos : -1;  // last key this row sees
+    const uint32_t trow = (uint32_t)lb << 16;
+
+    // Q tile: row r = q[q0 + pos0 + rpos][g * G + hs][:], 128-byte swizzle
+    {
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          p.q + ((long long)(q0 + pos0 + rpos) * p.hq + g * G + hs) * kHeadDim);
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        const uint4 v = rvalid ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t a = base + kOffQ + (ch >> 3) * kHalfBytes + sw128(r, ch & 7);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(b_q_ready);
+    }
+
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv && ok; ++j) {
+      // warp-uniform: tcgen05.ld / st below are warp-collective
+      ok = __all_sync(0xffffffffu, mbar_wait(b_s_full, j & 1, abort_flag, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const int key0 = j * kPfKeys;
+      // pass 1: row max over the keys this row sees
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float sv[32];
+        tmem_ld32(tmem_s + trow + cc * 32, sv);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (key0 + cc * 32 + i <= limit) mx = fmaxf(mx, sv[i]);
+      }
+      const float m_new = fmaxf(m, mx * c);
+      const float alpha = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
+      // P and O of the previous tile are in use until its PV MMA finishes
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(b_o_full, (j - 1) & 1, abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        // rows whose running max grew rescale their O row (warp-wide: collective ld/st)
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            float ov[32];
+            tmem_ld32(tmem_o + trow + cc * 32, ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+            tmem_st32(tmem_o + trow + cc * 32, ov);
+          }
+        }
+      }
+      // pass 2: P = exp2(S c - m) (S is read a second time), row sum, and the
+      // bf16 hi / lo parts of P straight into shared memory (A operands of
+      // the PV MMAs, 128-byte swizzle)
+      float psum = 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float sv[32];
+        tmem_ld32(tmem_s + trow + cc * 32, sv);
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            const int idx = q8 * 8 + i;
+            const int k0 = key0 + cc * 32 + idx;
+            const float e0 = k0 <= limit ? exp2f(fmaf(sv[idx], c, -m_new)) : 0.f;
+            const float e1 = k0 + 1 <= limit ? exp2f(fmaf(sv[idx + 1], c, -m_new)) : 0.f;
+            psum += e0 + e1;
+            hi[i / 2] = float2_to_bf16x2(e0, e1);
+            const float2 h2 = bf16x2_to_float2(hi[i / 2]);
+            lo[i / 2] = float2_to_bf16x2(e0 - h2.x, e1 - h2.y);
+          }
+          const int ch = cc * 4 + q8;  // 16-byte chunk (8 keys) of the 256-byte row
+          const uint32_t off = (ch >> 3) * kHalfBytes + sw128(r, ch & 7);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + kOffP + off),
+                       "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
+                       : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           base + kOffP + kTileBytes2 + off),
+                       "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
+                       : "memory");
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(b_s_free);  // S may be overwritten by the next QK MMA
+      l = l * alpha + psum;
+      m = m_new;
+      // keys past the end of the sequence: their V rows may hold anything;
+      // zero them so that 0-weight rows add exactly 0 (last tile only)
+      if (key0 + kPfKeys > n) {
+        const uint32_t vb = base + kOffV + (j & 1) * kTileBytes2;
+        for (int i = r; i < kPfKeys * 16; i += 128) {
+          const int key = i >> 4, ch = i & 15;
+          if (key0 + key >= n) {
+            const uint32_t a = vb + (ch >> 3) * kHalfBytes + sw128(key, ch & 7);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+          }
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(b_p_full);
+    }
+    // epilogue: O / l -> out[q0 + pos0 + rpos][g * G + hs][:]
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_o_full, (nkv - 1) & 1, abort_flag, p.err));
+    tc_fence_after();
+    if (ok) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const long long orow = ((long long)(q0 + pos0 + rpos) * p.hq + g * G + hs) * kHeadDim;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        float ov[32];
+        tmem_ld32(tmem_o + trow + cc * 32, ov);
+        if (rvalid) {
+          if (p.out_f32) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow + cc * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(ov[4 * i] * inv, ov[4 * i + 1] * inv, ov[4 * i + 2] * inv,
+                                   ov[4 * i + 3] * inv);
+          } else {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + orow + cc * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 w;
+              w.x = float2_to_bf16x2(ov[8 * i] * inv, ov[8 * i + 1] * inv);
+              w.y = float2_to_bf16x2(ov[8 * i + 2] * inv, ov[8 * i + 3] * inv);
+              w.z = float2_to_bf16x2(ov[8 * i + 4] * inv, ov[8 * i + 5] * inv);
+              w.w = float2_to_bf16x2(ov[8 * i + 6] * inv, ov[8 * i + 7] * inv);
+              dst[i] = w;
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// (dim 128, kv head, token slot) view of a pool; one box = 64 dims x 1 head x
+// 16 slots (one page of one head), 128-byte swizzle.
+bool pool_map(CUtensorMap *map, const void *pool, long long num_blocks, int hkv) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv,
+                        (cuuint64_t)num_blocks * kBlockSize};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hkv * kHeadDim * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kBlockSize};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int G>
+cudaError_t launch_prefill(const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &pp,
+                           int max_q_len, cudaStream_t s, int device) {
+  static bool configured[64] = {};
+  if (device < 0 || device >= 64 || !configured[device]) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        prefill_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (e != cudaSuccess) return e;
+    if (device >= 0 && device < 64) configured[device] = true;
+  }
+  constexpr int PT = kPfRows / G;
+  dim3 grid((max_q_len + PT - 1) / PT, pp.hkv, pp.num_seqs);
+  prefill_kernel<G><<<grid, kPfThreads, kPfSmem, s>>>(tk, tv, pp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace pa
 
 extern "C" pa_status pa_prefill_varlen(void *out, int32_t out_dtype, const void *q,
                                        const int32_t *cu_seqlens, int32_t num_seqs,
@@ -12,9 +538,60 @@ extern "C" pa_status pa_prefill_varlen(void *out, int32_t out_dtype, const void 
                                        int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim, int32_t block_size, float scale,
                                        int32_t *error_flags, void *stream) {
-  (void)out; (void)out_dtype; (void)q; (void)cu_seqlens; (void)num_seqs; (void)total_tokens;
-  (void)max_q_len; (void)k_cache; (void)v_cache; (void)num_blocks; (void)block_tables;
-  (void)block_table_stride; (void)context_lens; (void)num_q_heads; (void)num_kv_heads;
-  (void)head_dim; (void)block_size; (void)scale; (void)error_flags; (void)stream;
-  return PA_ERR_UNSUPPORTED;
+  using namespace pa;
+  if (num_seqs < 0 || total_tokens < 0 || max_q_len < 0 || num_blocks < 0)
+    return PA_ERR_INVALID_ARG;
+  if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (!(num_kv_heads == 1 || num_kv_heads == 2 || num_kv_heads == 4 || num_kv_heads == 8))
+    return PA_ERR_UNSUPPORTED;
+  if (num_q_heads < num_kv_heads || num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > 8)
+    return PA_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_tokens == 0 || max_q_len == 0) return PA_OK;
+  if (num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+  if (num_blocks < 1 || num_blocks > (long long)(0x7fffffff / kBlockSize))
+    return PA_ERR_INVALID_ARG;
+  if (!out || !q || !cu_seqlens || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PA_ERR_INVALID_ARG;
+  if (block_table_stride < 1) return PA_ERR_INVALID_ARG;
+  auto misaligned = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15) != 0; };
+  if (misaligned(out) || misaligned(q) || misaligned(k_cache) || misaligned(v_cache))
+    return PA_ERR_INVALID_ARG;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_DEVICE;
+  CUtensorMap tk, tv;
+  memset(&tk, 0, sizeof tk);
+  memset(&tv, 0, sizeof tv);
+  if (!pool_map(&tk, k_cache, num_blocks, num_kv_heads) ||
+      !pool_map(&tv, v_cache, num_blocks, num_kv_heads))
+    return PA_ERR_DEVICE;
+  PrefillParams pp;
+  pp.out = out;
+  pp.out_f32 = out_dtype == PA_DTYPE_F32;
+  pp.q = static_cast<const uint16_t *>(q);
+  pp.cu_seqlens = cu_seqlens;
+  pp.num_seqs = num_seqs;
+  pp.num_blocks = num_blocks;
+  pp.block_tables = block_tables;
+  pp.bt_stride = block_table_stride;
+  pp.context_lens = context_lens;
+  pp.hq = num_q_heads;
+  pp.hkv = num_kv_heads;
+  pp.qk_scale_log2 = scale * 1.4426950408889634f;
+  pp.err = error_flags;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int G = num_q_heads / num_kv_heads;
+  cudaError_t e;
+  switch (G) {
+    case 1: e = launch_prefill<1>(tk, tv, pp, max_q_len, st, device); break;
+    case 2: e = launch_prefill<2>(tk, tv, pp, max_q_len, st, device); break;
+    case 3: e = launch_prefill<3>(tk, tv, pp, max_q_len, st, device); break;
+    case 4: e = launch_prefill<4>(tk, tv, pp, max_q_len, st, device); break;
+    case 5: e = launch_prefill<5>(tk, tv, pp, max_q_len, st, device); break;
+    case 6: e = launch_prefill<6>(tk, tv, pp, max_q_len, st, device); break;
+    case 7: e = launch_prefill<7>(tk, tv, pp, max_q_len, st, device); break;
+    default: e = launch_prefill<8>(tk, tv, pp, max_q_len, st, device); break;
+  }
+  return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }
