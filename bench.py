@@ -63,10 +63,12 @@ def store_alg_bytes(tokens, hkv, d=128):
 
 
 def prefill_alg_flops(q_lens, ctx, hq, d=128):
+    """QK^T and PV multiply-adds of the causal chunks: query i of a chunk
+    behind a prefix of p keys sees p + i + 1 keys."""
     tot = 0
     for q, n in zip(q_lens, ctx):
-        p = n - q
-        tot += sum(p + i + 1 for i in range(q))
+        q, p = int(q), int(n) - int(q)
+        tot += q * (p + 1) + q * (q - 1) // 2
     return 4 * d * hq * tot
 
 
@@ -184,6 +186,117 @@ def dist_env():
 def aggregate(units_per_rank, seconds_per_rank):
     """Whole-job throughput of replicas: all units over the slowest rank."""
     return float(sum(units_per_rank)) / max(seconds_per_rank)
+
+
+# ---------------------------------------------------------------------------
+# extra workloads timed in the same run (reported beside the headline)
+# ---------------------------------------------------------------------------
+
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def time_graph(fn, calls, reps=5):
+    """Mean device time of `fn` over `calls` back-to-back launches captured
+    in one CUDA graph, best of `reps` replays (ms per call)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record()
+            g.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / calls
+        best = t if best is None else min(best, t)
+    return best
+
+
+def run_extras(ops, dev):
+    """Long-context split-K decode (batch 4 x 32768 keys, Hq 32 / Hkv 8; 4
+    layer pools so the 537 MB of KV per layer always comes from HBM) and the
+    varlen chunked prefill (8 one-token rows + 8 chunks of 512 behind paged
+    prefixes up to 2048, tensor cores)."""
+    import torch
+    from paged_kv_continuous_gb300 import synth
+    extra = {}
+    hbm, hbm_kind = hbm_peak()
+    # long decode: lengths and tables as the workload generator draws them,
+    # K/V filled on the device (values do not change the timing)
+    rng = np.random.default_rng(synth.SEED_BASE + 3)
+    B, ctxlen, hq, hkv, nb = 4, 32768, 32, 8, 10240
+    perm = rng.permutation(nb).astype(np.int32)
+    nblk = ctxlen // 16
+    tables = torch.from_numpy(perm[:B * nblk].reshape(B, nblk).copy()).to(dev)
+    ctx = torch.full((B,), ctxlen, dtype=torch.int32, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(synth.SEED_BASE + 3)
+    L = 4
+    pools = [(torch.randn((nb, 16, hkv, 128), generator=gen, device=dev, dtype=torch.bfloat16),
+              torch.randn((nb, 16, hkv, 128), generator=gen, device=dev, dtype=torch.bfloat16))
+             for _ in range(L)]
+    q = torch.randn((B, hq, 128), generator=gen, device=dev, dtype=torch.bfloat16)
+    out = torch.empty((B, hq, 128), dtype=torch.bfloat16, device=dev)
+    ws = ops.decode_workspace(hq, 0, 128, dev)
+    state = {"l": 0}
+
+    def dec():
+        kc, vc = pools[state["l"] % L]
+        state["l"] += 1
+        ops.decode(q, kc, vc, tables, ctx, 128 ** -0.5, out=out, workspace=ws)
+    ms = time_graph(dec, 4 * L)
+    nbytes = decode_alg_bytes(np.full(B, ctxlen), hq, hkv)
+    extra["long_decode_b4_ctx32768_h32_8"] = {
+        "us_per_call": ms * 1e3, "alg_bytes": nbytes, "GB_per_s": nbytes / ms / 1e6,
+        "frac_of_hbm": nbytes / ms / 1e6 / hbm, "peak_kind": hbm_kind}
+    del pools
+    # varlen prefill
+    w = synth.varlen_prefill(keep_seq=False)
+
+    def dev16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(
+            torch.bfloat16).to(dev)
+
+    def dev32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    kc, vc = dev16(w.k_cache), dev16(w.v_cache)
+    ops.store_kv(dev16(w.new_k), dev16(w.new_v), kc, vc, dev32(w.slot_mapping))
+    qv, cu = dev16(w.q), dev32(w.cu_seqlens)
+    bt, cl = dev32(w.block_tables), dev32(w.context_lens)
+    outp = torch.empty((w.q.shape[0], w.num_q_heads, 128), dtype=torch.bfloat16, device=dev)
+    mq = int(w.q_lens.max())
+
+    def pre():
+        ops.prefill_varlen(qv, cu, kc, vc, bt, cl, w.scale, mq, out=outp)
+    ms = time_graph(pre, 10)
+    flops = prefill_alg_flops(w.q_lens, w.context_lens, w.num_q_heads)
+    burst, sustained, kind = bf16_peak()
+    tf = flops / ms / 1e9
+    extra["varlen_prefill_8x1_8x512"] = {
+        "us_per_call": ms * 1e3, "alg_flops": flops, "TFLOP_per_s": tf,
+        "frac_of_bf16_burst": tf / burst, "frac_of_bf16_sustained": tf / sustained,
+        "peak_kind": kind, "rows": int(w.q.shape[0])}
+    return extra
 
 
 # ---------------------------------------------------------------------------
@@ -458,6 +571,8 @@ def run_ours(args):
         e2e_s = float(t.item())
     e2e_value = aggregate([step_bytes * e2e_steps] * world, [e2e_s] * world) / 1e9
 
+    extra = run_extras(ops, dev) if not args.no_extra else {}
+
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
@@ -509,6 +624,7 @@ def run_ours(args):
         "parity": {"ok": parity_ok, "max_abs_err": float(abs_err.max()),
                    "checked": "first step of layer 0 vs oracle, all 64x12x128 outputs"},
         "device_error_word": err_word,
+        "extra": extra,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -524,6 +640,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=8)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the long-context decode and prefill measurements")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")
