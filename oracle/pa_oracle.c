@@ -29,7 +29,7 @@
  *   [CEB]  PocketLLM, "cpp_engine Batching Implementation (Phase 3.1)",
  *          section "当前 KV cache 结构" (one token row = [kv_heads, head_dim]).
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *   - slot s of the pool is physical block s / block_size, row s % block_size;
  *   - the pool layout is [num_blocks][block_size][num_kv_heads][head_dim];
  *   - slot_mapping < 0 marks a padding token and is skipped;
