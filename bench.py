@@ -188,6 +188,19 @@ def aggregate(units_per_rank, seconds_per_rank):
     return float(sum(units_per_rank)) / max(seconds_per_rank)
 
 
+def max_over_ranks(seconds, device=None):
+    """Slowest rank's time (identity without a process group).  Works with
+    NCCL (device tensors) and gloo (CPU tensors)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(seconds)
+    t = torch.tensor([float(seconds)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------------------
 # extra workloads timed in the same run (reported beside the headline)
 # ---------------------------------------------------------------------------
@@ -500,12 +513,7 @@ def run_ours(args):
     t_host1 = time.monotonic()
     barrier()
     sampler.stop()
-    elapsed_s = start.elapsed_time(end) / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_s = float(t.item())
+    elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
     err_word = ops.read_error_word(ws)
 
     # per-kernel durations from the last replay of each graph copy
@@ -563,12 +571,7 @@ def run_ours(args):
         e2e_step(i % L)
     e1.record()
     torch.cuda.synchronize()
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
     e2e_value = aggregate([step_bytes * e2e_steps] * world, [e2e_s] * world) / 1e9
 
     extra = run_extras(ops, dev) if not args.no_extra else {}
