@@ -270,7 +270,7 @@ def run_extras(ops, dev):
              for _ in range(L)]
     q = torch.randn((B, hq, 128), generator=gen, device=dev, dtype=torch.bfloat16)
     out = torch.empty((B, hq, 128), dtype=torch.bfloat16, device=dev)
-    ws = ops.decode_workspace(hq, 0, 128, dev)
+    ws = ops.decode_workspace(hq, hkv, 0, 128, dev)
     state = {"l": 0}
 
     def dec():
@@ -421,8 +421,8 @@ def run_ours(args):
             nv = torch.randn((B, Hkv, D), generator=gen, device=dev, dtype=torch.bfloat16)
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
         layers.append(dict(kc=kc, vc=vc, q=q, nk=nk, nv=nv, out=out))
-    splits = ops.default_splits(local)
-    ws = ops.decode_workspace(Hq, splits, D, dev)
+    splits = ops.default_splits(Hq, Hkv, local)
+    ws = ops.decode_workspace(Hq, Hkv, splits, D, dev)
 
     def step(l, timing=None):
         x = layers[l]

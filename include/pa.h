@@ -65,7 +65,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 1
+#define PA_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define PA_API __attribute__((visibility("default")))
@@ -164,9 +164,11 @@ PA_API pa_status pa_store_kv(const void *k, const void *v, int64_t num_tokens,
  */
 PA_API size_t pa_decode_workspace_size(int32_t num_splits, int32_t num_q_heads, int32_t head_dim);
 
-/* num_splits used when pa_decode is given 0: one split per resident CTA of
- * `device` (its SM count for the shipped kernel).  Returns <= 0 on error. */
-PA_API int32_t pa_decode_default_splits(int32_t device);
+/* num_splits used when pa_decode is given 0 for this head shape: one split
+ * per CTA the decode kernel keeps resident on `device` (its SM count for the
+ * shipped kernel, whatever the head counts).  Returns <= 0 on error. */
+PA_API int32_t pa_decode_default_splits(int32_t device, int32_t num_q_heads,
+                                        int32_t num_kv_heads);
 
 /*
  * pa_decode -- paged GQA decode attention ([EAS] "自写 Triton Kernel",
@@ -235,9 +237,10 @@ PA_API pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *works
  * in a fixed 8 MiB array inside the library (a file-scope __device__ array,
  * held by every GPU that loads the library until the process exits);
  * device-side error bits go to `error_flags` (optional int32 word, may be
- * NULL).  Returns PA_ERR_WORKSPACE, launching nothing, when
- * pa_decode_workspace_size(S, num_q_heads, head_dim) exceeds 8 MiB for the
- * split count S in use (S <= 676 at 12 query heads, S <= 253 at 32).  The
+ * NULL).  num_splits = 0 takes pa_decode_default_splits, lowered where
+ * needed to the largest S whose pa_decode_workspace_size(S, num_q_heads,
+ * head_dim) fits in 8 MiB.  An explicit S that does not fit (S > 676 at 12
+ * query heads, S > 253 at 32) returns PA_ERR_WORKSPACE, launching nothing.  The
  * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  * routine.  The first call on a device, with that device current, looks up
  * the array's device address and caches it; make that first call before

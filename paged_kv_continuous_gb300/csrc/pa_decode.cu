@@ -183,7 +183,7 @@ pa_status check_decode_request(DecodeRequest &r, int *device_out) {
     return PA_ERR_INVALID_ARG;
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess || device < 0) return PA_ERR_DEVICE;
-  r.splits = r.num_splits > 0 ? r.num_splits : pa_decode_default_splits(device);
+  r.splits = r.num_splits > 0 ? r.num_splits : pa_decode_default_splits(device, hq, hkv);
   if (r.splits < 1) return PA_ERR_DEVICE;
   if (r.splits > PA_DECODE_MAX_SPLITS) r.splits = PA_DECODE_MAX_SPLITS;
   *device_out = device;
@@ -201,11 +201,13 @@ extern "C" size_t pa_decode_workspace_size(int32_t num_splits, int32_t num_q_hea
   return workspace_layout(num_splits, num_q_heads).total;
 }
 
-extern "C" int32_t pa_decode_default_splits(int32_t device) {
+extern "C" int32_t pa_decode_default_splits(int32_t device, int32_t num_q_heads,
+                                            int32_t num_kv_heads) {
+  if (num_q_heads < 1 || num_kv_heads < 1) return -1;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
     return -1;
-  return sms;  // the decode kernel runs one CTA per SM
+  return sms;  // the decode kernel keeps one CTA per SM for every head shape
 }
 
 extern "C" pa_status pa_decode(void *out, int32_t out_dtype, const void *q, const void *k_cache,

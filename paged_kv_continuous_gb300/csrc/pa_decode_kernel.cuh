@@ -13,16 +13,25 @@
 // partial (o normalised over its keys, natural-log sum-exp) to the
 // workspace and bumps the sequence's arrival counter; the CTA that brings
 // the counter to the piece count merges all partials of that sequence
-// (log-sum-exp) and writes its rows, then resets the counter to zero.
+// (log-sum-exp) and writes its rows, then resets the counter to zero.  Only
+// a CTA's first piece (cut at its head) and its final piece (cut at its
+// tail) can be cut.  The first one is published by the epilogue warp while
+// the consumers stream on.  For the final one the consumers read the
+// counter first: when every other piece has already arrived they merge at
+// once, with their own rows taken from shared memory, and skip publishing.
 //
-// CTA layout (320 threads).  Warps 0 and 1 are producers, filling alternate
+// CTA layout (352 threads).  Warps 0 and 1 are producers, filling alternate
 // stages of a ring of NST stages guarded by full/empty mbarriers: per
 // physical block they issue TMA box loads of K and V (16 tokens x 2 kv heads
-// x 64 dims each, 128-byte swizzle; 4 boxes per block at Hkv <= 2) plus a
-// bulk copy of the sequence's q row at the start of a piece.  Two producers
-// overlap the per-stage issue latency of one thread.  Warps 2..9 consume:
-// warp (g, ph) handles kv head g of every stage whose index is ph modulo
-// 8 / Hkv.
+// x 64 dims each, 128-byte swizzle; 4 boxes per block at Hkv <= 2), plus a
+// bulk copy of the sequence's q rows into each of the first NPH stages of a
+// piece.  Two producers overlap the per-stage issue latency of one thread.
+// Warp 2 is the epilogue warp.  Warps 3..10 consume: warp (g, ph) handles kv
+// head g of the stages whose index is ph modulo NPH = 8 / Hkv, and visits no
+// other stage: it takes its q rows from its own first stage of each piece.
+// NST is a multiple of NPH, so every slot of the ring holds stages of one
+// phase and its Hkv warps wait on each round of it in order.  All consumer
+// warps meet at every piece end to combine.
 //
 // Arithmetic per (block, kv head) on the tensor cores (mma.sync m16n8k16,
 // bf16 in, fp32 accumulate), with the G query heads of the group as the
@@ -61,9 +70,12 @@ struct DecodeParams {
 };
 
 constexpr int kDecodeProducerWarps = 2;
+constexpr int kDecodeEpilogueWarp = 2;       // warp index of the epilogue warp
+constexpr int kDecodeFirstConsumerWarp = 3;  // consumers are warps 3 .. 3 + CW - 1
 constexpr int kDecodeConsumerWarps = 8;
-constexpr int kDecodeThreads = 32 * (kDecodeProducerWarps + kDecodeConsumerWarps);
-constexpr int kDecodeSmemBudget = 227 * 1024;
+constexpr int kDecodeWarps = kDecodeFirstConsumerWarp + kDecodeConsumerWarps;
+constexpr int kDecodeThreads = 32 * kDecodeWarps;
+constexpr int kDecodeSmemBudget = 227 * 1024;  // dynamic shared memory of one CTA per SM
 constexpr int kTileBytes = kBlockSize * 64 * 2;  // 16 tokens x 64 dims bf16 = 2 KB per head
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -71,7 +83,8 @@ __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / 
 template <int G, int HKV>
 struct DecodeShape {
   static constexpr int HQ = G * HKV;
-  static constexpr int NPH = kDecodeConsumerWarps / HKV;  // stage phases = warps per kv head
+  static constexpr int CW = kDecodeConsumerWarps;
+  static constexpr int NPH = CW / HKV;  // stage phases = warps per kv head
   // one TMA box = 16 tokens x HB heads x 64 dims; a page of K (or V) takes
   // NPAIR * 2 boxes (head groups x dim halves)
   static constexpr int HB = HKV >= 2 ? 2 : 1;
@@ -80,10 +93,12 @@ struct DecodeShape {
   static constexpr int KV_BYTES = HKV * 2 * kTileBytes;     // one block of K (or V), all heads
   static constexpr int Q_BYTES = HQ * kHeadDim * 2;
   static constexpr int STAGE_BYTES = align_up(2 * KV_BYTES + Q_BYTES, 1024);
-  // per consumer warp and query head of its group: m, l, o[128]
-  static constexpr int RED_FLOATS_PER_HEAD = kHeadDim + 2;
+  // per consumer warp and query head of its group: o[128], m, l (rows of
+  // 132 floats keep the o vectors 16-byte aligned)
+  static constexpr int RED_FLOATS_PER_HEAD = kHeadDim + 4;
+  static constexpr int RED_M = kHeadDim, RED_L = kHeadDim + 1;
   static constexpr int RED_BYTES =
-      NPH > 1 ? align_up(kDecodeConsumerWarps * G * RED_FLOATS_PER_HEAD * 4, 1024) : 0;
+      NPH > 1 ? align_up(CW * G * RED_FLOATS_PER_HEAD * 4, 1024) : 0;
   static constexpr int CTL_BYTES = 256;
   // merge scratch: one weight per (piece, query head), up to MERGE_MAX_PIECES
   static constexpr int MERGE_FLOATS = 2048;
@@ -92,23 +107,44 @@ struct DecodeShape {
   static constexpr int NST_FIT =
       (kDecodeSmemBudget - 1024 - RED_BYTES - MERGE_BYTES - CTL_BYTES) / (STAGE_BYTES + 16);
   static constexpr int NST_CAP = NST_FIT > 12 ? 12 : NST_FIT;
-  // an even ring: each slot is always filled by the same producer warp
-  static constexpr int NST = NST_CAP >= 4 ? (NST_CAP & ~1) : NST_CAP;
+  // The ring is a multiple of 2 (each slot is always filled by the same one
+  // of the two producer warps) and of NPH (each slot always holds stages of
+  // the same phase, so the Hkv consumer warps of that phase wait on every
+  // round of the slot in order: a parity wait never skips a phase).
+  static constexpr int RING_MULT = NPH > 2 ? NPH : 2;
+  static constexpr int NST = NST_CAP - NST_CAP % RING_MULT;
   // +1024: the dynamic smem base is realigned to 1024 bytes for the swizzle
   static constexpr int SMEM =
       1024 + NST * STAGE_BYTES + RED_BYTES + MERGE_BYTES + NST * 16 + CTL_BYTES;
-  static_assert(NST >= 2, "stage does not fit twice in shared memory");
-  static_assert(kDecodeConsumerWarps % HKV == 0, "unsupported kv head count");
+  static_assert(NST >= RING_MULT && NST % RING_MULT == 0, "stage ring does not fit");
+  static_assert(CW % HKV == 0, "unsupported kv head count");
+  static_assert(SMEM <= kDecodeSmemBudget, "shared memory over budget");
+  // a final cut piece keeps its own rows (o, lse) in the ring
+  static_assert(HQ * (kHeadDim + 1) * 4 <= NST * STAGE_BYTES, "own rows do not fit the ring");
   static_assert(G >= 1 && G <= 8, "group size must fit the N = 8 MMA dimension");
+  // combine weights (NPH per query head) and lse live in the merge scratch
+  static_assert((NPH + 1) * HQ <= MERGE_FLOATS, "combine weights do not fit");
 };
 
 struct DecodeCtl {
-  unsigned long long total;  // N, blocks of all sequences
+  unsigned long long ew_bar;     // mbarrier: the first piece's epilogue is ready
+  unsigned long long merge_bar;  // mbarrier: the final merge's bulk copies
+  unsigned long long total;   // N, blocks of all sequences
   long long first_prefix;    // global index of block 0 of first_b
   int first_b;               // sequence holding this CTA's first block
   int abort;                 // set by a wait that gave up
   int last;                  // this CTA merges the current cut sequence
+  // the first piece's publication, handed to the epilogue warp
+  long long ew_cs0, ew_cs1;
+  int ew_kind;  // 1: publish sequence ew_b (splits ew_cs0..ew_cs1, ew_pieces pieces); 0: none
+  int ew_b, ew_pieces;
+  // the current piece's sequence: splits pc_cs0..pc_cs1 hold its blocks, in
+  // pc_pieces non-empty pieces (consumer thread 0 works them out at the
+  // piece start, off the epilogue's path)
+  long long pc_cs0, pc_cs1;
+  int pc_pieces;
 };
+static_assert(sizeof(DecodeCtl) <= 256, "control words do not fit their 256 bytes");
 
 __device__ __forceinline__ int seq_blocks(const int32_t *ctx, int b) {
   const int n = __ldg(ctx + b);
@@ -222,6 +258,10 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // ---- output writers ---------------------------------------------------------
 
 __device__ __forceinline__ void store_out1(void *out, int out_f32, long long idx, float a) {
@@ -324,55 +364,79 @@ __device__ __forceinline__ void merge_row(const float *part_o, const float *part
              make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
 }
 
-// Log-sum-exp merge of all partials of sequence b by the 256 consumer
+// Log-sum-exp merge of all partials of sequence b by the NT consumer
 // threads of one CTA, when the pieces are few enough for their weights to fit
-// in shared memory (k <= MAXP, every split of c0..c1 non-empty): one round of
-// loads brings every (piece, head) lse into `w`; each head's weights
-// exp(lse - M) / sum are formed there; then each (head, 4 dims) item loads
-// its k partial rows eight at a time.  Returns false (nothing done) when the
-// pieces do not fit; the caller then merges row by row with merge_row.
-template <int HQ, int MAXP>
+// in shared memory (k <= MAXP, every split of c0..c1 non-empty).  Work item =
+// (head, 4 dims).  The first partial rows of a thread's first items (eight
+// rows of one item, or four of two) are loaded together with the (piece,
+// head) lse values, so that for few pieces the merge costs one round of
+// global loads; the weights exp(lse - M) / sum
+// are formed in `w` meanwhile.  The piece of split c_own (if any) is read
+// from shared memory (own_o, own_lse) instead of the workspace.  Returns
+// false (nothing done) when the pieces do not fit; the caller then merges row
+// by row with merge_row.
+template <int HQ, int MAXP, int NT>
 __device__ bool merge_sequence_block(const DecodeParams &p, int b, long long c0, long long c1,
-                                     long long S, long long N, float *w, int ct, int nthreads,
-                                     int bar_id) {
+                                     long long S, long long N, float *w, int ct, int bar_id,
+                                     long long c_own, const float *own_o, const float *own_lse) {
   const long long k = c1 - c0 + 1;
   if (N < S || k > MAXP) return false;
-  auto row_of = [&](long long i, int h) -> long long {
+  constexpr int ITEMS = HQ * (kHeadDim / 4);
+  constexpr int PRE = ITEMS > NT ? 2 : 1;  // preloaded items per thread
+  constexpr int ROWS = 8 / PRE;            // preloaded rows per item
+  const int kk = (int)k;
+  auto row_of = [&](int i, int h) -> long long {
     const long long cc = c0 + i;
     return (cc * 2 + (i == 0 ? 1 : 0)) * HQ + h;
   };
-  for (int e = ct; e < (int)k * HQ; e += nthreads)
-    w[e] = __ldcg(p.part_lse + row_of(e / HQ, e % HQ));
-  named_barrier(bar_id, nthreads);
-  for (int h = ct; h < HQ; h += nthreads) {
+  auto load_row = [&](int i, int h, int d) -> float4 {
+    return c0 + i == c_own
+               ? *reinterpret_cast<const float4 *>(own_o + h * kHeadDim + d)
+               : __ldcg(reinterpret_cast<const float4 *>(p.part_o + row_of(i, h) * kHeadDim + d));
+  };
+  float4 pre[PRE][ROWS];
+#pragma unroll
+  for (int t = 0; t < PRE; ++t) {
+    const int item = ct + t * NT;
+    const int h = item / (kHeadDim / 4), d = (item % (kHeadDim / 4)) * 4;
+#pragma unroll
+    for (int u = 0; u < ROWS; ++u)
+      pre[t][u] = item < ITEMS && u < kk ? load_row(u, h, d) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int e = ct; e < kk * HQ; e += NT)
+    w[e] = c0 + e / HQ == c_own ? own_lse[e % HQ] : __ldcg(p.part_lse + row_of(e / HQ, e % HQ));
+  named_barrier(bar_id, NT);
+  for (int h = ct; h < HQ; h += NT) {
     float M = -INFINITY;
-    for (int i = 0; i < (int)k; ++i) M = fmaxf(M, w[i * HQ + h]);
+    for (int i = 0; i < kk; ++i) M = fmaxf(M, w[i * HQ + h]);
     float W = 0.f;
-    for (int i = 0; i < (int)k; ++i) {
+    for (int i = 0; i < kk; ++i) {
       const float lse = w[i * HQ + h];
       const float e = lse == -INFINITY ? 0.f : __expf(lse - M);
       w[i * HQ + h] = e;
       W += e;
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
-    for (int i = 0; i < (int)k; ++i) w[i * HQ + h] *= inv;
+    for (int i = 0; i < kk; ++i) w[i * HQ + h] *= inv;
   }
-  named_barrier(bar_id, nthreads);
-  for (int item = ct; item < HQ * (kHeadDim / 4); item += nthreads) {
+  named_barrier(bar_id, NT);
+  for (int item = ct, t = 0; item < ITEMS; item += NT, ++t) {
     const int h = item / (kHeadDim / 4);
     const int d = (item % (kHeadDim / 4)) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < (int)k; i0 += 8) {
-      float4 v[8];
+    for (int i0 = 0; i0 < kk; i0 += ROWS) {
+      float4 v[ROWS];
+      if (i0 == 0 && t < PRE) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        v[u] = i0 + u < (int)k
-                   ? __ldcg(reinterpret_cast<const float4 *>(p.part_o + row_of(i0 + u, h) * kHeadDim +
-                                                             d))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < ROWS; ++u) v[u] = t == 0 ? pre[0][u] : pre[PRE - 1][u];
+      } else {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (i0 + u < (int)k) {
+        for (int u = 0; u < ROWS; ++u)
+          v[u] = i0 + u < kk ? load_row(i0 + u, h, d) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < ROWS; ++u) {
+        if (i0 + u < kk) {
           const float wu = w[(i0 + u) * HQ + h];
           acc.x += wu * v[u].x;
           acc.y += wu * v[u].y;
@@ -380,6 +444,75 @@ __device__ bool merge_sequence_block(const DecodeParams &p, int b, long long c0,
           acc.w += wu * v[u].w;
         }
       }
+    }
+    store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d, acc);
+  }
+  return true;
+}
+
+// The same merge with the other pieces' partial rows brought into shared
+// memory (`buf`, 16-byte aligned, `buf_bytes` long) by one bulk copy per
+// piece, so that any k that fits costs one round trip; the lse values come
+// with ordinary loads meanwhile.  Needs every split of c0..c1 non-empty
+// (N >= S), k <= MAXP and room in `buf`, else returns false having done
+// nothing.  c_own (always in c0..c1 here) is read from own_o / own_lse.
+template <int HQ, int MAXP, int NT>
+__device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, long long c1,
+                                    long long S, long long N, float *w, int ct, int bar_id,
+                                    long long c_own, const float *own_o, const float *own_lse,
+                                    float *buf, long long buf_bytes, uint32_t mbar,
+                                    volatile int *abort_flag) {
+  constexpr int ROW_FLOATS = HQ * kHeadDim;  // one piece: HQ rows of o
+  const long long k = c1 - c0 + 1;
+  if (N < S || k > MAXP || k * ROW_FLOATS * 4 > buf_bytes) return false;
+  const int kk = (int)k;
+  auto row0 = [&](int i) -> long long {  // first workspace row of piece i
+    const long long cc = c0 + i;
+    return (cc * 2 + (i == 0 ? 1 : 0)) * HQ;
+  };
+  if (ct == 0) {
+    // the ring was last read through the generic proxy, and the partials
+    // were acquired through it; the copies below go through the async proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    mbar_arrive_expect_tx(mbar, (uint32_t)((kk - 1) * ROW_FLOATS * 4));
+    const uint64_t pol = l2_policy_evict_first();
+    for (int i = 0; i < kk; ++i)
+      if (c0 + i != c_own)
+        bulk_load(smem_addr(buf + (long long)i * ROW_FLOATS), p.part_o + row0(i) * kHeadDim,
+                  ROW_FLOATS * 4, mbar, pol);
+  }
+  for (int e = ct; e < kk * HQ; e += NT)
+    w[e] = c0 + e / HQ == c_own ? own_lse[e % HQ] : __ldcg(p.part_lse + row0(e / HQ) + e % HQ);
+  named_barrier(bar_id, NT);
+  for (int h = ct; h < HQ; h += NT) {
+    float M = -INFINITY;
+    for (int i = 0; i < kk; ++i) M = fmaxf(M, w[i * HQ + h]);
+    float W = 0.f;
+    for (int i = 0; i < kk; ++i) {
+      const float lse = w[i * HQ + h];
+      const float e = lse == -INFINITY ? 0.f : __expf(lse - M);
+      w[i * HQ + h] = e;
+      W += e;
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    for (int i = 0; i < kk; ++i) w[i * HQ + h] *= inv;
+  }
+  named_barrier(bar_id, NT);
+  // every consumer thread waits for the copies (warp-uniform; bounded)
+  __all_sync(0xffffffffu, mbar_wait(mbar, 0, abort_flag, p.err));
+  for (int item = ct; item < HQ * (kHeadDim / 4); item += NT) {
+    const int h = item / (kHeadDim / 4);
+    const int d = (item % (kHeadDim / 4)) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < kk; ++i) {
+      const float wi = w[i * HQ + h];
+      const float4 v = *reinterpret_cast<const float4 *>(
+          (c0 + i == c_own ? own_o : buf + (long long)i * ROW_FLOATS) + h * kHeadDim + d);
+      acc.x += wi * v.x;
+      acc.y += wi * v.y;
+      acc.z += wi * v.z;
+      acc.w += wi * v.w;
     }
     store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d, acc);
   }
@@ -433,7 +566,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // ---- 2. block-wide scan of sequence block counts: find the sequence that
   //         holds block `lo`; zero the rows of empty sequences this CTA owns.
   {
-    __shared__ long long warp_tot[kDecodeThreads / 32];
+    __shared__ long long warp_tot[kDecodeWarps];
     long long running = 0;
     for (int base = 0; base < p.batch; base += blockDim.x) {
       const int b = base + tid;
@@ -481,8 +614,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < S::NST; ++i) {
       mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, kDecodeConsumerWarps);
+      mbar_init(empty0 + 8 * i, HKV);  // the Hkv consumer warps of the slot's phase
     }
+    mbar_init(smem_addr(&ctl->ew_bar), 1);
+    mbar_init(smem_addr(&ctl->merge_bar), 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -516,7 +651,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       // all block-table entries of the chunk in one round of loads
       const bool in_row = lane < count && lj < p.bt_stride;
       const long long phys = in_row ? __ldg(p.block_tables + (long long)lb * p.bt_stride + lj) : -1;
-      const bool pfirst = (gb + lane == lo) || (lj == 0);
+      // the q rows go with the first NPH stages of every piece: each consumer
+      // warp reads them from its own first stage of the piece
+      const bool with_q = min(gb + lane - lo, (long long)lj) < S::NPH;
       for (int i = 0; i < count; ++i, ++issued) {
         if ((int)(issued % kDecodeProducerWarps) != pw) continue;
         const int st = (int)(issued % S::NST);
@@ -529,11 +666,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
         const long long ph_i = __shfl_sync(0xffffffffu, phys, i);
         const int b_i = __shfl_sync(0xffffffffu, lb, i);
-        const bool first_i = __shfl_sync(0xffffffffu, pfirst ? 1 : 0, i) != 0;
+        const bool q_i = __shfl_sync(0xffffffffu, with_q ? 1 : 0, i) != 0;
         const bool row_i = __shfl_sync(0xffffffffu, in_row ? 1 : 0, i) != 0;
         if (lane == 0) {
           const bool ok = ph_i >= 0 && ph_i < p.num_blocks;
-          const uint32_t bytes = (ok ? 2u * S::KV_BYTES : 0u) + (first_i ? S::Q_BYTES : 0u);
+          const uint32_t bytes = (ok ? 2u * S::KV_BYTES : 0u) + (q_i ? S::Q_BYTES : 0u);
           const uint32_t dst = stage0 + st * S::STAGE_BYTES;
           const uint32_t bar = full0 + 8 * st;
           mbar_arrive_expect_tx(bar, bytes);
@@ -553,7 +690,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             // outside the pool: reported, not read
             report(p.err, row_i ? PA_DEVERR_BLOCK_INDEX : PA_DEVERR_SHAPE);
           }
-          if (first_i)
+          if (q_i)
             bulk_load(dst + 2 * S::KV_BYTES, p.q + (long long)b_i * S::HQ * kHeadDim, S::Q_BYTES,
                       bar, pol_q);
         }
@@ -573,13 +710,38 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     return;
   }
 
-  // ---- 5. consumers -----------------------------------------------------------
-  const int cw = warp - kDecodeProducerWarps;  // consumer warp 0..7
+  if (warp == kDecodeEpilogueWarp) {
+    // ---- 5a. epilogue warp: publishes the CTA's first piece when it is a
+    //          cut one (fence, arrival; the merge too if it comes last), so
+    //          that the consumers do not wait on those global round trips.
+    const bool got = __all_sync(0xffffffffu,
+                                mbar_wait(smem_addr(&ctl->ew_bar), 0, abort_flag, p.err));
+    if (!got || ctl->ew_kind == 0) return;
+    const int b = ctl->ew_b;
+    const long long cs0 = ctl->ew_cs0, cs1 = ctl->ew_cs1;
+    int last = 0;
+    if (lane == 0) {
+      // the consumers' partial rows are ordered before this by the mbarrier
+      __threadfence();
+      last = atomicAdd(p.counters + cs1, 1) == ctl->ew_pieces - 1;
+    }
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+      __threadfence();
+      for (int h = 0; h < S::HQ; ++h)
+        merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * S::HQ + h, S::HQ, h, cs0,
+                  cs1, nsplit, N, lane);
+      if (lane == 0) p.counters[cs1] = 0;
+    }
+    return;
+  }
+
+  // ---- 5b. consumers ----------------------------------------------------------
+  const int cw = warp - kDecodeFirstConsumerWarp;  // consumer warp 0..CW-1
   const int g = cw % HKV;     // kv head of this warp
   const int ph = cw / HKV;    // stage phase of this warp
   const int gid = lane >> 2;  // fragment row group
   const int qd = lane & 3;    // fragment column pair
-  const int ct = tid - 32 * kDecodeProducerWarps;  // consumer thread index 0..255
+  const int ct = tid - 32 * kDecodeFirstConsumerWarp;  // consumer thread index
   // this warp's kv head inside the TMA boxes: box group, row offset
   const int gpair = g / S::HB, gsub = g % S::HB;
   const float cl2 = p.qk_scale_log2;
@@ -595,287 +757,389 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
 
+  bool ew_signalled = false;  // the epilogue warp has been told about the first piece
+  // consumer thread 0: the current piece's split words are in ctl
+  bool pc_done = false;
+  auto piece_splits = [&](long long gb, int j, int n) {
+    const long long P = gb - j;  // global index of block 0 of the sequence
+    const long long cs0 = split_of_block(P, nsplit, N);
+    const long long cs1 = split_of_block(P + n - 1, nsplit, N);
+    long long pieces = cs1 - cs0 + 1;
+    if (N < nsplit) {
+      pieces = 1;
+      for (long long cc = cs0 + 1; cc <= cs1; ++cc)
+        pieces += split_begin(cc, nsplit, N) < split_begin(cc + 1, nsplit, N) ? 1 : 0;
+    }
+    ctl->pc_cs0 = cs0;
+    ctl->pc_cs1 = cs1;
+    ctl->pc_pieces = (int)pieces;
+    pc_done = true;
+  };
+  bool need_q = true;  // the q rows of the current piece are not loaded yet
   int wb = first_b;
   int wctx = __ldg(p.context_lens + wb);
   int wj = (int)(lo - first_prefix);
-  int piece_j0 = wj;
-  long long it = 0;
-  int chunk_left = 0, chunk_pos = 0;
-  int lb = 0, lj = 0, lctx = 0;
-  for (long long gb = lo; gb < hi; ++gb, ++it) {
-    if (chunk_left == 0) {
-      chunk_left = walk_chunk(p.context_lens, p.batch, wb, wctx, wj, hi - gb, lane, lb, lj, lctx);
-      chunk_pos = 0;
-      if (chunk_left == 0) break;  // same decision in every consumer warp and the producer
-    }
-    const int b = __shfl_sync(0xffffffffu, lb, chunk_pos);
-    const int j = __shfl_sync(0xffffffffu, lj, chunk_pos);
-    const int ctx = __shfl_sync(0xffffffffu, lctx, chunk_pos);
-    const int n = ceil_div_blocks(ctx);
-    ++chunk_pos;
-    --chunk_left;
-    const bool piece_first = (gb == lo) || (j == 0);
-    const bool piece_last = (gb == hi - 1) || (j == n - 1);
-    const int sidx = (int)(it % S::NST);
-    const uint32_t sbase = stage0 + sidx * S::STAGE_BYTES;
-    // warp-uniform: the collective instructions below need every lane
-    const bool have = __all_sync(
-        0xffffffffu, mbar_wait(full0 + 8 * sidx, (int)((it / S::NST) & 1), abort_flag, p.err));
-    if (piece_first) {
-      piece_j0 = j;
+  long long it0 = 0;  // stage index of the chunk's first block
+  for (long long gb0 = lo; gb0 < hi;) {
+    // the next (up to) 32 blocks: lane L describes block gb0 + L
+    int lb = 0, lj = 0, lctx = 0;
+    const int count =
+        walk_chunk(p.context_lens, p.batch, wb, wctx, wj, hi - gb0, lane, lb, lj, lctx);
+    if (count == 0) break;  // same decision in every consumer warp and the producer
+    // A warp visits only the blocks that concern it: its own stages (index
+    // = ph mod NPH) and every piece end (all warps combine there).
+    const bool in_chunk = lane < count;
+    const int lnb = ceil_div_blocks(lctx);
+    const unsigned m_last =
+        __ballot_sync(0xffffffffu, in_chunk && (gb0 + lane == hi - 1 || lj == lnb - 1));
+    const unsigned m_mine =
+        __ballot_sync(0xffffffffu, in_chunk && (int)((it0 + lane) % S::NPH) == ph);
+    unsigned todo = m_last | m_mine;
+    while (todo) {
+      const int pos = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int b = __shfl_sync(0xffffffffu, lb, pos);
+      const int j = __shfl_sync(0xffffffffu, lj, pos);
+      const int ctx = __shfl_sync(0xffffffffu, lctx, pos);
+      const int n = ceil_div_blocks(ctx);
+      const long long gb = gb0 + pos, it = it0 + pos;
+      const bool piece_last = (m_last >> pos) & 1u;
+      if ((m_mine >> pos) & 1u) {
+        const int sidx = (int)(it % S::NST);
+        const uint32_t sbase = stage0 + sidx * S::STAGE_BYTES;
+        // warp-uniform: the collective instructions below need every lane
+        const bool have = __all_sync(
+            0xffffffffu, mbar_wait(full0 + 8 * sidx, (int)((it / S::NST) & 1), abort_flag, p.err));
+        if (need_q) {
+          // this warp's first stage of the piece: it carries the q rows
+          need_q = false;
+          if (ct == 0 && !pc_done) piece_splits(gb, j, n);
+          if (have) {
+            const uint32_t qrow = sbase + 2 * S::KV_BYTES + (g * G + gid) * kHeadDim * 2;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              uint32_t x0 = 0, x1 = 0;
+              if (gid < G) {
+                asm volatile("ld.shared.u32 %0, [%1];"
+                             : "=r"(x0)
+                             : "r"(qrow + (16 * ks + 2 * qd) * 2)
+                             : "memory");
+                asm volatile("ld.shared.u32 %0, [%1];"
+                             : "=r"(x1)
+                             : "r"(qrow + (16 * ks + 8 + 2 * qd) * 2)
+                             : "memory");
+              }
+              qf[ks][0] = x0;
+              qf[ks][1] = x1;
+            }
+          }
+        }
+        const int valid = min(kBlockSize, ctx - j * kBlockSize);  // keys of this block (>= 1)
+        if (have) {
+          // boxes of this head group: K at kb (+BOX_BYTES for dims 64..127), V at vb
+          const uint32_t kb = sbase + gpair * 2 * S::BOX_BYTES;
+          const uint32_t vb = sbase + S::KV_BYTES + gpair * 2 * S::BOX_BYTES;
+          // S^T = K . Q^T, two accumulation chains over the eight 16-dim k-steps
+          float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            const int mi = lane >> 3, r = lane & 7;
+            const int t = r + ((mi & 1) << 3);
+            const int row = t * S::HB + gsub;  // 128-byte row of token t, this head
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const int chunk = ((ks & 3) << 1) + (mi >> 1);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(kb + (ks >> 2) * S::BOX_BYTES + swz(row, chunk), a0, a1, a2, a3);
+              if (ks & 1)
+                mma_bf16(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              else
+                mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            }
+          }
+          // scores: [0] (token gid, head 2qd) [1] (gid, 2qd+1) [2] (gid+8, 2qd) [3] (gid+8, 2qd+1)
+          const bool v0 = gid < valid, v1 = gid + 8 < valid;
+          const float s0 = v0 ? sa[0] + sb[0] : -INFINITY;
+          const float s1 = v0 ? sa[1] + sb[1] : -INFINITY;
+          const float s2 = v1 ? sa[2] + sb[2] : -INFINITY;
+          const float s3 = v1 ? sa[3] + sb[3] : -INFINITY;
+          float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+            x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+          }
+          // token 0 of every block is a key, so x0, x1 are finite
+          const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+          const float al0 = exp2f((m0 - n0) * cl2), al1 = exp2f((m1 - n1) * cl2);
+          m0 = n0;
+          m1 = n1;
+          const float c0 = n0 * cl2, c1 = n1 * cl2;
+          const float p0 = exp2f(fmaf(s0, cl2, -c0)), p1 = exp2f(fmaf(s1, cl2, -c1));
+          const float p2 = exp2f(fmaf(s2, cl2, -c0)), p3 = exp2f(fmaf(s3, cl2, -c1));
+          l0 = fmaf(l0, al0, p0 + p2);
+          l1 = fmaf(l1, al1, p1 + p3);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+          }
+          // P^T fragments, hi + lo bf16 split
+          const uint32_t hA = float2_to_bf16x2(p0, p1), hB = float2_to_bf16x2(p2, p3);
+          const float2 fA = bf16x2_to_float2(hA), fB = bf16x2_to_float2(hB);
+          const uint32_t lA = float2_to_bf16x2(p0 - fA.x, p1 - fA.y);
+          const uint32_t lB = float2_to_bf16x2(p2 - fB.x, p3 - fB.y);
+          const uint32_t bh0 = movm_t(hA), bh1 = movm_t(hB);
+          const uint32_t bl0 = movm_t(lA), bl1 = movm_t(lB);
+          if (valid < kBlockSize) {
+            // rows past the last key may hold anything (NaN): zero them so that
+            // 0-weight rows contribute exactly 0 to the MMA
+            for (int i = lane; i < (kBlockSize - valid) * 16; i += 32) {
+              const int t = valid + (i >> 4), ch = i & 15;
+              const uint32_t a = vb + (ch >> 3) * S::BOX_BYTES + swz(t * S::HB + gsub, ch & 7);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+            }
+            __syncwarp();
+          }
+          // O^T += V^T . P^T
+          {
+            const int mi = lane >> 3, r = lane & 7;
+            const int t = r + ((mi >> 1) << 3);
+            const int row = t * S::HB + gsub;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              const int chunk = 2 * mt + (mi & 1);  // 8-dim chunk 0..15
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_t(vb + (chunk >> 3) * S::BOX_BYTES + swz(row, chunk & 7), a0, a1, a2, a3);
+              mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+              mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+            }
+          }
+          // generic-proxy writes above must be ordered before the TMA that
+          // reuses this stage
+          if (valid < kBlockSize) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * sidx);  // one of the slot's Hkv readers
+      }
+      if (!piece_last) continue;
+
+      // ---- end of a piece: merge the warps of each kv head, write rows -------
+      if (ct == 0 && !pc_done) piece_splits(gb, j, n);  // warp 0 had no stage in the piece
+      const bool head_cut = gb - j < lo;  // the sequence starts before this CTA's blocks
+      const bool tail_cut = j < n - 1;
+      const bool whole = !head_cut && !tail_cut;
+      // A cut piece is the CTA's first piece (cut at its head) or its final
+      // one (cut at its tail); pieces in between are whole sequences.
+      const bool final_piece = gb == hi - 1;
+      // own rows of a final cut piece, kept in the ring (every stage consumed);
+      // the rest of the ring receives the other pieces' rows for the merge
+      float *own_o = reinterpret_cast<float *>(smem);
+      float *own_lse = own_o + S::HQ * kHeadDim;
+      const bool keep_own = !whole && final_piece;
+      float L0 = l0, L1 = l1;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        L0 += __shfl_xor_sync(0xffffffffu, L0, off);
+        L1 += __shfl_xor_sync(0xffffffffu, L1, off);
+      }
+      const long long slot_row = (c * 2 + (head_cut ? 0 : 1)) * S::HQ;
+      const int ha = 2 * qd, hb = 2 * qd + 1;  // heads of this lane's fragment columns
+      if constexpr (S::NPH == 1) {
+        // one warp per kv head: write straight from the fragments
+        if (keep_own) named_barrier(1, S::CW * 32);  // all warps are past the ring
+        const float ia = L0 > 0.f ? 1.f / L0 : 0.f, ib = L1 > 0.f ? 1.f / L1 : 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int d = 16 * mt + gid + 8 * half;
+            if (ha < G) {
+              const int qh = g * G + ha;
+              const float v = o[mt][2 * half] * ia;
+              if (whole) {
+                store_out1(p.out, p.out_f32, ((long long)b * S::HQ + qh) * kHeadDim + d, v);
+              } else {
+                p.part_o[(slot_row + qh) * kHeadDim + d] = v;
+                if (keep_own) own_o[qh * kHeadDim + d] = v;
+              }
+            }
+            if (hb < G) {
+              const int qh = g * G + hb;
+              const float v = o[mt][2 * half + 1] * ib;
+              if (whole) {
+                store_out1(p.out, p.out_f32, ((long long)b * S::HQ + qh) * kHeadDim + d, v);
+              } else {
+                p.part_o[(slot_row + qh) * kHeadDim + d] = v;
+                if (keep_own) own_o[qh * kHeadDim + d] = v;
+              }
+            }
+          }
+        }
+        if (!whole && gid == 0) {
+          const float lse_a = L0 > 0.f ? (m0 * cl2 + __log2f(L0)) * 0.69314718055994531f : -INFINITY;
+          const float lse_b = L1 > 0.f ? (m1 * cl2 + __log2f(L1)) * 0.69314718055994531f : -INFINITY;
+          if (ha < G) {
+            p.part_lse[slot_row + g * G + ha] = lse_a;
+            if (keep_own) own_lse[g * G + ha] = lse_a;
+          }
+          if (hb < G) {
+            p.part_lse[slot_row + g * G + hb] = lse_b;
+            if (keep_own) own_lse[g * G + hb] = lse_b;
+          }
+        }
+        if (!whole) named_barrier(1, S::CW * 32);
+      } else {
+        // several warps share a kv head: combine through shared memory
+        if (ha < G) {
+          float *ra = red + (cw * G + ha) * S::RED_FLOATS_PER_HEAD;
+          if (gid == 0) {
+            ra[S::RED_M] = m0 == -INFINITY ? -INFINITY : m0 * cl2;
+            ra[S::RED_L] = L0;
+          }
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            ra[16 * mt + gid] = o[mt][0];
+            ra[16 * mt + gid + 8] = o[mt][2];
+          }
+        }
+        if (hb < G) {
+          float *rb = red + (cw * G + hb) * S::RED_FLOATS_PER_HEAD;
+          if (gid == 0) {
+            rb[S::RED_M] = m1 == -INFINITY ? -INFINITY : m1 * cl2;
+            rb[S::RED_L] = L1;
+          }
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            rb[16 * mt + gid] = o[mt][1];
+            rb[16 * mt + gid + 8] = o[mt][3];
+          }
+        }
+        named_barrier(1, S::CW * 32);
+        // one thread per query head: the normalised weight of each of its NPH
+        // warps (into the merge scratch) and the piece's lse
+        float *cwt = mw;  // [NPH][HQ]
+        if (ct < S::HQ) {
+          const int qh = ct, gh = qh / G, h = qh % G;
+          float mk[S::NPH], M = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < S::NPH; ++k) {
+            mk[k] = red[((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + S::RED_M];
+            M = fmaxf(M, mk[k]);
+          }
+          float L = 0.f;
+#pragma unroll
+          for (int k = 0; k < S::NPH; ++k) {
+            mk[k] = mk[k] == -INFINITY ? 0.f : exp2f(mk[k] - M);
+            L += red[((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + S::RED_L] * mk[k];
+          }
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+          for (int k = 0; k < S::NPH; ++k) cwt[k * S::HQ + qh] = mk[k] * inv;
+          if (!whole) {
+            const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+            p.part_lse[slot_row + qh] = lse;
+            if (keep_own) own_lse[qh] = lse;
+          }
+        }
+        named_barrier(1, S::CW * 32);
+        for (int item = ct; item < S::HQ * (kHeadDim / 4); item += S::CW * 32) {
+          const int qh = item / (kHeadDim / 4);
+          const int d = (item % (kHeadDim / 4)) * 4;
+          const int gh = qh / G, h = qh % G;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < S::NPH; ++k) {
+            const float wk = cwt[k * S::HQ + qh];
+            const float4 v = *reinterpret_cast<const float4 *>(
+                red + ((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + d);
+            acc.x += wk * v.x;
+            acc.y += wk * v.y;
+            acc.z += wk * v.z;
+            acc.w += wk * v.w;
+          }
+          if (whole) {
+            store_out4(p.out, p.out_f32, ((long long)b * S::HQ + qh) * kHeadDim + d, acc);
+          } else {
+            *reinterpret_cast<float4 *>(p.part_o + (slot_row + qh) * kHeadDim + d) = acc;
+            if (keep_own) *reinterpret_cast<float4 *>(own_o + qh * kHeadDim + d) = acc;
+          }
+        }
+        named_barrier(1, S::CW * 32);
+      }
+
+      if (!whole && !final_piece) {
+        // the CTA's first piece: the epilogue warp publishes it (fence, arrival)
+        // while the consumers go on with the next piece
+        if (ct == 0) {
+          ctl->ew_kind = 1;
+          ctl->ew_b = b;
+          ctl->ew_cs0 = ctl->pc_cs0;
+          ctl->ew_cs1 = ctl->pc_cs1;
+          ctl->ew_pieces = ctl->pc_pieces;
+          mbar_arrive(smem_addr(&ctl->ew_bar));
+        }
+        ew_signalled = true;
+      }
+      if (!ew_signalled) {
+        // the CTA's first piece needs no publishing: release the epilogue warp
+        if (ct == 0) {
+          ctl->ew_kind = 0;
+          mbar_arrive(smem_addr(&ctl->ew_bar));
+        }
+        ew_signalled = true;
+      }
+      if (keep_own) {
+        // The final piece, cut: publish it; the last piece of the sequence to
+        // arrive merges.  Nothing follows the final piece, which the jump out
+        // of the loops makes explicit: the accumulators are dead and the merge
+        // may use their registers.  Every consumer thread is past a barrier
+        // since consumer thread 0 wrote the piece's split words.
+        const long long cs0 = ctl->pc_cs0, cs1 = ctl->pc_cs1;
+        const int pieces = ctl->pc_pieces;
+        if (ct == 0) {
+          __threadfence();  // release: the rows before the arrival
+          const bool last = atomicAdd(p.counters + cs1, 1) == pieces - 1;
+          if (last) fence_acq_rel_gpu();  // acquire the other pieces' rows
+          ctl->last = last;
+        }
+        named_barrier(1, S::CW * 32);
+        if (ctl->last) {
+          // consumer thread 0 acquired the partials before the last barrier
+          float *mbuf = own_lse + ((S::HQ + 3) & ~3);
+          const long long mbuf_bytes =
+              (long long)S::NST * S::STAGE_BYTES - (long long)(mbuf - own_o) * 4;
+          if (!merge_sequence_bulk<S::HQ, S::MERGE_MAX_PIECES, S::CW * 32>(
+                  p, b, cs0, cs1, nsplit, N, mw, ct, 1, c, own_o, own_lse, mbuf, mbuf_bytes,
+                  smem_addr(&ctl->merge_bar), abort_flag) &&
+              !merge_sequence_block<S::HQ, S::MERGE_MAX_PIECES, S::CW * 32>(
+                  p, b, cs0, cs1, nsplit, N, mw, ct, 1, c, own_o, own_lse))
+            for (int h = cw; h < S::HQ; h += S::CW)
+              merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * S::HQ + h, S::HQ, h,
+                        cs0, cs1, nsplit, N, lane);
+          if (ct == 0) p.counters[cs1] = 0;
+        }
+        goto consumers_done;
+      }
+      // the next piece starts from nothing
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
       m0 = m1 = -INFINITY;
       l0 = l1 = 0.f;
-      if (have) {
-        const uint32_t qrow = sbase + 2 * S::KV_BYTES + (g * G + gid) * kHeadDim * 2;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint32_t x0 = 0, x1 = 0;
-          if (gid < G) {
-            asm volatile("ld.shared.u32 %0, [%1];"
-                         : "=r"(x0)
-                         : "r"(qrow + (16 * ks + 2 * qd) * 2)
-                         : "memory");
-            asm volatile("ld.shared.u32 %0, [%1];"
-                         : "=r"(x1)
-                         : "r"(qrow + (16 * ks + 8 + 2 * qd) * 2)
-                         : "memory");
-          }
-          qf[ks][0] = x0;
-          qf[ks][1] = x1;
-        }
-      }
+      need_q = true;
+      pc_done = false;
     }
-    const int valid = min(kBlockSize, ctx - j * kBlockSize);  // keys of this block (>= 1)
-    if (have && (int)(it % S::NPH) == ph) {
-      // boxes of this head group: K at kb (+BOX_BYTES for dims 64..127), V at vb
-      const uint32_t kb = sbase + gpair * 2 * S::BOX_BYTES;
-      const uint32_t vb = sbase + S::KV_BYTES + gpair * 2 * S::BOX_BYTES;
-      // S^T = K . Q^T, two accumulation chains over the eight 16-dim k-steps
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const int mi = lane >> 3, r = lane & 7;
-        const int t = r + ((mi & 1) << 3);
-        const int row = t * S::HB + gsub;  // 128-byte row of token t, this head
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const int chunk = ((ks & 3) << 1) + (mi >> 1);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(kb + (ks >> 2) * S::BOX_BYTES + swz(row, chunk), a0, a1, a2, a3);
-          if (ks & 1)
-            mma_bf16(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-          else
-            mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-        }
-      }
-      // scores: [0] (token gid, head 2qd) [1] (gid, 2qd+1) [2] (gid+8, 2qd) [3] (gid+8, 2qd+1)
-      const bool v0 = gid < valid, v1 = gid + 8 < valid;
-      const float s0 = v0 ? sa[0] + sb[0] : -INFINITY;
-      const float s1 = v0 ? sa[1] + sb[1] : -INFINITY;
-      const float s2 = v1 ? sa[2] + sb[2] : -INFINITY;
-      const float s3 = v1 ? sa[3] + sb[3] : -INFINITY;
-      float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
-        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
-      }
-      // token 0 of every block is a key, so x0, x1 are finite
-      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-      const float al0 = exp2f((m0 - n0) * cl2), al1 = exp2f((m1 - n1) * cl2);
-      m0 = n0;
-      m1 = n1;
-      const float c0 = n0 * cl2, c1 = n1 * cl2;
-      const float p0 = exp2f(fmaf(s0, cl2, -c0)), p1 = exp2f(fmaf(s1, cl2, -c1));
-      const float p2 = exp2f(fmaf(s2, cl2, -c0)), p3 = exp2f(fmaf(s3, cl2, -c1));
-      l0 = fmaf(l0, al0, p0 + p2);
-      l1 = fmaf(l1, al1, p1 + p3);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
-      }
-      // P^T fragments, hi + lo bf16 split
-      const uint32_t hA = float2_to_bf16x2(p0, p1), hB = float2_to_bf16x2(p2, p3);
-      const float2 fA = bf16x2_to_float2(hA), fB = bf16x2_to_float2(hB);
-      const uint32_t lA = float2_to_bf16x2(p0 - fA.x, p1 - fA.y);
-      const uint32_t lB = float2_to_bf16x2(p2 - fB.x, p3 - fB.y);
-      const uint32_t bh0 = movm_t(hA), bh1 = movm_t(hB);
-      const uint32_t bl0 = movm_t(lA), bl1 = movm_t(lB);
-      if (valid < kBlockSize) {
-        // rows past the last key may hold anything (NaN): zero them so that
-        // 0-weight rows contribute exactly 0 to the MMA
-        for (int i = lane; i < (kBlockSize - valid) * 16; i += 32) {
-          const int t = valid + (i >> 4), ch = i & 15;
-          const uint32_t a = vb + (ch >> 3) * S::BOX_BYTES + swz(t * S::HB + gsub, ch & 7);
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
-        }
-        __syncwarp();
-      }
-      // O^T += V^T . P^T
-      {
-        const int mi = lane >> 3, r = lane & 7;
-        const int t = r + ((mi >> 1) << 3);
-        const int row = t * S::HB + gsub;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int chunk = 2 * mt + (mi & 1);  // 8-dim chunk 0..15
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vb + (chunk >> 3) * S::BOX_BYTES + swz(row, chunk & 7), a0, a1, a2, a3);
-          mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
-          mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
-        }
-      }
-      // generic-proxy writes above must be ordered before the TMA that
-      // reuses this stage
-      if (valid < kBlockSize) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * sidx);
-
-    if (!piece_last) continue;
-
-    // ---- end of a piece: merge the warps of each kv head, write rows -------
-    const bool head_cut = piece_j0 > 0;
-    const bool tail_cut = j < n - 1;
-    const bool whole = !head_cut && !tail_cut;
-    float L0 = l0, L1 = l1;
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      L0 += __shfl_xor_sync(0xffffffffu, L0, off);
-      L1 += __shfl_xor_sync(0xffffffffu, L1, off);
-    }
-    const long long slot_row = (c * 2 + (head_cut ? 0 : 1)) * S::HQ;
-    const int ha = 2 * qd, hb = 2 * qd + 1;  // heads of this lane's fragment columns
-    if constexpr (S::NPH == 1) {
-      // one warp per kv head: write straight from the fragments
-      const float ia = L0 > 0.f ? 1.f / L0 : 0.f, ib = L1 > 0.f ? 1.f / L1 : 0.f;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int d = 16 * mt + gid + 8 * half;
-          if (ha < G) {
-            const long long row = whole ? (long long)b * S::HQ + g * G + ha : slot_row + g * G + ha;
-            const float v = o[mt][2 * half] * ia;
-            if (whole)
-              store_out1(p.out, p.out_f32, row * kHeadDim + d, v);
-            else
-              p.part_o[row * kHeadDim + d] = v;
-          }
-          if (hb < G) {
-            const long long row = whole ? (long long)b * S::HQ + g * G + hb : slot_row + g * G + hb;
-            const float v = o[mt][2 * half + 1] * ib;
-            if (whole)
-              store_out1(p.out, p.out_f32, row * kHeadDim + d, v);
-            else
-              p.part_o[row * kHeadDim + d] = v;
-          }
-        }
-      }
-      if (!whole && gid == 0) {
-        if (ha < G)
-          p.part_lse[slot_row + g * G + ha] =
-              L0 > 0.f ? (m0 * cl2 + __log2f(L0)) * 0.69314718055994531f : -INFINITY;
-        if (hb < G)
-          p.part_lse[slot_row + g * G + hb] =
-              L1 > 0.f ? (m1 * cl2 + __log2f(L1)) * 0.69314718055994531f : -INFINITY;
-      }
-    } else {
-      // several warps share a kv head: combine through shared memory
-      if (ha < G) {
-        float *ra = red + (cw * G + ha) * S::RED_FLOATS_PER_HEAD;
-        if (gid == 0) {
-          ra[0] = m0 == -INFINITY ? -INFINITY : m0 * cl2;
-          ra[1] = L0;
-        }
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          ra[2 + 16 * mt + gid] = o[mt][0];
-          ra[2 + 16 * mt + gid + 8] = o[mt][2];
-        }
-      }
-      if (hb < G) {
-        float *rb = red + (cw * G + hb) * S::RED_FLOATS_PER_HEAD;
-        if (gid == 0) {
-          rb[0] = m1 == -INFINITY ? -INFINITY : m1 * cl2;
-          rb[1] = L1;
-        }
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          rb[2 + 16 * mt + gid] = o[mt][1];
-          rb[2 + 16 * mt + gid + 8] = o[mt][3];
-        }
-      }
-      named_barrier(1, kDecodeConsumerWarps * 32);
-      for (int e = ct * 2; e < S::HQ * kHeadDim; e += kDecodeConsumerWarps * 32 * 2) {
-        const int qh = e / kHeadDim;
-        const int d = e % kHeadDim;
-        const int gh = qh / G;
-        const int h = qh % G;
-        float M = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < S::NPH; ++k)
-          M = fmaxf(M, red[((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD]);
-        float L = 0.f, oa = 0.f, ob = 0.f;
-#pragma unroll
-        for (int k = 0; k < S::NPH; ++k) {
-          const float *r = red + ((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD;
-          const float w = r[0] == -INFINITY ? 0.f : exp2f(r[0] - M);
-          L += r[1] * w;
-          oa += r[2 + d] * w;
-          ob += r[3 + d] * w;
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        if (whole) {
-          store_out2(p.out, p.out_f32, ((long long)b * S::HQ + qh) * kHeadDim + d, oa * inv,
-                     ob * inv);
-        } else {
-          *reinterpret_cast<float2 *>(p.part_o + (slot_row + qh) * kHeadDim + d) =
-              make_float2(oa * inv, ob * inv);
-          if (d == 0)
-            p.part_lse[slot_row + qh] =
-                L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
-        }
-      }
-      named_barrier(1, kDecodeConsumerWarps * 32);
-    }
-
-    if (!whole) {
-      // publish this partial; the CTA completing the sequence's set merges it
-      __threadfence();
-      named_barrier(1, kDecodeConsumerWarps * 32);
-      const long long P = gb - j;  // global index of block 0 of b
-      const long long cs0 = split_of_block(P, nsplit, N);
-      const long long cs1 = split_of_block(P + n - 1, nsplit, N);
-      if (ct == 0) {
-        // splits holding a piece of b (all of c0..c1 unless some split is empty)
-        long long pieces = cs1 - cs0 + 1;
-        if (N < nsplit) {
-          pieces = 1;
-          for (long long cc = cs0 + 1; cc <= cs1; ++cc)
-            pieces += split_begin(cc, nsplit, N) < split_begin(cc + 1, nsplit, N) ? 1 : 0;
-        }
-        const int prev = atomicAdd(p.counters + cs1, 1);
-        ctl->last = prev == (int)pieces - 1;
-      }
-      named_barrier(1, kDecodeConsumerWarps * 32);
-      if (ctl->last) {
-        __threadfence();
-        if (!merge_sequence_block<S::HQ, S::MERGE_MAX_PIECES>(p, b, cs0, cs1, nsplit, N, mw, ct,
-                                                               kDecodeConsumerWarps * 32, 1))
-          for (int h = cw; h < S::HQ; h += kDecodeConsumerWarps)
-            merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * S::HQ + h, S::HQ, h,
-                      cs0, cs1, nsplit, N, lane);
-        if (ct == 0) p.counters[cs1] = 0;
-      }
-      named_barrier(1, kDecodeConsumerWarps * 32);
-    }
+    gb0 += count;
+    it0 += count;
+  }
+consumers_done:
+  if (!ew_signalled && ct == 0) {
+    // the walk stopped before any piece ended (inconsistent input)
+    ctl->ew_kind = 0;
+    mbar_arrive(smem_addr(&ctl->ew_bar));
   }
 }
 

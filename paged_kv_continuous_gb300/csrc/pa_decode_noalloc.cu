@@ -68,7 +68,12 @@ extern "C" pa_status pa_decode_noalloc(void *out, int32_t out_dtype, const void 
   int device = -1;
   const pa_status st = check_decode_request(r, &device);
   if (st != PA_OK || batch == 0) return st;
-  // the partials and counters of `splits` splits must fit in the fixed array
+  // the partials and counters of `splits` splits must fit in the fixed array;
+  // a default split count is lowered to the largest that fits
+  if (num_splits == 0)
+    while (r.splits > 1 &&
+           pa_decode_workspace_size(r.splits, num_q_heads, head_dim) > kStaticScratchBytes)
+      --r.splits;
   const size_t need = pa_decode_workspace_size(r.splits, num_q_heads, head_dim);
   if (need == 0 || need > kStaticScratchBytes) return PA_ERR_WORKSPACE;
   void *scratch = nullptr;

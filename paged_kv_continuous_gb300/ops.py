@@ -52,7 +52,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_decode_workspace_size.restype = sz
     lib.pa_decode_workspace_size.argtypes = [i32, i32, i32]
     lib.pa_decode_default_splits.restype = i32
-    lib.pa_decode_default_splits.argtypes = [i32]
+    lib.pa_decode_default_splits.argtypes = [i32, i32, i32]
     lib.pa_decode.restype = i32
     lib.pa_decode.argtypes = [P, i32, P, P, P, i64, P, i32, P, i32, i32, i32, i32, i32, f32,
                               i32, P, sz, P]
@@ -135,13 +135,14 @@ def _device_index(device=None) -> int:
     return int(device)
 
 
-def default_splits(device=None) -> int:
-    return int(lib.pa_decode_default_splits(_device_index(device)))
+def default_splits(num_q_heads: int, num_kv_heads: int, device=None) -> int:
+    return int(lib.pa_decode_default_splits(_device_index(device), num_q_heads, num_kv_heads))
 
 
-def decode_workspace(num_q_heads: int, num_splits: int = 0, head_dim: int = 128, device=None):
-    """A zeroed workspace for pa_decode (the error word must start at zero)."""
-    s = num_splits if num_splits > 0 else default_splits(device)
+def decode_workspace(num_q_heads: int, num_kv_heads: int, num_splits: int = 0,
+                     head_dim: int = 128, device=None):
+    """A zeroed workspace for pa_decode (error word and counters start at zero)."""
+    s = num_splits if num_splits > 0 else default_splits(num_q_heads, num_kv_heads, device)
     n = int(lib.pa_decode_workspace_size(s, num_q_heads, head_dim))
     if n == 0:
         raise PagedAttentionError("bad workspace request")
@@ -165,7 +166,7 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
     if out is None:
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
     if workspace is None:
-        workspace = decode_workspace(Hq, num_splits, D, q.device)
+        workspace = decode_workspace(Hq, Hkv, num_splits, D, q.device)
     _check(lib.pa_decode(_ptr(out), _out_code(out.dtype), _ptr(q), _ptr(k_cache),
                          _ptr(v_cache), NB, _ptr(block_tables), block_tables.stride(0),
                          _ptr(context_lens), B, Hq, Hkv, D, bs, float(scale), int(num_splits),

@@ -38,7 +38,7 @@ class Dev:
             self.kc, self.vc = to_dev_bf16(kc), to_dev_bf16(vc)
 
     def decode(self, ops, out_dtype=torch.bfloat16, num_splits=0):
-        ws = ops.decode_workspace(self.w.num_q_heads, num_splits)
+        ws = ops.decode_workspace(self.w.num_q_heads, self.w.num_kv_heads, num_splits)
         out = ops.decode(self.q, self.kc, self.vc, self.tables, self.ctx, self.w.scale,
                          out_dtype=out_dtype, num_splits=num_splits, workspace=ws)
         torch.cuda.synchronize()
@@ -188,7 +188,7 @@ def test_decode_bad_block_index_sets_error_without_fault(ops):
     bad = w.block_tables.copy()
     bad[1, 1] = w.num_blocks + 5
     bad[0, 0] = -3
-    ws = ops.decode_workspace(w.num_q_heads, 4)
+    ws = ops.decode_workspace(w.num_q_heads, w.num_kv_heads, 4)
     ops.decode(d.q, d.kc, d.vc, to_dev_i32(bad), d.ctx, w.scale, num_splits=4, workspace=ws)
     torch.cuda.synchronize()
     assert ops.read_error_word(ws) & ops.DEVERR_BLOCK_INDEX
@@ -237,7 +237,7 @@ def test_merge_entry_point_against_oracle_partials(ops):
             slot = 1 if c == c0 else 0
             part_o[c, slot] = o[b]
             part_l[c, slot] = l[b]
-    ws = ops.decode_workspace(Hq, S)
+    ws = ops.decode_workspace(Hq, w.num_kv_heads, S)
     hdr = 256 + 4 * 4096                      # error word + fixed counter area
     po_bytes = ((S * 2 * Hq * D * 4 + 255) // 256) * 256
     ws[hdr:hdr + part_o.nbytes].copy_(torch.from_numpy(part_o.view(np.uint8).reshape(-1)))
@@ -258,7 +258,7 @@ def test_decode_reuses_one_workspace_across_calls(ops):
     """The in-kernel merge leaves its arrival counters at zero: one workspace
     serves many consecutive calls (different split counts, different
     batches) and every call matches the oracle."""
-    ws = ops.decode_workspace(12, 500)
+    ws = ops.decode_workspace(12, 2, 500)
     torch.cuda.synchronize()
     for name, splits in [("cb_decode_b64", 500), ("qwen_decode_b8", 97), ("cb_decode_b64", 31),
                          ("tiny_decode", 3), ("cb_decode_b64", 500)]:
