@@ -93,6 +93,25 @@ typedef int32_t pa_status;
 #define PA_DEVERR_WAIT_TIMEOUT 4  /* a pipeline wait gave up after ~2 s */
 #define PA_DEVERR_SHAPE 8         /* context_lens / cu_seqlens inconsistent */
 
+/*
+ * Launch flags (the `flags` argument of pa_store_kv, pa_decode and
+ * pa_decode_noalloc).  Any other bit returns PA_ERR_INVALID_ARG.
+ *
+ * PA_LAUNCH_PDL: programmatic dependent launch.  The call's kernel may begin
+ * while the kernel launched just before it on the same stream is still
+ * running, and lets the kernel launched after it begin early; a chain of
+ * such calls overlaps each kernel's start-up (launch, set-up, first loads)
+ * with the tail of the one before.  Before waiting for the previous kernel
+ * to complete, pa_decode / pa_decode_noalloc read context_lens and
+ * block_tables only (to partition the work and find the first pages); so
+ * with this flag those two must not be written by the kernel launched
+ * immediately before the call (host copies and earlier kernels are fine).
+ * pa_store_kv reads nothing before that wait.
+ * Every write and every other read happens after it, so the results are the
+ * same with and without the flag.
+ */
+#define PA_LAUNCH_PDL 1u
+
 /* ABI version of the loaded library (PA_ABI_VERSION it was built with). */
 PA_API int32_t pa_abi_version(void);
 
@@ -119,6 +138,7 @@ PA_API const char *pa_status_string(pa_status status);
  *   error_flags    optional int32 word (may be NULL); a slot >= num_blocks *
  *                  block_size sets PA_DEVERR_SLOT_INDEX and that token is
  *                  skipped.
+ *   flags          0 or PA_LAUNCH_PDL.
  */
 PA_API pa_status pa_store_kv(const void *k, const void *v, int64_t num_tokens,
                       int64_t k_tok_stride, int64_t k_head_stride,
@@ -126,7 +146,7 @@ PA_API pa_status pa_store_kv(const void *k, const void *v, int64_t num_tokens,
                       void *k_cache, void *v_cache, int64_t num_blocks,
                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
                       const int32_t *slot_mapping, int32_t *error_flags,
-                      void *stream);
+                      uint32_t flags, void *stream);
 
 /*
  * Decode split partition.  The decode work is the list of all KV blocks of
@@ -196,6 +216,9 @@ PA_API int32_t pa_decode_default_splits(int32_t device, int32_t num_q_heads,
  *                  0 = pa_decode_default_splits.
  *   workspace      device buffer of workspace_bytes >=
  *                  pa_decode_workspace_size(S, num_q_heads, head_dim).
+ *   flags          0 or PA_LAUNCH_PDL (then context_lens and block_tables
+ *                  must not be written by the kernel launched just before
+ *                  this call).
  * Results do not depend on how sequences are laid out in the pool; with a
  * fixed num_splits they are deterministic run to run.
  */
@@ -204,7 +227,7 @@ PA_API pa_status pa_decode(void *out, int32_t out_dtype, const void *q, const vo
                     int32_t block_table_stride, const int32_t *context_lens, int32_t batch,
                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                     int32_t block_size, float scale, int32_t num_splits, void *workspace,
-                    size_t workspace_bytes, void *stream);
+                    size_t workspace_bytes, uint32_t flags, void *stream);
 
 /*
  * pa_decode_merge -- log-sum-exp merge of decode partials (flash-decoding).
@@ -255,7 +278,8 @@ PA_API pa_status pa_decode_noalloc(void *out, int32_t out_dtype, const void *q,
                                    int32_t block_table_stride, const int32_t *context_lens,
                                    int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t block_size, float scale,
-                                   int32_t num_splits, int32_t *error_flags, void *stream);
+                                   int32_t num_splits, int32_t *error_flags, uint32_t flags,
+                                   void *stream);
 
 /*
  * pa_prefill_varlen -- causal varlen attention over a paged prefix ([MVT]

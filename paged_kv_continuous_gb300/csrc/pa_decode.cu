@@ -155,18 +155,20 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
       cudaMemsetAsync(p.counters, 0, (size_t)r.splits * sizeof(int32_t), s) != cudaSuccess)
     return PA_ERR_LAUNCH;
   const int G = r.num_q_heads / r.num_kv_heads;
+  const bool pdl = (r.flags & PA_LAUNCH_PDL) != 0;
   cudaError_t e;
   switch (r.num_kv_heads) {
-    case 1: e = launch_decode<1>(G, tk, tv, p, s, device); break;
-    case 2: e = launch_decode<2>(G, tk, tv, p, s, device); break;
-    case 4: e = launch_decode<4>(G, tk, tv, p, s, device); break;
-    default: e = launch_decode<8>(G, tk, tv, p, s, device); break;
+    case 1: e = launch_decode<1>(G, tk, tv, p, s, device, pdl); break;
+    case 2: e = launch_decode<2>(G, tk, tv, p, s, device, pdl); break;
+    case 4: e = launch_decode<4>(G, tk, tv, p, s, device, pdl); break;
+    default: e = launch_decode<8>(G, tk, tv, p, s, device, pdl); break;
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }
 
 pa_status check_decode_request(DecodeRequest &r, int *device_out) {
   if (r.batch < 0 || r.num_blocks < 0 || r.num_splits < 0) return PA_ERR_INVALID_ARG;
+  if (r.flags & ~static_cast<uint32_t>(PA_LAUNCH_PDL)) return PA_ERR_INVALID_ARG;
   if (r.num_splits > PA_DECODE_MAX_SPLITS) return PA_ERR_UNSUPPORTED;
   if (r.out_dtype != PA_DTYPE_BF16 && r.out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
   if (r.head_dim != kHeadDim || r.block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
@@ -216,11 +218,11 @@ extern "C" pa_status pa_decode(void *out, int32_t out_dtype, const void *q, cons
                                const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                float scale, int32_t num_splits, void *workspace,
-                               size_t workspace_bytes, void *stream) {
+                               size_t workspace_bytes, uint32_t flags, void *stream) {
   using namespace pa;
   DecodeRequest r{out, out_dtype, q, k_cache, v_cache, num_blocks, block_tables,
                   block_table_stride, context_lens, batch, num_q_heads, num_kv_heads, head_dim,
-                  block_size, scale, num_splits, 0, stream};
+                  block_size, scale, num_splits, 0, flags, stream};
   int device = -1;
   const pa_status st = check_decode_request(r, &device);
   if (st != PA_OK || batch == 0) return st;

@@ -12,7 +12,7 @@ namespace pa {
 namespace {
 template <int G>
 cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
-                     cudaStream_t s, int device) {
+                     cudaStream_t s, int device, bool pdl) {
   using Sh = DecodeShape<G, PA_HKV>;
   static bool configured[64] = {};
   if (device < 0 || device >= 64 || !configured[device]) {
@@ -21,23 +21,24 @@ cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeP
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < 64) configured[device] = true;
   }
-  decode_kernel<G, PA_HKV><<<p.num_splits, kDecodeThreads, Sh::SMEM, s>>>(tk, tv, p);
-  return cudaGetLastError();
+  return launch_kernel(decode_kernel<G, PA_HKV>, dim3(p.num_splits), dim3(kDecodeThreads),
+                       Sh::SMEM, s, pdl, tk, tv, p);
 }
 }  // namespace
 
 template <>
 cudaError_t launch_decode<PA_HKV>(int G, const CUtensorMap &tk, const CUtensorMap &tv,
-                                  const DecodeParams &p, cudaStream_t s, int device) {
+                                  const DecodeParams &p, cudaStream_t s, int device,
+                                  bool pdl) {
   switch (G) {
-    case 1: return launch_g<1>(tk, tv, p, s, device);
-    case 2: return launch_g<2>(tk, tv, p, s, device);
-    case 3: return launch_g<3>(tk, tv, p, s, device);
-    case 4: return launch_g<4>(tk, tv, p, s, device);
-    case 5: return launch_g<5>(tk, tv, p, s, device);
-    case 6: return launch_g<6>(tk, tv, p, s, device);
-    case 7: return launch_g<7>(tk, tv, p, s, device);
-    case 8: return launch_g<8>(tk, tv, p, s, device);
+    case 1: return launch_g<1>(tk, tv, p, s, device, pdl);
+    case 2: return launch_g<2>(tk, tv, p, s, device, pdl);
+    case 3: return launch_g<3>(tk, tv, p, s, device, pdl);
+    case 4: return launch_g<4>(tk, tv, p, s, device, pdl);
+    case 5: return launch_g<5>(tk, tv, p, s, device, pdl);
+    case 6: return launch_g<6>(tk, tv, p, s, device, pdl);
+    case 7: return launch_g<7>(tk, tv, p, s, device, pdl);
+    case 8: return launch_g<8>(tk, tv, p, s, device, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -36,6 +36,7 @@ struct DecodeRequest {
   float scale;
   int32_t num_splits;  // as given (0 = default)
   int32_t splits;      // resolved by check_decode_request
+  uint32_t flags;      // PA_LAUNCH_* bits
   void *stream;
 };
 

@@ -294,168 +294,57 @@ __device__ __forceinline__ void store_out4(void *out, int out_f32, long long idx
 // split-K partials of splits c0..c1 (slot 1 of c0, slot 0 of the others),
 // by one warp; lane l owns dims 4l..4l+3.  Partials are read through L2
 // (written by other CTAs).  When N >= S every split holds at least one
-// block, so no split can be empty and no division is needed.
+// block; otherwise empty splits are skipped.  Each lane walks the pieces in
+// split order with the same arithmetic as merge_sequence_bulk (weights
+// exp(lse - M) summed in order, then sum of w_i o_i in order), so the row
+// has the same bits whichever path merges it.
 __device__ __forceinline__ void merge_row(const float *part_o, const float *part_lse, void *out,
                                           int out_f32, long long out_row, int HQ, int h,
                                           long long c0, long long c1, long long S, long long N,
                                           int lane) {
   const bool dense = N >= S;
   auto piece = [&](long long cc) -> bool {
-    return cc <= c1 &&
-           (dense || cc == c0 || split_begin(cc, S, N) < split_begin(cc + 1, S, N));
+    return dense || cc == c0 || split_begin(cc, S, N) < split_begin(cc + 1, S, N);
   };
   auto row_of = [&](long long cc) -> long long { return (cc * 2 + (cc == c0 ? 1 : 0)) * HQ + h; };
   float M = -INFINITY;
   for (long long base = c0; base <= c1; base += 32) {
     const long long cc = base + lane;
-    if (piece(cc)) M = fmaxf(M, __ldcg(part_lse + row_of(cc)));
+    if (cc <= c1 && piece(cc)) M = fmaxf(M, __ldcg(part_lse + row_of(cc)));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float W = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (long long base = c0; base <= c1; base += 32) {
-    const long long cc = base + lane;
-    float w = 0.f;
-    if (piece(cc)) {
-      const float lse = __ldcg(part_lse + row_of(cc));
-      w = lse == -INFINITY ? 0.f : __expf(lse - M);
-    }
-    W += w;
-    unsigned mask = __ballot_sync(0xffffffffu, w > 0.f);
-    while (mask) {
-      // up to four rows in flight per round
-      int idx[4];
-      int cnt = 0;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        idx[u] = mask ? __ffs(mask) - 1 : -1;
-        if (mask) {
-          mask &= mask - 1;
-          ++cnt;
-        }
-      }
-      float4 v[4];
-      float wv[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int src = idx[u] < 0 ? 0 : idx[u];
-        wv[u] = __shfl_sync(0xffffffffu, w, src);
-        const long long ccu = base + src;
-        v[u] = u < cnt ? __ldcg(reinterpret_cast<const float4 *>(part_o + row_of(ccu) * kHeadDim) +
-                                lane)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (u < cnt) {
-          acc.x += wv[u] * v[u].x;
-          acc.y += wv[u] * v[u].y;
-          acc.z += wv[u] * v[u].z;
-          acc.w += wv[u] * v[u].w;
-        }
-      }
-    }
+  for (long long cc = c0; cc <= c1; ++cc) {
+    if (!piece(cc)) continue;
+    const float lse = __ldcg(part_lse + row_of(cc));
+    W += lse == -INFINITY ? 0.f : __expf(lse - M);
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
   const float inv = W > 0.f ? 1.f / W : 0.f;
-  store_out4(out, out_f32, out_row * kHeadDim + lane * 4,
-             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long cc = c0; cc <= c1; ++cc) {
+    if (!piece(cc)) continue;
+    const float lse = __ldcg(part_lse + row_of(cc));
+    const float wi = (lse == -INFINITY ? 0.f : __expf(lse - M)) * inv;
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(part_o + row_of(cc) * kHeadDim) + lane);
+    acc.x = fmaf(wi, v.x, acc.x);
+    acc.y = fmaf(wi, v.y, acc.y);
+    acc.z = fmaf(wi, v.z, acc.z);
+    acc.w = fmaf(wi, v.w, acc.w);
+  }
+  store_out4(out, out_f32, out_row * kHeadDim + lane * 4, acc);
 }
 
 // Log-sum-exp merge of all partials of sequence b by the NT consumer
-// threads of one CTA, when the pieces are few enough for their weights to fit
-// in shared memory (k <= MAXP, every split of c0..c1 non-empty).  Work item =
-// (head, 4 dims).  The first partial rows of a thread's first items (eight
-// rows of one item, or four of two) are loaded together with the (piece,
-// head) lse values, so that for few pieces the merge costs one round of
-// global loads; the weights exp(lse - M) / sum
-// are formed in `w` meanwhile.  The piece of split c_own (if any) is read
-// from shared memory (own_o, own_lse) instead of the workspace.  Returns
-// false (nothing done) when the pieces do not fit; the caller then merges row
-// by row with merge_row.
-template <int HQ, int MAXP, int NT>
-__device__ bool merge_sequence_block(const DecodeParams &p, int b, long long c0, long long c1,
-                                     long long S, long long N, float *w, int ct, int bar_id,
-                                     long long c_own, const float *own_o, const float *own_lse) {
-  const long long k = c1 - c0 + 1;
-  if (N < S || k > MAXP) return false;
-  constexpr int ITEMS = HQ * (kHeadDim / 4);
-  constexpr int PRE = ITEMS > NT ? 2 : 1;  // preloaded items per thread
-  constexpr int ROWS = 8 / PRE;            // preloaded rows per item
-  const int kk = (int)k;
-  auto row_of = [&](int i, int h) -> long long {
-    const long long cc = c0 + i;
-    return (cc * 2 + (i == 0 ? 1 : 0)) * HQ + h;
-  };
-  auto load_row = [&](int i, int h, int d) -> float4 {
-    return c0 + i == c_own
-               ? *reinterpret_cast<const float4 *>(own_o + h * kHeadDim + d)
-               : __ldcg(reinterpret_cast<const float4 *>(p.part_o + row_of(i, h) * kHeadDim + d));
-  };
-  float4 pre[PRE][ROWS];
-#pragma unroll
-  for (int t = 0; t < PRE; ++t) {
-    const int item = ct + t * NT;
-    const int h = item / (kHeadDim / 4), d = (item % (kHeadDim / 4)) * 4;
-#pragma unroll
-    for (int u = 0; u < ROWS; ++u)
-      pre[t][u] = item < ITEMS && u < kk ? load_row(u, h, d) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  for (int e = ct; e < kk * HQ; e += NT)
-    w[e] = c0 + e / HQ == c_own ? own_lse[e % HQ] : __ldcg(p.part_lse + row_of(e / HQ, e % HQ));
-  named_barrier(bar_id, NT);
-  for (int h = ct; h < HQ; h += NT) {
-    float M = -INFINITY;
-    for (int i = 0; i < kk; ++i) M = fmaxf(M, w[i * HQ + h]);
-    float W = 0.f;
-    for (int i = 0; i < kk; ++i) {
-      const float lse = w[i * HQ + h];
-      const float e = lse == -INFINITY ? 0.f : __expf(lse - M);
-      w[i * HQ + h] = e;
-      W += e;
-    }
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-    for (int i = 0; i < kk; ++i) w[i * HQ + h] *= inv;
-  }
-  named_barrier(bar_id, NT);
-  for (int item = ct, t = 0; item < ITEMS; item += NT, ++t) {
-    const int h = item / (kHeadDim / 4);
-    const int d = (item % (kHeadDim / 4)) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i0 = 0; i0 < kk; i0 += ROWS) {
-      float4 v[ROWS];
-      if (i0 == 0 && t < PRE) {
-#pragma unroll
-        for (int u = 0; u < ROWS; ++u) v[u] = t == 0 ? pre[0][u] : pre[PRE - 1][u];
-      } else {
-#pragma unroll
-        for (int u = 0; u < ROWS; ++u)
-          v[u] = i0 + u < kk ? load_row(i0 + u, h, d) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < ROWS; ++u) {
-        if (i0 + u < kk) {
-          const float wu = w[(i0 + u) * HQ + h];
-          acc.x += wu * v[u].x;
-          acc.y += wu * v[u].y;
-          acc.z += wu * v[u].z;
-          acc.w += wu * v[u].w;
-        }
-      }
-    }
-    store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d, acc);
-  }
-  return true;
-}
-
-// The same merge with the other pieces' partial rows brought into shared
-// memory (`buf`, 16-byte aligned, `buf_bytes` long) by one bulk copy per
-// piece, so that any k that fits costs one round trip; the lse values come
-// with ordinary loads meanwhile.  Needs every split of c0..c1 non-empty
-// (N >= S), k <= MAXP and room in `buf`, else returns false having done
-// nothing.  c_own (always in c0..c1 here) is read from own_o / own_lse.
+// threads of one CTA (needs every split of c0..c1 non-empty, N >= S, and
+// k = c1 - c0 + 1 <= MAXP; else returns false having done nothing).  One
+// round of loads brings every (piece, head) lse into `w`, where each head's
+// weights exp(lse - M) / sum are formed.  The pieces' partial rows come into
+// shared memory (`buf`, 16-byte aligned, `buf_bytes` long) by one bulk copy
+// per piece, as many pieces per batch as `buf` holds (all of them for the
+// common few-piece case: one round trip); each thread keeps the weighted
+// sums of its (head, 4 dims) items in registers across batches.  The piece
+// of split c_own (always in c0..c1 here) is read from own_o / own_lse.
 template <int HQ, int MAXP, int NT>
 __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, long long c1,
                                     long long S, long long N, float *w, int ct, int bar_id,
@@ -463,24 +352,32 @@ __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, 
                                     float *buf, long long buf_bytes, uint32_t mbar,
                                     volatile int *abort_flag) {
   constexpr int ROW_FLOATS = HQ * kHeadDim;  // one piece: HQ rows of o
+  constexpr int ITEMS = HQ * (kHeadDim / 4);
+  constexpr int IPT = (ITEMS + NT - 1) / NT;  // items per thread
   const long long k = c1 - c0 + 1;
-  if (N < S || k > MAXP || k * ROW_FLOATS * 4 > buf_bytes) return false;
-  const int kk = (int)k;
+  const long long per_batch = buf_bytes / (ROW_FLOATS * 4);
+  if (N < S || k > MAXP || per_batch < 1) return false;
+  const int kk = (int)k, kb = (int)(per_batch < k ? per_batch : k);
   auto row0 = [&](int i) -> long long {  // first workspace row of piece i
     const long long cc = c0 + i;
     return (cc * 2 + (i == 0 ? 1 : 0)) * HQ;
   };
+  auto issue = [&](int i0) {
+    const int i1 = i0 + kb < kk ? i0 + kb : kk;
+    const bool own_in = c_own >= c0 + i0 && c_own < c0 + i1;
+    mbar_arrive_expect_tx(mbar, (uint32_t)((i1 - i0 - (own_in ? 1 : 0)) * ROW_FLOATS * 4));
+    const uint64_t pol = l2_policy_evict_first();
+    for (int i = i0; i < i1; ++i)
+      if (c0 + i != c_own)
+        bulk_load(smem_addr(buf + (long long)(i - i0) * ROW_FLOATS),
+                  p.part_o + row0(i) * kHeadDim, ROW_FLOATS * 4, mbar, pol);
+  };
   if (ct == 0) {
     // the ring was last read through the generic proxy, and the partials
-    // were acquired through it; the copies below go through the async proxy
+    // were acquired through it; the copies go through the async proxy
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("fence.proxy.async.global;" ::: "memory");
-    mbar_arrive_expect_tx(mbar, (uint32_t)((kk - 1) * ROW_FLOATS * 4));
-    const uint64_t pol = l2_policy_evict_first();
-    for (int i = 0; i < kk; ++i)
-      if (c0 + i != c_own)
-        bulk_load(smem_addr(buf + (long long)i * ROW_FLOATS), p.part_o + row0(i) * kHeadDim,
-                  ROW_FLOATS * 4, mbar, pol);
+    issue(0);
   }
   for (int e = ct; e < kk * HQ; e += NT)
     w[e] = c0 + e / HQ == c_own ? own_lse[e % HQ] : __ldcg(p.part_lse + row0(e / HQ) + e % HQ);
@@ -499,22 +396,45 @@ __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, 
     for (int i = 0; i < kk; ++i) w[i * HQ + h] *= inv;
   }
   named_barrier(bar_id, NT);
-  // every consumer thread waits for the copies (warp-uniform; bounded)
-  __all_sync(0xffffffffu, mbar_wait(mbar, 0, abort_flag, p.err));
-  for (int item = ct; item < HQ * (kHeadDim / 4); item += NT) {
-    const int h = item / (kHeadDim / 4);
-    const int d = (item % (kHeadDim / 4)) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < kk; ++i) {
-      const float wi = w[i * HQ + h];
-      const float4 v = *reinterpret_cast<const float4 *>(
-          (c0 + i == c_own ? own_o : buf + (long long)i * ROW_FLOATS) + h * kHeadDim + d);
-      acc.x += wi * v.x;
-      acc.y += wi * v.y;
-      acc.z += wi * v.z;
-      acc.w += wi * v.w;
+  float4 acc[IPT];
+#pragma unroll
+  for (int t = 0; t < IPT; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int own_i = (int)(c_own - c0);
+  for (int i0 = 0, batch = 0; i0 < kk; i0 += kb, ++batch) {
+    // every consumer thread waits for the batch (warp-uniform; bounded)
+    __all_sync(0xffffffffu, mbar_wait(mbar, batch & 1, abort_flag, p.err));
+    const int i1 = i0 + kb < kk ? i0 + kb : kk;
+#pragma unroll
+    for (int t = 0; t < IPT; ++t) {
+      const int item = ct + t * NT;
+      if (item < ITEMS) {
+        const int h = item / (kHeadDim / 4), d = (item % (kHeadDim / 4)) * 4;
+        // pieces in split order whichever CTA merges: the sums are the same
+        // bits run to run (merge_row keeps the same order and arithmetic)
+        for (int i = i0; i < i1; ++i) {
+          const float wi = w[i * HQ + h];
+          const float4 v = *reinterpret_cast<const float4 *>(
+              (i == own_i ? own_o : buf + (long long)(i - i0) * ROW_FLOATS) + h * kHeadDim + d);
+          acc[t].x = fmaf(wi, v.x, acc[t].x);
+          acc[t].y = fmaf(wi, v.y, acc[t].y);
+          acc[t].z = fmaf(wi, v.z, acc[t].z);
+          acc[t].w = fmaf(wi, v.w, acc[t].w);
+        }
+      }
     }
-    store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d, acc);
+    if (i1 < kk) {
+      // the next batch reuses the buffer once every thread is done with it
+      named_barrier(bar_id, NT);
+      if (ct == 0) issue(i1);
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < IPT; ++t) {
+    const int item = ct + t * NT;
+    if (item < ITEMS) {
+      const int h = item / (kHeadDim / 4), d = (item % (kHeadDim / 4)) * 4;
+      store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d, acc[t]);
+    }
   }
   return true;
 }
@@ -564,7 +484,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const long long hi = N ? split_begin(c + 1, nsplit, N) : 0;
 
   // ---- 2. block-wide scan of sequence block counts: find the sequence that
-  //         holds block `lo`; zero the rows of empty sequences this CTA owns.
+  //         holds block `lo`.
   {
     __shared__ long long warp_tot[kDecodeWarps];
     long long running = 0;
@@ -589,21 +509,30 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           ctl->first_b = b;
           ctl->first_prefix = prefix;
         }
-        const bool owns_empty =
-            n == 0 && ((lo <= prefix && prefix < hi) || (prefix >= N && c == nsplit - 1));
-        if (owns_empty) {
-          const long long row0 = (long long)b * S::HQ * kHeadDim;
-          for (int i = 0; i < S::HQ * kHeadDim; i += 2)
-            store_out2(p.out, p.out_f32, row0 + i, 0.f, 0.f);
-        }
       }
       running += chunk_total;
       __syncthreads();
     }
   }
-  if (lo >= hi) return;    // no block for this CTA (N < S)
-  if (ctl->first_b < 0) {  // cannot happen for consistent inputs; never walk from b = -1
-    if (tid == 0) report(p.err, PA_DEVERR_SHAPE);
+  // ---- 2b. Under a programmatic dependent launch the previous kernel in the
+  //          stream may still be running.  Context lengths and block tables
+  //          may be read before griddep_wait(); q, the pools, the workspace
+  //          and every write come after it.
+  griddep_launch_dependents();
+  // rows of empty sequences: sequence b is zeroed by CTA b mod S, by threads
+  // t0, t0 + nt, ...
+  auto zero_empty_rows = [&](int t0, int nt) {
+    for (long long b = c; b < p.batch; b += nsplit)
+      if (__ldg(p.context_lens + b) <= 0)
+        for (int i = 2 * t0; i < S::HQ * kHeadDim; i += 2 * nt)
+          store_out2(p.out, p.out_f32, b * S::HQ * kHeadDim + i, 0.f, 0.f);
+  };
+  if (lo >= hi || ctl->first_b < 0) {
+    // no block for this CTA (N < S), or inconsistent input (never walk from
+    // b = -1): only the empty rows and the error bit remain
+    griddep_wait();
+    zero_empty_rows(tid, blockDim.x);
+    if (lo < hi && tid == 0) report(p.err, PA_DEVERR_SHAPE);
     return;
   }
 
@@ -641,16 +570,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     int j = (int)(lo - first_prefix);
     long long gb = lo, issued = 0;
     bool stop = false;
+    bool waited = false;
     while (gb < hi && !stop) {
       int lb, lj, lctx;
       const int count = walk_chunk(p.context_lens, p.batch, b, ctx, j, hi - gb, lane, lb, lj, lctx);
       if (count == 0) {
+        griddep_wait();
         if (lane == 0) report(p.err, PA_DEVERR_SHAPE);
         break;
       }
       // all block-table entries of the chunk in one round of loads
       const bool in_row = lane < count && lj < p.bt_stride;
       const long long phys = in_row ? __ldg(p.block_tables + (long long)lb * p.bt_stride + lj) : -1;
+      if (!waited) {
+        // the first chunk's descriptors are ready; the copies wait for the
+        // previous kernel (it may write the pools)
+        griddep_wait();
+        waited = true;
+      }
       // the q rows go with the first NPH stages of every piece: each consumer
       // warp reads them from its own first stage of the piece
       const bool with_q = min(gb + lane - lo, (long long)lj) < S::NPH;
@@ -714,6 +651,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // ---- 5a. epilogue warp: publishes the CTA's first piece when it is a
     //          cut one (fence, arrival; the merge too if it comes last), so
     //          that the consumers do not wait on those global round trips.
+    griddep_wait();
     const bool got = __all_sync(0xffffffffu,
                                 mbar_wait(smem_addr(&ctl->ew_bar), 0, abort_flag, p.err));
     if (!got || ctl->ew_kind == 0) return;
@@ -737,6 +675,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   // ---- 5b. consumers ----------------------------------------------------------
   const int cw = warp - kDecodeFirstConsumerWarp;  // consumer warp 0..CW-1
+  griddep_wait();
+  zero_empty_rows(tid - 32 * kDecodeFirstConsumerWarp, S::CW * 32);
   const int g = cw % HKV;     // kv head of this warp
   const int ph = cw / HKV;    // stage phase of this warp
   const int gid = lane >> 2;  // fragment row group
@@ -1112,9 +1052,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               (long long)S::NST * S::STAGE_BYTES - (long long)(mbuf - own_o) * 4;
           if (!merge_sequence_bulk<S::HQ, S::MERGE_MAX_PIECES, S::CW * 32>(
                   p, b, cs0, cs1, nsplit, N, mw, ct, 1, c, own_o, own_lse, mbuf, mbuf_bytes,
-                  smem_addr(&ctl->merge_bar), abort_flag) &&
-              !merge_sequence_block<S::HQ, S::MERGE_MAX_PIECES, S::CW * 32>(
-                  p, b, cs0, cs1, nsplit, N, mw, ct, 1, c, own_o, own_lse))
+                  smem_addr(&ctl->merge_bar), abort_flag))
             for (int h = cw; h < S::HQ; h += S::CW)
               merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * S::HQ + h, S::HQ, h,
                         cs0, cs1, nsplit, N, lane);
@@ -1146,6 +1084,6 @@ consumers_done:
 // Launches decode_kernel<G, HKV> for one G (defined per HKV in pa_decode_h*.cu).
 template <int HKV>
 cudaError_t launch_decode(int G, const CUtensorMap &tk, const CUtensorMap &tv,
-                          const DecodeParams &p, cudaStream_t s, int device);
+                          const DecodeParams &p, cudaStream_t s, int device, bool pdl);
 
 }  // namespace pa

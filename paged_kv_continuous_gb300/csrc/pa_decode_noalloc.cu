@@ -60,11 +60,12 @@ extern "C" pa_status pa_decode_noalloc(void *out, int32_t out_dtype, const void 
                                        int32_t block_table_stride, const int32_t *context_lens,
                                        int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim, int32_t block_size, float scale,
-                                       int32_t num_splits, int32_t *error_flags, void *stream) {
+                                       int32_t num_splits, int32_t *error_flags, uint32_t flags,
+                                       void *stream) {
   using namespace pa;
   DecodeRequest r{out, out_dtype, q, k_cache, v_cache, num_blocks, block_tables,
                   block_table_stride, context_lens, batch, num_q_heads, num_kv_heads, head_dim,
-                  block_size, scale, num_splits, 0, stream};
+                  block_size, scale, num_splits, 0, flags, stream};
   int device = -1;
   const pa_status st = check_decode_request(r, &device);
   if (st != PA_OK || batch == 0) return st;

@@ -18,6 +18,9 @@ __global__ void __launch_bounds__(256) store_kv_kernel(
     uint16_t *__restrict__ k_cache, uint16_t *__restrict__ v_cache, long long num_slots,
     int hkv, const int32_t *__restrict__ slot_mapping, int32_t *err) {
   constexpr int kChunks = kHeadDim / 8;  // 16-byte chunks per head row
+  // the rows, slots and pools may come from or go to the previous kernel
+  griddep_wait();
+  griddep_launch_dependents();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long total = num_tokens * hkv * kChunks;
   if (idx >= total) return;
@@ -56,11 +59,12 @@ extern "C" pa_status pa_store_kv(const void *k, const void *v, int64_t num_token
                                  void *v_cache, int64_t num_blocks, int32_t block_size,
                                  int32_t num_kv_heads, int32_t head_dim,
                                  const int32_t *slot_mapping, int32_t *error_flags,
-                                 void *stream) {
+                                 uint32_t flags, void *stream) {
   using namespace pa;
   if (num_tokens < 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
   if (head_dim != kHeadDim || block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
   if (num_kv_heads < 1 || num_kv_heads > 64) return PA_ERR_UNSUPPORTED;
+  if (flags & ~static_cast<uint32_t>(PA_LAUNCH_PDL)) return PA_ERR_INVALID_ARG;
   if (num_tokens == 0) return PA_OK;
   if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
   if (k_tok_stride < 0 || k_head_stride < 0 || v_tok_stride < 0 || v_head_stride < 0)
@@ -81,13 +85,11 @@ extern "C" pa_status pa_store_kv(const void *k, const void *v, int64_t num_token
   auto *vp = static_cast<const uint16_t *>(v);
   auto *kc = static_cast<uint16_t *>(k_cache);
   auto *vc = static_cast<uint16_t *>(v_cache);
-  if (aligned)
-    store_kv_kernel<true><<<(unsigned)blocks, threads, 0, s>>>(
-        kp, vp, num_tokens, k_tok_stride, k_head_stride, v_tok_stride, v_head_stride, kc, vc,
-        num_slots, num_kv_heads, slot_mapping, error_flags);
-  else
-    store_kv_kernel<false><<<(unsigned)blocks, threads, 0, s>>>(
-        kp, vp, num_tokens, k_tok_stride, k_head_stride, v_tok_stride, v_head_stride, kc, vc,
-        num_slots, num_kv_heads, slot_mapping, error_flags);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+  const bool pdl = (flags & PA_LAUNCH_PDL) != 0;
+  const cudaError_t e = launch_kernel(
+      aligned ? store_kv_kernel<true> : store_kv_kernel<false>, dim3((unsigned)blocks),
+      dim3(threads), 0, s, pdl, kp, vp, num_tokens, (long long)k_tok_stride,
+      (long long)k_head_stride, (long long)v_tok_stride, (long long)v_head_stride, kc, vc,
+      num_slots, (int)num_kv_heads, slot_mapping, error_flags);
+  return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }

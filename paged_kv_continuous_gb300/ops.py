@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libpa_gb300.so")
 PA_OK = 0
 PA_DTYPE_BF16 = 0
 PA_DTYPE_F32 = 1
+PA_LAUNCH_PDL = 1  # programmatic dependent launch (see include/pa.h)
 DEVERR_BLOCK_INDEX = 1
 DEVERR_SLOT_INDEX = 2
 DEVERR_WAIT_TIMEOUT = 4
@@ -41,26 +42,27 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         raise PagedAttentionError(
             f"{path} is missing: build it with `python -m paged_kv_continuous_gb300.build`")
     lib = ctypes.CDLL(path)
-    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
-                            ctypes.c_size_t)
+    P, i32, i64, f32, sz, u32 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                 ctypes.c_float, ctypes.c_size_t, ctypes.c_uint32)
     lib.pa_abi_version.restype = i32
     lib.pa_abi_version.argtypes = []
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [i32]
     lib.pa_store_kv.restype = i32
-    lib.pa_store_kv.argtypes = [P, P, i64, i64, i64, i64, i64, P, P, i64, i32, i32, i32, P, P, P]
+    lib.pa_store_kv.argtypes = [P, P, i64, i64, i64, i64, i64, P, P, i64, i32, i32, i32, P, P,
+                                u32, P]
     lib.pa_decode_workspace_size.restype = sz
     lib.pa_decode_workspace_size.argtypes = [i32, i32, i32]
     lib.pa_decode_default_splits.restype = i32
     lib.pa_decode_default_splits.argtypes = [i32, i32, i32]
     lib.pa_decode.restype = i32
     lib.pa_decode.argtypes = [P, i32, P, P, P, i64, P, i32, P, i32, i32, i32, i32, i32, f32,
-                              i32, P, sz, P]
+                              i32, P, sz, u32, P]
     lib.pa_decode_merge.restype = i32
     lib.pa_decode_merge.argtypes = [P, i32, P, sz, P, i32, i32, i32, i32, i32, P]
     lib.pa_decode_noalloc.restype = i32
     lib.pa_decode_noalloc.argtypes = [P, i32, P, P, P, i64, P, i32, P, i32, i32, i32, i32, i32,
-                                      f32, i32, P, P]
+                                      f32, i32, P, u32, P]
     lib.pa_prefill_varlen.restype = i32
     lib.pa_prefill_varlen.argtypes = [P, i32, P, P, i32, i32, i32, P, P, i64, P, i32, P, i32,
                                       i32, i32, i32, f32, P, P]
@@ -101,9 +103,10 @@ def _out_code(dtype):
     raise PagedAttentionError(f"unsupported output dtype {dtype}")
 
 
-def store_kv(k, v, k_cache, v_cache, slot_mapping, error_flags=None, stream=None):
+def store_kv(k, v, k_cache, v_cache, slot_mapping, error_flags=None, stream=None, pdl=False):
     """pa_store_kv: k/v bf16 [T, Hkv, D] (any token/head strides, unit dim
-    stride) into the pools at slot_mapping (int32 [T])."""
+    stride) into the pools at slot_mapping (int32 [T]).  pdl: launch with
+    PA_LAUNCH_PDL."""
     _need(k, torch.bfloat16, "k", 3)
     _need(v, torch.bfloat16, "v", 3)
     _need(k_cache, torch.bfloat16, "k_cache", 4)
@@ -121,7 +124,8 @@ def store_kv(k, v, k_cache, v_cache, slot_mapping, error_flags=None, stream=None
         raise PagedAttentionError("slot_mapping must have one entry per token")
     _check(lib.pa_store_kv(_ptr(k), _ptr(v), T, k.stride(0), k.stride(1), v.stride(0),
                            v.stride(1), _ptr(k_cache), _ptr(v_cache), NB, bs, Hkv, D,
-                           _ptr(slot_mapping), _ptr(error_flags), _stream(stream)),
+                           _ptr(slot_mapping), _ptr(error_flags),
+                           PA_LAUNCH_PDL if pdl else 0, _stream(stream)),
            "pa_store_kv")
 
 
@@ -150,8 +154,10 @@ def decode_workspace(num_q_heads: int, num_kv_heads: int, num_splits: int = 0,
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
-           out_dtype=torch.bfloat16, num_splits=0, workspace=None, stream=None):
-    """pa_decode: q bf16 [B, Hq, D] over the paged pools; returns out [B, Hq, D]."""
+           out_dtype=torch.bfloat16, num_splits=0, workspace=None, stream=None, pdl=False):
+    """pa_decode: q bf16 [B, Hq, D] over the paged pools; returns out [B, Hq, D].
+    pdl: launch with PA_LAUNCH_PDL (context_lens and block_tables must then
+    not be written by the kernel launched just before)."""
     _need(q, torch.bfloat16, "q", 3)
     _need(k_cache, torch.bfloat16, "k_cache", 4)
     _need(v_cache, torch.bfloat16, "v_cache", 4)
@@ -171,7 +177,7 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
                          _ptr(v_cache), NB, _ptr(block_tables), block_tables.stride(0),
                          _ptr(context_lens), B, Hq, Hkv, D, bs, float(scale), int(num_splits),
                          _ptr(workspace), workspace.numel() * workspace.element_size(),
-                         _stream(stream)), "pa_decode")
+                         PA_LAUNCH_PDL if pdl else 0, _stream(stream)), "pa_decode")
     return out
 
 

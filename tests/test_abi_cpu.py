@@ -73,27 +73,31 @@ def test_argument_checks_before_any_launch():
     nul = None
     # unsupported head_dim / block size / group size
     assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 64, 16, 0.1, 0, nul, 0,
-                       nul) == 2
-    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 32, 0.1, 0, nul,
                        0, nul) == 2
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 32, 0.1, 0, nul,
+                       0, 0, nul) == 2
     assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 18, 2, 128, 16, 0.1, 0, nul,
-                       0, nul) == 2          # group of 9
+                       0, 0, nul) == 2          # group of 9
     assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 3, 128, 16, 0.1, 0, nul,
-                       0, nul) == 2          # 3 kv heads
+                       0, 0, nul) == 2          # 3 kv heads
     # bad dtype / negative batch / NaN scale / null pointers
     assert L.pa_decode(nul, 7, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 16, 0.1, 0, nul, 0,
-                       nul) == 1
-    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, -1, 12, 2, 128, 16, 0.1, 0, nul,
                        0, nul) == 1
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, -1, 12, 2, 128, 16, 0.1, 0, nul,
+                       0, 0, nul) == 1
     assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 16, float("nan"),
-                       0, nul, 0, nul) == 1
+                       0, nul, 0, 0, nul) == 1
     assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 16, 0.1, 0, nul, 0,
-                       nul) == 1
+                       0, nul) == 1
     # empty batch is a no-op
     assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 0, 12, 2, 128, 16, 0.1, 0, nul, 0,
-                       nul) == 0
-    assert L.pa_store_kv(nul, nul, 0, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, nul) == 0
-    assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, nul) == 1
-    assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 96, nul, nul, nul) == 2
+                       0, nul) == 0
+    assert L.pa_store_kv(nul, nul, 0, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, 0, nul) == 0
+    assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, 0, nul) == 1
+    assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 96, nul, nul, 0, nul) == 2
+    # launch flags other than PA_LAUNCH_PDL are rejected
+    assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, 2, nul) == 1
+    assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 16, 0.1, 0, nul, 0,
+                       4, nul) == 1
     assert L.pa_decode_merge(nul, 0, nul, 0, nul, 1, 12, 128, 16, 0, nul) == 1
     assert L.pa_decode_merge(nul, 0, nul, 0, nul, 1, 12, 128, 16, 4, nul) == 1

@@ -157,6 +157,66 @@ def test_decode_sees_key_stored_same_step_over_several_steps(ops):
         assert_attention_close(dev_to_f64(got), ref, f"step {s}", strict=True)
 
 
+def _pdl_chain(ops, kc, vc, tables, steps_in, ws, outs, num_splits):
+    for (nk, nv, slots, q, ctx), out in zip(steps_in, outs):
+        ops.store_kv(nk, nv, kc, vc, slots, pdl=True)
+        ops.decode(q, kc, vc, tables, ctx, 128 ** -0.5, out=out, num_splits=num_splits,
+                   workspace=ws, pdl=True)
+
+
+def test_decode_pdl_chain_matches_oracle(ops):
+    """store -> decode -> store -> decode ... all launched with PA_LAUNCH_PDL,
+    back to back with no host synchronisation (each kernel may start while the
+    one before finishes), eagerly and replayed from a CUDA graph: every step's
+    rows match the oracle, and the graph replay gives the eager bits."""
+    rng = np.random.default_rng(43)
+    lens0 = np.array([100, 17, 300, 1, 230, 64])
+    steps = 6
+    full = lens0 + steps
+    ks = [normal_bits(rng, (n, 2, 128)) for n in full]
+    vs = [normal_bits(rng, (n, 2, 128)) for n in full]
+    t = random_tables(rng, full, 160)
+    kpool = scatter_pool([k[:n] for k, n in zip(ks, lens0)], t, 160)
+    vpool = scatter_pool([v[:n] for v, n in zip(vs, lens0)], t, 160)
+    kref, vref = kpool.copy(), vpool.copy()
+    tables = to_dev_i32(t)
+    B = len(lens0)
+    steps_in, refs = [], []
+    for s in range(steps):
+        pos = lens0 + s
+        slots = (t[np.arange(B), pos // 16] * 16 + pos % 16).astype(np.int32)
+        nk = np.stack([k[p] for k, p in zip(ks, pos)])
+        nv = np.stack([v[p] for v, p in zip(vs, pos)])
+        q = normal_bits(rng, (B, 12, 128))
+        ctx = (pos + 1).astype(np.int32)
+        oracle.store_kv(nk, nv, kref, vref, slots)
+        refs.append(oracle.decode(q, kref, vref, t, ctx, 128 ** -0.5))
+        steps_in.append((to_dev_bf16(nk), to_dev_bf16(nv), to_dev_i32(slots), to_dev_bf16(q),
+                         to_dev_i32(ctx)))
+    splits = 7  # long sequences are cut: the chain exercises the in-kernel merges
+    ws = ops.decode_workspace(12, 2, splits)
+    # eager chain
+    kc, vc = to_dev_bf16(kpool), to_dev_bf16(vpool)
+    outs = [torch.empty((B, 12, 128), dtype=torch.float32, device="cuda") for _ in range(steps)]
+    _pdl_chain(ops, kc, vc, tables, steps_in, ws, outs, splits)
+    torch.cuda.synchronize()
+    assert ops.read_error_word(ws) == 0
+    for s in range(steps):
+        assert_attention_close(dev_to_f64(outs[s]), refs[s], f"pdl step {s}", strict=True)
+    # the same chain captured in a graph and replayed on fresh pools
+    kc2, vc2 = to_dev_bf16(kpool), to_dev_bf16(vpool)
+    outs2 = [torch.empty_like(o) for o in outs]
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        _pdl_chain(ops, kc2, vc2, tables, steps_in, ws, outs2, splits)
+    g.replay()
+    torch.cuda.synchronize()
+    for s in range(steps):
+        assert torch.equal(outs2[s], outs[s]), f"graph replay step {s}"
+
+
 def test_decode_closed_forms_on_gpu(ops):
     """Single key -> v exactly (up to output rounding); equal V rows -> that row;
     head-marked V -> kv head index."""

@@ -26,7 +26,7 @@ def _call_noalloc(ops, q, kc, vc, tables, ctx, scale, out, splits, err):
         P(out.data_ptr()), ops.PA_DTYPE_F32 if out.dtype == torch.float32 else ops.PA_DTYPE_BF16,
         P(q.data_ptr()), P(kc.data_ptr()), P(vc.data_ptr()), NB, P(tables.data_ptr()),
         tables.stride(0), P(ctx.data_ptr()), B, Hq, Hkv, D, bs, float(scale), splits,
-        P(err.data_ptr()), P(torch.cuda.current_stream().cuda_stream))
+        P(err.data_ptr()), 0, P(torch.cuda.current_stream().cuda_stream))
 
 
 @pytest.mark.parametrize("name,splits", [("cb_decode_b64", 0), ("long_decode_b4", 0),
