@@ -15,10 +15,12 @@
 // the counter to the piece count merges all partials of that sequence
 // (log-sum-exp) and writes its rows, then resets the counter to zero.  Only
 // a CTA's first piece (cut at its head) and its final piece (cut at its
-// tail) can be cut.  The first one is published by the epilogue warp while
-// the consumers stream on.  For the final one the consumers read the
-// counter first: when every other piece has already arrived they merge at
-// once, with their own rows taken from shared memory, and skip publishing.
+// tail) can be cut.  Every piece but the final one is handed to the epilogue
+// warp: the consumer warps drop their rows into one of two shared buffers and
+// stream on, while the epilogue warp combines them, writes the output rows or
+// the partial and publishes a cut piece.  The consumers combine and publish
+// the final piece themselves, and merge when it arrives last, with their own
+// rows taken from shared memory and the others' brought in by bulk copies.
 //
 // CTA layout (352 threads).  Warps 0 and 1 are producers, filling alternate
 // stages of a ring of NST stages guarded by full/empty mbarriers: per
@@ -97,15 +99,20 @@ struct DecodeShape {
   // 132 floats keep the o vectors 16-byte aligned)
   static constexpr int RED_FLOATS_PER_HEAD = kHeadDim + 4;
   static constexpr int RED_M = kHeadDim, RED_L = kHeadDim + 1;
-  static constexpr int RED_BYTES =
-      NPH > 1 ? align_up(CW * G * RED_FLOATS_PER_HEAD * 4, 1024) : 0;
+  // two buffers: the epilogue warp combines piece i from one while the
+  // consumers already fill the other at the end of piece i + 1
+  static constexpr int RED_ONE_FLOATS = align_up(CW * G * RED_FLOATS_PER_HEAD, 256);
+  static constexpr int RED_BYTES = NPH > 1 ? 2 * RED_ONE_FLOATS * 4 : 0;
   static constexpr int CTL_BYTES = 256;
+  // the epilogue warp's combine weights: NPH per query head (NPH * HQ = CW * G)
+  static constexpr int EWW_BYTES = 256;
   // merge scratch: one weight per (piece, query head), up to MERGE_MAX_PIECES
   static constexpr int MERGE_FLOATS = 2048;
   static constexpr int MERGE_MAX_PIECES = MERGE_FLOATS / HQ;
   static constexpr int MERGE_BYTES = MERGE_FLOATS * 4;
   static constexpr int NST_FIT =
-      (kDecodeSmemBudget - 1024 - RED_BYTES - MERGE_BYTES - CTL_BYTES) / (STAGE_BYTES + 16);
+      (kDecodeSmemBudget - 1024 - RED_BYTES - MERGE_BYTES - CTL_BYTES - EWW_BYTES) /
+      (STAGE_BYTES + 16);
   static constexpr int NST_CAP = NST_FIT > 12 ? 12 : NST_FIT;
   // The ring is a multiple of 2 (each slot is always filled by the same one
   // of the two producer warps) and of NPH (each slot always holds stages of
@@ -115,7 +122,7 @@ struct DecodeShape {
   static constexpr int NST = NST_CAP - NST_CAP % RING_MULT;
   // +1024: the dynamic smem base is realigned to 1024 bytes for the swizzle
   static constexpr int SMEM =
-      1024 + NST * STAGE_BYTES + RED_BYTES + MERGE_BYTES + NST * 16 + CTL_BYTES;
+      1024 + NST * STAGE_BYTES + RED_BYTES + MERGE_BYTES + NST * 16 + CTL_BYTES + EWW_BYTES;
   static_assert(NST >= RING_MULT && NST % RING_MULT == 0, "stage ring does not fit");
   static_assert(CW % HKV == 0, "unsupported kv head count");
   static_assert(SMEM <= kDecodeSmemBudget, "shared memory over budget");
@@ -124,20 +131,38 @@ struct DecodeShape {
   static_assert(G >= 1 && G <= 8, "group size must fit the N = 8 MMA dimension");
   // combine weights (NPH per query head) and lse live in the merge scratch
   static_assert((NPH + 1) * HQ <= MERGE_FLOATS, "combine weights do not fit");
+  static_assert(CW * G * 4 <= EWW_BYTES, "epilogue warp weights do not fit");
 };
 
+// A piece handed to the epilogue warp (one per red buffer).
+struct PieceDesc {
+  long long slot_row;  // first workspace row of a cut piece's partial
+  long long cs0, cs1;  // splits holding the sequence's blocks
+  int b;               // sequence
+  int kind;            // kPieceWhole, kPieceCut or kPieceEnd
+  int pieces;          // non-empty pieces of the sequence
+  int pad;
+};
+constexpr int kPieceWhole = 0;  // write the sequence's output rows
+constexpr int kPieceCut = 1;    // write a partial, publish it (the merge if it comes last)
+constexpr int kPieceEnd = 2;    // no further piece: the epilogue warp exits
+
 struct DecodeCtl {
-  unsigned long long ew_bar;     // mbarrier: the first piece's epilogue is ready
-  unsigned long long merge_bar;  // mbarrier: the final merge's bulk copies
+  unsigned long long red_full[2];   // mbarriers: red buffer k holds a piece (CW arrivals)
+  unsigned long long red_empty[2];  // mbarriers: the epilogue warp is done with buffer k
+  unsigned long long merge_bar;     // mbarrier: the final merge's bulk copies
+  unsigned long long merge_bar2;    // mbarrier: the deferred merge's bulk copies
+  unsigned long long ew_done;       // mbarrier: the epilogue warp has finished
+  PieceDesc desc[2];
+  // a cut piece the epilogue warp published last: the consumers merge its
+  // sequence at their end (def_pending = 1)
+  long long def_cs0, def_cs1;
+  int def_b, def_pending;
   unsigned long long total;   // N, blocks of all sequences
   long long first_prefix;    // global index of block 0 of first_b
   int first_b;               // sequence holding this CTA's first block
   int abort;                 // set by a wait that gave up
   int last;                  // this CTA merges the current cut sequence
-  // the first piece's publication, handed to the epilogue warp
-  long long ew_cs0, ew_cs1;
-  int ew_kind;  // 1: publish sequence ew_b (splits ew_cs0..ew_cs1, ew_pieces pieces); 0: none
-  int ew_b, ew_pieces;
   // the current piece's sequence: splits pc_cs0..pc_cs1 hold its blocks, in
   // pc_pieces non-empty pieces (consumer thread 0 works them out at the
   // piece start, off the epilogue's path)
@@ -314,23 +339,39 @@ __device__ __forceinline__ void merge_row(const float *part_o, const float *part
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  // eight pieces' loads in flight at a time; the sums stay in split order
   float W = 0.f;
-  for (long long cc = c0; cc <= c1; ++cc) {
-    if (!piece(cc)) continue;
-    const float lse = __ldcg(part_lse + row_of(cc));
-    W += lse == -INFINITY ? 0.f : __expf(lse - M);
+  for (long long base = c0; base <= c1; base += 8) {
+    float lv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      lv[u] = base + u <= c1 && piece(base + u) ? __ldcg(part_lse + row_of(base + u)) : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (base + u <= c1 && piece(base + u)) W += lv[u] == -INFINITY ? 0.f : __expf(lv[u] - M);
   }
   const float inv = W > 0.f ? 1.f / W : 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (long long cc = c0; cc <= c1; ++cc) {
-    if (!piece(cc)) continue;
-    const float lse = __ldcg(part_lse + row_of(cc));
-    const float wi = (lse == -INFINITY ? 0.f : __expf(lse - M)) * inv;
-    const float4 v = __ldcg(reinterpret_cast<const float4 *>(part_o + row_of(cc) * kHeadDim) + lane);
-    acc.x = fmaf(wi, v.x, acc.x);
-    acc.y = fmaf(wi, v.y, acc.y);
-    acc.z = fmaf(wi, v.z, acc.z);
-    acc.w = fmaf(wi, v.w, acc.w);
+  for (long long base = c0; base <= c1; base += 8) {
+    float lv[8];
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool in = base + u <= c1 && piece(base + u);
+      lv[u] = in ? __ldcg(part_lse + row_of(base + u)) : -INFINITY;
+      v[u] = in ? __ldcg(reinterpret_cast<const float4 *>(part_o + row_of(base + u) * kHeadDim) +
+                         lane)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (!(base + u <= c1 && piece(base + u))) continue;
+      const float wi = (lv[u] == -INFINITY ? 0.f : __expf(lv[u] - M)) * inv;
+      acc.x = fmaf(wi, v[u].x, acc.x);
+      acc.y = fmaf(wi, v[u].y, acc.y);
+      acc.z = fmaf(wi, v[u].z, acc.z);
+      acc.w = fmaf(wi, v[u].w, acc.w);
+    }
   }
   store_out4(out, out_f32, out_row * kHeadDim + lane * 4, acc);
 }
@@ -344,7 +385,8 @@ __device__ __forceinline__ void merge_row(const float *part_o, const float *part
 // per piece, as many pieces per batch as `buf` holds (all of them for the
 // common few-piece case: one round trip); each thread keeps the weighted
 // sums of its (head, 4 dims) items in registers across batches.  The piece
-// of split c_own (always in c0..c1 here) is read from own_o / own_lse.
+// of split c_own is read from own_o / own_lse (c_own = -1: every piece comes
+// from the workspace).
 template <int HQ, int MAXP, int NT>
 __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, long long c1,
                                     long long S, long long N, float *w, int ct, int bar_id,
@@ -454,6 +496,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                                                 S::MERGE_BYTES);
   uint64_t *empty = full + S::NST;
   DecodeCtl *ctl = reinterpret_cast<DecodeCtl *>(empty + S::NST);
+  float *eww = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ctl) + S::CTL_BYTES);
   volatile int *abort_flag = &ctl->abort;
 
   const int tid = threadIdx.x;
@@ -545,8 +588,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, HKV);  // the Hkv consumer warps of the slot's phase
     }
-    mbar_init(smem_addr(&ctl->ew_bar), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_addr(&ctl->red_full[k]), S::CW);
+      mbar_init(smem_addr(&ctl->red_empty[k]), 1);
+    }
     mbar_init(smem_addr(&ctl->merge_bar), 1);
+    mbar_init(smem_addr(&ctl->merge_bar2), 1);
+    mbar_init(smem_addr(&ctl->ew_done), 1);
+    ctl->def_pending = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -648,29 +697,94 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
 
   if (warp == kDecodeEpilogueWarp) {
-    // ---- 5a. epilogue warp: publishes the CTA's first piece when it is a
-    //          cut one (fence, arrival; the merge too if it comes last), so
-    //          that the consumers do not wait on those global round trips.
+    // ---- 5a. epilogue warp: takes every piece that ends before the CTA's
+    //          final one, in order, from red buffer (piece index mod 2).  With
+    //          several warps per kv head it combines their rows and writes
+    //          the output rows (whole sequence) or the partial (cut piece);
+    //          with one warp per kv head the consumers wrote the rows already.
+    //          For a cut piece it then publishes: fence, arrival, and the
+    //          merge if the piece arrives last.  The consumers never wait for
+    //          this, except to reuse a buffer two pieces later.
     griddep_wait();
-    const bool got = __all_sync(0xffffffffu,
-                                mbar_wait(smem_addr(&ctl->ew_bar), 0, abort_flag, p.err));
-    if (!got || ctl->ew_kind == 0) return;
-    const int b = ctl->ew_b;
-    const long long cs0 = ctl->ew_cs0, cs1 = ctl->ew_cs1;
-    int last = 0;
-    if (lane == 0) {
-      // the consumers' partial rows are ordered before this by the mbarrier
-      __threadfence();
-      last = atomicAdd(p.counters + cs1, 1) == ctl->ew_pieces - 1;
+    for (int npe = 0;; ++npe) {
+      const int k = npe & 1;
+      const bool got = __all_sync(
+          0xffffffffu,
+          mbar_wait(smem_addr(&ctl->red_full[k]), (npe >> 1) & 1, abort_flag, p.err));
+      const PieceDesc d = ctl->desc[k];
+      if (!got || d.kind == kPieceEnd) {
+        if (lane == 0) mbar_arrive(smem_addr(&ctl->ew_done));
+        return;
+      }
+      if constexpr (S::NPH > 1) {
+        const float *rk = red + k * S::RED_ONE_FLOATS;
+        // per query head: the normalised weight of each of its NPH warps
+        for (int qh = lane; qh < S::HQ; qh += 32) {
+          const int gh = qh / G, h = qh % G;
+          float mk[S::NPH], M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < S::NPH; ++w) {
+            mk[w] = rk[((gh + w * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + S::RED_M];
+            M = fmaxf(M, mk[w]);
+          }
+          float L = 0.f;
+#pragma unroll
+          for (int w = 0; w < S::NPH; ++w) {
+            mk[w] = mk[w] == -INFINITY ? 0.f : exp2f(mk[w] - M);
+            L += rk[((gh + w * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + S::RED_L] * mk[w];
+          }
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+          for (int w = 0; w < S::NPH; ++w) eww[w * S::HQ + qh] = mk[w] * inv;
+          if (d.kind == kPieceCut)
+            p.part_lse[d.slot_row + qh] =
+                L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+        }
+        __syncwarp();
+        for (int item = lane; item < S::HQ * (kHeadDim / 4); item += 32) {
+          const int qh = item / (kHeadDim / 4);
+          const int dd = (item % (kHeadDim / 4)) * 4;
+          const int gh = qh / G, h = qh % G;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < S::NPH; ++w) {
+            const float wk = eww[w * S::HQ + qh];
+            const float4 v = *reinterpret_cast<const float4 *>(
+                rk + ((gh + w * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + dd);
+            acc.x += wk * v.x;
+            acc.y += wk * v.y;
+            acc.z += wk * v.z;
+            acc.w += wk * v.w;
+          }
+          if (d.kind == kPieceWhole)
+            store_out4(p.out, p.out_f32, ((long long)d.b * S::HQ + qh) * kHeadDim + dd, acc);
+          else
+            *reinterpret_cast<float4 *>(p.part_o + (d.slot_row + qh) * kHeadDim + dd) = acc;
+        }
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive(smem_addr(&ctl->red_empty[k]));  // buffer k is free again
+      if (d.kind == kPieceCut) {
+        int last = 0;
+        if (lane == 0) {
+          // release: the partial rows (this warp's, or the consumers' that
+          // the red_full barrier ordered before) precede the arrival
+          __threadfence();
+          last = atomicAdd(p.counters + d.cs1, 1) == d.pieces - 1;
+        }
+        if (lane == 0 && last) {
+          // arrived last: acquire the other pieces' partials and leave the
+          // merge to the consumer warps, which merge with all their threads
+          // once the CTA's own blocks are done
+          fence_acq_rel_gpu();
+          ctl->def_b = d.b;
+          ctl->def_cs0 = d.cs0;
+          ctl->def_cs1 = d.cs1;
+          ctl->def_pending = 1;
+        }
+        __syncwarp();
+      }
     }
-    if (__shfl_sync(0xffffffffu, last, 0)) {
-      __threadfence();
-      for (int h = 0; h < S::HQ; ++h)
-        merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * S::HQ + h, S::HQ, h, cs0,
-                  cs1, nsplit, N, lane);
-      if (lane == 0) p.counters[cs1] = 0;
-    }
-    return;
   }
 
   // ---- 5b. consumers ----------------------------------------------------------
@@ -697,7 +811,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
 
-  bool ew_signalled = false;  // the epilogue warp has been told about the first piece
+  int npieces = 0;  // pieces ended so far (every consumer warp counts the same)
   // consumer thread 0: the current piece's split words are in ctl
   bool pc_done = false;
   auto piece_splits = [&](long long gb, int j, int n) {
@@ -886,6 +1000,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       const long long slot_row = (c * 2 + (head_cut ? 0 : 1)) * S::HQ;
       const int ha = 2 * qd, hb = 2 * qd + 1;  // heads of this lane's fragment columns
+      // red buffer of this piece; the epilogue warp must be done with its use
+      // two pieces ago
+      const int kbuf = npieces & 1;
+      float *const rbuf = red + kbuf * S::RED_ONE_FLOATS;
+      if (npieces >= 2)
+        __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->red_empty[kbuf]),
+                                          ((npieces >> 1) - 1) & 1, abort_flag, p.err));
       if constexpr (S::NPH == 1) {
         // one warp per kv head: write straight from the fragments
         if (keep_own) named_barrier(1, S::CW * 32);  // all warps are past the ring
@@ -929,11 +1050,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (keep_own) own_lse[g * G + hb] = lse_b;
           }
         }
-        if (!whole) named_barrier(1, S::CW * 32);
+        if (final_piece && !whole) named_barrier(1, S::CW * 32);
       } else {
         // several warps share a kv head: combine through shared memory
         if (ha < G) {
-          float *ra = red + (cw * G + ha) * S::RED_FLOATS_PER_HEAD;
+          float *ra = rbuf + (cw * G + ha) * S::RED_FLOATS_PER_HEAD;
           if (gid == 0) {
             ra[S::RED_M] = m0 == -INFINITY ? -INFINITY : m0 * cl2;
             ra[S::RED_L] = L0;
@@ -945,7 +1066,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
         }
         if (hb < G) {
-          float *rb = red + (cw * G + hb) * S::RED_FLOATS_PER_HEAD;
+          float *rb = rbuf + (cw * G + hb) * S::RED_FLOATS_PER_HEAD;
           if (gid == 0) {
             rb[S::RED_M] = m1 == -INFINITY ? -INFINITY : m1 * cl2;
             rb[S::RED_L] = L1;
@@ -956,81 +1077,81 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             rb[16 * mt + gid + 8] = o[mt][3];
           }
         }
-        named_barrier(1, S::CW * 32);
-        // one thread per query head: the normalised weight of each of its NPH
-        // warps (into the merge scratch) and the piece's lse
-        float *cwt = mw;  // [NPH][HQ]
-        if (ct < S::HQ) {
-          const int qh = ct, gh = qh / G, h = qh % G;
-          float mk[S::NPH], M = -INFINITY;
+      }
+      if constexpr (S::NPH > 1) {
+        // the final piece: the consumers combine it themselves (nothing else
+        // is left for them to do); other pieces go to the epilogue warp
+        if (final_piece) {
+          named_barrier(1, S::CW * 32);
+          // one thread per query head: the normalised weight of each of its NPH
+          // warps (into the merge scratch) and the piece's lse
+          float *cwt = mw;  // [NPH][HQ]
+          if (ct < S::HQ) {
+            const int qh = ct, gh = qh / G, h = qh % G;
+            float mk[S::NPH], M = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < S::NPH; ++k) {
-            mk[k] = red[((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + S::RED_M];
-            M = fmaxf(M, mk[k]);
-          }
-          float L = 0.f;
+            for (int k = 0; k < S::NPH; ++k) {
+              mk[k] = rbuf[((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + S::RED_M];
+              M = fmaxf(M, mk[k]);
+            }
+            float L = 0.f;
 #pragma unroll
-          for (int k = 0; k < S::NPH; ++k) {
-            mk[k] = mk[k] == -INFINITY ? 0.f : exp2f(mk[k] - M);
-            L += red[((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + S::RED_L] * mk[k];
-          }
-          const float inv = L > 0.f ? 1.f / L : 0.f;
+            for (int k = 0; k < S::NPH; ++k) {
+              mk[k] = mk[k] == -INFINITY ? 0.f : exp2f(mk[k] - M);
+              L += rbuf[((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + S::RED_L] * mk[k];
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-          for (int k = 0; k < S::NPH; ++k) cwt[k * S::HQ + qh] = mk[k] * inv;
-          if (!whole) {
-            const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
-            p.part_lse[slot_row + qh] = lse;
-            if (keep_own) own_lse[qh] = lse;
+            for (int k = 0; k < S::NPH; ++k) cwt[k * S::HQ + qh] = mk[k] * inv;
+            if (!whole) {
+              const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+              p.part_lse[slot_row + qh] = lse;
+              if (keep_own) own_lse[qh] = lse;
+            }
           }
+          named_barrier(1, S::CW * 32);
+          for (int item = ct; item < S::HQ * (kHeadDim / 4); item += S::CW * 32) {
+            const int qh = item / (kHeadDim / 4);
+            const int d = (item % (kHeadDim / 4)) * 4;
+            const int gh = qh / G, h = qh % G;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < S::NPH; ++k) {
+              const float wk = cwt[k * S::HQ + qh];
+              const float4 v = *reinterpret_cast<const float4 *>(
+                  rbuf + ((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + d);
+              acc.x += wk * v.x;
+              acc.y += wk * v.y;
+              acc.z += wk * v.z;
+              acc.w += wk * v.w;
+            }
+            if (whole) {
+              store_out4(p.out, p.out_f32, ((long long)b * S::HQ + qh) * kHeadDim + d, acc);
+            } else {
+              *reinterpret_cast<float4 *>(p.part_o + (slot_row + qh) * kHeadDim + d) = acc;
+              if (keep_own) *reinterpret_cast<float4 *>(own_o + qh * kHeadDim + d) = acc;
+            }
+          }
+          named_barrier(1, S::CW * 32);
         }
-        named_barrier(1, S::CW * 32);
-        for (int item = ct; item < S::HQ * (kHeadDim / 4); item += S::CW * 32) {
-          const int qh = item / (kHeadDim / 4);
-          const int d = (item % (kHeadDim / 4)) * 4;
-          const int gh = qh / G, h = qh % G;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int k = 0; k < S::NPH; ++k) {
-            const float wk = cwt[k * S::HQ + qh];
-            const float4 v = *reinterpret_cast<const float4 *>(
-                red + ((gh + k * HKV) * G + h) * S::RED_FLOATS_PER_HEAD + d);
-            acc.x += wk * v.x;
-            acc.y += wk * v.y;
-            acc.z += wk * v.z;
-            acc.w += wk * v.w;
-          }
-          if (whole) {
-            store_out4(p.out, p.out_f32, ((long long)b * S::HQ + qh) * kHeadDim + d, acc);
-          } else {
-            *reinterpret_cast<float4 *>(p.part_o + (slot_row + qh) * kHeadDim + d) = acc;
-            if (keep_own) *reinterpret_cast<float4 *>(own_o + qh * kHeadDim + d) = acc;
-          }
-        }
-        named_barrier(1, S::CW * 32);
       }
 
-      if (!whole && !final_piece) {
-        // the CTA's first piece: the epilogue warp publishes it (fence, arrival)
-        // while the consumers go on with the next piece
+      if (!final_piece) {
+        // hand the piece to the epilogue warp (its rows are in rbuf, or
+        // already written with one warp per kv head) and stream on
         if (ct == 0) {
-          ctl->ew_kind = 1;
-          ctl->ew_b = b;
-          ctl->ew_cs0 = ctl->pc_cs0;
-          ctl->ew_cs1 = ctl->pc_cs1;
-          ctl->ew_pieces = ctl->pc_pieces;
-          mbar_arrive(smem_addr(&ctl->ew_bar));
+          PieceDesc &pd = ctl->desc[kbuf];
+          pd.slot_row = slot_row;
+          pd.cs0 = ctl->pc_cs0;
+          pd.cs1 = ctl->pc_cs1;
+          pd.b = b;
+          pd.kind = whole ? kPieceWhole : kPieceCut;
+          pd.pieces = ctl->pc_pieces;
         }
-        ew_signalled = true;
-      }
-      if (!ew_signalled) {
-        // the CTA's first piece needs no publishing: release the epilogue warp
-        if (ct == 0) {
-          ctl->ew_kind = 0;
-          mbar_arrive(smem_addr(&ctl->ew_bar));
-        }
-        ew_signalled = true;
-      }
-      if (keep_own) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ctl->red_full[kbuf]));
+        ++npieces;
+      } else if (keep_own) {
         // The final piece, cut: publish it; the last piece of the sequence to
         // arrive merges.  Nothing follows the final piece, which the jump out
         // of the loops makes explicit: the accumulators are dead and the merge
@@ -1074,10 +1195,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     it0 += count;
   }
 consumers_done:
-  if (!ew_signalled && ct == 0) {
-    // the walk stopped before any piece ended (inconsistent input)
-    ctl->ew_kind = 0;
-    mbar_arrive(smem_addr(&ctl->ew_bar));
+  {
+    // tell the epilogue warp that no piece follows, once it is done with the
+    // buffer it would look at next
+    const int kbuf = npieces & 1;
+    if (npieces >= 2)
+      __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->red_empty[kbuf]),
+                                        ((npieces >> 1) - 1) & 1, abort_flag, p.err));
+    if (ct == 0) ctl->desc[kbuf].kind = kPieceEnd;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&ctl->red_full[kbuf]));
+    // a merge the epilogue warp left (its piece arrived last)
+    __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->ew_done), 0, abort_flag, p.err));
+    if (ctl->def_pending) {
+      named_barrier(1, S::CW * 32);  // every consumer is done with the ring
+      const int db = ctl->def_b;
+      const long long d0 = ctl->def_cs0, d1 = ctl->def_cs1;
+      if (!merge_sequence_bulk<S::HQ, S::MERGE_MAX_PIECES, S::CW * 32>(
+              p, db, d0, d1, nsplit, N, mw, ct, 1, -1, nullptr, nullptr,
+              reinterpret_cast<float *>(smem), (long long)S::NST * S::STAGE_BYTES,
+              smem_addr(&ctl->merge_bar2), abort_flag))
+        for (int h = cw; h < S::HQ; h += S::CW)
+          merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)db * S::HQ + h, S::HQ, h,
+                    d0, d1, nsplit, N, lane);
+      if (ct == 0) p.counters[d1] = 0;
+    }
   }
 }
 
