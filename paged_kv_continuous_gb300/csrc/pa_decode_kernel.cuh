@@ -108,7 +108,7 @@ struct DecodeShape {
   static constexpr int EWW_BYTES = 256;
   // merge scratch: one weight per (piece, query head), up to MERGE_MAX_PIECES
   static constexpr int MERGE_FLOATS = 2048;
-  static constexpr int MERGE_MAX_PIECES = MERGE_FLOATS / HQ;
+  static constexpr int MERGE_MAX_PIECES = MERGE_FLOATS / HQ - 1;  // + one row of 1 / sums
   static constexpr int MERGE_BYTES = MERGE_FLOATS * 4;
   static constexpr int NST_FIT =
       (kDecodeSmemBudget - 1024 - RED_BYTES - MERGE_BYTES - CTL_BYTES - EWW_BYTES) /
@@ -153,11 +153,16 @@ struct DecodeCtl {
   unsigned long long merge_bar;     // mbarrier: the final merge's bulk copies
   unsigned long long merge_bar2;    // mbarrier: the deferred merge's bulk copies
   unsigned long long ew_done;       // mbarrier: the epilogue warp has finished
+  unsigned long long seen_bar;      // mbarrier: every other piece of the final one arrived
   PieceDesc desc[2];
   // a cut piece the epilogue warp published last: the consumers merge its
   // sequence at their end (def_pending = 1)
   long long def_cs0, def_cs1;
   int def_b, def_pending;
+  // the CTA's final piece, cut: its sequence's counter and piece count, for
+  // the epilogue warp to watch (fin_valid = 1 once written)
+  long long fin_cs1;
+  int fin_pieces, fin_valid;
   unsigned long long total;   // N, blocks of all sequences
   long long first_prefix;    // global index of block 0 of first_b
   int first_b;               // sequence holding this CTA's first block
@@ -283,6 +288,12 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int *ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
@@ -321,8 +332,9 @@ __device__ __forceinline__ void store_out4(void *out, int out_f32, long long idx
 // (written by other CTAs).  When N >= S every split holds at least one
 // block; otherwise empty splits are skipped.  Each lane walks the pieces in
 // split order with the same arithmetic as merge_sequence_bulk (weights
-// exp(lse - M) summed in order, then sum of w_i o_i in order), so the row
-// has the same bits whichever path merges it.
+// e_i = exp(lse_i - M) summed in order, sum of e_i o_i in order, one scale
+// by the reciprocal of the first sum), so the row has the same bits
+// whichever path merges it.
 __device__ __forceinline__ void merge_row(const float *part_o, const float *part_lse, void *out,
                                           int out_f32, long long out_row, int HQ, int h,
                                           long long c0, long long c1, long long S, long long N,
@@ -366,22 +378,24 @@ __device__ __forceinline__ void merge_row(const float *part_o, const float *part
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (!(base + u <= c1 && piece(base + u))) continue;
-      const float wi = (lv[u] == -INFINITY ? 0.f : __expf(lv[u] - M)) * inv;
+      const float wi = lv[u] == -INFINITY ? 0.f : __expf(lv[u] - M);
       acc.x = fmaf(wi, v[u].x, acc.x);
       acc.y = fmaf(wi, v[u].y, acc.y);
       acc.z = fmaf(wi, v[u].z, acc.z);
       acc.w = fmaf(wi, v[u].w, acc.w);
     }
   }
-  store_out4(out, out_f32, out_row * kHeadDim + lane * 4, acc);
+  store_out4(out, out_f32, out_row * kHeadDim + lane * 4,
+             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
 }
 
 // Log-sum-exp merge of all partials of sequence b by the NT consumer
 // threads of one CTA (needs every split of c0..c1 non-empty, N >= S, and
 // k = c1 - c0 + 1 <= MAXP; else returns false having done nothing).  One
 // round of loads brings every (piece, head) lse into `w`, where each head's
-// weights exp(lse - M) / sum are formed.  The pieces' partial rows come into
-// shared memory (`buf`, 16-byte aligned, `buf_bytes` long) by one bulk copy
+// terms e_i = exp(lse_i - M) and the reciprocal of their sum are formed.
+// The pieces' partial rows come into shared memory (`buf`, 16-byte aligned,
+// `buf_bytes` long) by one bulk copy
 // per piece, as many pieces per batch as `buf` holds (all of them for the
 // common few-piece case: one round trip); each thread keeps the weighted
 // sums of its (head, 4 dims) items in registers across batches.  The piece
@@ -424,18 +438,38 @@ __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, 
   for (int e = ct; e < kk * HQ; e += NT)
     w[e] = c0 + e / HQ == c_own ? own_lse[e % HQ] : __ldcg(p.part_lse + row0(e / HQ) + e % HQ);
   named_barrier(bar_id, NT);
+  // per head: e_i = exp(lse_i - M) in w (summed in split order) and the
+  // reciprocal of the sum in winv; up to 16 pieces in registers
+  float *winv = w + kk * HQ;
   for (int h = ct; h < HQ; h += NT) {
-    float M = -INFINITY;
-    for (int i = 0; i < kk; ++i) M = fmaxf(M, w[i * HQ + h]);
     float W = 0.f;
-    for (int i = 0; i < kk; ++i) {
-      const float lse = w[i * HQ + h];
-      const float e = lse == -INFINITY ? 0.f : __expf(lse - M);
-      w[i * HQ + h] = e;
-      W += e;
+    if (kk <= 16) {
+      float lv[16];
+      float M = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        lv[i] = i < kk ? w[i * HQ + h] : -INFINITY;
+        M = fmaxf(M, lv[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (i < kk) {
+          const float e = lv[i] == -INFINITY ? 0.f : __expf(lv[i] - M);
+          w[i * HQ + h] = e;
+          W += e;
+        }
+      }
+    } else {
+      float M = -INFINITY;
+      for (int i = 0; i < kk; ++i) M = fmaxf(M, w[i * HQ + h]);
+      for (int i = 0; i < kk; ++i) {
+        const float lse = w[i * HQ + h];
+        const float e = lse == -INFINITY ? 0.f : __expf(lse - M);
+        w[i * HQ + h] = e;
+        W += e;
+      }
     }
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-    for (int i = 0; i < kk; ++i) w[i * HQ + h] *= inv;
+    winv[h] = W > 0.f ? 1.f / W : 0.f;
   }
   named_barrier(bar_id, NT);
   float4 acc[IPT];
@@ -475,7 +509,9 @@ __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, 
     const int item = ct + t * NT;
     if (item < ITEMS) {
       const int h = item / (kHeadDim / 4), d = (item % (kHeadDim / 4)) * 4;
-      store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d, acc[t]);
+      const float inv = winv[h];
+      store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d,
+                 make_float4(acc[t].x * inv, acc[t].y * inv, acc[t].z * inv, acc[t].w * inv));
     }
   }
   return true;
@@ -595,7 +631,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     mbar_init(smem_addr(&ctl->merge_bar), 1);
     mbar_init(smem_addr(&ctl->merge_bar2), 1);
     mbar_init(smem_addr(&ctl->ew_done), 1);
+    mbar_init(smem_addr(&ctl->seen_bar), 1);
     ctl->def_pending = 0;
+    ctl->fin_valid = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -706,11 +744,47 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     //          merge if the piece arrives last.  The consumers never wait for
     //          this, except to reuse a buffer two pieces later.
     griddep_wait();
+    // While it waits for the next piece, lane 0 watches the arrival counter
+    // of the CTA's final piece (once the consumers have named it): when every
+    // other piece of that sequence has arrived it completes seen_bar, and the
+    // consumers merge at once, without publishing their own piece.
+    int snoop = 0;  // 0: final piece not named yet, 1: watching, 2: done
+    long long fin_cs1 = 0;
+    int fin_pieces = 0;
+    auto wait_full = [&](uint32_t bar, int parity) -> bool {
+      const long long t0 = clock64();
+      while (true) {
+        int done = lane == 0 ? (int)mbar_test_wait(bar, parity) : 0;
+        if (lane == 0 && !done && snoop < 2) {
+          if (snoop == 0 && *reinterpret_cast<volatile int *>(&ctl->fin_valid)) {
+            __threadfence_block();
+            fin_cs1 = ctl->fin_cs1;
+            fin_pieces = ctl->fin_pieces;
+            snoop = 1;
+          }
+          if (snoop == 1 && ld_acquire_gpu(p.counters + fin_cs1) == fin_pieces - 1) {
+            mbar_arrive(smem_addr(&ctl->seen_bar));
+            snoop = 2;
+          }
+        }
+        if (__shfl_sync(0xffffffffu, done, 0)) {
+          __syncwarp();  // the other lanes are ordered after lane 0's observation
+          return true;
+        }
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitTimeoutCycles) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report(p.err, PA_DEVERR_WAIT_TIMEOUT);
+          }
+          return false;
+        }
+        __nanosleep(256);
+      }
+    };
     for (int npe = 0;; ++npe) {
       const int k = npe & 1;
-      const bool got = __all_sync(
-          0xffffffffu,
-          mbar_wait(smem_addr(&ctl->red_full[k]), (npe >> 1) & 1, abort_flag, p.err));
+      const bool got = wait_full(smem_addr(&ctl->red_full[k]), (npe >> 1) & 1);
       const PieceDesc d = ctl->desc[k];
       if (!got || d.kind == kPieceEnd) {
         if (lane == 0) mbar_arrive(smem_addr(&ctl->ew_done));
@@ -828,6 +902,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     ctl->pc_cs1 = cs1;
     ctl->pc_pieces = (int)pieces;
     pc_done = true;
+    const long long last_blk = P + n - 1;
+    if (last_blk >= hi - 1 && (P < lo || last_blk > hi - 1) && N >= nsplit &&
+        pieces <= S::MERGE_MAX_PIECES) {
+      // the CTA's final piece, cut (and mergeable from shared memory): the
+      // epilogue warp watches its sequence's arrival counter meanwhile
+      ctl->fin_cs1 = cs1;
+      ctl->fin_pieces = (int)pieces;
+      __threadfence_block();
+      *reinterpret_cast<volatile int *>(&ctl->fin_valid) = 1;
+    }
   };
   bool need_q = true;  // the q rows of the current piece are not loaded yet
   int wb = first_b;
@@ -1160,10 +1244,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const long long cs0 = ctl->pc_cs0, cs1 = ctl->pc_cs1;
         const int pieces = ctl->pc_pieces;
         if (ct == 0) {
-          __threadfence();  // release: the rows before the arrival
-          const bool last = atomicAdd(p.counters + cs1, 1) == pieces - 1;
-          if (last) fence_acq_rel_gpu();  // acquire the other pieces' rows
-          ctl->last = last;
+          if (mbar_test_wait(smem_addr(&ctl->seen_bar), 0)) {
+            // every other piece had arrived (the epilogue warp acquired their
+            // rows): this piece is the last, no arrival and no publication
+            ctl->last = 1;
+          } else {
+            __threadfence();  // release: the rows before the arrival
+            const bool last = atomicAdd(p.counters + cs1, 1) == pieces - 1;
+            if (last) fence_acq_rel_gpu();  // acquire the other pieces' rows
+            ctl->last = last;
+          }
         }
         named_barrier(1, S::CW * 32);
         if (ctl->last) {
