@@ -11,14 +11,20 @@
 // pool serves the whole GQA group.  Per 128-key tile j:
 //   S   = Q K_j^T      tcgen05.mma (M 128, N 128, K 128), fp32 in TMEM
 //   P   = exp2(S * c - m)  per row, with the causal and length masks (fp32)
-//   O  += P V_j        tcgen05.mma, O accumulated in TMEM; when a row's
-//                      running max grows, its O row is rescaled in TMEM.
+//   O  += P V_j        tcgen05.mma, O accumulated in TMEM.  A row's
+//                      exponentials use a reference max that moves only when
+//                      a tile's max exceeds it by more than 8 (base 2), so
+//                      O is rescaled in TMEM rarely; P stays <= 256.
 //                      P is split into bf16 hi + lo parts (two MMA passes)
 //                      so the product keeps ~16 bits of the fp32 weights.
-// Warp 0 issues TMA loads of the K/V pages (two stages), warp 1 issues the
-// MMAs (one thread) and owns the TMEM allocation, warps 2..5 (one TMEM lane
-// = one row per thread) run the softmax, write P to shared memory as the A
-// operand of the second MMA, and store the output.
+// Warps: 0 loads K tiles and 2 loads V tiles (TMA, two stages each; the 8
+// block-table entries of a tile come in one round of lane loads); 1 issues
+// the MMAs (one thread) and owns the TMEM allocation (S of tile j in buffer
+// j & 1, then O); 3..6 (one TMEM lane = one row per thread) run the softmax,
+// write P to shared memory as the A operand of the second MMA, and store the
+// output.  QK of tile j + 1 is issued before PV of tile j, and the softmax
+// forms tile j + 1's exponentials in registers while PV of tile j runs, so
+// the MMAs overlap the softmax.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -31,19 +37,19 @@
 namespace pa {
 namespace {
 
-constexpr int kPfThreads = 192;
+constexpr int kPfThreads = 224;  // K loader, MMA, V loader, 4 softmax warps
 constexpr int kPfRows = 128;      // M
 constexpr int kPfKeys = 128;      // keys per KV tile (N of the first MMA)
 constexpr int kHalfBytes = 128 * 128;  // 128 rows x 64 dims (bf16) with the 128-byte swizzle
 constexpr int kTileBytes2 = 2 * kHalfBytes;  // one 128 x 128 bf16 operand tile = 32 KB
 // shared memory (offsets from a 1024-aligned base)
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes2;        // 2 stages
-constexpr int kOffV = kOffK + 2 * kTileBytes2;    // 2 stages
-constexpr int kOffP = kOffV + 2 * kTileBytes2;   // P hi, then P lo
+constexpr int kOffK = kOffQ + kTileBytes2;      // K tile j in stage j & 1
+constexpr int kOffV = kOffK + 2 * kTileBytes2;  // V tile j in stage j & 1
+constexpr int kOffP = kOffV + 2 * kTileBytes2;  // P: hi, then lo
 constexpr int kOffBar = kOffP + 2 * kTileBytes2;
 constexpr int kPfSmem = 1024 + kOffBar + 256;
-constexpr int kTmemCols = 256;  // S: columns 0..127, O: 128..255
+constexpr int kTmemCols = 512;  // S0: columns 0..127, S1: 128..255, O: 256..383
 
 struct PrefillParams {
   void *out;
@@ -152,6 +158,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// 2^x by the special-function unit (ex2.approx, relative error ~2^-22).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Byte offset of (row, 16-byte chunk) inside a [128 rows][128 B] swizzled half.
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
@@ -168,18 +181,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t base = smem_addr(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
   // barrier slots
-  const uint32_t b_kv_full0 = smem_addr(bars + 0);   // + 8 * stage
-  const uint32_t b_kv_empty0 = smem_addr(bars + 2);  // + 8 * stage
-  const uint32_t b_q_ready = smem_addr(bars + 4);
-  const uint32_t b_s_full = smem_addr(bars + 5);
-  const uint32_t b_s_free = smem_addr(bars + 6);
-  const uint32_t b_p_full = smem_addr(bars + 7);
-  const uint32_t b_o_full = smem_addr(bars + 8);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 11);
+  // barrier slots ("0" slots: + 8 * (tile & 1))
+  const uint32_t b_k_full0 = smem_addr(bars + 0);
+  const uint32_t b_k_empty0 = smem_addr(bars + 2);
+  const uint32_t b_v_full0 = smem_addr(bars + 4);
+  const uint32_t b_v_empty0 = smem_addr(bars + 6);
+  const uint32_t b_q_ready = smem_addr(bars + 8);
+  const uint32_t b_s_full0 = smem_addr(bars + 9);
+  const uint32_t b_s_free0 = smem_addr(bars + 11);
+  const uint32_t b_p_full = smem_addr(bars + 13);
+  const uint32_t b_o_full0 = smem_addr(bars + 14);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int mt = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  // the last tiles of a chunk see the most keys (causal): they start first
+  const int mt = (int)gridDim.x - 1 - (int)blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int q0 = __ldg(p.cu_seqlens + s);
   const int q_len = __ldg(p.cu_seqlens + s + 1) - q0;
   const int pos0 = mt * PT;
@@ -200,15 +217,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const float c = p.qk_scale_log2;
 
   if (tid == 0) {
-    mbar_init(b_kv_full0, 1);
-    mbar_init(b_kv_full0 + 8, 1);
-    mbar_init(b_kv_empty0, 1);
-    mbar_init(b_kv_empty0 + 8, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_k_full0 + 8 * i, 1);
+      mbar_init(b_k_empty0 + 8 * i, 1);
+      mbar_init(b_v_full0 + 8 * i, 1);
+      mbar_init(b_v_empty0 + 8 * i, 1);
+    }
     mbar_init(b_q_ready, 128);
-    mbar_init(b_s_full, 1);
-    mbar_init(b_s_free, 128);
+    mbar_init(b_s_full0, 1);
+    mbar_init(b_s_full0 + 8, 1);
+    mbar_init(b_s_free0, 128);
+    mbar_init(b_s_free0 + 8, 128);
     mbar_init(b_p_full, 128);
-    mbar_init(b_o_full, 1);
+    mbar_init(b_o_full0, 1);
+    mbar_init(b_o_full0 + 8, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -223,106 +245,123 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 128;
+  const uint32_t tmem_o = tmem + 256;  // S of tile j: tmem + 128 * (j & 1)
 
-  if (warp == 0) {
-    // ---- TMA producer: K and V pages of tile j into stage j & 1 ------------
-    if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k))
-                   : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v))
-                   : "memory");
-      const int32_t *row = p.block_tables + (long long)s * p.bt_stride;
-      int j = 0;
-      for (; j < nkv; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !mbar_wait(b_kv_empty0 + 8 * st, ((j >> 1) - 1) & 1, abort_flag, p.err))
-          break;
-        const uint32_t kdst = base + kOffK + st * kTileBytes2;
-        const uint32_t vdst = base + kOffV + st * kTileBytes2;
-        // pages of this tile that hold keys (the rest stays as it is: masked)
-        int nb = 0;
-        for (int blk = 0; blk < kPfKeys / kBlockSize; ++blk)
-          if (j * kPfKeys + blk * kBlockSize < n) ++nb;
-        uint32_t bytes = 0;
-        bool okall = true;
-        long long phys[kPfKeys / kBlockSize];
-        for (int blk = 0; blk < nb; ++blk) {
-          const int lb = j * (kPfKeys / kBlockSize) + blk;
-          const long long ph = lb < p.bt_stride ? __ldg(row + lb) : -1;
-          phys[blk] = (ph >= 0 && ph < p.num_blocks) ? ph : -1;
-          if (phys[blk] >= 0) bytes += 4 * kBlockSize * 64 * 2;
-          else okall = false;
-        }
-        if (!okall) report(p.err, PA_DEVERR_BLOCK_INDEX);
-        mbar_arrive_expect_tx(b_kv_full0 + 8 * st, bytes);
-        for (int blk = 0; blk < nb; ++blk) {
-          if (phys[blk] < 0) continue;
-          const int z = (int)(phys[blk] * kBlockSize);
+  if (warp == 0 || warp == 2) {
+    // ---- TMA loaders: warp 0 brings the K tiles, warp 2 the V tiles, each
+    //      into stage j & 1 once the MMA that read tile j - 2 there is done;
+    //      separate loaders halve the per-tile issue time (16 boxes each) ----
+    const bool is_k = warp == 0;
+    const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
+    const uint32_t dst0 = base + (is_k ? kOffK : kOffV);
+    const uint32_t b_full0 = is_k ? b_k_full0 : b_v_full0;
+    const uint32_t b_empty0 = is_k ? b_k_empty0 : b_v_empty0;
+    if (lane == 0)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+    const int32_t *row = p.block_tables + (long long)s * p.bt_stride;
+    // block-table entries of four tiles (32 pages) per round of loads, one per
+    // lane: -1 = no key in the page (left as it is: masked), -2 = bad entry
+    long long ph_lane = -1;
+    int j = 0;
+    for (; j < nkv; ++j) {
+      const int st = j & 1;
+      const uint32_t dst = dst0 + st * kTileBytes2, b_full = b_full0 + 8 * st;
+      if ((j & 3) == 0) {
+        const int lb = j * (kPfKeys / kBlockSize) + lane;
+        const bool has = lb * kBlockSize < n;
+        const long long ph = has && lb < p.bt_stride ? __ldg(row + lb) : -2;
+        ph_lane = !has ? -1 : (ph >= 0 && ph < p.num_blocks) ? ph : -2;
+      }
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(b_empty0 + 8 * st, ((j >> 1) - 1) & 1,
+                                                        abort_flag, p.err)))
+        break;
+      // lane L < 8 handles page L of the tile
+      const long long phys = __shfl_sync(0xffffffffu, ph_lane, (j & 3) * 8 + (lane & 7));
+      const bool mine = lane < kPfKeys / kBlockSize;
+      const unsigned okm = __ballot_sync(0xffffffffu, mine && phys >= 0);
+      if (is_k && (__ballot_sync(0xffffffffu, mine && phys == -2) != 0u) && lane == 0)
+        report(p.err, PA_DEVERR_BLOCK_INDEX);
+      if (lane == 0) mbar_arrive_expect_tx(b_full, __popc(okm) * 2u * kBlockSize * 64 * 2);
+      __syncwarp();
+      if (mine && phys >= 0) {
+        const int z = (int)(phys * kBlockSize);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t off = h * kHalfBytes + blk * kBlockSize * 128;
-            tma_load_3d(kdst + off, &tmap_k, h * 64, g, z, b_kv_full0 + 8 * st);
-            tma_load_3d(vdst + off, &tmap_v, h * 64, g, z, b_kv_full0 + 8 * st);
-          }
-        }
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(dst + h * kHalfBytes + lane * kBlockSize * 128, map, h * 64, g, z, b_full);
       }
-      if (*abort_flag) {
-        volatile int never = 0;
-        for (int i = j > 2 ? j - 2 : 0; i < j; ++i)
-          mbar_wait(b_kv_full0 + 8 * (i & 1), (i >> 1) & 1, &never, nullptr);
-      }
+    }
+    if (lane == 0 && *abort_flag) {
+      // copies in flight must land before the CTA's shared memory is released
+      volatile int never = 0;
+      for (int i = j > 2 ? j - 2 : 0; i < j; ++i)
+        mbar_wait(b_full0 + 8 * (i & 1), (i >> 1) & 1, &never, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---- MMA issuer -------------------------------------------------------------
+    // ---- MMA issuer: QK of tile j + 1 goes out before PV of tile j, so the
+    //      score MMA of the next tile overlaps the softmax of this one ------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc(0), idesc_pv = umma_idesc(1);
       bool ok = mbar_wait(b_q_ready, 0, abort_flag, p.err);
       tc_fence_after();
-      int j = 0;
-      for (; j < nkv && ok; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(b_kv_full0 + 8 * st, (j >> 1) & 1, abort_flag, p.err)) break;
-        if (j > 0 && !mbar_wait(b_s_free, (j - 1) & 1, abort_flag, p.err)) break;
+      uint32_t last_bar = 0;  // barrier of the latest commit (drained on abort)
+      int last_par = 0;
+      // S_j = Q K_j^T into S buffer j & 1: 8 k-steps of 16 dims (4 per 64-dim half)
+      auto issue_qk = [&](int j) -> bool {
+        const int sb = j & 1;
+        if (!mbar_wait(b_k_full0 + 8 * sb, (j >> 1) & 1, abort_flag, p.err)) return false;
+        // the softmax of tile j - 2 has read this S buffer
+        if (j >= 2 && !mbar_wait(b_s_free0 + 8 * sb, ((j >> 1) - 1) & 1, abort_flag, p.err))
+          return false;
         tc_fence_after();
-        // S = Q K^T: 8 k-steps of 16 dims (4 per 64-dim swizzled half)
-        const uint32_t kb = base + kOffK + st * kTileBytes2;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          umma_f16(tmem_s, umma_desc(base + kOffQ + off, 16, 1024), umma_desc(kb + off, 16, 1024),
-                   idesc_qk, ks > 0);
+          umma_f16(tmem + 128 * sb, umma_desc(base + kOffQ + off, 16, 1024),
+                   umma_desc(base + kOffK + sb * kTileBytes2 + off, 16, 1024), idesc_qk, ks > 0);
         }
-        umma_commit(b_s_full);
-        // O += (P_hi + P_lo) V: 2 x 8 k-steps of 16 keys; V is MN-major (dims
+        umma_commit(b_s_full0 + 8 * sb);
+        umma_commit(b_k_empty0 + 8 * sb);  // the K stage may be refilled
+        last_bar = b_s_full0 + 8 * sb;
+        last_par = (j >> 1) & 1;
+        return true;
+      };
+      if (ok && nkv > 0) ok = issue_qk(0);
+      int j = 0;
+      for (; j < nkv && ok; ++j) {
+        if (j + 1 < nkv && !issue_qk(j + 1)) break;
+        // O += (P_hi + P_lo) V_j: 2 x 8 k-steps of 16 keys; V is MN-major (dims
         // contiguous): LBO = distance between the two 64-dim halves, SBO = 8 keys
         if (!mbar_wait(b_p_full, j & 1, abort_flag, p.err)) break;
+        if (!mbar_wait(b_v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t vb = base + kOffV + st * kTileBytes2;
+        const uint32_t pb = base + kOffP;
+        const uint32_t vb = base + kOffV + (j & 1) * kTileBytes2;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t pa =
-                base + kOffP + part * kTileBytes2 + (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+            const uint32_t pa = pb + part * kTileBytes2 + (ks >> 2) * kHalfBytes + (ks & 3) * 32;
             umma_f16(tmem_o, umma_desc(pa, 16, 1024),
                      umma_desc(vb + ks * 16 * 128, kHalfBytes, 1024), idesc_pv,
                      (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
           }
         }
-        umma_commit(b_o_full);
-        umma_commit(b_kv_empty0 + 8 * st);
+        umma_commit(b_o_full0 + 8 * (j & 1));
+        umma_commit(b_v_empty0 + 8 * (j & 1));  // the V stage may be refilled
+        last_bar = b_o_full0 + 8 * (j & 1);
+        last_par = (j >> 1) & 1;
       }
-      if (*abort_flag) {
+      if (*abort_flag && last_bar) {
         // let issued MMAs finish before TMEM is released (bounded)
         volatile int never = 0;
-        if (j > 0) mbar_wait(b_o_full, (j - 1) & 1, &never, nullptr);
+        mbar_wait(last_bar, last_par, &never, nullptr);
       }
     }
     __syncwarp();
   } else {
-    // ---- softmax / epilogue warps: thread = row r ---------------------------------
+    // ---- softmax / epilogue warps 3..6: thread = row r (TMEM lane quarter
+    //      w % 4, rows 32 (w % 4) .. + 31) ------------------------------------------
     const int lb = 32 * (warp & 3);  // TMEM lanes this warp may access
     const int r = lb + lane;         // row of the tile
     const int rpos = r / G;          // query position in the tile
@@ -347,32 +386,79 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_arrive(b_q_ready);
     }
 
+    // m: reference max (base-2 units) of this row's exponentials.  It moves
+    // only when a tile's max exceeds it by more than 8 (a factor 256), so P
+    // stays <= 256 and O needs rescaling (after the previous PV) rarely.
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv && ok; ++j) {
+      const int sb = j & 1;  // S buffer of tile j
       // warp-uniform: tcgen05.ld / st below are warp-collective
-      ok = __all_sync(0xffffffffu, mbar_wait(b_s_full, j & 1, abort_flag, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(b_s_full0 + 8 * sb, (j >> 1) & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
       const int key0 = j * kPfKeys;
-      // pass 1: row max over the keys this row sees
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        float sv[32];
-        tmem_ld32(tmem_s + trow + cc * 32, sv);
+      // every row of the tile sees every key of it: no masks
+      const bool tile_full = key0 + kPfKeys - 1 <= prefix + pos0;
+      // the S row into registers, read once; the buffer is then free for QK
+      // of tile j + 2
+      float sv[4][32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (key0 + cc * 32 + i <= limit) mx = fmaxf(mx, sv[i]);
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + 128 * sb + trow + cc * 32, sv[cc]);
+      tc_fence_before();
+      mbar_arrive(b_s_free0 + 8 * sb);
+      // branch-free: masked keys are selected out (a branch per element cost
+      // ~30 cycles each)
+      // eight independent max chains
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+      if (tile_full) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[cc][i]);
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            mx8[i & 7] =
+                fmaxf(mx8[i & 7], key0 + cc * 32 + i <= limit ? sv[cc][i] : -INFINITY);
       }
-      const float m_new = fmaxf(m, mx * c);
-      const float alpha = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
-      // P and O of the previous tile are in use until its PV MMA finishes
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mxc = mx * c;
+      const bool grow = mxc > m + 8.f;
+      const float m_new = grow ? mxc : m;
+      const float alpha = grow && m != -INFINITY ? exp2f(m - m_new) : 1.f;
+      m = m_new;
+      // P = exp2(S c - m) in place, and the row sum (four chains), before
+      // waiting for the previous PV (this overlaps it).  A masked key gets the
+      // exponent -inf, whose 2^x is +0: no branch.
+      float ps8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float x = fmaf(sv[cc][i], c, -m);
+          if (!tile_full) x = key0 + cc * 32 + i <= limit ? x : -INFINITY;
+          const float e = ex2_approx(x);
+          sv[cc][i] = e;
+          ps8[i & 7] += e;
+        }
+      const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) +
+                         ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+      // P and O are in use until the PV of tile j - 1 is done
       if (j > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(b_o_full, (j - 1) & 1, abort_flag, p.err));
+        ok = __all_sync(0xffffffffu, mbar_wait(b_o_full0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1,
+                                              abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
-        // rows whose running max grew rescale their O row (warp-wide: collective ld/st)
+        // rows whose reference max moved rescale their O row (warp-wide:
+        // tcgen05.ld / st are collective)
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
           for (int cc = 0; cc < 4; ++cc) {
@@ -384,27 +470,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
-      // pass 2: P = exp2(S c - m) (S is read a second time), row sum, and the
-      // bf16 hi / lo parts of P straight into shared memory (A operands of
-      // the PV MMAs, 128-byte swizzle)
-      float psum = 0.f;
-#pragma unroll 1
+      l = l * alpha + psum;
+      // P as bf16 hi + lo into shared memory (A operands of the PV MMAs,
+      // 128-byte swizzle).  hi is e with the low 16 mantissa bits cleared
+      // (exactly a bf16); lo = e - hi is exact in fp32 and rounded to bf16,
+      // so hi + lo keeps ~16 bits of e.  Only lo needs a conversion.
+#pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        float sv[32];
-        tmem_ld32(tmem_s + trow + cc * 32, sv);
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int i = 0; i < 8; i += 2) {
             const int idx = q8 * 8 + i;
-            const int k0 = key0 + cc * 32 + idx;
-            const float e0 = k0 <= limit ? exp2f(fmaf(sv[idx], c, -m_new)) : 0.f;
-            const float e1 = k0 + 1 <= limit ? exp2f(fmaf(sv[idx + 1], c, -m_new)) : 0.f;
-            psum += e0 + e1;
-            hi[i / 2] = float2_to_bf16x2(e0, e1);
-            const float2 h2 = bf16x2_to_float2(hi[i / 2]);
-            lo[i / 2] = float2_to_bf16x2(e0 - h2.x, e1 - h2.y);
+            const uint32_t u0 = __float_as_uint(sv[cc][idx]), u1 = __float_as_uint(sv[cc][idx + 1]);
+            hi[i / 2] = __byte_perm(u0, u1, 0x7632);
+            lo[i / 2] = float2_to_bf16x2(sv[cc][idx] - __uint_as_float(u0 & 0xFFFF0000u),
+                                         sv[cc][idx + 1] - __uint_as_float(u1 & 0xFFFF0000u));
           }
           const int ch = cc * 4 + q8;  // 16-byte chunk (8 keys) of the 256-byte row
           const uint32_t off = (ch >> 3) * kHalfBytes + sw128(r, ch & 7);
@@ -417,13 +499,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                        : "memory");
         }
       }
-      tc_fence_before();
-      mbar_arrive(b_s_free);  // S may be overwritten by the next QK MMA
-      l = l * alpha + psum;
-      m = m_new;
       // keys past the end of the sequence: their V rows may hold anything;
-      // zero them so that 0-weight rows add exactly 0 (last tile only)
+      // zero them so that 0-weight rows add exactly 0 (last tile only, once
+      // the V tile has landed)
       if (key0 + kPfKeys > n) {
+        ok = __all_sync(0xffffffffu, mbar_wait(b_v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag,
+                                              p.err));
+        if (!ok) break;
         const uint32_t vb = base + kOffV + (j & 1) * kTileBytes2;
         for (int i = r; i < kPfKeys * 16; i += 128) {
           const int key = i >> 4, ch = i & 15;
@@ -438,7 +520,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_arrive(b_p_full);
     }
     // epilogue: O / l -> out[q0 + pos0 + rpos][g * G + hs][:]
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_o_full, (nkv - 1) & 1, abort_flag, p.err));
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(b_o_full0 + 8 * ((nkv - 1) & 1),
+                                            ((nkv - 1) >> 1) & 1, abort_flag, p.err));
     tc_fence_after();
     if (ok) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
