@@ -20,9 +20,9 @@
 // Warps: 0 loads K tiles and 2 loads V tiles (TMA, two stages each; the 8
 // block-table entries of a tile come in one round of lane loads); 1 issues
 // the MMAs (one thread) and owns the TMEM allocation (S of tile j in buffer
-// j & 1, then O); 3..6 (one TMEM lane = one row per thread) run the softmax,
-// write P to shared memory as the A operand of the second MMA, and store the
-// output.  QK of tile j + 1 is issued before PV of tile j, and the softmax
+// j & 1, then O and P); 3..6 (one TMEM lane = one row per thread) run the
+// softmax, write P into their TMEM lanes (the second MMA reads its A operand
+// from tensor memory), and store the output.  QK of tile j + 1 is issued before PV of tile j, and the softmax
 // forms tile j + 1's exponentials in registers while PV of tile j runs, so
 // the MMAs overlap the softmax.
 #include <cmath>
@@ -46,10 +46,12 @@ constexpr int kTileBytes2 = 2 * kHalfBytes;  // one 128 x 128 bf16 operand tile 
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileBytes2;      // K tile j in stage j & 1
 constexpr int kOffV = kOffK + 2 * kTileBytes2;  // V tile j in stage j & 1
-constexpr int kOffP = kOffV + 2 * kTileBytes2;  // P: hi, then lo
-constexpr int kOffBar = kOffP + 2 * kTileBytes2;
+constexpr int kOffBar = kOffV + 2 * kTileBytes2;
 constexpr int kPfSmem = 1024 + kOffBar + 256;
-constexpr int kTmemCols = 512;  // S0: columns 0..127, S1: 128..255, O: 256..383
+// TMEM columns: S of tile j at 128 (j & 1) (fp32), O at 256 (fp32), P at 384:
+// bf16 hi parts in 384..447, lo parts in 448..511 (two keys per column)
+constexpr int kTmemCols = 512;
+constexpr int kTmemO = 256, kTmemP = 384;
 
 struct PrefillParams {
   void *out;
@@ -94,6 +96,18 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// As umma_f16, with A (M x 16, K-major, two bf16 per 32-bit column) read
+// from tensor memory at column address a_tmem.
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -146,6 +160,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane; completes at the
+// next tmem_wait_st().
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
@@ -245,7 +275,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem + 256;  // S of tile j: tmem + 128 * (j & 1)
+  const uint32_t tmem_o = tmem + kTmemO;  // S of tile j: tmem + 128 * (j & 1)
+  const uint32_t tmem_p = tmem + kTmemP;
 
   if (warp == 0 || warp == 2) {
     // ---- TMA loaders: warp 0 brings the K tiles, warp 2 the V tiles, each
@@ -330,22 +361,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       int j = 0;
       for (; j < nkv && ok; ++j) {
         if (j + 1 < nkv && !issue_qk(j + 1)) break;
-        // O += (P_hi + P_lo) V_j: 2 x 8 k-steps of 16 keys; V is MN-major (dims
-        // contiguous): LBO = distance between the two 64-dim halves, SBO = 8 keys
+        // O += (P_hi + P_lo) V_j: 2 x 8 k-steps of 16 keys, P from TMEM (8
+        // columns per step); V is MN-major (dims contiguous): LBO = distance
+        // between the two 64-dim halves, SBO = 8 keys
         if (!mbar_wait(b_p_full, j & 1, abort_flag, p.err)) break;
         if (!mbar_wait(b_v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t pb = base + kOffP;
         const uint32_t vb = base + kOffV + (j & 1) * kTileBytes2;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t pa = pb + part * kTileBytes2 + (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-            umma_f16(tmem_o, umma_desc(pa, 16, 1024),
-                     umma_desc(vb + ks * 16 * 128, kHalfBytes, 1024), idesc_pv,
-                     (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            umma_f16_ta(tmem_o, tmem_p + part * 64 + ks * 8,
+                        umma_desc(vb + ks * 16 * 128, kHalfBytes, 1024), idesc_pv,
+                        (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
         }
         umma_commit(b_o_full0 + 8 * (j & 1));
         umma_commit(b_v_empty0 + 8 * (j & 1));  // the V stage may be refilled
@@ -471,34 +500,26 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       }
       l = l * alpha + psum;
-      // P as bf16 hi + lo into shared memory (A operands of the PV MMAs,
-      // 128-byte swizzle).  hi is e with the low 16 mantissa bits cleared
-      // (exactly a bf16); lo = e - hi is exact in fp32 and rounded to bf16,
-      // so hi + lo keeps ~16 bits of e.  Only lo needs a conversion.
+      // P as bf16 hi + lo into this row's TMEM lane (A operands of the PV
+      // MMAs; keys 2i and 2i + 1 share column i, the even key in the low
+      // half).  hi is e with the low 16 mantissa bits cleared (exactly a
+      // bf16); lo = e - hi is exact in fp32 and rounded to bf16, so hi + lo
+      // keeps ~16 bits of e.  Only lo needs a conversion.
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
+        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int i = 0; i < 8; i += 2) {
-            const int idx = q8 * 8 + i;
-            const uint32_t u0 = __float_as_uint(sv[cc][idx]), u1 = __float_as_uint(sv[cc][idx + 1]);
-            hi[i / 2] = __byte_perm(u0, u1, 0x7632);
-            lo[i / 2] = float2_to_bf16x2(sv[cc][idx] - __uint_as_float(u0 & 0xFFFF0000u),
-                                         sv[cc][idx + 1] - __uint_as_float(u1 & 0xFFFF0000u));
-          }
-          const int ch = cc * 4 + q8;  // 16-byte chunk (8 keys) of the 256-byte row
-          const uint32_t off = (ch >> 3) * kHalfBytes + sw128(r, ch & 7);
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(base + kOffP + off),
-                       "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3])
-                       : "memory");
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           base + kOffP + kTileBytes2 + off),
-                       "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
-                       : "memory");
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t u0 = __float_as_uint(sv[cc][2 * i]);
+          const uint32_t u1 = __float_as_uint(sv[cc][2 * i + 1]);
+          hi[i] = __byte_perm(u0, u1, 0x7632);
+          lo[i] = float2_to_bf16x2(sv[cc][2 * i] - __uint_as_float(u0 & 0xFFFF0000u),
+                                   sv[cc][2 * i + 1] - __uint_as_float(u1 & 0xFFFF0000u));
         }
+        tmem_st16(tmem_p + trow + cc * 16, hi);
+        tmem_st16(tmem_p + trow + 64 + cc * 16, lo);
       }
+      tmem_wait_st();
       // keys past the end of the sequence: their V rows may hold anything;
       // zero them so that 0-weight rows add exactly 0 (last tile only, once
       // the V tile has landed)
@@ -514,8 +535,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
           }
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(b_p_full);
     }
