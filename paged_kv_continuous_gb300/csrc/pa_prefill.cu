@@ -436,25 +436,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + 128 * sb + trow + cc * 32, sv[cc]);
       tc_fence_before();
       mbar_arrive(b_s_free0 + 8 * sb);
-      // branch-free: masked keys are selected out (a branch per element cost
-      // ~30 cycles each)
-      // eight independent max chains
-      float mx8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-      if (tile_full) {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[cc][i]);
-      } else {
+      // masked keys (diagonal and last tiles only) become -inf before the
+      // max, so the max and the exponentials below have a single, unmasked
+      // body (selects, not branches; one copy of the code keeps the
+      // instruction cache warm)
+      if (!tile_full) {
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            mx8[i & 7] =
-                fmaxf(mx8[i & 7], key0 + cc * 32 + i <= limit ? sv[cc][i] : -INFINITY);
+            sv[cc][i] = key0 + cc * 32 + i <= limit ? sv[cc][i] : -INFINITY;
       }
+      // eight independent max chains
+      float mx8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[cc][i]);
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float mxc = mx * c;
@@ -462,9 +462,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float m_new = grow ? mxc : m;
       const float alpha = grow && m != -INFINITY ? exp2f(m - m_new) : 1.f;
       m = m_new;
-      // P = exp2(S c - m) in place, and the row sum (four chains), before
-      // waiting for the previous PV (this overlaps it).  A masked key gets the
-      // exponent -inf, whose 2^x is +0: no branch.
+      // P = exp2(S c - m) in place, and the row sum (eight chains), before
+      // waiting for the previous PV (this overlaps it).  A masked key has
+      // S = -inf, so its exponent is -inf and 2^x = +0; a row with no key yet
+      // (m = -inf: rows past the chunk) takes offset 0 instead of +inf, which
+      // keeps it -inf rather than NaN.
+      const float neg_m = m == -INFINITY ? 0.f : -m;
       float ps8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
@@ -472,9 +475,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          float x = fmaf(sv[cc][i], c, -m);
-          if (!tile_full) x = key0 + cc * 32 + i <= limit ? x : -INFINITY;
-          const float e = ex2_approx(x);
+          const float e = ex2_approx(fmaf(sv[cc][i], c, neg_m));
           sv[cc][i] = e;
           ps8[i & 7] += e;
         }
@@ -503,8 +504,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // P as bf16 hi + lo into this row's TMEM lane (A operands of the PV
       // MMAs; keys 2i and 2i + 1 share column i, the even key in the low
       // half).  hi is e with the low 16 mantissa bits cleared (exactly a
-      // bf16); lo = e - hi is exact in fp32 and rounded to bf16, so hi + lo
-      // keeps ~16 bits of e.  Only lo needs a conversion.
+      // bf16); lo = e - hi is exact in fp32 and likewise truncated to bf16,
+      // so hi + lo is e within 2^-14 relative.  Both are byte permutes.
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t hi[16], lo[16];
@@ -513,8 +514,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const uint32_t u0 = __float_as_uint(sv[cc][2 * i]);
           const uint32_t u1 = __float_as_uint(sv[cc][2 * i + 1]);
           hi[i] = __byte_perm(u0, u1, 0x7632);
-          lo[i] = float2_to_bf16x2(sv[cc][2 * i] - __uint_as_float(u0 & 0xFFFF0000u),
-                                   sv[cc][2 * i + 1] - __uint_as_float(u1 & 0xFFFF0000u));
+          lo[i] = __byte_perm(__float_as_uint(sv[cc][2 * i] - __uint_as_float(u0 & 0xFFFF0000u)),
+                              __float_as_uint(sv[cc][2 * i + 1] -
+                                              __uint_as_float(u1 & 0xFFFF0000u)),
+                              0x7632);
         }
         tmem_st16(tmem_p + trow + cc * 16, hi);
         tmem_st16(tmem_p + trow + 64 + cc * 16, lo);
