@@ -17,14 +17,15 @@
 //                      O is rescaled in TMEM rarely; P stays <= 256.
 //                      P is split into bf16 hi + lo parts (two MMA passes)
 //                      so the product keeps ~16 bits of the fp32 weights.
-// Warps: 0 loads K tiles and 2 loads V tiles (TMA, two stages each; the 8
+// Warps: 0 loads K tiles and 2 loads V tiles (TMA, 3 and 2 stages; the 8
 // block-table entries of a tile come in one round of lane loads); 1 issues
-// the MMAs (one thread) and owns the TMEM allocation (S of tile j in buffer
-// j & 1, then O and P); 3..6 (one TMEM lane = one row per thread) run the
-// softmax, write P into their TMEM lanes (the second MMA reads its A operand
-// from tensor memory), and store the output.  QK of tile j + 1 is issued before PV of tile j, and the softmax
-// forms tile j + 1's exponentials in registers while PV of tile j runs, so
-// the MMAs overlap the softmax.
+// the MMAs (one thread) and owns the TMEM allocation (S, O and two P
+// buffers); 3..10 run the softmax, two warps per TMEM lane quarter, each
+// thread one half (64 keys, 64 output columns) of one row: they write P into
+// their TMEM lanes (the second MMA reads its A operand from tensor memory)
+// and store the output.  QK of tile j + 1 is issued as soon as the softmax
+// has copied S_j to registers, and P_{j+1} goes to the other P buffer, so the
+// softmax of tile j + 1 runs while the PV MMA of tile j still reads P_j.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -37,21 +38,31 @@
 namespace pa {
 namespace {
 
-constexpr int kPfThreads = 224;  // K loader, MMA, V loader, 4 softmax warps
+constexpr int kPfSoftWarps = 8;   // two per TMEM lane quarter: each takes half of a row
+constexpr int kPfThreads = 32 * (3 + kPfSoftWarps);  // K loader, MMA, V loader, softmax
 constexpr int kPfRows = 128;      // M
 constexpr int kPfKeys = 128;      // keys per KV tile (N of the first MMA)
 constexpr int kHalfBytes = 128 * 128;  // 128 rows x 64 dims (bf16) with the 128-byte swizzle
 constexpr int kTileBytes2 = 2 * kHalfBytes;  // one 128 x 128 bf16 operand tile = 32 KB
 // shared memory (offsets from a 1024-aligned base)
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes2;      // K tile j in stage j & 1
-constexpr int kOffV = kOffK + 2 * kTileBytes2;  // V tile j in stage j & 1
-constexpr int kOffBar = kOffV + 2 * kTileBytes2;
-constexpr int kPfSmem = 1024 + kOffBar + 256;
-// TMEM columns: S of tile j at 128 (j & 1) (fp32), O at 256 (fp32), P at 384:
-// bf16 hi parts in 384..447, lo parts in 448..511 (two keys per column)
+// K tiles are needed first (the score MMA of tile j + 1 is issued before
+// the PV MMA of tile j), so their ring is one stage deeper
+constexpr int kKStages = 3, kVStages = 2;
+constexpr int kOffK = kOffQ + kTileBytes2;               // K tile j in stage j % 3
+constexpr int kOffV = kOffK + kKStages * kTileBytes2;    // V tile j in stage j % 2
+constexpr int kOffBar = kOffV + kVStages * kTileBytes2;
+// partial row maxima / sums exchanged by the two halves of a row:
+// [tile parity][half][row] fp32
+constexpr int kOffX = kOffBar + 256;
+constexpr int kPfSmem = 1024 + kOffX + 2 * 2 * kPfRows * 4;
+// TMEM columns: S at 0..127 (fp32; the softmax copies it to registers at
+// once), O at 128..255 (fp32), P of tile j at 256 + 128 (j & 1): bf16 hi
+// parts in the first 64 columns, lo parts in the next 64 (two keys per
+// column).  Two P buffers let the softmax of tile j + 1 run while the PV MMA
+// of tile j still reads P_j.
 constexpr int kTmemCols = 512;
-constexpr int kTmemO = 256, kTmemP = 384;
+constexpr int kTmemS = 0, kTmemO = 128, kTmemP = 256;
 
 struct PrefillParams {
   void *out;
@@ -89,12 +100,18 @@ __host__ __device__ constexpr uint32_t umma_idesc(int b_mn) {
          ((uint32_t)(kPfKeys >> 3) << 17) | ((uint32_t)(kPfRows >> 4) << 24);
 }
 
+// The MMA, commit and TMA helpers below are executed by a whole converged
+// warp whose role branch the compiler can see is warp-uniform: every lane
+// computes the same operands (kept in uniform registers) and one lane, picked
+// by elect.sync, issues.  Issued from a lone lane in a divergent branch, each
+// MMA cost about three times its tensor-pipe time.
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -104,17 +121,21 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
 __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -182,8 +203,10 @@ __device__ __forceinline__ void tmem_wait_st() {
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             int z, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
@@ -210,21 +233,26 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t base = smem_addr(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-  // barrier slots
-  // barrier slots ("0" slots: + 8 * (tile & 1))
+  // barrier slots ("0" slots: + 8 * stage, or + 8 * (tile & 1))
   const uint32_t b_k_full0 = smem_addr(bars + 0);
-  const uint32_t b_k_empty0 = smem_addr(bars + 2);
-  const uint32_t b_v_full0 = smem_addr(bars + 4);
-  const uint32_t b_v_empty0 = smem_addr(bars + 6);
-  const uint32_t b_q_ready = smem_addr(bars + 8);
-  const uint32_t b_s_full0 = smem_addr(bars + 9);
-  const uint32_t b_s_free0 = smem_addr(bars + 11);
-  const uint32_t b_p_full = smem_addr(bars + 13);
-  const uint32_t b_o_full0 = smem_addr(bars + 14);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
+  const uint32_t b_k_empty0 = smem_addr(bars + 3);
+  const uint32_t b_v_full0 = smem_addr(bars + 6);
+  const uint32_t b_v_empty0 = smem_addr(bars + 8);
+  const uint32_t b_q_ready = smem_addr(bars + 10);
+  const uint32_t b_s_full = smem_addr(bars + 11);
+  const uint32_t b_s_free = smem_addr(bars + 12);
+  const uint32_t b_p_full0 = smem_addr(bars + 13);
+  const uint32_t b_o_full0 = smem_addr(bars + 15);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 18);
+  // exchange barrier of lane quarter qq, tile parity t: bars + 19 + 2 qq + t
+  const uint32_t b_x0 = smem_addr(bars + 19);
+  float *xch = reinterpret_cast<float *>(smem + kOffX);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31;
+  // broadcast from lane 0: the compiler then knows every role branch below
+  // is warp-uniform
+  const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
   // the last tiles of a chunk see the most keys (causal): they start first
   const int mt = (int)gridDim.x - 1 - (int)blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int q0 = __ldg(p.cu_seqlens + s);
@@ -247,18 +275,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const float c = p.qk_scale_log2;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(b_k_full0 + 8 * i, 1);
       mbar_init(b_k_empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(b_v_full0 + 8 * i, 1);
       mbar_init(b_v_empty0 + 8 * i, 1);
     }
-    mbar_init(b_q_ready, 128);
-    mbar_init(b_s_full0, 1);
-    mbar_init(b_s_full0 + 8, 1);
-    mbar_init(b_s_free0, 128);
-    mbar_init(b_s_free0 + 8, 128);
-    mbar_init(b_p_full, 128);
+    constexpr int kSoft = 32 * kPfSoftWarps;
+    mbar_init(b_q_ready, kSoft);
+    mbar_init(b_s_full, 1);
+    mbar_init(b_s_free, kSoft);
+    mbar_init(b_p_full0, kSoft);
+    mbar_init(b_p_full0 + 8, kSoft);
+    for (int i = 0; i < 8; ++i) mbar_init(b_x0 + 8 * i, 64);
     mbar_init(b_o_full0, 1);
     mbar_init(b_o_full0 + 8, 1);
     *abort_flag = 0;
@@ -275,18 +306,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem + kTmemO;  // S of tile j: tmem + 128 * (j & 1)
-  const uint32_t tmem_p = tmem + kTmemP;
+  const uint32_t tmem_s = tmem + kTmemS, tmem_o = tmem + kTmemO, tmem_p = tmem + kTmemP;
 
   if (warp == 0 || warp == 2) {
     // ---- TMA loaders: warp 0 brings the K tiles, warp 2 the V tiles, each
-    //      into stage j & 1 once the MMA that read tile j - 2 there is done;
+    //      into stage j % stages once the MMA that read the stage's previous
+    //      tile is done;
     //      separate loaders halve the per-tile issue time (16 boxes each) ----
     const bool is_k = warp == 0;
     const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
     const uint32_t dst0 = base + (is_k ? kOffK : kOffV);
     const uint32_t b_full0 = is_k ? b_k_full0 : b_v_full0;
     const uint32_t b_empty0 = is_k ? b_k_empty0 : b_v_empty0;
+    const int nst = is_k ? kKStages : kVStages;
     if (lane == 0)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
     const int32_t *row = p.block_tables + (long long)s * p.bt_stride;
@@ -295,7 +327,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     long long ph_lane = -1;
     int j = 0;
     for (; j < nkv; ++j) {
-      const int st = j & 1;
+      const int st = j % nst, round = j / nst;
       const uint32_t dst = dst0 + st * kTileBytes2, b_full = b_full0 + 8 * st;
       if ((j & 3) == 0) {
         const int lb = j * (kPfKeys / kBlockSize) + lane;
@@ -303,8 +335,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const long long ph = has && lb < p.bt_stride ? __ldg(row + lb) : -2;
         ph_lane = !has ? -1 : (ph >= 0 && ph < p.num_blocks) ? ph : -2;
       }
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(b_empty0 + 8 * st, ((j >> 1) - 1) & 1,
-                                                        abort_flag, p.err)))
+      if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(b_empty0 + 8 * st, (round - 1) & 1,
+                                                           abort_flag, p.err)))
         break;
       // lane L < 8 handles page L of the tile
       const long long phys = __shfl_sync(0xffffffffu, ph_lane, (j & 3) * 8 + (lane & 7));
@@ -314,65 +346,76 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         report(p.err, PA_DEVERR_BLOCK_INDEX);
       if (lane == 0) mbar_arrive_expect_tx(b_full, __popc(okm) * 2u * kBlockSize * 64 * 2);
       __syncwarp();
-      if (mine && phys >= 0) {
-        const int z = (int)(phys * kBlockSize);
+      // one page at a time, its index broadcast to the whole warp
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(dst + h * kHalfBytes + lane * kBlockSize * 128, map, h * 64, g, z, b_full);
+      for (int pg = 0; pg < kPfKeys / kBlockSize; ++pg) {
+        const long long ph = __shfl_sync(0xffffffffu, phys, pg);
+        if (ph >= 0) {
+          const int z = (int)(ph * kBlockSize);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(dst + h * kHalfBytes + pg * kBlockSize * 128, map, h * 64, g, z, b_full);
+        }
       }
     }
     if (lane == 0 && *abort_flag) {
       // copies in flight must land before the CTA's shared memory is released
       volatile int never = 0;
-      for (int i = j > 2 ? j - 2 : 0; i < j; ++i)
-        mbar_wait(b_full0 + 8 * (i & 1), (i >> 1) & 1, &never, nullptr);
+      for (int i = j > nst ? j - nst : 0; i < j; ++i)
+        mbar_wait(b_full0 + 8 * (i % nst), (i / nst) & 1, &never, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---- MMA issuer: QK of tile j + 1 goes out before PV of tile j, so the
-    //      score MMA of the next tile overlaps the softmax of this one ------------
-    if (lane == 0) {
+    // ---- MMA issuer: QK of tile j + 1 goes out (once the softmax has copied
+    //      S_j to registers) before PV of tile j, so the score MMA of the next
+    //      tile overlaps the softmax of this one ----------------------------------
+    {  // the whole warp, converged (see umma_f16)
       constexpr uint32_t idesc_qk = umma_idesc(0), idesc_pv = umma_idesc(1);
-      bool ok = mbar_wait(b_q_ready, 0, abort_flag, p.err);
+      constexpr unsigned kAll = 0xffffffffu;
+      bool ok = __all_sync(kAll, mbar_wait(b_q_ready, 0, abort_flag, p.err));
       tc_fence_after();
       uint32_t last_bar = 0;  // barrier of the latest commit (drained on abort)
       int last_par = 0;
-      // S_j = Q K_j^T into S buffer j & 1: 8 k-steps of 16 dims (4 per 64-dim half)
+      // S_j = Q K_j^T: 8 k-steps of 16 dims (4 per 64-dim half)
       auto issue_qk = [&](int j) -> bool {
-        const int sb = j & 1;
-        if (!mbar_wait(b_k_full0 + 8 * sb, (j >> 1) & 1, abort_flag, p.err)) return false;
-        // the softmax of tile j - 2 has read this S buffer
-        if (j >= 2 && !mbar_wait(b_s_free0 + 8 * sb, ((j >> 1) - 1) & 1, abort_flag, p.err))
+        const int ks3 = j % kKStages;
+        if (!__all_sync(kAll, mbar_wait(b_k_full0 + 8 * ks3, (j / kKStages) & 1, abort_flag,
+                                        p.err)))
+          return false;
+        // the softmax has copied S_{j-1} to its registers
+        if (j >= 1 && !__all_sync(kAll, mbar_wait(b_s_free, (j - 1) & 1, abort_flag, p.err)))
           return false;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          umma_f16(tmem + 128 * sb, umma_desc(base + kOffQ + off, 16, 1024),
-                   umma_desc(base + kOffK + sb * kTileBytes2 + off, 16, 1024), idesc_qk, ks > 0);
+          umma_f16(tmem_s, umma_desc(base + kOffQ + off, 16, 1024),
+                   umma_desc(base + kOffK + ks3 * kTileBytes2 + off, 16, 1024), idesc_qk, ks > 0);
         }
-        umma_commit(b_s_full0 + 8 * sb);
-        umma_commit(b_k_empty0 + 8 * sb);  // the K stage may be refilled
-        last_bar = b_s_full0 + 8 * sb;
-        last_par = (j >> 1) & 1;
+        umma_commit(b_s_full);
+        umma_commit(b_k_empty0 + 8 * ks3);  // the K stage may be refilled
+        last_bar = b_s_full;
+        last_par = j & 1;
         return true;
       };
       if (ok && nkv > 0) ok = issue_qk(0);
       int j = 0;
       for (; j < nkv && ok; ++j) {
         if (j + 1 < nkv && !issue_qk(j + 1)) break;
-        // O += (P_hi + P_lo) V_j: 2 x 8 k-steps of 16 keys, P from TMEM (8
-        // columns per step); V is MN-major (dims contiguous): LBO = distance
-        // between the two 64-dim halves, SBO = 8 keys
-        if (!mbar_wait(b_p_full, j & 1, abort_flag, p.err)) break;
-        if (!mbar_wait(b_v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.err)) break;
+        // O += (P_hi + P_lo) V_j: 2 x 8 k-steps of 16 keys, P_j from TMEM
+        // buffer j & 1 (8 columns per step); V is MN-major (dims contiguous):
+        // LBO = distance between the two 64-dim halves, SBO = 8 keys
+        if (!__all_sync(kAll, mbar_wait(b_p_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.err)))
+          break;
+        if (!__all_sync(kAll, mbar_wait(b_v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.err)))
+          break;
         tc_fence_after();
         const uint32_t vb = base + kOffV + (j & 1) * kTileBytes2;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_f16_ta(tmem_o, tmem_p + part * 64 + ks * 8,
+            umma_f16_ta(tmem_o, tmem_p + (j & 1) * 128 + part * 64 + ks * 8,
                         umma_desc(vb + ks * 16 * 128, kHalfBytes, 1024), idesc_pv,
                         (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
         }
@@ -381,7 +424,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         last_bar = b_o_full0 + 8 * (j & 1);
         last_par = (j >> 1) & 1;
       }
-      if (*abort_flag && last_bar) {
+      if (__any_sync(kAll, *abort_flag != 0) && last_bar) {
         // let issued MMAs finish before TMEM is released (bounded)
         volatile int never = 0;
         mbar_wait(last_bar, last_par, &never, nullptr);
@@ -389,24 +432,40 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---- softmax / epilogue warps 3..6: thread = row r (TMEM lane quarter
-    //      w % 4, rows 32 (w % 4) .. + 31) ------------------------------------------
+    // ---- softmax / epilogue warps 3..10: warp w serves TMEM lane quarter
+    //      w % 4 (rows 32 (w % 4) .. + 31) and half hf of every row's keys
+    //      and output columns; the two warps of a quarter exchange partial
+    //      row maxima (and, at the end, sums) through shared memory ---------
     const int lb = 32 * (warp & 3);  // TMEM lanes this warp may access
+    const int hf = (warp - 3) >> 2;  // 0: keys / columns 0..63, 1: 64..127
     const int r = lb + lane;         // row of the tile
     const int rpos = r / G;          // query position in the tile
     const int hs = r % G;            // query head in the group
     const bool rvalid = r < rows;
     const int limit = rvalid ? prefix + pos0 + rpos : -1;  // last key this row sees
     const uint32_t trow = (uint32_t)lb << 16;
+    const uint32_t b_x = b_x0 + 8 * 2 * (warp & 3);  // + 8 * parity
+    // partial value v of this half for exchange t; returns the other half's
+    // (bounded wait: false on abort)
+    auto exchange = [&](int t, float v, float &other) -> bool {
+      xch[((t & 1) * 2 + hf) * kPfRows + r] = v;
+      mbar_arrive(b_x + 8 * (t & 1));
+      if (!__all_sync(0xffffffffu, mbar_wait(b_x + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.err)))
+        return false;
+      other = xch[((t & 1) * 2 + (hf ^ 1)) * kPfRows + r];
+      return true;
+    };
 
-    // Q tile: row r = q[q0 + pos0 + rpos][g * G + hs][:], 128-byte swizzle
+    // Q tile: row r = q[q0 + pos0 + rpos][g * G + hs][:], 128-byte swizzle;
+    // this half brings dims 64 hf .. 64 hf + 63
     {
       const uint4 *src = reinterpret_cast<const uint4 *>(
           p.q + ((long long)(q0 + pos0 + rpos) * p.hq + g * G + hs) * kHeadDim);
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const int ch = hf * 8 + c8;
         const uint4 v = rvalid ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t a = base + kOffQ + (ch >> 3) * kHalfBytes + sw128(r, ch & 7);
+        const uint32_t a = base + kOffQ + hf * kHalfBytes + sw128(r, c8);
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
                      "r"(v.z), "r"(v.w)
                      : "memory");
@@ -415,64 +474,70 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_arrive(b_q_ready);
     }
 
-    // m: reference max (base-2 units) of this row's exponentials.  It moves
+    // m: reference max (base-2 units) of this row's exponentials, the same
+    // in both halves (both combine the same two partial maxima).  It moves
     // only when a tile's max exceeds it by more than 8 (a factor 256), so P
     // stays <= 256 and O needs rescaling (after the previous PV) rarely.
+    // l: this half's share of the row sum.
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv && ok; ++j) {
-      const int sb = j & 1;  // S buffer of tile j
       // warp-uniform: tcgen05.ld / st below are warp-collective
-      ok = __all_sync(0xffffffffu, mbar_wait(b_s_full0 + 8 * sb, (j >> 1) & 1, abort_flag, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(b_s_full, j & 1, abort_flag, p.err));
       if (!ok) break;
       tc_fence_after();
-      const int key0 = j * kPfKeys;
+      const int key0 = j * kPfKeys + hf * 64;  // first key of this half
       // every row of the tile sees every key of it: no masks
-      const bool tile_full = key0 + kPfKeys - 1 <= prefix + pos0;
-      // the S row into registers, read once; the buffer is then free for QK
-      // of tile j + 2
-      float sv[4][32];
+      const bool tile_full = j * kPfKeys + kPfKeys - 1 <= prefix + pos0;
+      // this half of the S row into registers, read once; S is then free for
+      // QK of tile j + 1
+      float sv[2][32];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + 128 * sb + trow + cc * 32, sv[cc]);
+      for (int cc = 0; cc < 2; ++cc) tmem_ld32(tmem_s + hf * 64 + trow + cc * 32, sv[cc]);
       tc_fence_before();
-      mbar_arrive(b_s_free0 + 8 * sb);
+      mbar_arrive(b_s_free);
       // masked keys (diagonal and last tiles only) become -inf before the
       // max, so the max and the exponentials below have a single, unmasked
       // body (selects, not branches; one copy of the code keeps the
       // instruction cache warm)
       if (!tile_full) {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             sv[cc][i] = key0 + cc * 32 + i <= limit ? sv[cc][i] : -INFINITY;
       }
-      // eight independent max chains
+      // eight independent max chains, then the other half's partial max
       float mx8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+      for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
         for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[cc][i]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mx_mine = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                  fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      float mx_other;
+      ok = exchange(j, mx_mine, mx_other);
+      if (!ok) break;
+      // the same operands in the same order in both halves: the same m
+      const float mx = hf == 0 ? fmaxf(mx_mine, mx_other) : fmaxf(mx_other, mx_mine);
       const float mxc = mx * c;
       const bool grow = mxc > m + 8.f;
       const float m_new = grow ? mxc : m;
       const float alpha = grow && m != -INFINITY ? exp2f(m - m_new) : 1.f;
       m = m_new;
-      // P = exp2(S c - m) in place, and the row sum (eight chains), before
-      // waiting for the previous PV (this overlaps it).  A masked key has
-      // S = -inf, so its exponent is -inf and 2^x = +0; a row with no key yet
-      // (m = -inf: rows past the chunk) takes offset 0 instead of +inf, which
-      // keeps it -inf rather than NaN.
+      // P = exp2(S c - m) in place, and this half's sum (eight chains),
+      // before waiting for the previous PV (this overlaps it).  A masked key
+      // has S = -inf, so its exponent is -inf and 2^x = +0; a row with no key
+      // yet (m = -inf: rows past the chunk) takes offset 0 instead of +inf,
+      // which keeps it -inf rather than NaN.
       const float neg_m = m == -INFINITY ? 0.f : -m;
       float ps8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+      for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float e = ex2_approx(fmaf(sv[cc][i], c, neg_m));
@@ -481,33 +546,39 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) +
                          ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
-      // P and O are in use until the PV of tile j - 1 is done
-      if (j > 0) {
+      // P buffer j & 1 was last read by the PV MMA of tile j - 2
+      if (j >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(b_o_full0 + 8 * (j & 1), ((j - 2) >> 1) & 1,
+                                              abort_flag, p.err));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      // rows whose reference max moved rescale this half of their O row, once
+      // O holds tile j - 1 (warp-wide: tcgen05.ld / st are collective; alpha
+      // != 1 needs an earlier finite max, so j >= 1)
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
         ok = __all_sync(0xffffffffu, mbar_wait(b_o_full0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1,
                                               abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
-        // rows whose reference max moved rescale their O row (warp-wide:
-        // tcgen05.ld / st are collective)
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            float ov[32];
-            tmem_ld32(tmem_o + trow + cc * 32, ov);
+        for (int cc = 0; cc < 2; ++cc) {
+          float ov[32];
+          tmem_ld32(tmem_o + hf * 64 + trow + cc * 32, ov);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-            tmem_st32(tmem_o + trow + cc * 32, ov);
-          }
+          for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+          tmem_st32(tmem_o + hf * 64 + trow + cc * 32, ov);
         }
       }
       l = l * alpha + psum;
       // P as bf16 hi + lo into this row's TMEM lane (A operands of the PV
       // MMAs; keys 2i and 2i + 1 share column i, the even key in the low
-      // half).  hi is e with the low 16 mantissa bits cleared (exactly a
+      // half; this half's 64 keys are columns 32 hf .. 32 hf + 31 of each
+      // part).  hi is e with the low 16 mantissa bits cleared (exactly a
       // bf16); lo = e - hi is exact in fp32 and likewise truncated to bf16,
       // so hi + lo is e within 2^-14 relative.  Both are byte permutes.
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -519,21 +590,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                               __uint_as_float(u1 & 0xFFFF0000u)),
                               0x7632);
         }
-        tmem_st16(tmem_p + trow + cc * 16, hi);
-        tmem_st16(tmem_p + trow + 64 + cc * 16, lo);
+        tmem_st16(tmem_p + (j & 1) * 128 + trow + hf * 32 + cc * 16, hi);
+        tmem_st16(tmem_p + (j & 1) * 128 + trow + 64 + hf * 32 + cc * 16, lo);
       }
       tmem_wait_st();
       // keys past the end of the sequence: their V rows may hold anything;
       // zero them so that 0-weight rows add exactly 0 (last tile only, once
       // the V tile has landed)
-      if (key0 + kPfKeys > n) {
+      if (j * kPfKeys + kPfKeys > n) {
         ok = __all_sync(0xffffffffu, mbar_wait(b_v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag,
                                               p.err));
         if (!ok) break;
         const uint32_t vb = base + kOffV + (j & 1) * kTileBytes2;
-        for (int i = r; i < kPfKeys * 16; i += 128) {
+        for (int i = hf * kPfRows + r; i < kPfKeys * 16; i += 2 * kPfRows) {
           const int key = i >> 4, ch = i & 15;
-          if (key0 + key >= n) {
+          if (j * kPfKeys + key >= n) {
             const uint32_t a = vb + (ch >> 3) * kHalfBytes + sw128(key, ch & 7);
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
           }
@@ -541,20 +612,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       tc_fence_before();
-      mbar_arrive(b_p_full);
+      mbar_arrive(b_p_full0 + 8 * (j & 1));
     }
-    // epilogue: O / l -> out[q0 + pos0 + rpos][g * G + hs][:]
+    // epilogue: O / l -> out[q0 + pos0 + rpos][g * G + hs][64 hf .. 64 hf + 63]
+    float l_other = 0.f;
+    if (ok) ok = exchange(nkv, l, l_other);
     if (ok)
       ok = __all_sync(0xffffffffu, mbar_wait(b_o_full0 + 8 * ((nkv - 1) & 1),
                                             ((nkv - 1) >> 1) & 1, abort_flag, p.err));
     tc_fence_after();
     if (ok) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const long long orow = ((long long)(q0 + pos0 + rpos) * p.hq + g * G + hs) * kHeadDim;
+      const float lt = hf == 0 ? l + l_other : l_other + l;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const long long orow =
+          ((long long)(q0 + pos0 + rpos) * p.hq + g * G + hs) * kHeadDim + hf * 64;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         float ov[32];
-        tmem_ld32(tmem_o + trow + cc * 32, ov);
+        tmem_ld32(tmem_o + hf * 64 + trow + cc * 32, ov);
         if (rvalid) {
           if (p.out_f32) {
             float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow + cc * 32);
