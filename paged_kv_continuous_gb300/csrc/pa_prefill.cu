@@ -19,13 +19,12 @@
 //                      so the product keeps ~16 bits of the fp32 weights.
 // Warps: 0 loads K tiles and 2 loads V tiles (TMA, 3 and 2 stages; the 8
 // block-table entries of a tile come in one round of lane loads); 1 issues
-// the MMAs (one thread) and owns the TMEM allocation (S, O and two P
-// buffers); 3..10 run the softmax, two warps per TMEM lane quarter, each
-// thread one half (64 keys, 64 output columns) of one row: they write P into
-// their TMEM lanes (the second MMA reads its A operand from tensor memory)
-// and store the output.  QK of tile j + 1 is issued as soon as the softmax
-// has copied S_j to registers, and P_{j+1} goes to the other P buffer, so the
-// softmax of tile j + 1 runs while the PV MMA of tile j still reads P_j.
+// the MMAs (converged warp, one elected lane) and owns the TMEM allocation
+// (S, O, P and Q); 3..10 run the softmax, two warps per TMEM lane quarter,
+// each thread one half (64 keys, 64 output columns) of one row: they put Q
+// and then each P into their TMEM lanes (both MMAs read their A operand from
+// tensor memory) and store the output.  QK of tile j + 1 is issued as soon
+// as the softmax has copied S_j to registers, so it runs under the softmax.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -45,11 +44,10 @@ constexpr int kPfKeys = 128;      // keys per KV tile (N of the first MMA)
 constexpr int kHalfBytes = 128 * 128;  // 128 rows x 64 dims (bf16) with the 128-byte swizzle
 constexpr int kTileBytes2 = 2 * kHalfBytes;  // one 128 x 128 bf16 operand tile = 32 KB
 // shared memory (offsets from a 1024-aligned base)
-constexpr int kOffQ = 0;
 // K tiles are needed first (the score MMA of tile j + 1 is issued before
 // the PV MMA of tile j), so their ring is one stage deeper
 constexpr int kKStages = 3, kVStages = 2;
-constexpr int kOffK = kOffQ + kTileBytes2;               // K tile j in stage j % 3
+constexpr int kOffK = 0;                                 // K tile j in stage j % 3
 constexpr int kOffV = kOffK + kKStages * kTileBytes2;    // V tile j in stage j % 2
 constexpr int kOffBar = kOffV + kVStages * kTileBytes2;
 // partial row maxima / sums exchanged by the two halves of a row:
@@ -57,12 +55,13 @@ constexpr int kOffBar = kOffV + kVStages * kTileBytes2;
 constexpr int kOffX = kOffBar + 256;
 constexpr int kPfSmem = 1024 + kOffX + 2 * 2 * kPfRows * 4;
 // TMEM columns: S at 0..127 (fp32; the softmax copies it to registers at
-// once), O at 128..255 (fp32), P of tile j at 256 + 128 (j & 1): bf16 hi
-// parts in the first 64 columns, lo parts in the next 64 (two keys per
-// column).  Two P buffers let the softmax of tile j + 1 run while the PV MMA
-// of tile j still reads P_j.
+// once), O at 128..255 (fp32), P at 256..383 (bf16 hi parts in 256..319, lo
+// parts in 320..383, two keys per column), Q at 384..447 (bf16, two dims per
+// column).  Both MMAs take their A operand (Q, then P) from tensor memory, so
+// shared memory serves only the K and V tiles: its bandwidth is shared by the
+// B operands and the TMA writes alone.
 constexpr int kTmemCols = 512;
-constexpr int kTmemS = 0, kTmemO = 128, kTmemP = 256;
+constexpr int kTmemS = 0, kTmemO = 128, kTmemP = 256, kTmemQ = 384;
 
 struct PrefillParams {
   void *out;
@@ -105,19 +104,9 @@ __host__ __device__ constexpr uint32_t umma_idesc(int b_mn) {
 // computes the same operands (kept in uniform registers) and one lane, picked
 // by elect.sync, issues.  Issued from a lone lane in a divergent branch, each
 // MMA cost about three times its tensor-pipe time.
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// As umma_f16, with A (M x 16, K-major, two bf16 per 32-bit column) read
-// from tensor memory at column address a_tmem.
+//
+// D (+)= A B with A (M x 16, K-major, two bf16 per 32-bit column) read from
+// tensor memory at column address a_tmem and B described by b.
 __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -241,7 +230,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t b_q_ready = smem_addr(bars + 10);
   const uint32_t b_s_full = smem_addr(bars + 11);
   const uint32_t b_s_free = smem_addr(bars + 12);
-  const uint32_t b_p_full0 = smem_addr(bars + 13);
+  const uint32_t b_p_full = smem_addr(bars + 13);
   const uint32_t b_o_full0 = smem_addr(bars + 15);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 18);
@@ -287,8 +276,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_init(b_q_ready, kSoft);
     mbar_init(b_s_full, 1);
     mbar_init(b_s_free, kSoft);
-    mbar_init(b_p_full0, kSoft);
-    mbar_init(b_p_full0 + 8, kSoft);
+    mbar_init(b_p_full, kSoft);
     for (int i = 0; i < 8; ++i) mbar_init(b_x0 + 8 * i, 64);
     mbar_init(b_o_full0, 1);
     mbar_init(b_o_full0 + 8, 1);
@@ -307,6 +295,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tmem_s = tmem + kTmemS, tmem_o = tmem + kTmemO, tmem_p = tmem + kTmemP;
+  const uint32_t tmem_q = tmem + kTmemQ;
 
   if (warp == 0 || warp == 2) {
     // ---- TMA loaders: warp 0 brings the K tiles, warp 2 the V tiles, each
@@ -369,7 +358,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ---- MMA issuer: QK of tile j + 1 goes out (once the softmax has copied
     //      S_j to registers) before PV of tile j, so the score MMA of the next
     //      tile overlaps the softmax of this one ----------------------------------
-    {  // the whole warp, converged (see umma_f16)
+    {  // the whole warp, converged (see umma_f16_ta)
       constexpr uint32_t idesc_qk = umma_idesc(0), idesc_pv = umma_idesc(1);
       constexpr unsigned kAll = 0xffffffffu;
       bool ok = __all_sync(kAll, mbar_wait(b_q_ready, 0, abort_flag, p.err));
@@ -389,8 +378,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          umma_f16(tmem_s, umma_desc(base + kOffQ + off, 16, 1024),
-                   umma_desc(base + kOffK + ks3 * kTileBytes2 + off, 16, 1024), idesc_qk, ks > 0);
+          umma_f16_ta(tmem_s, tmem_q + ks * 8,
+                      umma_desc(base + kOffK + ks3 * kTileBytes2 + off, 16, 1024), idesc_qk, ks > 0);
         }
         umma_commit(b_s_full);
         umma_commit(b_k_empty0 + 8 * ks3);  // the K stage may be refilled
@@ -405,7 +394,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // O += (P_hi + P_lo) V_j: 2 x 8 k-steps of 16 keys, P_j from TMEM
         // buffer j & 1 (8 columns per step); V is MN-major (dims contiguous):
         // LBO = distance between the two 64-dim halves, SBO = 8 keys
-        if (!__all_sync(kAll, mbar_wait(b_p_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.err)))
+        if (!__all_sync(kAll, mbar_wait(b_p_full, j & 1, abort_flag, p.err)))
           break;
         if (!__all_sync(kAll, mbar_wait(b_v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.err)))
           break;
@@ -415,7 +404,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_f16_ta(tmem_o, tmem_p + (j & 1) * 128 + part * 64 + ks * 8,
+            umma_f16_ta(tmem_o, tmem_p + part * 64 + ks * 8,
                         umma_desc(vb + ks * 16 * 128, kHalfBytes, 1024), idesc_pv,
                         (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
         }
@@ -456,21 +445,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       return true;
     };
 
-    // Q tile: row r = q[q0 + pos0 + rpos][g * G + hs][:], 128-byte swizzle;
-    // this half brings dims 64 hf .. 64 hf + 63
+    // Q tile into this row's TMEM lane: row r = q[q0 + pos0 + rpos][g * G +
+    // hs][:], two dims per column in memory order (the even dim in the low
+    // half); this half brings dims 64 hf .. 64 hf + 63 (columns 32 hf ..)
     {
       const uint4 *src = reinterpret_cast<const uint4 *>(
           p.q + ((long long)(q0 + pos0 + rpos) * p.hq + g * G + hs) * kHeadDim);
+      float qv[32];
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
-        const int ch = hf * 8 + c8;
-        const uint4 v = rvalid ? __ldg(src + ch) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t a = base + kOffQ + hf * kHalfBytes + sw128(r, c8);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
-                     "r"(v.z), "r"(v.w)
-                     : "memory");
+        const uint4 v = rvalid ? __ldg(src + hf * 8 + c8) : make_uint4(0u, 0u, 0u, 0u);
+        qv[4 * c8] = __uint_as_float(v.x);
+        qv[4 * c8 + 1] = __uint_as_float(v.y);
+        qv[4 * c8 + 2] = __uint_as_float(v.z);
+        qv[4 * c8 + 3] = __uint_as_float(v.w);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_st32(tmem_q + trow + hf * 32, qv);
+      tc_fence_before();
       mbar_arrive(b_q_ready);
     }
 
@@ -546,21 +537,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) +
                          ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
-      // P buffer j & 1 was last read by the PV MMA of tile j - 2
-      if (j >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(b_o_full0 + 8 * (j & 1), ((j - 2) >> 1) & 1,
-                                              abort_flag, p.err));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      // rows whose reference max moved rescale this half of their O row, once
-      // O holds tile j - 1 (warp-wide: tcgen05.ld / st are collective; alpha
-      // != 1 needs an earlier finite max, so j >= 1)
-      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      // P and O are in use until the PV MMA of tile j - 1 is done
+      if (j >= 1) {
         ok = __all_sync(0xffffffffu, mbar_wait(b_o_full0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1,
                                               abort_flag, p.err));
         if (!ok) break;
         tc_fence_after();
+      }
+      // rows whose reference max moved rescale this half of their O row
+      // (warp-wide: tcgen05.ld / st are collective)
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
           float ov[32];
@@ -590,8 +576,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                                               __uint_as_float(u1 & 0xFFFF0000u)),
                               0x7632);
         }
-        tmem_st16(tmem_p + (j & 1) * 128 + trow + hf * 32 + cc * 16, hi);
-        tmem_st16(tmem_p + (j & 1) * 128 + trow + 64 + hf * 32 + cc * 16, lo);
+        tmem_st16(tmem_p + trow + hf * 32 + cc * 16, hi);
+        tmem_st16(tmem_p + trow + 64 + hf * 32 + cc * 16, lo);
       }
       tmem_wait_st();
       // keys past the end of the sequence: their V rows may hold anything;
@@ -612,7 +598,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       tc_fence_before();
-      mbar_arrive(b_p_full0 + 8 * (j & 1));
+      mbar_arrive(b_p_full);
     }
     // epilogue: O / l -> out[q0 + pos0 + rpos][g * G + hs][64 hf .. 64 hf + 63]
     float l_other = 0.f;
