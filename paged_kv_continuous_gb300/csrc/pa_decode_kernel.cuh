@@ -242,12 +242,30 @@ __device__ __forceinline__ int walk_chunk(const int32_t *ctx_arr, int batch, int
 // ---- tensor-core and TMA helpers -------------------------------------------
 
 // 3-D tile load (dims: dim, kv head, token slot) completing on an mbarrier.
+// Executed by a whole converged warp with warp-uniform operands (a role
+// branch the compiler can see is uniform); one lane, picked by elect.sync,
+// issues the copy.  This is the issue pattern the tensor-core MMAs need to
+// run at full rate; for these copies it measured neutral.
 __device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap *map, int x, int y,
                                              int z, uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// bulk_load by one elected lane of a converged warp (as tma_load_box).
+__device__ __forceinline__ void bulk_load_elect(uint32_t dst, const void *src, uint32_t bytes,
+                                                uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;\n\t}" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -536,7 +554,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   volatile int *abort_flag = &ctl->abort;
 
   const int tid = threadIdx.x;
-  const int warp = tid >> 5;
+  // broadcast from lane 0: the compiler then knows every role branch below
+  // is warp-uniform
+  const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
   const int lane = tid & 31;
   const long long nsplit = p.num_splits;
   const long long c = blockIdx.x;
@@ -692,32 +712,33 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int b_i = __shfl_sync(0xffffffffu, lb, i);
         const bool q_i = __shfl_sync(0xffffffffu, with_q ? 1 : 0, i) != 0;
         const bool row_i = __shfl_sync(0xffffffffu, in_row ? 1 : 0, i) != 0;
+        // every value here is warp-uniform (shuffled from lane i); lane 0
+        // arms the barrier, then the warp issues the copies (elect.sync)
+        const bool ok = ph_i >= 0 && ph_i < p.num_blocks;
+        const uint32_t dst = stage0 + st * S::STAGE_BYTES;
+        const uint32_t bar = full0 + 8 * st;
         if (lane == 0) {
-          const bool ok = ph_i >= 0 && ph_i < p.num_blocks;
-          const uint32_t bytes = (ok ? 2u * S::KV_BYTES : 0u) + (q_i ? S::Q_BYTES : 0u);
-          const uint32_t dst = stage0 + st * S::STAGE_BYTES;
-          const uint32_t bar = full0 + 8 * st;
-          mbar_arrive_expect_tx(bar, bytes);
-          if (ok) {
-            const int z = (int)(ph_i * kBlockSize);
-#pragma unroll
-            for (int pr = 0; pr < S::NPAIR; ++pr) {
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint32_t off = (pr * 2 + h) * S::BOX_BYTES;
-                tma_load_box(dst + off, &tmap_k, h * 64, pr * S::HB, z, bar, pol_kv);
-                tma_load_box(dst + S::KV_BYTES + off, &tmap_v, h * 64, pr * S::HB, z, bar, pol_kv);
-              }
-            }
-          } else {
-            // a context longer than the table row (caller error) or an entry
-            // outside the pool: reported, not read
-            report(p.err, row_i ? PA_DEVERR_BLOCK_INDEX : PA_DEVERR_SHAPE);
-          }
-          if (q_i)
-            bulk_load(dst + 2 * S::KV_BYTES, p.q + (long long)b_i * S::HQ * kHeadDim, S::Q_BYTES,
-                      bar, pol_q);
+          mbar_arrive_expect_tx(bar, (ok ? 2u * S::KV_BYTES : 0u) + (q_i ? S::Q_BYTES : 0u));
+          // a context longer than the table row (caller error) or an entry
+          // outside the pool: reported, not read
+          if (!ok) report(p.err, row_i ? PA_DEVERR_BLOCK_INDEX : PA_DEVERR_SHAPE);
         }
+        __syncwarp();
+        if (ok) {
+          const int z = (int)(ph_i * kBlockSize);
+#pragma unroll
+          for (int pr = 0; pr < S::NPAIR; ++pr) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t off = (pr * 2 + h) * S::BOX_BYTES;
+              tma_load_box(dst + off, &tmap_k, h * 64, pr * S::HB, z, bar, pol_kv);
+              tma_load_box(dst + S::KV_BYTES + off, &tmap_v, h * 64, pr * S::HB, z, bar, pol_kv);
+            }
+          }
+        }
+        if (q_i)
+          bulk_load_elect(dst + 2 * S::KV_BYTES, p.q + (long long)b_i * S::HQ * kHeadDim,
+                          S::Q_BYTES, bar, pol_q);
       }
       gb += count;
     }
