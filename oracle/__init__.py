@@ -66,6 +66,7 @@ def _load():
                                                    i32, i32, i32, i32, dbl]
             lib.pa_oracle_merge.argtypes = [P, P, P, i64, i32, i32]
             lib.pa_oracle_merge.restype = None
+            lib.pa_oracle_rope.argtypes = [P, P, i64, i64, i32, i32, P, P, P, i64]
             _lib = lib
     return _lib
 
@@ -191,3 +192,54 @@ def merge(part_o, part_lse):
     out = np.zeros((R, D), np.float64)
     lib.pa_oracle_merge(_ptr(out), _ptr(po), _ptr(pl), R, S, D)
     return out
+
+
+def rope(x, positions, cos_table, sin_table):
+    """Rotary embedding (table lookup, rotate-half pairs i and i + D/2).
+
+    ``x`` uint16 (bf16 bits) [T, H, D], any token stride, heads contiguous;
+    ``positions`` int32 [T]; ``cos_table``/``sin_table`` float32
+    [max_position, D/2].  Returns float64 [T, H, D]; see ``pa_oracle_rope``.
+    """
+    lib = _load()
+    assert x.dtype == np.uint16 and x.strides[2] == 2 and x.strides[1] == 2 * x.shape[2]
+    T, H, D = x.shape
+    cos_t = _c(cos_table, np.float32)
+    sin_t = _c(sin_table, np.float32)
+    assert cos_t.shape == sin_t.shape and cos_t.shape[1] == D // 2
+    pos = _c(positions, np.int32)
+    out = np.zeros((T, H, D), np.float64)
+    rc = lib.pa_oracle_rope(_ptr(out), _ptr(x), T, x.strides[0] // 2, H, D, _ptr(pos),
+                            _ptr(cos_t), _ptr(sin_t), cos_t.shape[0])
+    _check(rc, "rope")
+    return out
+
+
+def round_to_bf16_bits(x):
+    """float64 -> bf16 bit patterns, one rounding to nearest (ties to even).
+
+    For finite values in the normal range, which is all the oracle produces:
+    the significand is rounded to 8 bits in float64 (exact), then the value
+    (now exactly representable in bf16, hence in float32) is truncated to its
+    top 16 bits.
+    """
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)                      # x = m 2^e, 0.5 <= |m| < 1
+    y = np.ldexp(np.rint(m * 256.0) / 256.0, e)
+    return (y.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def rope_store_kv(q, k, v, positions, cos_table, sin_table, k_cache, v_cache, slot_mapping,
+                  block_size=16):
+    """Fused rotary embedding + slot_mapping store ([EAS] "自写 Triton Kernel",
+    fused_rope_and_cache_store_kernel).
+
+    q is rotated (returned as float64 [T, Hq, D]); k is rotated (returned as
+    float64 [T, Hkv, D]) and, rounded once to bf16, stored with the unrotated
+    v through slot_mapping exactly as ``store_kv`` does (pools updated in
+    place).  Returns (q_rot, k_rot).
+    """
+    q_rot = rope(q, positions, cos_table, sin_table)
+    k_rot = rope(k, positions, cos_table, sin_table)
+    store_kv(round_to_bf16_bits(k_rot), v, k_cache, v_cache, slot_mapping, block_size)
+    return q_rot, k_rot

@@ -417,3 +417,49 @@ void pa_oracle_merge(double *out, const double *part_o, const double *part_lse,
         }
     }
 }
+
+/*
+ * Rotary position embedding by table lookup, rotate-half form.  [EAS]
+ * "开发时间线" (days 4-5: RoPE rebuilt from the complex form into a
+ * real-valued table lookup), "算子融合与模型优化" (rotate_half applied in
+ * place) and "自写 Triton Kernel" (fused_rope_and_cache_store_kernel: q
+ * rotated and written back contiguous, k rotated and, with v, stored
+ * through slot_mapping).
+ *
+ * Reading: dimension i of a head pairs with dimension i + D/2 (the
+ * rotate_half convention the page names), and the tables hold one angle per
+ * (position, pair): for token t at p = positions[t], head h, i < D/2,
+ *   c = cos_table[p * D/2 + i],  s = sin_table[p * D/2 + i],
+ *   out[t][h][i]       = x[t][h][i] * c - x[t][h][i + D/2] * s
+ *   out[t][h][i + D/2] = x[t][h][i + D/2] * c + x[t][h][i] * s,
+ * which is x * cos + rotate_half(x) * sin with rotate_half(x) = (-x2, x1)
+ * and each half-length table row repeated over both halves.  fp64; x
+ * element (t, h, d) is x[t * tok_stride + h * head_dim + d]; out is
+ * contiguous [num_tokens][num_heads][head_dim].
+ */
+int pa_oracle_rope(double *out, const uint16_t *x, int64_t num_tokens, int64_t tok_stride,
+                   int num_heads, int head_dim, const int32_t *positions,
+                   const float *cos_table, const float *sin_table, int64_t max_position)
+{
+    if (num_tokens < 0 || num_heads <= 0 || head_dim <= 0 || head_dim % 2 != 0)
+        return ORACLE_BAD_ARG;
+    const int half = head_dim / 2;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t p = positions[t];
+        if (p < 0 || p >= max_position)
+            return ORACLE_BAD_INDEX;
+        for (int h = 0; h < num_heads; ++h) {
+            const uint16_t *row = x + t * tok_stride + (int64_t)h * head_dim;
+            double *o = out + (t * num_heads + h) * (int64_t)head_dim;
+            for (int i = 0; i < half; ++i) {
+                double c = (double)cos_table[p * half + i];
+                double s = (double)sin_table[p * half + i];
+                double x1 = bf16_to_double(row[i]);
+                double x2 = bf16_to_double(row[i + half]);
+                o[i] = x1 * c - x2 * s;
+                o[i + half] = x2 * c + x1 * s;
+            }
+        }
+    }
+    return ORACLE_OK;
+}

@@ -28,6 +28,10 @@ MUTANTS = {
                              "int64_t row = (slot / block_size) % block_size;"),
     "merge_unweighted": ("acc += exp(lse[s] - M) * part_o", "acc += part_o"),
     "lse_natural_log_dropped": ("return m + log(l);", "return m + log2(l);"),
+    "rope_first_half_sign": ("o[i] = x1 * c - x2 * s;", "o[i] = x1 * c + x2 * s;"),
+    "rope_second_half_sign": ("o[i + half] = x2 * c + x1 * s;",
+                              "o[i + half] = x2 * c - x1 * s;"),
+    "rope_token_index_as_position": ("int64_t p = positions[t];", "int64_t p = t;"),
 }
 
 

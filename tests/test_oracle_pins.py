@@ -399,3 +399,139 @@ def test_synth_slot_mapping_places_new_token_at_last_position():
     expect = w.block_tables[np.arange(w.batch), pos // bs] * bs + pos % bs
     assert np.array_equal(w.slot_mapping, expect)
     assert np.all(w.context_lens >= 1) and np.all(w.context_lens <= 8192)
+
+
+# --------------------------------------------------------------------------
+# rotary embedding (fused RoPE + store)
+# --------------------------------------------------------------------------
+
+def _rope_tables(max_pos, D, base=10000.0):
+    """Standard RoPE angles theta_{p,i} = p * base^(-2i/D), as float32 tables."""
+    inv = base ** (-np.arange(D // 2, dtype=np.float64) * 2.0 / D)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def test_rope_complex_form():
+    """Rotate-half RoPE is multiplication of the complex numbers
+    x_i + j x_{i+D/2} by c + j s ([EAS] day 4-5: the complex form the
+    table-lookup version replaced).  Catches a sign error in either term,
+    an interleaved (2i, 2i+1) pairing and a wrong table row or column."""
+    rng = np.random.default_rng(31)
+    T, H, D, P = 9, 3, 128, 64
+    x = normal_bits(rng, (T, H, D))
+    pos = rng.integers(0, P, T).astype(np.int32)
+    cos_t = rng.uniform(-1, 1, (P, D // 2)).astype(np.float32)   # arbitrary angles,
+    sin_t = rng.uniform(-1, 1, (P, D // 2)).astype(np.float32)   # not unit: any table
+    out = oracle.rope(x, pos, cos_t, sin_t)
+    xf = bf16_to_f64(x)
+    z = xf[..., :D // 2] + 1j * xf[..., D // 2:]
+    w = cos_t[pos].astype(np.float64) + 1j * sin_t[pos].astype(np.float64)
+    r = z * w[:, None, :]
+    assert np.allclose(out[..., :D // 2], r.real, rtol=1e-14, atol=1e-14)
+    assert np.allclose(out[..., D // 2:], r.imag, rtol=1e-14, atol=1e-14)
+
+
+def test_rope_position_zero_is_identity_and_norms_are_kept():
+    """cos 1 / sin 0 returns the input exactly; unit (cos, sin) keeps the
+    norm of every (i, i + D/2) pair (catches a scaled or mixed-up term)."""
+    rng = np.random.default_rng(32)
+    T, H, D = 6, 2, 128
+    x = normal_bits(rng, (T, H, D))
+    cos_t, sin_t = _rope_tables(4096, D)
+    zero = np.zeros(T, np.int32)
+    assert np.array_equal(oracle.rope(x, zero, cos_t, sin_t), bf16_to_f64(x))
+    pos = rng.integers(0, 4096, T).astype(np.int32)
+    out = oracle.rope(x, pos, cos_t, sin_t)
+    xf = bf16_to_f64(x)
+    n_in = xf[..., :D // 2] ** 2 + xf[..., D // 2:] ** 2
+    n_out = out[..., :D // 2] ** 2 + out[..., D // 2:] ** 2
+    unit = (cos_t[pos].astype(np.float64) ** 2 + sin_t[pos].astype(np.float64) ** 2)[:, None, :]
+    assert np.allclose(n_out, n_in * unit, rtol=1e-12, atol=1e-12)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    """The defining property of RoPE: <R(q, m), R(k, n)> depends on m - n
+    alone.  With standard frequency tables, shifting both positions by the
+    same amount leaves the score unchanged up to the float32 table rounding
+    (catches using the token index instead of positions[t], and an angle
+    applied with the wrong sign on one side)."""
+    rng = np.random.default_rng(33)
+    D = 128
+    cos_t, sin_t = _rope_tables(8192, D)
+    q = normal_bits(rng, (1, 1, D))
+    k = normal_bits(rng, (1, 1, D))
+    scores = []
+    for shift in (0, 37, 1000, 5000):
+        m, n = np.array([100 + shift], np.int32), np.array([60 + shift], np.int32)
+        qr = oracle.rope(q, m, cos_t, sin_t)
+        kr = oracle.rope(k, n, cos_t, sin_t)
+        scores.append(float(np.sum(qr * kr)))
+    mag = float(np.sum(np.abs(bf16_to_f64(q)) * np.abs(bf16_to_f64(k))))
+    assert max(scores) - min(scores) < 1e-5 * mag
+    # and the score does move with the offset itself
+    qr = oracle.rope(q, np.array([100], np.int32), cos_t, sin_t)
+    kr = oracle.rope(k, np.array([90], np.int32), cos_t, sin_t)
+    assert abs(float(np.sum(qr * kr)) - scores[0]) > 1e-3 * mag
+
+
+def test_rope_uses_each_tokens_position():
+    """Tokens rotated in one call equal tokens rotated one at a time, and
+    permuting the tokens (with their positions) permutes the output."""
+    rng = np.random.default_rng(34)
+    T, H, D = 8, 2, 128
+    x = normal_bits(rng, (T, H, D))
+    cos_t, sin_t = _rope_tables(512, D)
+    pos = rng.integers(0, 512, T).astype(np.int32)
+    full = oracle.rope(x, pos, cos_t, sin_t)
+    for t in range(T):
+        one = oracle.rope(x[t:t + 1], pos[t:t + 1], cos_t, sin_t)
+        assert np.array_equal(one[0], full[t])
+    perm = rng.permutation(T)
+    assert np.array_equal(oracle.rope(np.ascontiguousarray(x[perm]), pos[perm], cos_t, sin_t),
+                          full[perm])
+
+
+def test_rope_store_places_rounded_rotated_k_and_plain_v():
+    """The fused store: v lands bit-for-bit, k lands as its rotation rounded
+    once to bf16 (checked against float32 arithmetic where it is exact),
+    through slot_mapping with padding skipped; other slots untouched."""
+    rng = np.random.default_rng(35)
+    NB, bs, Hq, Hkv, D, T = 16, 16, 12, 2, 128, 24
+    qkv = normal_bits(rng, (T, Hq + 2 * Hkv, D))
+    q, k, v = qkv[:, :Hq], qkv[:, Hq:Hq + Hkv], qkv[:, Hq + Hkv:]
+    cos_t, sin_t = _rope_tables(2048, D)
+    pos = rng.integers(0, 2048, T).astype(np.int32)
+    slots = rng.choice(NB * bs, size=T, replace=False).astype(np.int32)
+    slots[5] = -1
+    kc = np.full((NB, bs, Hkv, D), 0x1234, np.uint16)
+    vc = np.full((NB, bs, Hkv, D), 0x4321, np.uint16)
+    q_rot, k_rot = oracle.rope_store_kv(q, k, v, pos, cos_t, sin_t, kc, vc, slots)
+    assert np.array_equal(q_rot, oracle.rope(q, pos, cos_t, sin_t))
+    fk, fv = kc.reshape(NB * bs, Hkv, D), vc.reshape(NB * bs, Hkv, D)
+    ok = slots >= 0
+    assert np.array_equal(fv[slots[ok]], v[ok])
+    stored = bf16_to_f64(fk[slots[ok]])
+    exact = k_rot[ok]
+    # one rounding to nearest: within half a bf16 ulp (8 significant bits:
+    # at most 2^-8 relative) and equal to the independent rounding below
+    assert np.all(np.abs(stored - exact) <= np.abs(exact) * 2.0 ** -8)
+    assert np.array_equal(fk[slots[ok]], oracle.round_to_bf16_bits(exact))
+    untouched = np.ones(NB * bs, bool)
+    untouched[slots[ok]] = False
+    assert np.all(fk[untouched] == 0x1234) and np.all(fv[untouched] == 0x4321)
+
+
+def test_round_to_bf16_bits_ties_and_carries():
+    """Round-to-nearest-even at the halfway points, and the carry into the
+    exponent; equal to float32 rounding where float32 holds the value."""
+    x = np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -8 + 2 ** -30,
+                  -(1.0 + 2 ** -8), 2.0 - 2 ** -9, 3.0, 0.0])
+    got = (oracle.round_to_bf16_bits(x).astype(np.uint32) << 16).view(np.float32)
+    assert got.tolist() == [1.0, 1.0 + 2 ** -6, 1.0 + 2 ** -7, -1.0, 2.0, 3.0, 0.0]
+    rng = np.random.default_rng(36)
+    f = rng.standard_normal(1000).astype(np.float32)
+    # float32 -> bf16 by integer rounding of the bit pattern (ties to even)
+    u = f.view(np.uint32).astype(np.uint64)
+    ref = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    assert np.array_equal(oracle.round_to_bf16_bits(f.astype(np.float64)), ref)
