@@ -41,12 +41,19 @@
  *     0 .. n - q_len + i inclusive;
  *   - q head h reads kv head h / (num_q_heads / num_kv_heads);
  *   - a query with no key gets the zero vector (lse = -inf).
+ *   - rotary embedding: rotate-half pairs (i, i + D/2), angles from
+ *     caller-supplied cos / sin tables indexed [position][i], q rotated and
+ *     returned, k rotated then stored (rounded once to bf16), v stored
+ *     unrotated.
  *
  * Pinning: the tests check these functions against brute force over
  * contiguous K/V built before paging, closed forms (one key, equal rows,
  * zero query, two keys with known weights, head-marked and position-marked
  * values), invariance under block placement, the varlen equivalence stated
- * in [MVT], and the merge identity.  See tests/test_oracle_pins.py.
+ * in [MVT], and the merge identity; the rotary embedding against the
+ * complex-multiplication form, the identity at angle 0, norm preservation
+ * and the relative-position property of the scores.  See
+ * tests/test_oracle_pins.py.
  */
 #include <math.h>
 #include <stdint.h>
