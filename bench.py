@@ -62,6 +62,12 @@ def store_alg_bytes(tokens, hkv, d=128):
     return tokens * hkv * d * 2 * 2 * 2 + tokens * 4  # read + write K and V, slots
 
 
+def rope_store_alg_bytes(tokens, hq, hkv, d=128):
+    """Fused RoPE + store: q read and written, k and v read and written to
+    the pool, the token's cos and sin rows, its position and slot."""
+    return tokens * (hq * d * 2 * 2 + hkv * d * 2 * 2 * 2 + d // 2 * 4 * 2 + 8)
+
+
 def prefill_alg_flops(q_lens, ctx, hq, d=128):
     """QK^T and PV multiply-adds of the causal chunks: query i of a chunk
     behind a prefix of p keys sees p + i + 1 keys."""
@@ -247,9 +253,9 @@ def time_graph(fn, calls, reps=5):
 
 def run_extras(ops, dev):
     """Long-context split-K decode (batch 4 x 32768 keys, Hq 32 / Hkv 8; 4
-    layer pools so the 537 MB of KV per layer always comes from HBM) and the
+    layer pools so the 537 MB of KV per layer always comes from HBM), the
     varlen chunked prefill (8 one-token rows + 8 chunks of 512 behind paged
-    prefixes up to 2048, tensor cores)."""
+    prefixes up to 2048, tensor cores) and the fused RoPE + store."""
     import torch
     from paged_kv_continuous_gb300 import synth
     extra = {}
@@ -309,6 +315,32 @@ def run_extras(ops, dev):
         "us_per_call": ms * 1e3, "alg_flops": flops, "TFLOP_per_s": tf,
         "frac_of_bf16_burst": tf / burst, "frac_of_bf16_sustained": tf / sustained,
         "peak_kind": kind, "rows": int(w.q.shape[0])}
+    del kc, vc
+    # fused RoPE + store (Hq 12 / Hkv 2, positions drawn from [0, 32768)):
+    # the 64 new tokens of a cb_decode_b64 step (launch-bound), and a
+    # 32768-token batch (285 MB moved per call, larger than L2: HBM-bound)
+    for name, T in (("rope_store_decode_b64", 64), ("rope_store_32k_tokens", 32768)):
+        rng = np.random.default_rng(synth.SEED_BASE + 5)
+        hq, hkv, max_pos = 12, 2, 32768
+        nb = (T + 15) // 16 + 8
+        cos_np, sin_np = synth.rope_tables(max_pos)
+        cos_t, sin_t = torch.from_numpy(cos_np).to(dev), torch.from_numpy(sin_np).to(dev)
+        pos = dev32(rng.integers(0, max_pos, T))
+        slots = dev32(rng.permutation(nb * 16)[:T])
+        qkv = torch.randn((T, hq + 2 * hkv, 128), generator=gen, device=dev,
+                          dtype=torch.bfloat16)
+        q_in, k_in, v_in = qkv[:, :hq], qkv[:, hq:hq + hkv], qkv[:, hq + hkv:]
+        q_out = torch.empty((T, hq, 128), dtype=torch.bfloat16, device=dev)
+        kcr = torch.zeros((nb, 16, hkv, 128), dtype=torch.bfloat16, device=dev)
+        vcr = torch.zeros_like(kcr)
+
+        def rope():
+            ops.rope_store_kv(q_in, k_in, v_in, pos, cos_t, sin_t, kcr, vcr, slots, q_out=q_out)
+        ms = time_graph(rope, 20 if T > 1000 else 200)
+        nbytes = rope_store_alg_bytes(T, hq, hkv)
+        extra[name] = {"us_per_call": ms * 1e3, "tokens": T, "alg_bytes": nbytes,
+                       "GB_per_s": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / hbm,
+                       "peak_kind": hbm_kind}
     return extra
 
 

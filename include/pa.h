@@ -1,11 +1,13 @@
 /*
  * pa.h -- C ABI of the GB300 paged-KV attention library (libpa_gb300.so).
  *
- * Four operations over a block-paged KV cache, each a hand-written sm_103a
+ * Five operations over a block-paged KV cache, each a hand-written sm_103a
  * CUDA kernel enqueued on the caller's stream:
  *
  *   pa_store_kv        write each new token's K/V rows into the pool slot
  *                      named by slot_mapping;
+ *   pa_rope_store_kv   the same store fused with the rotary position
+ *                      embedding of q and k;
  *   pa_decode          paged GQA decode attention (one query per sequence),
  *                      split across CTAs with log-sum-exp partials;
  *   pa_decode_merge    combine those partials into the final rows;
@@ -16,9 +18,11 @@
  *   [EAS] koas-w, "errors and solutions" (Qwen2.5-1.5B inference from
  *         scratch): sections "KV Cache 管理" (global pool of 16-token
  *         blocks, logical->physical block_table), "自写 Triton Kernel"
- *         (store_kvcache_kernel; Decode_Paged_GQAAttention_Kernel), "CUDA
- *         Graph" (static slot_mapping / block_table / context_lens buffers)
- *         and "开发过程遇到的错误汇总" types 1, 2 and 5.
+ *         (store_kvcache_kernel; Decode_Paged_GQAAttention_Kernel;
+ *         fused_rope_and_cache_store_kernel), "开发时间线" (days 4-5: RoPE
+ *         as a real-valued table lookup), "算子融合与模型优化"
+ *         (rotate_half), "CUDA Graph" (static slot_mapping / block_table /
+ *         context_lens buffers) and "开发过程遇到的错误汇总" types 1, 2 and 5.
  *   [MVT] mini-vllm tutorial, "step14_7 -- Batched Forward": sections
  *         "解决方案：变长 batch（varlen）" and "cu_seqlens 只在 Attention 里才需要".
  *   [CEB] PocketLLM, "cpp_engine Batching Implementation (Phase 3.1)",
@@ -65,7 +69,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 2
+#define PA_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define PA_API __attribute__((visibility("default")))
@@ -92,10 +96,12 @@ typedef int32_t pa_status;
 #define PA_DEVERR_SLOT_INDEX 2    /* slot_mapping entry outside the pool */
 #define PA_DEVERR_WAIT_TIMEOUT 4  /* a pipeline wait gave up after ~2 s */
 #define PA_DEVERR_SHAPE 8         /* context_lens / cu_seqlens inconsistent */
+#define PA_DEVERR_POSITION 16     /* a position outside the rotary tables */
 
 /*
- * Launch flags (the `flags` argument of pa_store_kv, pa_decode and
- * pa_decode_noalloc).  Any other bit returns PA_ERR_INVALID_ARG.
+ * Launch flags (the `flags` argument of pa_store_kv, pa_rope_store_kv,
+ * pa_decode and pa_decode_noalloc).  Any other bit returns
+ * PA_ERR_INVALID_ARG.
  *
  * PA_LAUNCH_PDL: programmatic dependent launch.  The call's kernel may begin
  * while the kernel launched just before it on the same stream is still
@@ -106,7 +112,7 @@ typedef int32_t pa_status;
  * block_tables only (to partition the work and find the first pages); so
  * with this flag those two must not be written by the kernel launched
  * immediately before the call (host copies and earlier kernels are fine).
- * pa_store_kv reads nothing before that wait.
+ * pa_store_kv and pa_rope_store_kv read nothing before that wait.
  * Every write and every other read happens after it, so the results are the
  * same with and without the flag.
  */
@@ -147,6 +153,57 @@ PA_API pa_status pa_store_kv(const void *k, const void *v, int64_t num_tokens,
                       int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
                       const int32_t *slot_mapping, int32_t *error_flags,
                       uint32_t flags, void *stream);
+
+/*
+ * pa_rope_store_kv -- rotary position embedding fused with the slot_mapping
+ * store ([EAS] "自写 Triton Kernel", fused_rope_and_cache_store_kernel: q is
+ * rotated and written back contiguous, k is rotated and stored with v
+ * through slot_mapping; RoPE by table lookup, "开发时间线" days 4-5;
+ * rotate_half, "算子融合与模型优化").
+ *
+ * With D = head_dim, for every token t < num_tokens at p = positions[t] and
+ * every i < D/2, c = cos_table[p * D/2 + i], s = sin_table[p * D/2 + i], a
+ * head row x is rotated in rotate-half pairs:
+ *     x'[i]       = x[i] * c - x[i + D/2] * s
+ *     x'[i + D/2] = x[i + D/2] * c + x[i] * s.
+ * Every q head of token t is rotated into q_out.  Every kv head of k is
+ * rotated and stored, with the v row unrotated, at slot_mapping[t] exactly
+ * as pa_store_kv stores (slot < 0: padding, no pool row is written, q_out
+ * still is).  Arithmetic is fp32 from the bf16 rows and fp32 tables (fused
+ * multiply-add), rounded once to bf16 (nearest even); v moves bit-exactly.
+ *
+ *   q, k, v        bf16; element (t, h, d) of x lives at
+ *                  x + t * x_tok_stride + h * head_dim + d (heads
+ *                  contiguous, so the three may be column slices of one
+ *                  fused QKV row).
+ *   q_out          bf16, (t, h, d) at q_out + t * q_out_tok_stride +
+ *                  h * head_dim + d.  May be q itself (rotation in place);
+ *                  any other overlap with q, k or v is a caller error.
+ *   positions      int32 [num_tokens], absolute positions.
+ *   cos_table,
+ *   sin_table      fp32 [max_position][head_dim / 2], 16-byte aligned; the
+ *                  caller chooses the angles (e.g. p * base^(-2i / D)).
+ *   k_cache,
+ *   v_cache        pools, [num_blocks][block_size][num_kv_heads][head_dim].
+ *   slot_mapping   int32 [num_tokens].
+ *   error_flags    optional int32 word (may be NULL): a position outside
+ *                  [0, max_position) sets PA_DEVERR_POSITION and the whole
+ *                  token is skipped (no q_out row, no pool row); a slot >=
+ *                  num_blocks * block_size sets PA_DEVERR_SLOT_INDEX and
+ *                  the token's pool rows are skipped.
+ *   flags          0 or PA_LAUNCH_PDL.
+ * Supported: head_dim 128, block_size 16, 1 <= num_kv_heads <= 64,
+ * 1 <= num_q_heads <= 512.
+ */
+PA_API pa_status pa_rope_store_kv(const void *q, int64_t q_tok_stride, void *q_out,
+                                  int64_t q_out_tok_stride, const void *k, int64_t k_tok_stride,
+                                  const void *v, int64_t v_tok_stride, int64_t num_tokens,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  const int32_t *positions, const float *cos_table,
+                                  const float *sin_table, int64_t max_position, void *k_cache,
+                                  void *v_cache, int64_t num_blocks, int32_t block_size,
+                                  const int32_t *slot_mapping, int32_t *error_flags,
+                                  uint32_t flags, void *stream);
 
 /*
  * Decode split partition.  The decode work is the list of all KV blocks of

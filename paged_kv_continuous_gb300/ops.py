@@ -25,11 +25,12 @@ DEVERR_BLOCK_INDEX = 1
 DEVERR_SLOT_INDEX = 2
 DEVERR_WAIT_TIMEOUT = 4
 DEVERR_SHAPE = 8
+DEVERR_POSITION = 16
 
 EXPORTED = (
     "pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
     "pa_decode_default_splits", "pa_decode", "pa_decode_merge", "pa_prefill_varlen",
-    "pa_decode_noalloc",
+    "pa_decode_noalloc", "pa_rope_store_kv",
 )
 
 
@@ -51,6 +52,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_store_kv.restype = i32
     lib.pa_store_kv.argtypes = [P, P, i64, i64, i64, i64, i64, P, P, i64, i32, i32, i32, P, P,
                                 u32, P]
+    lib.pa_rope_store_kv.restype = i32
+    lib.pa_rope_store_kv.argtypes = [P, i64, P, i64, P, i64, P, i64, i64, i32, i32, i32, P, P,
+                                     P, i64, P, P, i64, i32, P, P, u32, P]
     lib.pa_decode_workspace_size.restype = sz
     lib.pa_decode_workspace_size.argtypes = [i32, i32, i32]
     lib.pa_decode_default_splits.restype = i32
@@ -127,6 +131,52 @@ def store_kv(k, v, k_cache, v_cache, slot_mapping, error_flags=None, stream=None
                            _ptr(slot_mapping), _ptr(error_flags),
                            PA_LAUNCH_PDL if pdl else 0, _stream(stream)),
            "pa_store_kv")
+
+
+def rope_store_kv(q, k, v, positions, cos_table, sin_table, k_cache, v_cache, slot_mapping,
+                  q_out=None, error_flags=None, stream=None, pdl=False):
+    """pa_rope_store_kv: rotate q (bf16 [T, Hq, D]) into q_out (new tensor,
+    or q itself for in place) and k (bf16 [T, Hkv, D]) by the rotary tables
+    (float32 [max_position, D/2]) at positions (int32 [T]); store the rotated
+    k and the plain v at slot_mapping.  q/k/v may be views of a fused QKV
+    buffer (any token stride; heads contiguous).  Returns q_out."""
+    for t, n, d in ((q, "q", 3), (k, "k", 3), (v, "v", 3)):
+        _need(t, torch.bfloat16, n, d)
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise PagedAttentionError(f"{n} needs contiguous heads ([T, H, D], unit dim stride)")
+    _need(positions, torch.int32, "positions", 1)
+    _need(cos_table, torch.float32, "cos_table", 2)
+    _need(sin_table, torch.float32, "sin_table", 2)
+    _need(k_cache, torch.bfloat16, "k_cache", 4)
+    _need(v_cache, torch.bfloat16, "v_cache", 4)
+    _need(slot_mapping, torch.int32, "slot_mapping", 1)
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise PagedAttentionError("pools must be contiguous")
+    if not (cos_table.is_contiguous() and sin_table.is_contiguous()):
+        raise PagedAttentionError("rotary tables must be contiguous")
+    T, Hq, D = q.shape
+    _, Hkv, _ = k.shape
+    NB, bs, Hkv2, D2 = k_cache.shape
+    if k.shape != (T, Hkv, D) or v.shape != k.shape or (Hkv2, D2) != (Hkv, D) or \
+            v_cache.shape != k_cache.shape:
+        raise PagedAttentionError("shape mismatch between q/k/v and the pools")
+    if cos_table.shape != sin_table.shape or cos_table.shape[1] != D // 2:
+        raise PagedAttentionError("rotary tables must be [max_position, head_dim / 2]")
+    if positions.shape[0] != T or slot_mapping.shape[0] != T:
+        raise PagedAttentionError("positions and slot_mapping need one entry per token")
+    if q_out is None:
+        q_out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+    _need(q_out, torch.bfloat16, "q_out", 3)
+    if q_out.shape != q.shape or q_out.stride(2) != 1 or q_out.stride(1) != D:
+        raise PagedAttentionError("q_out must be [T, Hq, D] with contiguous heads")
+    _check(lib.pa_rope_store_kv(_ptr(q), q.stride(0), _ptr(q_out), q_out.stride(0), _ptr(k),
+                                k.stride(0), _ptr(v), v.stride(0), T, Hq, Hkv, D,
+                                _ptr(positions), _ptr(cos_table), _ptr(sin_table),
+                                cos_table.shape[0], _ptr(k_cache), _ptr(v_cache), NB, bs,
+                                _ptr(slot_mapping), _ptr(error_flags),
+                                PA_LAUNCH_PDL if pdl else 0, _stream(stream)),
+           "pa_rope_store_kv")
+    return q_out
 
 
 def _device_index(device=None) -> int:

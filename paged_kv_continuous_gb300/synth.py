@@ -76,6 +76,16 @@ class PagedWorkload:
     def q_lens(self) -> np.ndarray:
         return np.diff(self.cu_seqlens).astype(np.int32)
 
+    @property
+    def positions(self) -> np.ndarray:
+        """int32 [rows]: absolute position of each new token (the last q_len
+        positions of its sequence, in order)."""
+        ql = self.q_lens.astype(np.int64)
+        first = np.repeat(self.context_lens.astype(np.int64) - ql, ql)
+        within = np.arange(int(ql.sum()), dtype=np.int64) - np.repeat(
+            self.cu_seqlens[:-1].astype(np.int64), ql)
+        return (first + within).astype(np.int32)
+
     def stored_caches(self):
         """Copies of the pools with the step's new tokens already placed."""
         kc, vc = self.k_cache.copy(), self.v_cache.copy()
@@ -208,6 +218,16 @@ def varlen_prefill(seed: int = SEED_BASE + 4, chunk: int = 512, n_decode: int = 
     need = int(((ctx + 15) // 16).sum())
     return make_paged(rng, "varlen_prefill_8x1_8x512", ctx, kinds,
                       num_blocks=int(need * 1.25) + 1, keep_seq=keep_seq)
+
+
+def rope_tables(max_position: int, head_dim: int = 128, base: float = 1.0e6):
+    """Rotary-embedding inputs: float32 cos / sin tables [max_position,
+    head_dim / 2] of the angles p * base^(-2i / head_dim), evaluated in
+    float64 and rounded once.  base 1e6 is the Qwen2.5 configuration value
+    (the pages leave it open; any table is a valid input)."""
+    inv = base ** (-np.arange(head_dim // 2, dtype=np.float64) * 2.0 / head_dim)
+    ang = np.arange(max_position, dtype=np.float64)[:, None] * inv[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
 
 
 CONFIGS = {

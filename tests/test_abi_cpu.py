@@ -23,9 +23,10 @@ def declared_functions():
     return sorted(set(re.findall(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text)))
 
 
-def test_header_declares_the_four_operations():
+def test_header_declares_the_five_operations():
     names = declared_functions()
-    for op in ("pa_store_kv", "pa_decode", "pa_decode_merge", "pa_prefill_varlen"):
+    for op in ("pa_store_kv", "pa_rope_store_kv", "pa_decode", "pa_decode_merge",
+               "pa_prefill_varlen"):
         assert op in names
 
 
@@ -43,7 +44,7 @@ def test_binding_names_match_header():
 
 def test_version_and_status_strings(lib):
     lib.pa_abi_version.restype = ctypes.c_int32
-    assert lib.pa_abi_version() == 2
+    assert lib.pa_abi_version() == 3
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [ctypes.c_int32]
     assert lib.pa_status_string(0) == b"ok"
@@ -101,3 +102,29 @@ def test_argument_checks_before_any_launch():
                        4, nul) == 1
     assert L.pa_decode_merge(nul, 0, nul, 0, nul, 1, 12, 128, 16, 0, nul) == 1
     assert L.pa_decode_merge(nul, 0, nul, 0, nul, 1, 12, 128, 16, 4, nul) == 1
+
+
+def test_rope_store_kv_argument_checks(lib):
+    """pa_rope_store_kv validates before launching: empty is a no-op, null
+    pointers and negative strides are invalid, other shapes unsupported,
+    unknown flags rejected, misaligned tables rejected."""
+    L = lib
+    P, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
+    L.pa_rope_store_kv.restype = i32
+    L.pa_rope_store_kv.argtypes = [P, i64, P, i64, P, i64, P, i64, i64, i32, i32, i32, P, P, P,
+                                   i64, P, P, i64, i32, P, P, u32, P]
+    nul = None
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: every case fails before a launch
+
+    def call(T=4, Hq=12, Hkv=2, D=128, bs=16, q_tok=1536, flags=0, ptr=fake, tab=fake):
+        return L.pa_rope_store_kv(ptr, q_tok, ptr, q_tok, ptr, 256, ptr, 256, T, Hq, Hkv, D,
+                                  ptr, tab, tab, 4096, ptr, ptr, 64, bs, ptr, nul, flags, nul)
+
+    assert call(T=0, ptr=nul, tab=nul) == 0
+    assert call(ptr=nul) == 1
+    assert call(q_tok=-1) == 1
+    assert call(D=64) == 2
+    assert call(bs=32) == 2
+    assert call(Hkv=0) == 2
+    assert call(flags=2) == 1
+    assert call(tab=ctypes.c_void_p(0x10004)) == 1
