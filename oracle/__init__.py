@@ -12,8 +12,9 @@ the readings taken where the pages are silent).  Inputs are bf16 bit patterns
 held in ``np.uint16`` arrays and int32 index arrays, all on the host.
 
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
-against brute force over contiguous K/V, closed forms and invariants; none is
-"parity unpinned".
+against brute force over contiguous K/V, closed forms and invariants (the
+E4M3 codec also against torch's float8_e4m3fn conversions); none is "parity
+unpinned".
 """
 from __future__ import annotations
 
@@ -67,6 +68,8 @@ def _load():
             lib.pa_oracle_merge.argtypes = [P, P, P, i64, i32, i32]
             lib.pa_oracle_merge.restype = None
             lib.pa_oracle_rope.argtypes = [P, P, i64, i64, i32, i32, P, P, P, i64]
+            lib.pa_oracle_decode_f64.argtypes = [P, P, P, P, P, i64, P, i64, P, i32, i32, i32,
+                                                 i32, i32, dbl]
             _lib = lib
     return _lib
 
@@ -243,3 +246,102 @@ def rope_store_kv(q, k, v, positions, cos_table, sin_table, k_cache, v_cache, sl
     k_rot = rope(k, positions, cos_table, sin_table)
     store_kv(round_to_bf16_bits(k_rot), v, k_cache, v_cache, slot_mapping, block_size)
     return q_rot, k_rot
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) KV cache with per-kv-head scales
+#
+# Reading of the pages: koas-w / PocketLLM, "cpp_engine Batching
+# Implementation (Phase 3.1)", section "当前 KV cache 结构", keeps k_scale /
+# v_scale tensors beside the caches "for FP8/INT8 quantisation" and says no
+# more.  Taken here: E4M3 codes (1 sign bit, 4 exponent bits with bias 7, 3
+# mantissa bits; exponent 0 subnormal; exponent 15 with mantissa 7 is NaN;
+# largest finite 448; no infinities), one float32 scale per kv head for K and
+# one for V, stored value = round_to_nearest_even(x / scale) saturated to
+# +-448, read value = code value * scale.  K pages keep the bf16 layout
+# [num_blocks][block_size][Hkv][D]; V pages are dim-major inside a block,
+# [num_blocks][Hkv][D][block_size].
+# ---------------------------------------------------------------------------
+
+def e4m3_values():
+    """float64 value of each of the 256 E4M3 codes, from the field formula."""
+    vals = np.empty(256, np.float64)
+    for c in range(256):
+        sign = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 0x7
+        if e == 15 and m == 7:
+            vals[c] = np.nan
+        elif e == 0:
+            vals[c] = sign * m * 2.0 ** -9           # 0.m * 2^(1 - 7)
+        else:
+            vals[c] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+def e4m3_encode(y):
+    """Nearest E4M3 code of each value (ties to the even code), magnitudes
+    beyond 448 saturated to 448, NaN to 0x7F.  Codes 0..126 are the
+    non-negative finite values in increasing order; the sign is bit 7."""
+    y = np.asarray(y, np.float64)
+    pos = e4m3_values()[:127]
+    a = np.abs(y)
+    hi = np.clip(np.searchsorted(pos, a), 1, 126)          # pos[hi-1] <= a <= pos[hi] (in range)
+    lo = hi - 1
+    d_lo, d_hi = a - pos[lo], pos[hi] - a
+    code = np.where(d_lo < d_hi, lo, hi)
+    tie = d_lo == d_hi
+    code = np.where(tie, np.where(lo % 2 == 0, lo, hi), code)
+    code = np.where(a >= 448.0, 126, code)
+    code = code.astype(np.uint8) | np.where(np.signbit(y), 0x80, 0).astype(np.uint8)
+    return np.where(np.isnan(y), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def quantize_fp8(x_bits, scale):
+    """bf16 rows [T, H, D] -> E4M3 codes of x / scale[h]; the division is
+    IEEE float32 (the precision the stored code is decided in)."""
+    xf = (x_bits.astype(np.uint32) << 16).view(np.float32)
+    y = xf / np.asarray(scale, np.float32)[None, :, None]
+    return e4m3_encode(y.astype(np.float32))
+
+
+def store_kv_fp8(k, v, k_pool, v_pool, k_scale, v_scale, slot_mapping, block_size=16):
+    """Quantise each token's K/V rows and place them at slot_mapping[t]
+    (slot < 0 skipped): K at [block][row][h][:], V at [block][h][:][row]."""
+    kq, vq = quantize_fp8(k, k_scale), quantize_fp8(v, v_scale)
+    nslots = k_pool.shape[0] * block_size
+    for t, slot in enumerate(np.asarray(slot_mapping, np.int64)):
+        if slot < 0:
+            continue
+        if slot >= nslots:
+            raise ValueError("oracle store_kv_fp8: index out of range")
+        blk, row = divmod(int(slot), block_size)
+        k_pool[blk, row] = kq[t]
+        v_pool[blk, :, :, row] = vq[t]
+
+
+def dequantize_pools_fp8(k_pool, v_pool, k_scale, v_scale):
+    """float64 pools in the bf16 layout [NB][bs][Hkv][D]: code value * scale."""
+    vals = e4m3_values()
+    kf = vals[k_pool] * np.asarray(k_scale, np.float32).astype(np.float64)[None, None, :, None]
+    vf = vals[v_pool] * np.asarray(v_scale, np.float32).astype(np.float64)[None, :, None, None]
+    return kf, np.ascontiguousarray(vf.transpose(0, 3, 1, 2))
+
+
+def decode_fp8(q, k_pool, v_pool, k_scale, v_scale, block_tables, context_lens, scale,
+               with_lse=False):
+    """Paged GQA decode over FP8 pools: every code widened exactly and
+    multiplied by its head's scale, then the same attention as ``decode``."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    B, Hq, D = q.shape
+    kf, vf = dequantize_pools_fp8(k_pool, v_pool, k_scale, v_scale)
+    NB, bs, Hkv, _ = kf.shape
+    bt = _c(block_tables, np.int32)
+    ctx = _c(context_lens, np.int32)
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = lib.pa_oracle_decode_f64(_ptr(out), _ptr(lse), _ptr(q), _ptr(kf), _ptr(vf), NB,
+                                  _ptr(bt), bt.shape[1], _ptr(ctx), B, Hq, Hkv, D, bs,
+                                  float(scale))
+    _check(rc, "decode_fp8")
+    return (out, lse) if with_lse else out

@@ -41,6 +41,11 @@
  *     0 .. n - q_len + i inclusive;
  *   - q head h reads kv head h / (num_q_heads / num_kv_heads);
  *   - a query with no key gets the zero vector (lse = -inf).
+ *   - FP8 KV cache (codec, store and dequantisation in oracle/__init__.py):
+ *     E4M3 codes with one float32 scale per kv head for K and for V, stored
+ *     value = nearest-even E4M3 of x / scale (float32 division, saturated to
+ *     448), read value = code value * scale; pa_oracle_decode_f64 then runs
+ *     the same attention on the widened pools;
  *   - rotary embedding: rotate-half pairs (i, i + D/2), angles from
  *     caller-supplied cos / sin tables indexed [position][i], q rotated and
  *     returned, k rotated then stored (rounded once to bf16), v stored
@@ -469,4 +474,114 @@ int pa_oracle_rope(double *out, const uint16_t *x, int64_t num_tokens, int64_t t
         }
     }
     return ORACLE_OK;
+}
+
+/*
+ * Decode over pools given as fp64 values (same layout as the bf16 pools,
+ * [num_blocks][block_size][num_kv_heads][head_dim]; q stays bf16).  Used
+ * for the FP8 KV cache: the caller widens every stored code to its exact
+ * value times its head's scale, and this is then the same gather and the
+ * same two-pass softmax as pa_oracle_decode, in double.
+ */
+static int gather_head_f64(const double *cache, const int32_t *table_row, int64_t n,
+                           int64_t num_blocks, int block_size, int num_kv_heads,
+                           int head_dim, int kv_head, double *dst)
+{
+    for (int64_t j = 0; j < n; ++j) {
+        int64_t block = table_row[j / block_size];
+        if (block < 0 || block >= num_blocks)
+            return ORACLE_BAD_INDEX;
+        int64_t row = j % block_size;
+        const double *src =
+            cache + ((block * block_size + row) * num_kv_heads + kv_head) * head_dim;
+        memcpy(dst + j * head_dim, src, (size_t)head_dim * sizeof(double));
+    }
+    return ORACLE_OK;
+}
+
+static double attend_row_f64(const uint16_t *q, const double *K, const double *V, int64_t n,
+                             int head_dim, double scale, double *scores, double *o)
+{
+    for (int d = 0; d < head_dim; ++d)
+        o[d] = 0.0;
+    if (n <= 0)
+        return -INFINITY;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < head_dim; ++d)
+            dot += bf16_to_double(q[d]) * K[j * head_dim + d];
+        double s = scale * dot;
+        scores[j] = s;
+        if (s > m)
+            m = s;
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+        double p = exp(scores[j] - m);
+        scores[j] = p;
+        l += p;
+    }
+    for (int d = 0; d < head_dim; ++d) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < n; ++j)
+            acc += scores[j] * V[j * head_dim + d];
+        o[d] = acc / l;
+    }
+    return m + log(l);
+}
+
+int pa_oracle_decode_f64(double *out, double *lse, const uint16_t *q, const double *k_cache,
+                         const double *v_cache, int64_t num_blocks,
+                         const int32_t *block_tables, int64_t block_table_stride,
+                         const int32_t *context_lens, int batch, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, double scale)
+{
+    if (!check_heads(num_q_heads, num_kv_heads) || head_dim <= 0 || block_size <= 0 ||
+        batch < 0)
+        return ORACLE_BAD_ARG;
+    for (int b = 0; b < batch; ++b)
+        if (context_lens[b] < 0 ||
+            (int64_t)(context_lens[b] + block_size - 1) / block_size > block_table_stride)
+            return ORACLE_BAD_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    int status = ORACLE_OK;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+#endif
+    for (int b = 0; b < batch; ++b) {
+        for (int g = 0; g < num_kv_heads; ++g) {
+            const int64_t n = context_lens[b];
+            double *K = malloc((size_t)(n > 0 ? n : 1) * head_dim * sizeof(double));
+            double *V = malloc((size_t)(n > 0 ? n : 1) * head_dim * sizeof(double));
+            double *scores = malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+            int rc = (K && V && scores) ? ORACLE_OK : ORACLE_NO_MEMORY;
+            const int32_t *row = block_tables + (int64_t)b * block_table_stride;
+            if (rc == ORACLE_OK)
+                rc = gather_head_f64(k_cache, row, n, num_blocks, block_size, num_kv_heads,
+                                     head_dim, g, K);
+            if (rc == ORACLE_OK)
+                rc = gather_head_f64(v_cache, row, n, num_blocks, block_size, num_kv_heads,
+                                     head_dim, g, V);
+            if (rc == ORACLE_OK) {
+                for (int hi = 0; hi < group; ++hi) {
+                    const int64_t r = (int64_t)b * num_q_heads + g * group + hi;
+                    double e = attend_row_f64(q + r * head_dim, K, V, n, head_dim, scale,
+                                              scores, out + r * head_dim);
+                    if (lse)
+                        lse[r] = e;
+                }
+            }
+            free(K);
+            free(V);
+            free(scores);
+            if (rc != ORACLE_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+                status = rc;
+            }
+        }
+    }
+    return status;
 }

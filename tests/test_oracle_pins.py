@@ -535,3 +535,104 @@ def test_round_to_bf16_bits_ties_and_carries():
     u = f.view(np.uint32).astype(np.uint64)
     ref = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
     assert np.array_equal(oracle.round_to_bf16_bits(f.astype(np.float64)), ref)
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) KV cache
+# --------------------------------------------------------------------------
+
+def test_e4m3_values_closed_forms_and_library():
+    """Closed forms of the format (largest finite 448, smallest subnormal
+    2^-9, smallest normal 2^-6, one = 0x38, NaN = 0x7F) and agreement with
+    torch's float8_e4m3fn widening on all 256 codes (an independent
+    implementation of the same format)."""
+    v = oracle.e4m3_values()
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0
+    assert v[0x01] == 2.0 ** -9 and v[0x08] == 2.0 ** -6 and v[0x38] == 1.0
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and v[0x80] == 0.0
+    assert np.all(np.diff(v[:127]) > 0)           # codes 0..126 increase
+    torch = pytest.importorskip("torch")
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+    assert np.array_equal(np.nan_to_num(v, nan=7e7), np.nan_to_num(lib, nan=7e7))
+
+
+def test_e4m3_encode_round_trip_ties_and_saturation():
+    """Every finite code encodes back to itself; a value halfway between two
+    codes goes to the even one; beyond 448 saturates; agreement with torch's
+    float32 -> float8_e4m3fn rounding on random in-range values."""
+    v = oracle.e4m3_values()
+    finite = np.array([c for c in range(256) if not np.isnan(v[c]) and c != 0x80])
+    assert np.array_equal(oracle.e4m3_encode(v[finite]), finite.astype(np.uint8))
+    mids = (v[0:126] + v[1:127]) / 2.0
+    got = oracle.e4m3_encode(mids)
+    even = np.where(np.arange(126) % 2 == 0, np.arange(126), np.arange(1, 127))
+    assert np.array_equal(got, even.astype(np.uint8))
+    assert oracle.e4m3_encode(np.array([449.0, 500.0, 1e30]))[0] == 0x7E
+    assert oracle.e4m3_encode(np.array([-1e30]))[0] == 0xFE
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(41)
+    y = (rng.standard_normal(20000) * 50).astype(np.float32)
+    y = y[np.abs(y) < 440]
+    lib = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(y), lib)
+
+
+def test_store_kv_fp8_layout_and_quantisation():
+    """K codes land token-major at [block][row][h], V codes dim-major at
+    [block][h][:][row]; codes are the rounding of x / scale[h] in float32;
+    padding skipped; other slots untouched."""
+    rng = np.random.default_rng(42)
+    NB, bs, Hkv, D, T = 8, 16, 2, 128, 10
+    k = normal_bits(rng, (T, Hkv, D))
+    v = normal_bits(rng, (T, Hkv, D))
+    ks = np.array([0.01, 0.02], np.float32)
+    vs = np.array([0.015, 0.005], np.float32)
+    slots = rng.choice(NB * bs, size=T, replace=False).astype(np.int32)
+    slots[4] = -1
+    kp = np.full((NB, bs, Hkv, D), 0x55, np.uint8)
+    vp = np.full((NB, Hkv, D, bs), 0x66, np.uint8)
+    oracle.store_kv_fp8(k, v, kp, vp, ks, vs, slots)
+    for t in range(T):
+        if slots[t] < 0:
+            continue
+        blk, row = divmod(int(slots[t]), bs)
+        for h in range(Hkv):
+            kf = bf16_to_f64(k[t, h]).astype(np.float32) / ks[h]
+            vf = bf16_to_f64(v[t, h]).astype(np.float32) / vs[h]
+            assert np.array_equal(kp[blk, row, h], oracle.e4m3_encode(kf))
+            assert np.array_equal(vp[blk, h, :, row], oracle.e4m3_encode(vf))
+    live = slots[slots >= 0]
+    mask = np.ones(NB * bs, bool)
+    mask[live] = False
+    assert np.all(kp.reshape(NB * bs, Hkv, D)[mask] == 0x55)
+    vflat = vp.transpose(0, 3, 1, 2).reshape(NB * bs, Hkv, D)
+    assert np.all(vflat[mask] == 0x66)
+
+
+def test_decode_fp8_equals_bf16_decode_on_exact_values():
+    """With power-of-two scales every code * scale is exactly a bf16 value:
+    the FP8 decode must then equal the (pinned) bf16 decode bit for bit over
+    pools holding those values (catches a wrong scale, a wrong head's scale,
+    or V read in the token-major order)."""
+    rng = np.random.default_rng(43)
+    NB, bs, Hq, Hkv, D = 24, 16, 12, 2, 128
+    ctx = np.array([1, 17, 40, 100], np.int32)
+    tables = random_tables(rng, ctx, NB)
+    ks = np.array([0.125, 2.0], np.float32)
+    vs = np.array([0.5, 0.0625], np.float32)
+    v = oracle.e4m3_values()
+    finite = np.array([c for c in range(256) if not np.isnan(v[c])], np.uint8)
+    kp = rng.choice(finite, size=(NB, bs, Hkv, D)).astype(np.uint8)
+    vp = rng.choice(finite, size=(NB, Hkv, D, bs)).astype(np.uint8)
+    kf, vf = oracle.dequantize_pools_fp8(kp, vp, ks, vs)
+    kb, vb = bf16_bits(kf.astype(np.float32)), bf16_bits(vf.astype(np.float32))
+    assert np.array_equal(bf16_to_f64(kb), kf) and np.array_equal(bf16_to_f64(vb), vf)
+    q = normal_bits(rng, (len(ctx), Hq, D))
+    a = oracle.decode(q, kb, vb, tables, ctx, SCALE)
+    b = oracle.decode_fp8(q, kp, vp, ks, vs, tables, ctx, SCALE)
+    assert np.array_equal(a, b)
+    # and the V layout matters: reading V token-major gives something else
+    wrong = oracle.decode_fp8(q, kp, np.ascontiguousarray(
+        vp.transpose(0, 1, 3, 2)).reshape(NB, Hkv, D, bs), ks, vs, tables, ctx, SCALE)
+    assert not np.allclose(wrong, a)
