@@ -50,9 +50,9 @@ DECODE_SOURCES = ["paged_kv_continuous_gb300/csrc/pa_decode_kernel.cuh",
 # algorithmic work (what the method must move; no padding, no partials)
 # ---------------------------------------------------------------------------
 
-def decode_alg_bytes(ctx, hq, hkv, d=128, bs=16):
+def decode_alg_bytes(ctx, hq, hkv, d=128, bs=16, kv_bytes=2):
     ctx = np.asarray(ctx, np.int64)
-    kv = int(ctx.sum()) * hkv * d * 2 * 2            # K and V, bf16
+    kv = int(ctx.sum()) * hkv * d * kv_bytes * 2     # K and V (bf16: 2 bytes, FP8: 1)
     qo = len(ctx) * hq * d * 2 * 2                   # q read + out written, bf16
     tables = int(((ctx + bs - 1) // bs).sum()) * 4
     return kv + qo + tables + len(ctx) * 4
@@ -341,6 +341,48 @@ def run_extras(ops, dev):
         extra[name] = {"us_per_call": ms * 1e3, "tokens": T, "alg_bytes": nbytes,
                        "GB_per_s": nbytes / ms / 1e6, "frac_of_hbm": nbytes / ms / 1e6 / hbm,
                        "peak_kind": hbm_kind}
+        del qkv, q_out, kcr, vcr
+    # FP8 KV cache on the headline workload: the cb_decode_b64 step (store of
+    # the 64 new tokens + decode) over 8 layers of E4M3 pools (2.6 GB, well
+    # past L2), both launches with PDL, captured in one graph per 8 layers
+    w = synth.cb_decode_b64(keep_seq=False)
+    L8 = 8
+    tables8, ctx8 = dev32(w.block_tables), dev32(w.context_lens)
+    slots8 = dev32(w.slot_mapping)
+    NB8, B8, hq8, hkv8 = w.num_blocks, w.batch, w.num_q_heads, w.num_kv_heads
+    ks8 = torch.full((hkv8,), 0.01, dtype=torch.float32, device=dev)
+    vs8 = torch.full((hkv8,), 0.01, dtype=torch.float32, device=dev)
+    fl = []
+    for _ in range(L8):
+        kp, vp = ops.fp8_pools(NB8, hkv8, device=dev)
+        kp.random_(0, 0x7F, generator=gen)     # finite positive codes
+        vp.random_(0, 0x7F, generator=gen)
+        fl.append(dict(kp=kp, vp=vp,
+                       q=torch.randn((B8, hq8, 128), generator=gen, device=dev,
+                                     dtype=torch.bfloat16),
+                       nk=torch.randn((B8, hkv8, 128), generator=gen, device=dev,
+                                      dtype=torch.bfloat16),
+                       nv=torch.randn((B8, hkv8, 128), generator=gen, device=dev,
+                                      dtype=torch.bfloat16),
+                       out=torch.empty((B8, hq8, 128), dtype=torch.bfloat16, device=dev)))
+    splits8 = ops.default_splits(hq8, hkv8, dev.index if dev.index is not None else 0)
+    ws8 = ops.decode_workspace(hq8, hkv8, splits8, 128, dev)
+    st8 = {"l": 0}
+
+    def fp8_step():
+        x = fl[st8["l"] % L8]
+        st8["l"] += 1
+        ops.store_kv_fp8(x["nk"], x["nv"], x["kp"], x["vp"], ks8, vs8, slots8, pdl=True)
+        ops.decode_fp8(x["q"], x["kp"], x["vp"], ks8, vs8, tables8, ctx8, w.scale, out=x["out"],
+                       num_splits=splits8, workspace=ws8, pdl=True)
+    ms = time_graph(fp8_step, 4 * L8)
+    nbytes = decode_alg_bytes(w.context_lens, hq8, hkv8, kv_bytes=1)
+    extra["cb_decode_b64_fp8_e4m3"] = {
+        "us_per_step": ms * 1e3, "alg_bytes": nbytes, "GB_per_s": nbytes / ms / 1e6,
+        "frac_of_hbm": nbytes / ms / 1e6 / hbm, "seq_steps_per_s": B8 / (ms / 1e3),
+        "step": "pa_store_kv_fp8(64 tokens) + pa_decode_fp8, PDL, 8 layer pools",
+        "peak_kind": hbm_kind}
+    del fl
     return extra
 
 

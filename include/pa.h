@@ -12,7 +12,9 @@
  *                      split across CTAs with log-sum-exp partials;
  *   pa_decode_merge    combine those partials into the final rows;
  *   pa_prefill_varlen  causal varlen attention of cu_seqlens-packed query
- *                      chunks over each sequence's paged keys.
+ *                      chunks over each sequence's paged keys;
+ * and an FP8 (E4M3) KV cache: pa_store_kv_fp8 quantises into it and
+ * pa_decode_fp8 decodes over it.
  *
  * Sources (web pages that describe the method):
  *   [EAS] koas-w, "errors and solutions" (Qwen2.5-1.5B inference from
@@ -26,7 +28,8 @@
  *   [MVT] mini-vllm tutorial, "step14_7 -- Batched Forward": sections
  *         "解决方案：变长 batch（varlen）" and "cu_seqlens 只在 Attention 里才需要".
  *   [CEB] PocketLLM, "cpp_engine Batching Implementation (Phase 3.1)",
- *         section "当前 KV cache 结构" (one token row is [kv_heads, head_dim]).
+ *         section "当前 KV cache 结构" (one token row is [kv_heads, head_dim];
+ *         k_scale / v_scale kept beside the caches for FP8/INT8).
  *
  * Conventions shared by every entry point
  *   - All array arguments are DEVICE pointers into caller-owned memory; the
@@ -69,7 +72,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 3
+#define PA_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define PA_API __attribute__((visibility("default")))
@@ -99,8 +102,8 @@ typedef int32_t pa_status;
 #define PA_DEVERR_POSITION 16     /* a position outside the rotary tables */
 
 /*
- * Launch flags (the `flags` argument of pa_store_kv, pa_rope_store_kv,
- * pa_decode and pa_decode_noalloc).  Any other bit returns
+ * Launch flags (the `flags` argument of pa_store_kv, pa_store_kv_fp8,
+ * pa_rope_store_kv, pa_decode, pa_decode_fp8 and pa_decode_noalloc).  Any other bit returns
  * PA_ERR_INVALID_ARG.
  *
  * PA_LAUNCH_PDL: programmatic dependent launch.  The call's kernel may begin
@@ -206,6 +209,33 @@ PA_API pa_status pa_rope_store_kv(const void *q, int64_t q_tok_stride, void *q_o
                                   uint32_t flags, void *stream);
 
 /*
+ * FP8 KV cache ([CEB] "当前 KV cache 结构": k_scale / v_scale beside the
+ * caches, "FP8/INT8 量化时使用"; the pages fix nothing more, so:)
+ *   - every element is an E4M3 code (1 sign bit, 4 exponent bits with bias
+ *     7, 3 mantissa bits; largest finite 448; 0x7F / 0xFF are NaN);
+ *   - k_scale and v_scale are fp32 [num_kv_heads] device arrays; the value
+ *     of a K code of head h is code * k_scale[h] (V likewise);
+ *   - K pool: uint8 [num_blocks][block_size][num_kv_heads][head_dim], the
+ *     bf16 layout with one byte per element;
+ *   - V pool: uint8 [num_blocks][num_kv_heads][head_dim][block_size]:
+ *     dim-major inside a block (token row s % block_size of dim d of head h
+ *     of block s / block_size is byte (((s / bs) * Hkv + h) * D + d) * bs +
+ *     s % bs), so that the decode's tensor-core operands are whole words.
+ *
+ * pa_store_kv_fp8 -- pa_store_kv into FP8 pools: the code of element x of
+ * kv head h is the E4M3 value nearest to x / scale[h] (IEEE fp32 division;
+ * ties to the even code; magnitudes past 448 saturate to +-448).  Arguments
+ * as pa_store_kv, plus k_scale / v_scale; k_cache must be 8-byte aligned.
+ */
+PA_API pa_status pa_store_kv_fp8(const void *k, const void *v, int64_t num_tokens,
+                                 int64_t k_tok_stride, int64_t k_head_stride,
+                                 int64_t v_tok_stride, int64_t v_head_stride, void *k_cache,
+                                 void *v_cache, const float *k_scale, const float *v_scale,
+                                 int64_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                                 int32_t head_dim, const int32_t *slot_mapping,
+                                 int32_t *error_flags, uint32_t flags, void *stream);
+
+/*
  * Decode split partition.  The decode work is the list of all KV blocks of
  * all sequences, sequence after sequence: sequence b owns
  * n_b = ceil(context_lens[b] / block_size) blocks, the global block index of
@@ -285,6 +315,25 @@ PA_API pa_status pa_decode(void *out, int32_t out_dtype, const void *q, const vo
                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                     int32_t block_size, float scale, int32_t num_splits, void *workspace,
                     size_t workspace_bytes, uint32_t flags, void *stream);
+
+/*
+ * pa_decode_fp8 -- pa_decode over FP8 pools (layout and scales above).
+ * Codes are widened exactly; the dot products and P . V run on the tensor
+ * cores in f16 (q is rounded to f16, which is exact for bf16 values of
+ * magnitude 2^-14 .. 65504; larger magnitudes saturate to 65504), with fp32
+ * accumulation, and the result meets the same tolerance as pa_decode
+ * against the attention over the widened values.  Same workspace, splits,
+ * flags and outputs as pa_decode.  Returns PA_ERR_INVALID_ARG when k_scale
+ * or v_scale is NULL.
+ */
+PA_API pa_status pa_decode_fp8(void *out, int32_t out_dtype, const void *q, const void *k_cache,
+                               const void *v_cache, const float *k_scale, const float *v_scale,
+                               int64_t num_blocks, const int32_t *block_tables,
+                               int32_t block_table_stride, const int32_t *context_lens,
+                               int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, float scale,
+                               int32_t num_splits, void *workspace, size_t workspace_bytes,
+                               uint32_t flags, void *stream);
 
 /*
  * pa_decode_merge -- log-sum-exp merge of decode partials (flash-decoding).

@@ -106,6 +106,34 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, long long num_blocks, i
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// FP8 pools.  K: (128 dims, kv head, token slot) of bytes; one box = 128
+// dims x min(Hkv, 2) heads x 16 slots, 128-byte swizzle.  V, dim-major inside
+// a block: (16 tokens, 128 dims, block * Hkv + head); one box = 16 tokens x
+// 128 dims x min(Hkv, 2) heads, no swizzle (16-byte rows).
+bool encode_pool_maps_fp8(CUtensorMap *mk, CUtensorMap *mv, const void *k_pool,
+                          const void *v_pool, long long num_blocks, int hkv) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint32_t hb = (cuuint32_t)(hkv >= 2 ? 2 : 1);
+  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint64_t kd[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv,
+                      (cuuint64_t)num_blocks * kBlockSize};
+  cuuint64_t ks[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv * kHeadDim};
+  cuuint32_t kbox[3] = {(cuuint32_t)kHeadDim, hb, (cuuint32_t)kBlockSize};
+  cuuint64_t vd[3] = {(cuuint64_t)kBlockSize, (cuuint64_t)kHeadDim,
+                      (cuuint64_t)num_blocks * hkv};
+  cuuint64_t vs[2] = {(cuuint64_t)kBlockSize, (cuuint64_t)kHeadDim * kBlockSize};
+  cuuint32_t vbox[3] = {(cuuint32_t)kBlockSize, (cuuint32_t)kHeadDim, hb};
+  return enc(mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(k_pool), kd, ks, kbox,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+             CUDA_SUCCESS &&
+         enc(mv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(v_pool), vd, vs, vbox,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+             CUDA_SUCCESS;
+}
+
 cudaError_t launch_merge(const MergeParams &m, cudaStream_t s) {
   dim3 grid((m.batch + kMergeSeqPerCta - 1) / kMergeSeqPerCta, m.num_q_heads);
   merge_kernel<<<grid, 32 * kMergeSeqPerCta, 0, s>>>(m);
@@ -131,9 +159,12 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
   memset(&tk, 0, sizeof tk);
   memset(&tv, 0, sizeof tv);
   if (r.num_blocks > 0) {
-    if (!encode_pool_map(&tk, r.k_cache, r.num_blocks, r.num_kv_heads) ||
-        !encode_pool_map(&tv, r.v_cache, r.num_blocks, r.num_kv_heads))
-      return PA_ERR_DEVICE;
+    const bool ok =
+        r.fp8 ? encode_pool_maps_fp8(&tk, &tv, r.k_cache, r.v_cache, r.num_blocks,
+                                     r.num_kv_heads)
+              : encode_pool_map(&tk, r.k_cache, r.num_blocks, r.num_kv_heads) &&
+                    encode_pool_map(&tv, r.v_cache, r.num_blocks, r.num_kv_heads);
+    if (!ok) return PA_ERR_DEVICE;
   }
   DecodeParams p;
   p.out = r.out;
@@ -150,6 +181,8 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
   p.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
   p.counters = reinterpret_cast<int32_t *>(ws + L.counters);
   p.err = err;
+  p.k_scale = r.k_scale;
+  p.v_scale = r.v_scale;
   cudaStream_t s = static_cast<cudaStream_t>(r.stream);
   if (clear_counters &&
       cudaMemsetAsync(p.counters, 0, (size_t)r.splits * sizeof(int32_t), s) != cudaSuccess)
@@ -157,11 +190,20 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
   const int G = r.num_q_heads / r.num_kv_heads;
   const bool pdl = (r.flags & PA_LAUNCH_PDL) != 0;
   cudaError_t e;
-  switch (r.num_kv_heads) {
-    case 1: e = launch_decode<1>(G, tk, tv, p, s, device, pdl); break;
-    case 2: e = launch_decode<2>(G, tk, tv, p, s, device, pdl); break;
-    case 4: e = launch_decode<4>(G, tk, tv, p, s, device, pdl); break;
-    default: e = launch_decode<8>(G, tk, tv, p, s, device, pdl); break;
+  if (r.fp8) {
+    switch (r.num_kv_heads) {
+      case 1: e = launch_decode<1, true>(G, tk, tv, p, s, device, pdl); break;
+      case 2: e = launch_decode<2, true>(G, tk, tv, p, s, device, pdl); break;
+      case 4: e = launch_decode<4, true>(G, tk, tv, p, s, device, pdl); break;
+      default: e = launch_decode<8, true>(G, tk, tv, p, s, device, pdl); break;
+    }
+  } else {
+    switch (r.num_kv_heads) {
+      case 1: e = launch_decode<1, false>(G, tk, tv, p, s, device, pdl); break;
+      case 2: e = launch_decode<2, false>(G, tk, tv, p, s, device, pdl); break;
+      case 4: e = launch_decode<4, false>(G, tk, tv, p, s, device, pdl); break;
+      default: e = launch_decode<8, false>(G, tk, tv, p, s, device, pdl); break;
+    }
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
 }
@@ -226,6 +268,32 @@ extern "C" pa_status pa_decode(void *out, int32_t out_dtype, const void *q, cons
   int device = -1;
   const pa_status st = check_decode_request(r, &device);
   if (st != PA_OK || batch == 0) return st;
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < pa_decode_workspace_size(r.splits, num_q_heads, head_dim))
+    return PA_ERR_WORKSPACE;
+  return run_decode(r, workspace, static_cast<int32_t *>(workspace), device, false);
+}
+
+extern "C" pa_status pa_decode_fp8(void *out, int32_t out_dtype, const void *q,
+                                   const void *k_cache, const void *v_cache, const float *k_scale,
+                                   const float *v_scale, int64_t num_blocks,
+                                   const int32_t *block_tables, int32_t block_table_stride,
+                                   const int32_t *context_lens, int32_t batch,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, float scale, int32_t num_splits,
+                                   void *workspace, size_t workspace_bytes, uint32_t flags,
+                                   void *stream) {
+  using namespace pa;
+  DecodeRequest r{out, out_dtype, q, k_cache, v_cache, num_blocks, block_tables,
+                  block_table_stride, context_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                  block_size, scale, num_splits, 0, flags, stream};
+  r.fp8 = true;
+  r.k_scale = k_scale;
+  r.v_scale = v_scale;
+  int device = -1;
+  const pa_status st = check_decode_request(r, &device);
+  if (st != PA_OK || batch == 0) return st;
+  if (!k_scale || !v_scale) return PA_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < pa_decode_workspace_size(r.splits, num_q_heads, head_dim))
     return PA_ERR_WORKSPACE;

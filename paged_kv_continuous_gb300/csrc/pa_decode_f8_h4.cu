@@ -1,0 +1,4 @@
+// decode_kernel instantiations for FP8 (E4M3) pools, 4 kv head(s) per sequence.
+#define PA_HKV 4
+#define PA_F8 true
+#include "pa_decode_inst.cuh"

@@ -1,0 +1,4 @@
+// decode_kernel instantiations for FP8 (E4M3) pools, 8 kv head(s) per sequence.
+#define PA_HKV 8
+#define PA_F8 true
+#include "pa_decode_inst.cuh"

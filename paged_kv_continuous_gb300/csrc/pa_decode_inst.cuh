@@ -1,10 +1,14 @@
-// Instantiates decode_kernel<G, PA_HKV> for G = 1..8 and the launcher the
-// host ABI dispatches to.  Included once per kv-head count by
-// pa_decode_h{1,2,4,8}.cu so that the instantiations compile in parallel.
+// Instantiates decode_kernel<G, PA_HKV, PA_F8> for G = 1..8 and the launcher
+// the host ABI dispatches to.  Included once per kv-head count and pool type
+// by pa_decode_h{1,2,4,8}.cu (bf16 pools) and pa_decode_f8_h{1,2,4,8}.cu
+// (FP8 pools) so that the instantiations compile in parallel.
 #include "pa_decode_kernel.cuh"
 
 #ifndef PA_HKV
 #error "define PA_HKV before including pa_decode_inst.cuh"
+#endif
+#ifndef PA_F8
+#define PA_F8 false
 #endif
 
 namespace pa {
@@ -13,21 +17,21 @@ namespace {
 template <int G>
 cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                      cudaStream_t s, int device, bool pdl) {
-  using Sh = DecodeShape<G, PA_HKV>;
+  using Sh = DecodeShape<G, PA_HKV, PA_F8>;
   static bool configured[64] = {};
   if (device < 0 || device >= 64 || !configured[device]) {
     const cudaError_t e = cudaFuncSetAttribute(
-        decode_kernel<G, PA_HKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
+        decode_kernel<G, PA_HKV, PA_F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < 64) configured[device] = true;
   }
-  return launch_kernel(decode_kernel<G, PA_HKV>, dim3(p.num_splits), dim3(kDecodeThreads),
+  return launch_kernel(decode_kernel<G, PA_HKV, PA_F8>, dim3(p.num_splits), dim3(kDecodeThreads),
                        Sh::SMEM, s, pdl, tk, tv, p);
 }
 }  // namespace
 
 template <>
-cudaError_t launch_decode<PA_HKV>(int G, const CUtensorMap &tk, const CUtensorMap &tv,
+cudaError_t launch_decode<PA_HKV, PA_F8>(int G, const CUtensorMap &tk, const CUtensorMap &tv,
                                   const DecodeParams &p, cudaStream_t s, int device,
                                   bool pdl) {
   switch (G) {

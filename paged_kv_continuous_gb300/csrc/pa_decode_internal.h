@@ -38,6 +38,10 @@ struct DecodeRequest {
   int32_t splits;      // resolved by check_decode_request
   uint32_t flags;      // PA_LAUNCH_* bits
   void *stream;
+  // FP8 (E4M3) pools: K token-major, V dim-major per block, per-kv-head scales
+  bool fp8 = false;
+  const float *k_scale = nullptr;
+  const float *v_scale = nullptr;
 };
 
 // Host checks shared by both decode entry points; resolves r.splits.

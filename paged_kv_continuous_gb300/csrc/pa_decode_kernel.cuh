@@ -69,6 +69,8 @@ struct DecodeParams {
   float *part_lse;    // [S][2][HQ], natural log
   int32_t *counters;  // [S] arrival counters, zero between calls
   int32_t *err;
+  const float *k_scale;  // FP8 pools only: per kv head, value = code * scale
+  const float *v_scale;
 };
 
 constexpr int kDecodeProducerWarps = 2;
@@ -82,7 +84,10 @@ constexpr int kTileBytes = kBlockSize * 64 * 2;  // 16 tokens x 64 dims bf16 = 2
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-template <int G, int HKV>
+// F8: the pools hold E4M3 codes (one byte per element) with per-kv-head
+// scales; K pages keep the token-major layout, V pages are dim-major inside a
+// block ([Hkv][128 dims][16 tokens]).
+template <int G, int HKV, bool F8 = false>
 struct DecodeShape {
   static constexpr int HQ = G * HKV;
   static constexpr int CW = kDecodeConsumerWarps;
@@ -91,8 +96,11 @@ struct DecodeShape {
   // NPAIR * 2 boxes (head groups x dim halves)
   static constexpr int HB = HKV >= 2 ? 2 : 1;
   static constexpr int NPAIR = HKV / HB;
+  // bf16: 16 tokens x HB heads x 64 dims (two boxes per head pair);
+  // F8: K 16 tokens x HB heads x 128 dims, V HB heads x 128 dims x 16 tokens
+  // (one box each per head pair); 2 KB per head either way
   static constexpr int BOX_BYTES = HB * kTileBytes;
-  static constexpr int KV_BYTES = HKV * 2 * kTileBytes;     // one block of K (or V), all heads
+  static constexpr int KV_BYTES = HKV * (F8 ? 1 : 2) * kTileBytes;  // one block of K (or V)
   static constexpr int Q_BYTES = HQ * kHeadDim * 2;
   static constexpr int STAGE_BYTES = align_up(2 * KV_BYTES + Q_BYTES, 1024);
   // per consumer warp and query head of its group: o[128], m, l (rows of
@@ -298,6 +306,46 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d += A(16x16, row) . B(16x8, col), f16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 codes (low byte first) to two f16 values (low half first); every
+// E4M3 value is exact in f16.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)(codes & 0xFFFFu)));
+  return r;
+}
+
+// Round two floats to f16 (nearest even, saturated to +-65504), lo in the
+// low half.
+__device__ __forceinline__ uint32_t float2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\t"
+      "cvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w));
+  return make_float2(lo, hi);
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 // Byte offset of (row, 16-byte chunk) in a tile written by TMA with the
@@ -535,11 +583,11 @@ __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, 
   return true;
 }
 
-template <int G, int HKV>
+template <int G, int HKV, bool F8 = false>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-  using S = DecodeShape<G, HKV>;
+  using S = DecodeShape<G, HKV, F8>;
   extern __shared__ uint8_t smem_raw[];
   // realign to 1024 bytes: the 128-byte swizzle pattern repeats every 1 KB
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -726,13 +774,26 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         __syncwarp();
         if (ok) {
           const int z = (int)(ph_i * kBlockSize);
+          if constexpr (F8) {
+            // K: (128 dims, head, slot) box of a head pair; V: (16 tokens,
+            // 128 dims, block * Hkv + head) box of the same pair
 #pragma unroll
-          for (int pr = 0; pr < S::NPAIR; ++pr) {
+            for (int pr = 0; pr < S::NPAIR; ++pr) {
+              const uint32_t off = pr * S::BOX_BYTES;
+              tma_load_box(dst + off, &tmap_k, 0, pr * S::HB, z, bar, pol_kv);
+              tma_load_box(dst + S::KV_BYTES + off, &tmap_v, 0, 0,
+                           (int)(ph_i * HKV) + pr * S::HB, bar, pol_kv);
+            }
+          } else {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t off = (pr * 2 + h) * S::BOX_BYTES;
-              tma_load_box(dst + off, &tmap_k, h * 64, pr * S::HB, z, bar, pol_kv);
-              tma_load_box(dst + S::KV_BYTES + off, &tmap_v, h * 64, pr * S::HB, z, bar, pol_kv);
+            for (int pr = 0; pr < S::NPAIR; ++pr) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t off = (pr * 2 + h) * S::BOX_BYTES;
+                tma_load_box(dst + off, &tmap_k, h * 64, pr * S::HB, z, bar, pol_kv);
+                tma_load_box(dst + S::KV_BYTES + off, &tmap_v, h * 64, pr * S::HB, z, bar,
+                             pol_kv);
+              }
             }
           }
         }
@@ -893,7 +954,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int ct = tid - 32 * kDecodeFirstConsumerWarp;  // consumer thread index
   // this warp's kv head inside the TMA boxes: box group, row offset
   const int gpair = g / S::HB, gsub = g % S::HB;
-  const float cl2 = p.qk_scale_log2;
+  // F8: the K scale of this kv head folds into the score scale, the V scale
+  // into the rows at each piece end (codes widen exactly, so the products
+  // equal those of the widened values)
+  const float cl2 = F8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) : p.qk_scale_log2;
+  const float vsc = F8 ? __ldg(p.v_scale + g) : 1.f;
+  // F8: the 16 score rows of an MMA are the tokens tperm(r), so that a
+  // thread's two token pairs of the PV operand are 4 consecutive bytes of
+  // a dim-major V row: rows 2i, 2i + 1 -> tokens 4i, 4i + 1 and rows
+  // 8 + 2i, 9 + 2i -> tokens 4i + 2, 4i + 3 (any order of the tokens gives
+  // the same sums; the same order is used for K, the mask and V)
+  const int tok0 = F8 ? (((gid >> 1) << 2) | (gid & 1)) : gid;           // row gid
+  const int tok1 = F8 ? (((gid >> 1) << 2) | 2 | (gid & 1)) : gid + 8;   // row gid + 8
 
   uint32_t qf[8][2];  // Q^T fragments of the group, per 16-dim k-step
   float o[8][4];      // O^T rows 16 mt + {gid, gid + 8}, head columns 2 qd, 2 qd + 1
@@ -979,14 +1051,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             for (int ks = 0; ks < 8; ++ks) {
               uint32_t x0 = 0, x1 = 0;
               if (gid < G) {
-                asm volatile("ld.shared.u32 %0, [%1];"
-                             : "=r"(x0)
-                             : "r"(qrow + (16 * ks + 2 * qd) * 2)
-                             : "memory");
-                asm volatile("ld.shared.u32 %0, [%1];"
-                             : "=r"(x1)
-                             : "r"(qrow + (16 * ks + 8 + 2 * qd) * 2)
-                             : "memory");
+                if constexpr (F8) {
+                  // f16 operands; the k-step's dims in the order the K
+                  // fragments use: columns 2qd, 2qd + 1 = dims 4qd, 4qd + 1,
+                  // columns 2qd + 8, 2qd + 9 = dims 4qd + 2, 4qd + 3
+                  const uint32_t w0 = lds32(qrow + (16 * ks + 4 * qd) * 2);
+                  const uint32_t w1 = lds32(qrow + (16 * ks + 4 * qd + 2) * 2);
+                  const float2 f0 = bf16x2_to_float2(w0), f1 = bf16x2_to_float2(w1);
+                  x0 = float2_to_f16x2(f0.x, f0.y);
+                  x1 = float2_to_f16x2(f1.x, f1.y);
+                } else {
+                  x0 = lds32(qrow + (16 * ks + 2 * qd) * 2);
+                  x1 = lds32(qrow + (16 * ks + 8 + 2 * qd) * 2);
+                }
               }
               qf[ks][0] = x0;
               qf[ks][1] = x1;
@@ -995,12 +1072,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
         const int valid = min(kBlockSize, ctx - j * kBlockSize);  // keys of this block (>= 1)
         if (have) {
-          // boxes of this head group: K at kb (+BOX_BYTES for dims 64..127), V at vb
-          const uint32_t kb = sbase + gpair * 2 * S::BOX_BYTES;
-          const uint32_t vb = sbase + S::KV_BYTES + gpair * 2 * S::BOX_BYTES;
+          // boxes of this head group: K at kb (bf16: +BOX_BYTES for dims
+          // 64..127), V at vb
+          const uint32_t kb = sbase + gpair * (F8 ? 1 : 2) * S::BOX_BYTES;
+          const uint32_t vb = sbase + S::KV_BYTES + gpair * (F8 ? 1 : 2) * S::BOX_BYTES;
           // S^T = K . Q^T, two accumulation chains over the eight 16-dim k-steps
           float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-          {
+          if constexpr (F8) {
+            // 128-byte rows of E4M3 codes (token, head), 128-byte swizzle:
+            // four consecutive dims of rows tok0 and tok1 per k-step
+            const int row0 = tok0 * S::HB + gsub, row1 = tok1 * S::HB + gsub;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t w0 = lds32(kb + swz(row0, ks) + 4 * qd);
+              const uint32_t w1 = lds32(kb + swz(row1, ks) + 4 * qd);
+              const uint32_t a0 = e4m3x2_to_f16x2(w0), a2 = e4m3x2_to_f16x2(w0 >> 16);
+              const uint32_t a1 = e4m3x2_to_f16x2(w1), a3 = e4m3x2_to_f16x2(w1 >> 16);
+              if (ks & 1)
+                mma_f16(sb, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+              else
+                mma_f16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+            }
+          } else {
             const int mi = lane >> 3, r = lane & 7;
             const int t = r + ((mi & 1) << 3);
             const int row = t * S::HB + gsub;  // 128-byte row of token t, this head
@@ -1015,8 +1108,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
             }
           }
-          // scores: [0] (token gid, head 2qd) [1] (gid, 2qd+1) [2] (gid+8, 2qd) [3] (gid+8, 2qd+1)
-          const bool v0 = gid < valid, v1 = gid + 8 < valid;
+          // scores: [0] (token tok0, head 2qd) [1] (tok0, 2qd+1) [2] (tok1, 2qd)
+          // [3] (tok1, 2qd+1)
+          const bool v0 = tok0 < valid, v1 = tok1 < valid;
           const float s0 = v0 ? sa[0] + sb[0] : -INFINITY;
           const float s1 = v0 ? sa[1] + sb[1] : -INFINITY;
           const float s2 = v1 ? sa[2] + sb[2] : -INFINITY;
@@ -1044,25 +1138,67 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             o[mt][2] *= al0;
             o[mt][3] *= al1;
           }
-          // P^T fragments, hi + lo bf16 split
-          const uint32_t hA = float2_to_bf16x2(p0, p1), hB = float2_to_bf16x2(p2, p3);
-          const float2 fA = bf16x2_to_float2(hA), fB = bf16x2_to_float2(hB);
-          const uint32_t lA = float2_to_bf16x2(p0 - fA.x, p1 - fA.y);
-          const uint32_t lB = float2_to_bf16x2(p2 - fB.x, p3 - fB.y);
+          // P^T fragments, hi + lo split (bf16, or f16 with F8 pools)
+          uint32_t hA, hB, lA, lB;
+          if constexpr (F8) {
+            hA = float2_to_f16x2(p0, p1);
+            hB = float2_to_f16x2(p2, p3);
+            const float2 fA = f16x2_to_float2(hA), fB = f16x2_to_float2(hB);
+            lA = float2_to_f16x2(p0 - fA.x, p1 - fA.y);
+            lB = float2_to_f16x2(p2 - fB.x, p3 - fB.y);
+          } else {
+            hA = float2_to_bf16x2(p0, p1);
+            hB = float2_to_bf16x2(p2, p3);
+            const float2 fA = bf16x2_to_float2(hA), fB = bf16x2_to_float2(hB);
+            lA = float2_to_bf16x2(p0 - fA.x, p1 - fA.y);
+            lB = float2_to_bf16x2(p2 - fB.x, p3 - fB.y);
+          }
           const uint32_t bh0 = movm_t(hA), bh1 = movm_t(hB);
           const uint32_t bl0 = movm_t(lA), bl1 = movm_t(lB);
           if (valid < kBlockSize) {
             // rows past the last key may hold anything (NaN): zero them so that
             // 0-weight rows contribute exactly 0 to the MMA
-            for (int i = lane; i < (kBlockSize - valid) * 16; i += 32) {
-              const int t = valid + (i >> 4), ch = i & 15;
-              const uint32_t a = vb + (ch >> 3) * S::BOX_BYTES + swz(t * S::HB + gsub, ch & 7);
-              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+            if constexpr (F8) {
+              // dim-major: bytes valid .. 15 of each of this head's 128 dim rows
+              const uint32_t hb = vb + gsub * (kHeadDim * kBlockSize);
+              for (int d = lane; d < kHeadDim; d += 32) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  const int keep = min(max(valid - 4 * w, 0), 4);
+                  if (keep < 4) {
+                    const uint32_t a = hb + d * kBlockSize + 4 * w;
+                    const uint32_t mask = keep == 0 ? 0u : (1u << (8 * keep)) - 1u;
+                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(lds32(a) & mask)
+                                 : "memory");
+                  }
+                }
+              }
+            } else {
+              for (int i = lane; i < (kBlockSize - valid) * 16; i += 32) {
+                const int t = valid + (i >> 4), ch = i & 15;
+                const uint32_t a = vb + (ch >> 3) * S::BOX_BYTES + swz(t * S::HB + gsub, ch & 7);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u)
+                             : "memory");
+              }
             }
             __syncwarp();
           }
           // O^T += V^T . P^T
-          {
+          if constexpr (F8) {
+            // dim rows 16 mt + gid (a0, a2) and + 8 (a1, a3): bytes 4qd .. 4qd + 3
+            // are the tokens of k-rows 2qd, 2qd + 1 (a0 / a1) and 2qd + 8,
+            // 2qd + 9 (a2 / a3) in the score-row order above
+            const uint32_t hb = vb + gsub * (kHeadDim * kBlockSize) + gid * kBlockSize + 4 * qd;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              const uint32_t w0 = lds32(hb + 16 * mt * kBlockSize);
+              const uint32_t w1 = lds32(hb + (16 * mt + 8) * kBlockSize);
+              const uint32_t a0 = e4m3x2_to_f16x2(w0), a2 = e4m3x2_to_f16x2(w0 >> 16);
+              const uint32_t a1 = e4m3x2_to_f16x2(w1), a3 = e4m3x2_to_f16x2(w1 >> 16);
+              mma_f16(o[mt], a0, a1, a2, a3, bh0, bh1);
+              mma_f16(o[mt], a0, a1, a2, a3, bl0, bl1);
+            }
+          } else {
             const int mi = lane >> 3, r = lane & 7;
             const int t = r + ((mi >> 1) << 3);
             const int row = t * S::HB + gsub;
@@ -1085,6 +1221,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       if (!piece_last) continue;
 
       // ---- end of a piece: merge the warps of each kv head, write rows -------
+      if constexpr (F8) {
+        // the V scale of this warp's kv head, once per piece
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[mt][i] *= vsc;
+      }
       if (ct == 0 && !pc_done) piece_splits(gb, j, n);  // warp 0 had no stage in the piece
       const bool head_cut = gb - j < lo;  // the sequence starts before this CTA's blocks
       const bool tail_cut = j < n - 1;
@@ -1334,8 +1477,9 @@ consumers_done:
   }
 }
 
-// Launches decode_kernel<G, HKV> for one G (defined per HKV in pa_decode_h*.cu).
-template <int HKV>
+// Launches decode_kernel<G, HKV, F8> for one G (defined per HKV and F8 in
+// pa_decode_h*.cu and pa_decode_f8_h*.cu).
+template <int HKV, bool F8>
 cudaError_t launch_decode(int G, const CUtensorMap &tk, const CUtensorMap &tv,
                           const DecodeParams &p, cudaStream_t s, int device, bool pdl);
 

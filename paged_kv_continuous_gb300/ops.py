@@ -30,7 +30,7 @@ DEVERR_POSITION = 16
 EXPORTED = (
     "pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
     "pa_decode_default_splits", "pa_decode", "pa_decode_merge", "pa_prefill_varlen",
-    "pa_decode_noalloc", "pa_rope_store_kv",
+    "pa_decode_noalloc", "pa_rope_store_kv", "pa_store_kv_fp8", "pa_decode_fp8",
 )
 
 
@@ -62,6 +62,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_decode.restype = i32
     lib.pa_decode.argtypes = [P, i32, P, P, P, i64, P, i32, P, i32, i32, i32, i32, i32, f32,
                               i32, P, sz, u32, P]
+    lib.pa_decode_fp8.restype = i32
+    lib.pa_decode_fp8.argtypes = [P, i32, P, P, P, P, P, i64, P, i32, P, i32, i32, i32, i32,
+                                  i32, f32, i32, P, sz, u32, P]
+    lib.pa_store_kv_fp8.restype = i32
+    lib.pa_store_kv_fp8.argtypes = [P, P, i64, i64, i64, i64, i64, P, P, P, P, i64, i32, i32,
+                                    i32, P, P, u32, P]
     lib.pa_decode_merge.restype = i32
     lib.pa_decode_merge.argtypes = [P, i32, P, sz, P, i32, i32, i32, i32, i32, P]
     lib.pa_decode_noalloc.restype = i32
@@ -228,6 +234,78 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
                          _ptr(context_lens), B, Hq, Hkv, D, bs, float(scale), int(num_splits),
                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                          PA_LAUNCH_PDL if pdl else 0, _stream(stream)), "pa_decode")
+    return out
+
+
+def fp8_pools(num_blocks, num_kv_heads, head_dim=128, block_size=16, device=None):
+    """Empty FP8 pools: K uint8 [NB, bs, Hkv, D] (token-major), V uint8
+    [NB, Hkv, D, bs] (dim-major inside a block)."""
+    k = torch.empty((num_blocks, block_size, num_kv_heads, head_dim), dtype=torch.uint8,
+                    device=device)
+    v = torch.empty((num_blocks, num_kv_heads, head_dim, block_size), dtype=torch.uint8,
+                    device=device)
+    return k, v
+
+
+def _need_fp8_pools(k_cache, v_cache, k_scale, v_scale):
+    _need(k_cache, torch.uint8, "k_cache", 4)
+    _need(v_cache, torch.uint8, "v_cache", 4)
+    _need(k_scale, torch.float32, "k_scale", 1)
+    _need(v_scale, torch.float32, "v_scale", 1)
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise PagedAttentionError("pools must be contiguous")
+    NB, bs, Hkv, D = k_cache.shape
+    if tuple(v_cache.shape) != (NB, Hkv, D, bs):
+        raise PagedAttentionError("FP8 V pool must be [num_blocks, Hkv, D, block_size]")
+    if k_scale.shape[0] != Hkv or v_scale.shape[0] != Hkv:
+        raise PagedAttentionError("k_scale / v_scale need one entry per kv head")
+    return NB, bs, Hkv, D
+
+
+def store_kv_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, error_flags=None,
+                 stream=None, pdl=False):
+    """pa_store_kv_fp8: quantise k/v bf16 [T, Hkv, D] (any token/head
+    strides) into the FP8 pools (see fp8_pools) at slot_mapping."""
+    _need(k, torch.bfloat16, "k", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    _need(slot_mapping, torch.int32, "slot_mapping", 1)
+    if k.stride(2) != 1 or v.stride(2) != 1:
+        raise PagedAttentionError("k/v need a unit stride along head_dim")
+    NB, bs, Hkv, D = _need_fp8_pools(k_cache, v_cache, k_scale, v_scale)
+    T = k.shape[0]
+    if tuple(k.shape) != (T, Hkv, D) or v.shape != k.shape or slot_mapping.shape[0] != T:
+        raise PagedAttentionError("shape mismatch between k/v, the pools and slot_mapping")
+    _check(lib.pa_store_kv_fp8(_ptr(k), _ptr(v), T, k.stride(0), k.stride(1), v.stride(0),
+                               v.stride(1), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                               _ptr(v_scale), NB, bs, Hkv, D, _ptr(slot_mapping),
+                               _ptr(error_flags), PA_LAUNCH_PDL if pdl else 0, _stream(stream)),
+           "pa_store_kv_fp8")
+
+
+def decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
+               out=None, out_dtype=torch.bfloat16, num_splits=0, workspace=None, stream=None,
+               pdl=False):
+    """pa_decode_fp8: q bf16 [B, Hq, D] over the FP8 pools with per-kv-head
+    scales; returns out [B, Hq, D]."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    if not q.is_contiguous():
+        raise PagedAttentionError("q must be contiguous")
+    if block_tables.stride(1) != 1:
+        raise PagedAttentionError("block_tables rows must be contiguous")
+    NB, bs, Hkv, _ = _need_fp8_pools(k_cache, v_cache, k_scale, v_scale)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(Hq, Hkv, num_splits, D, q.device)
+    _check(lib.pa_decode_fp8(_ptr(out), _out_code(out.dtype), _ptr(q), _ptr(k_cache),
+                             _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), NB,
+                             _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), B,
+                             Hq, Hkv, D, bs, float(scale), int(num_splits), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(),
+                             PA_LAUNCH_PDL if pdl else 0, _stream(stream)), "pa_decode_fp8")
     return out
 
 
