@@ -108,8 +108,8 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, long long num_blocks, i
 
 // FP8 pools.  K: (128 dims, kv head, token slot) of bytes; one box = 128
 // dims x min(Hkv, 2) heads x 16 slots, 128-byte swizzle.  V, dim-major inside
-// a block: (16 tokens, 128 dims, block * Hkv + head); one box = 16 tokens x
-// 128 dims x min(Hkv, 2) heads, no swizzle (16-byte rows).
+// a block, is read by plain bulk copies (one per block); its map -- (16
+// tokens, 128 dims, block * Hkv + head) -- only validates the pool.
 bool encode_pool_maps_fp8(CUtensorMap *mk, CUtensorMap *mv, const void *k_pool,
                           const void *v_pool, long long num_blocks, int hkv) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -183,6 +183,7 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
   p.err = err;
   p.k_scale = r.k_scale;
   p.v_scale = r.v_scale;
+  p.v_pool = r.fp8 ? static_cast<const uint8_t *>(r.v_cache) : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(r.stream);
   if (clear_counters &&
       cudaMemsetAsync(p.counters, 0, (size_t)r.splits * sizeof(int32_t), s) != cudaSuccess)

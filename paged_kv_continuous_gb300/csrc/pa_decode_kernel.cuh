@@ -71,6 +71,7 @@ struct DecodeParams {
   int32_t *err;
   const float *k_scale;  // FP8 pools only: per kv head, value = code * scale
   const float *v_scale;
+  const uint8_t *v_pool;  // FP8 pools only: V, [num_blocks][Hkv][128][16] bytes
 };
 
 constexpr int kDecodeProducerWarps = 2;
@@ -775,15 +776,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (ok) {
           const int z = (int)(ph_i * kBlockSize);
           if constexpr (F8) {
-            // K: (128 dims, head, slot) box of a head pair; V: (16 tokens,
-            // 128 dims, block * Hkv + head) box of the same pair
+            // K: (128 dims, head, slot) box of each head pair, 128-byte
+            // swizzle; V: the block's dim-major page is one contiguous run
+            // (Hkv x 2 KB): one bulk copy (a tensor box would move 16-byte
+            // rows)
 #pragma unroll
-            for (int pr = 0; pr < S::NPAIR; ++pr) {
-              const uint32_t off = pr * S::BOX_BYTES;
-              tma_load_box(dst + off, &tmap_k, 0, pr * S::HB, z, bar, pol_kv);
-              tma_load_box(dst + S::KV_BYTES + off, &tmap_v, 0, 0,
-                           (int)(ph_i * HKV) + pr * S::HB, bar, pol_kv);
-            }
+            for (int pr = 0; pr < S::NPAIR; ++pr)
+              tma_load_box(dst + pr * S::BOX_BYTES, &tmap_k, 0, pr * S::HB, z, bar, pol_kv);
+            bulk_load_elect(dst + S::KV_BYTES, p.v_pool + ph_i * S::KV_BYTES, S::KV_BYTES, bar,
+                            pol_kv);
           } else {
 #pragma unroll
             for (int pr = 0; pr < S::NPAIR; ++pr) {
