@@ -4,8 +4,10 @@
 Workload: the continuous-batching mix -- 64 sequences with lognormal context
 lengths (median 1024, clipped to [1, 8192]), Qwen2.5-1.5B attention shapes
 (12 query heads, 2 KV heads, head_dim 128, 16-token blocks), a 40000-block
-shuffled pool per layer.  One step = pa_store_kv of the 64 new tokens, then
-pa_decode (balanced split-K + merge) over all sequences, for one layer.
+shuffled pool per layer.  One step = the store of the 64 new tokens and the
+decode (balanced split-K + merge) of all sequences, for one layer, in one
+kernel (pa_store_decode; the two-launch form, pa_store_kv then pa_decode, is
+timed beside it as "unfused_step").
 Steps cycle over L = 8 independent layer pools (same lengths and tables,
 different data), so every step reads its KV from HBM, not from L2 (8 x ~105
 MB of live KV >> the 126 MB L2).  Steps run as CUDA-graph replays (one graph
@@ -499,16 +501,22 @@ def run_ours(args):
     ws = ops.decode_workspace(Hq, Hkv, splits, D, dev)
 
     def step(l, timing=None):
+        # one decode step of one layer: the 64 new tokens stored and every
+        # sequence decoded, in one kernel (pa_store_decode)
         x = layers[l]
         if timing:
             timing[0].record()
-        ops.store_kv(x["nk"], x["nv"], x["kc"], x["vc"], slots, pdl=True)
+        ops.store_decode(x["q"], x["nk"], x["nv"], x["kc"], x["vc"], slots, tables, ctx,
+                         w.scale, out=x["out"], num_splits=splits, workspace=ws, pdl=True)
         if timing:
             timing[1].record()
+
+    def step_unfused(l):
+        # the same step as two launches: pa_store_kv, then pa_decode
+        x = layers[l]
+        ops.store_kv(x["nk"], x["nv"], x["kc"], x["vc"], slots, pdl=True)
         ops.decode(x["q"], x["kc"], x["vc"], tables, ctx, w.scale, out=x["out"],
                    num_splits=splits, workspace=ws, pdl=True)
-        if timing:
-            timing[2].record()
 
     # first step of layer 0 checked against the oracle (bench-time parity)
     step(0)
@@ -535,7 +543,7 @@ def run_ours(args):
         for l in range(L):
             try:
                 evs.append([torch.cuda.Event(enable_timing=True, external=True)
-                            for _ in range(3)] if c == 0 else None)
+                            for _ in range(2)] if c == 0 else None)
             except TypeError:
                 ext_ok = False
                 evs.append(None)
@@ -551,7 +559,7 @@ def run_ours(args):
         with torch.cuda.graph(rem_graph, stream=s):
             for l in range(rem):
                 step(l)
-    launches_per_step = 2  # store_kv_kernel + decode_kernel (the merge runs inside decode)
+    launches_per_step = 1  # decode_kernel: store, decode and merge in one launch
 
     def barrier():
         if world > 1:
@@ -594,13 +602,19 @@ def run_ours(args):
     err_word = ops.read_error_word(ws)
 
     # per-kernel durations from the last replay of each graph copy
-    store_ms, decode_ms = [], []
+    decode_ms = []
     if ext_ok and full >= 1:
         for l in range(L):
             e = events[0][l]
             if e is not None:
-                store_ms.append(e[0].elapsed_time(e[1]))
-                decode_ms.append(e[1].elapsed_time(e[2]))
+                decode_ms.append(e[0].elapsed_time(e[1]))
+    # the same step as two launches (pa_store_kv, then pa_decode), for comparison
+    st_u = {"l": 0}
+
+    def unfused():
+        step_unfused(st_u["l"] % L)
+        st_u["l"] += 1
+    unfused_ms = time_graph(unfused, 4 * L)
 
     ms_per_step = elapsed_s * 1e3 / args.steps
     dec_bytes = decode_alg_bytes(w.context_lens, Hq, Hkv, D)
@@ -632,9 +646,8 @@ def run_ours(args):
         tables.copy_(h_tab, non_blocking=True)
         ctx.copy_(h_ctx, non_blocking=True)
         slots.copy_(h_slot, non_blocking=True)
-        ops.store_kv(d_nk, d_nv, x["kc"], x["vc"], slots, pdl=True)
-        ops.decode(d_q, x["kc"], x["vc"], tables, ctx, w.scale, out=x["out"],
-                   num_splits=splits, workspace=ws, pdl=True)
+        ops.store_decode(d_q, d_nk, d_nv, x["kc"], x["vc"], slots, tables, ctx, w.scale,
+                         out=x["out"], num_splits=splits, workspace=ws, pdl=True)
         h_out.copy_(x["out"], non_blocking=True)
 
     for i in range(min(args.warmup, 50)):
@@ -668,14 +681,15 @@ def run_ours(args):
 
     peak, peak_kind = hbm_peak()
     dec_s = float(np.mean(decode_ms)) / 1e3 if decode_ms else None
-    achieved = dec_bytes / dec_s / 1e9 if dec_s else None
+    achieved = step_bytes / dec_s / 1e9 if dec_s else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak if achieved else None,
                 "traffic": recorded_traffic("decode_kernel", w.name),
                 "peak_kind": f"{peak_kind} HBM copy bandwidth",
                 "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS if achieved else None,
-                "kernel": "decode_kernel<6,2> (pa_decode; split-K merge fused in the kernel)",
-                "alg_bytes_per_launch": dec_bytes,
+                "kernel": "decode_kernel<6,2> (pa_store_decode: the new tokens' store, the "
+                          "decode and the split-K merge in one kernel)",
+                "alg_bytes_per_launch": step_bytes,
                 "launch_ms_mean": dec_s * 1e3 if dec_s else None,
                 "launch_samples": len(decode_ms)}
     clocks = sampler.summary(t_host0, t_host1)
@@ -691,10 +705,13 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: {L} layer pools cycled "
                          f"(~{dec_bytes * L / 1e6:.0f} MB of live KV)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "step": "pa_store_kv(64 tokens) + pa_decode(+merge), one layer",
-                   "launch": "PA_LAUNCH_PDL (programmatic dependent launch) on both calls"},
+                   "step": "pa_store_decode: store of the 64 new tokens + decode (+merge) "
+                           "in one kernel, one layer",
+                   "launch": "PA_LAUNCH_PDL (programmatic dependent launch)"},
         "seq_steps_per_s": world * B * args.steps / elapsed_s,
-        "store_ms_mean": float(np.mean(store_ms)) if store_ms else None,
+        "unfused_step": {"us_per_step": unfused_ms * 1e3,
+                         "GB_per_s": step_bytes / unfused_ms / 1e6,
+                         "step": "pa_store_kv + pa_decode, two launches, PDL"},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),

@@ -13,8 +13,9 @@
  *   pa_decode_merge    combine those partials into the final rows;
  *   pa_prefill_varlen  causal varlen attention of cu_seqlens-packed query
  *                      chunks over each sequence's paged keys;
- * and an FP8 (E4M3) KV cache: pa_store_kv_fp8 quantises into it and
- * pa_decode_fp8 decodes over it.
+ * pa_store_decode fuses pa_store_kv and pa_decode for a decode step; and an
+ * FP8 (E4M3) KV cache: pa_store_kv_fp8 quantises into it and pa_decode_fp8
+ * decodes over it.
  *
  * Sources (web pages that describe the method):
  *   [EAS] koas-w, "errors and solutions" (Qwen2.5-1.5B inference from
@@ -72,7 +73,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 4
+#define PA_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define PA_API __attribute__((visibility("default")))
@@ -103,7 +104,8 @@ typedef int32_t pa_status;
 
 /*
  * Launch flags (the `flags` argument of pa_store_kv, pa_store_kv_fp8,
- * pa_rope_store_kv, pa_decode, pa_decode_fp8 and pa_decode_noalloc).  Any other bit returns
+ * pa_rope_store_kv, pa_decode, pa_store_decode, pa_decode_fp8 and
+ * pa_decode_noalloc).  Any other bit returns
  * PA_ERR_INVALID_ARG.
  *
  * PA_LAUNCH_PDL: programmatic dependent launch.  The call's kernel may begin
@@ -315,6 +317,33 @@ PA_API pa_status pa_decode(void *out, int32_t out_dtype, const void *q, const vo
                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                     int32_t block_size, float scale, int32_t num_splits, void *workspace,
                     size_t workspace_bytes, uint32_t flags, void *stream);
+
+/*
+ * pa_store_decode -- pa_store_kv and pa_decode of one decode step in one
+ * kernel (bf16 pools).  Every sequence b has one new token, at position
+ * context_lens[b] - 1, whose K/V rows are new_k / new_v + b *
+ * new_*_tok_stride + h * head_dim (heads contiguous; 16-byte aligned rows,
+ * token strides multiples of 8 elements); slot_mapping[b] is its pool slot
+ * (< 0: the token is not stored and the pool row is used as it is).
+ * The result equals pa_store_kv followed by pa_decode, but the new rows
+ * reach the attention directly: the CTA that consumes a sequence's last
+ * block patches them into its staged tile and writes them to the pool, so
+ * no second launch and no store-to-load dependency stands between the two.
+ * slot_mapping[b] must be the slot of that position under the block table
+ * (table[b][(ctx - 1) / 16] * 16 + (ctx - 1) % 16); any other value sets
+ * PA_DEVERR_SLOT_INDEX in the workspace error word and that row is neither
+ * stored nor patched.  Other arguments, the workspace and the flags as for
+ * pa_decode.
+ */
+PA_API pa_status pa_store_decode(void *out, int32_t out_dtype, const void *q, const void *new_k,
+                                 const void *new_v, int64_t new_k_tok_stride,
+                                 int64_t new_v_tok_stride, const int32_t *slot_mapping,
+                                 void *k_cache, void *v_cache, int64_t num_blocks,
+                                 const int32_t *block_tables, int32_t block_table_stride,
+                                 const int32_t *context_lens, int32_t batch, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                 float scale, int32_t num_splits, void *workspace,
+                                 size_t workspace_bytes, uint32_t flags, void *stream);
 
 /*
  * pa_decode_fp8 -- pa_decode over FP8 pools (layout and scales above).

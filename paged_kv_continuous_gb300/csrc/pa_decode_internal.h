@@ -42,6 +42,11 @@ struct DecodeRequest {
   bool fp8 = false;
   const float *k_scale = nullptr;
   const float *v_scale = nullptr;
+  // fused store of each sequence's new token (bf16 pools; null: none)
+  const void *new_k = nullptr;
+  const void *new_v = nullptr;
+  int64_t new_k_tok = 0, new_v_tok = 0;
+  const int32_t *slot_mapping = nullptr;
 };
 
 // Host checks shared by both decode entry points; resolves r.splits.

@@ -72,6 +72,16 @@ struct DecodeParams {
   const float *k_scale;  // FP8 pools only: per kv head, value = code * scale
   const float *v_scale;
   const uint8_t *v_pool;  // FP8 pools only: V, [num_blocks][Hkv][128][16] bytes
+  // Fused store (bf16 pools; new_k == nullptr: none).  Sequence b's new
+  // token (position context_lens[b] - 1) has K/V rows new_k / new_v + b *
+  // new_tok + h * 128; it goes to pool slot slot_mapping[b] (< 0: none) and,
+  // in shared memory, into the staged tile of the sequence's last block.
+  const uint16_t *new_k;
+  const uint16_t *new_v;
+  long long new_k_tok, new_v_tok;
+  const int32_t *slot_mapping;
+  uint16_t *k_pool;
+  uint16_t *v_pool16;
 };
 
 constexpr int kDecodeProducerWarps = 2;
@@ -1072,11 +1082,47 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
         }
         const int valid = min(kBlockSize, ctx - j * kBlockSize);  // keys of this block (>= 1)
+        bool patched = false;  // generic-proxy writes into the stage (fence before release)
         if (have) {
           // boxes of this head group: K at kb (bf16: +BOX_BYTES for dims
           // 64..127), V at vb
           const uint32_t kb = sbase + gpair * (F8 ? 1 : 2) * S::BOX_BYTES;
           const uint32_t vb = sbase + S::KV_BYTES + gpair * (F8 ? 1 : 2) * S::BOX_BYTES;
+          if constexpr (!F8) {
+            if (p.new_k != nullptr && j == n - 1) {
+              // Fused store: this is the sequence's last block, the one that
+              // holds its new token (row valid - 1).  The pool row may not
+              // hold it yet: its K/V rows of this warp's head go into the
+              // staged tile (lane L: 16-byte chunk L & 15 of K, L < 16, or of
+              // V) and to the pool slot, which must be that row's slot.
+              const long long slot = __ldg(p.slot_mapping + b);
+              if (slot >= 0) {
+                const long long want =
+                    (long long)__ldg(p.block_tables + (long long)b * p.bt_stride + j) *
+                        kBlockSize + (valid - 1);
+                if (slot != want) {
+                  if (lane == 0) report(p.err, PA_DEVERR_SLOT_INDEX);
+                } else {
+                  const int c = lane & 15;
+                  const bool is_v = lane >= 16;
+                  const uint16_t *src =
+                      (is_v ? p.new_v + b * p.new_v_tok : p.new_k + b * p.new_k_tok) +
+                      g * kHeadDim + c * 8;
+                  const uint4 val = *reinterpret_cast<const uint4 *>(src);
+                  uint16_t *dstg = (is_v ? p.v_pool16 : p.k_pool) +
+                                   (slot * HKV + g) * kHeadDim + c * 8;
+                  *reinterpret_cast<uint4 *>(dstg) = val;
+                  const uint32_t a = (is_v ? vb : kb) + (c >> 3) * S::BOX_BYTES +
+                                     swz((valid - 1) * S::HB + gsub, c & 7);
+                  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(val.x),
+                               "r"(val.y), "r"(val.z), "r"(val.w)
+                               : "memory");
+                  patched = true;
+                  __syncwarp();
+                }
+              }
+            }
+          }
           // S^T = K . Q^T, two accumulation chains over the eight 16-dim k-steps
           float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
           if constexpr (F8) {
@@ -1214,7 +1260,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
           // generic-proxy writes above must be ordered before the TMA that
           // reuses this stage
-          if (valid < kBlockSize) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          if (valid < kBlockSize || patched)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * sidx);  // one of the slot's Hkv readers
