@@ -14,8 +14,8 @@
  *   pa_prefill_varlen  causal varlen attention of cu_seqlens-packed query
  *                      chunks over each sequence's paged keys;
  * pa_store_decode fuses pa_store_kv and pa_decode for a decode step; and an
- * FP8 (E4M3) KV cache: pa_store_kv_fp8 quantises into it and pa_decode_fp8
- * decodes over it.
+ * FP8 (E4M3) KV cache: pa_store_kv_fp8 quantises into it, pa_decode_fp8
+ * decodes over it and pa_store_decode_fp8 does both for a decode step.
  *
  * Sources (web pages that describe the method):
  *   [EAS] koas-w, "errors and solutions" (Qwen2.5-1.5B inference from
@@ -73,7 +73,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 5
+#define PA_ABI_VERSION 6
 
 #if defined(__GNUC__)
 #define PA_API __attribute__((visibility("default")))
@@ -104,8 +104,8 @@ typedef int32_t pa_status;
 
 /*
  * Launch flags (the `flags` argument of pa_store_kv, pa_store_kv_fp8,
- * pa_rope_store_kv, pa_decode, pa_store_decode, pa_decode_fp8 and
- * pa_decode_noalloc).  Any other bit returns
+ * pa_rope_store_kv, pa_decode, pa_store_decode, pa_decode_fp8,
+ * pa_store_decode_fp8 and pa_decode_noalloc).  Any other bit returns
  * PA_ERR_INVALID_ARG.
  *
  * PA_LAUNCH_PDL: programmatic dependent launch.  The call's kernel may begin
@@ -344,6 +344,25 @@ PA_API pa_status pa_store_decode(void *out, int32_t out_dtype, const void *q, co
                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                  float scale, int32_t num_splits, void *workspace,
                                  size_t workspace_bytes, uint32_t flags, void *stream);
+
+/*
+ * pa_store_decode_fp8 -- pa_store_decode over FP8 pools: each sequence's new
+ * token is quantised (as pa_store_kv_fp8 does, bit for bit) into the pools
+ * and into the staged tiles of its last block, and every sequence is decoded
+ * as pa_decode_fp8 does, in one kernel.  Arguments as pa_store_decode plus
+ * k_scale / v_scale (NULL: PA_ERR_INVALID_ARG).
+ */
+PA_API pa_status pa_store_decode_fp8(void *out, int32_t out_dtype, const void *q,
+                                     const void *new_k, const void *new_v,
+                                     int64_t new_k_tok_stride, int64_t new_v_tok_stride,
+                                     const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                                     const float *k_scale, const float *v_scale,
+                                     int64_t num_blocks, const int32_t *block_tables,
+                                     int32_t block_table_stride, const int32_t *context_lens,
+                                     int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t block_size, float scale,
+                                     int32_t num_splits, void *workspace, size_t workspace_bytes,
+                                     uint32_t flags, void *stream);
 
 /*
  * pa_decode_fp8 -- pa_decode over FP8 pools (layout and scales above).

@@ -82,6 +82,8 @@ struct DecodeParams {
   const int32_t *slot_mapping;
   uint16_t *k_pool;
   uint16_t *v_pool16;
+  uint8_t *k_pool8;  // FP8 pools, fused store
+  uint8_t *v_pool8;
 };
 
 constexpr int kDecodeProducerWarps = 2;
@@ -351,6 +353,14 @@ __device__ __forceinline__ float2 f16x2_to_float2(uint32_t w) {
       : "=f"(lo), "=f"(hi)
       : "r"(w));
   return make_float2(lo, hi);
+}
+
+// Two floats to two E4M3 codes (lo in the low byte): nearest even, saturated
+// to +-448 (the same rounding as the FP8 store kernel).
+__device__ __forceinline__ uint32_t float2_to_e4m3x2_sat(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -1100,7 +1110,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 const long long want =
                     (long long)__ldg(p.block_tables + (long long)b * p.bt_stride + j) *
                         kBlockSize + (valid - 1);
-                if (slot != want) {
+                // the slot must be the new position's, and inside the pool
+                // (a table entry outside it would make both agree on a slot
+                // past the pool)
+                if (slot != want || slot >= p.num_blocks * kBlockSize) {
                   if (lane == 0) report(p.err, PA_DEVERR_SLOT_INDEX);
                 } else {
                   const int c = lane & 15;
@@ -1117,6 +1130,74 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(val.x),
                                "r"(val.y), "r"(val.z), "r"(val.w)
                                : "memory");
+                  patched = true;
+                  __syncwarp();
+                }
+              }
+            }
+          } else {
+            if (p.new_k != nullptr && j == n - 1) {
+              // Fused FP8 store: quantise the new token's rows of this head
+              // (code = nearest-even E4M3 of x / scale, saturated) into the
+              // staged tiles and the pools.  K: lane L < 8 takes dims
+              // 16L .. 16L + 15 (one 16-byte chunk of the swizzled row); V:
+              // lane L takes dims 4L .. 4L + 3 (the token's byte in each of
+              // four dim-major rows).
+              const long long slot = __ldg(p.slot_mapping + b);
+              if (slot >= 0) {
+                const long long phys_j = __ldg(p.block_tables + (long long)b * p.bt_stride + j);
+                const long long want = phys_j * kBlockSize + (valid - 1);
+                // the slot must be the new position's, and inside the pool
+                // (a table entry outside it would make both agree on a slot
+                // past the pool)
+                if (slot != want || slot >= p.num_blocks * kBlockSize) {
+                  if (lane == 0) report(p.err, PA_DEVERR_SLOT_INDEX);
+                } else {
+                  const int trow = valid - 1;
+                  if (lane < 8) {
+                    const float ksc = __ldg(p.k_scale + g);
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        p.new_k + b * p.new_k_tok + g * kHeadDim + 16 * lane);
+                    const uint4 x0 = src[0], x1 = src[1];
+                    const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    uint32_t cw[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                      const float2 f0 = bf16x2_to_float2(xw[2 * i]);
+                      const float2 f1 = bf16x2_to_float2(xw[2 * i + 1]);
+                      cw[i] = float2_to_e4m3x2_sat(__fdiv_rn(f0.x, ksc), __fdiv_rn(f0.y, ksc)) |
+                              (float2_to_e4m3x2_sat(__fdiv_rn(f1.x, ksc), __fdiv_rn(f1.y, ksc))
+                               << 16);
+                    }
+                    *reinterpret_cast<uint4 *>(p.k_pool8 + (slot * HKV + g) * kHeadDim +
+                                               16 * lane) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                    const uint32_t a = kb + swz(trow * S::HB + gsub, lane);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(cw[0]),
+                                 "r"(cw[1]), "r"(cw[2]), "r"(cw[3])
+                                 : "memory");
+                  }
+                  {
+                    const float vsc_raw = __ldg(p.v_scale + g);
+                    const uint2 xv = *reinterpret_cast<const uint2 *>(
+                        p.new_v + b * p.new_v_tok + g * kHeadDim + 4 * lane);
+                    const float2 f0 = bf16x2_to_float2(xv.x), f1 = bf16x2_to_float2(xv.y);
+                    const uint32_t c01 =
+                        float2_to_e4m3x2_sat(__fdiv_rn(f0.x, vsc_raw), __fdiv_rn(f0.y, vsc_raw));
+                    const uint32_t c23 =
+                        float2_to_e4m3x2_sat(__fdiv_rn(f1.x, vsc_raw), __fdiv_rn(f1.y, vsc_raw));
+                    const uint32_t codes = c01 | (c23 << 16);
+                    uint8_t *vg = p.v_pool8 + ((phys_j * HKV + g) * kHeadDim + 4 * lane) *
+                                                  kBlockSize + trow;
+                    const uint32_t vsm =
+                        vb + gsub * (kHeadDim * kBlockSize) + 4 * lane * kBlockSize + trow;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                      const uint32_t c = (codes >> (8 * i)) & 0xFFu;
+                      vg[i * kBlockSize] = (uint8_t)c;
+                      asm volatile("st.shared.u8 [%0], %1;" ::"r"(vsm + i * kBlockSize), "r"(c)
+                                   : "memory");
+                    }
+                  }
                   patched = true;
                   __syncwarp();
                 }

@@ -31,7 +31,7 @@ EXPORTED = (
     "pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
     "pa_decode_default_splits", "pa_decode", "pa_decode_merge", "pa_prefill_varlen",
     "pa_decode_noalloc", "pa_rope_store_kv", "pa_store_kv_fp8", "pa_decode_fp8",
-    "pa_store_decode",
+    "pa_store_decode", "pa_store_decode_fp8",
 )
 
 
@@ -66,6 +66,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_store_decode.restype = i32
     lib.pa_store_decode.argtypes = [P, i32, P, P, P, i64, i64, P, P, P, i64, P, i32, P, i32,
                                     i32, i32, i32, i32, f32, i32, P, sz, u32, P]
+    lib.pa_store_decode_fp8.restype = i32
+    lib.pa_store_decode_fp8.argtypes = [P, i32, P, P, P, i64, i64, P, P, P, P, P, i64, P, i32,
+                                        P, i32, i32, i32, i32, i32, f32, i32, P, sz, u32, P]
     lib.pa_decode_fp8.restype = i32
     lib.pa_decode_fp8.argtypes = [P, i32, P, P, P, P, P, i64, P, i32, P, i32, i32, i32, i32,
                                   i32, f32, i32, P, sz, u32, P]
@@ -350,6 +353,44 @@ def decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens
                              Hq, Hkv, D, bs, float(scale), int(num_splits), _ptr(workspace),
                              workspace.numel() * workspace.element_size(),
                              PA_LAUNCH_PDL if pdl else 0, _stream(stream)), "pa_decode_fp8")
+    return out
+
+
+def store_decode_fp8(q, new_k, new_v, k_cache, v_cache, k_scale, v_scale, slot_mapping,
+                     block_tables, context_lens, scale, out=None, out_dtype=torch.bfloat16,
+                     num_splits=0, workspace=None, stream=None, pdl=False):
+    """pa_store_decode_fp8: store_decode over FP8 pools (see fp8_pools)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(new_k, torch.bfloat16, "new_k", 3)
+    _need(new_v, torch.bfloat16, "new_v", 3)
+    _need(slot_mapping, torch.int32, "slot_mapping", 1)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    if not q.is_contiguous():
+        raise PagedAttentionError("q must be contiguous")
+    for t, n in ((new_k, "new_k"), (new_v, "new_v")):
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise PagedAttentionError(f"{n} needs contiguous heads")
+    if block_tables.stride(1) != 1:
+        raise PagedAttentionError("block_tables rows must be contiguous")
+    NB, bs, Hkv, _ = _need_fp8_pools(k_cache, v_cache, k_scale, v_scale)
+    B, Hq, D = q.shape
+    if tuple(new_k.shape) != (B, Hkv, D) or new_v.shape != new_k.shape or \
+            slot_mapping.shape[0] != B:
+        raise PagedAttentionError("new_k / new_v / slot_mapping need one row per sequence")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(Hq, Hkv, num_splits, D, q.device)
+    _check(lib.pa_store_decode_fp8(_ptr(out), _out_code(out.dtype), _ptr(q), _ptr(new_k),
+                                   _ptr(new_v), new_k.stride(0), new_v.stride(0),
+                                   _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(k_scale), _ptr(v_scale), NB, _ptr(block_tables),
+                                   block_tables.stride(0), _ptr(context_lens), B, Hq, Hkv, D, bs,
+                                   float(scale), int(num_splits), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(),
+                                   PA_LAUNCH_PDL if pdl else 0, _stream(stream)),
+           "pa_store_decode_fp8")
     return out
 
 

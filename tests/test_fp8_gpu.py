@@ -167,3 +167,36 @@ def test_fp8_decode_empty_and_single_key_rows(ops):
     ref = oracle.decode_fp8(q, kp, vp, ks, vs, tables, ctx, 1 / np.sqrt(128))
     assert np.all(got[0] == 0.0)
     assert_close(got, ref)
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "qwen_decode_b8", "cb_decode_b64"])
+@pytest.mark.parametrize("num_splits", [0, 5])
+def test_fp8_store_decode_equals_store_then_decode(ops, name, num_splits):
+    """pa_store_decode_fp8 (quantised store fused into the decode) leaves
+    the same codes as pa_store_kv_fp8 and gives the same output bits as
+    pa_store_kv_fp8 followed by pa_decode_fp8, and matches the oracle."""
+    w = synth.CONFIGS[name]()
+    ks = np.array([0.011, 0.0095], np.float32)[:w.num_kv_heads]
+    vs = np.array([0.0105, 0.012], np.float32)[:w.num_kv_heads]
+    kp, vp = fp8_pools_from(w, ks, vs)
+    kref, vref = kp.copy(), vp.copy()
+    oracle.store_kv_fp8(w.new_k, w.new_v, kref, vref, ks, vs, w.slot_mapping)
+    ksd, vsd = torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()
+    q, nk, nv = to_dev_bf16(w.q), to_dev_bf16(w.new_k), to_dev_bf16(w.new_v)
+    bt, cl, sm = to_dev_i32(w.block_tables), to_dev_i32(w.context_lens), to_dev_i32(w.slot_mapping)
+    kf, vf = dev_u8(kp), dev_u8(vp)
+    ws = ops.decode_workspace(w.num_q_heads, w.num_kv_heads, num_splits, 128, "cuda")
+    out_f = ops.store_decode_fp8(q, nk, nv, kf, vf, ksd, vsd, sm, bt, cl, w.scale,
+                                 out_dtype=torch.float32, num_splits=num_splits, workspace=ws)
+    torch.cuda.synchronize()
+    assert ops.read_error_word(ws) == 0
+    assert np.array_equal(kf.cpu().numpy(), kref) and np.array_equal(vf.cpu().numpy(), vref)
+    ku, vu = dev_u8(kp), dev_u8(vp)
+    ops.store_kv_fp8(nk, nv, ku, vu, ksd, vsd, sm)
+    out_u = ops.decode_fp8(q, ku, vu, ksd, vsd, bt, cl, w.scale, out_dtype=torch.float32,
+                           num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert torch.equal(out_f, out_u)
+    kc, vc, t2 = compact(kref, vref, w.block_tables)
+    ref = oracle.decode_fp8(w.q, kc, vc, ks, vs, t2, w.context_lens, w.scale)
+    assert_close(out_f.cpu().numpy().astype(np.float64), ref)
