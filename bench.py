@@ -317,6 +317,20 @@ def run_extras(ops, dev):
         "us_per_call": ms * 1e3, "alg_flops": flops, "TFLOP_per_s": tf,
         "frac_of_bf16_burst": tf / burst, "frac_of_bf16_sustained": tf / sustained,
         "peak_kind": kind, "rows": int(w.q.shape[0])}
+    # the same step with the chunks' store fused in (pa_prefill_store_varlen)
+    nk_p, nv_p, sl_p = dev16(w.new_k), dev16(w.new_v), dev32(w.slot_mapping)
+
+    def pre_fused():
+        ops.prefill_store_varlen(qv, nk_p, nv_p, sl_p, cu, kc, vc, bt, cl, w.scale, mq, out=outp)
+
+    def pre_unfused():
+        ops.store_kv(nk_p, nv_p, kc, vc, sl_p)
+        ops.prefill_varlen(qv, cu, kc, vc, bt, cl, w.scale, mq, out=outp)
+    ms_f = time_graph(pre_fused, 10)
+    ms_u = time_graph(pre_unfused, 10)
+    extra["varlen_prefill_8x1_8x512"].update({
+        "with_store_fused_us": ms_f * 1e3, "with_store_unfused_us": ms_u * 1e3,
+        "with_store_fused_TFLOP_per_s": flops / ms_f / 1e9})
     del kc, vc
     # fused RoPE + store (Hq 12 / Hkv 2, positions drawn from [0, 32768)):
     # the 64 new tokens of a cb_decode_b64 step (launch-bound), and a

@@ -12,7 +12,8 @@
  *                      split across CTAs with log-sum-exp partials;
  *   pa_decode_merge    combine those partials into the final rows;
  *   pa_prefill_varlen  causal varlen attention of cu_seqlens-packed query
- *                      chunks over each sequence's paged keys;
+ *                      chunks over each sequence's paged keys
+ *                      (pa_prefill_store_varlen: with the chunks' store);
  * pa_store_decode fuses pa_store_kv and pa_decode for a decode step; and an
  * FP8 (E4M3) KV cache: pa_store_kv_fp8 quantises into it, pa_decode_fp8
  * decodes over it and pa_store_decode_fp8 does both for a decode step.
@@ -73,7 +74,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 6
+#define PA_ABI_VERSION 7
 
 #if defined(__GNUC__)
 #define PA_API __attribute__((visibility("default")))
@@ -466,6 +467,34 @@ PA_API pa_status pa_prefill_varlen(void *out, int32_t out_dtype, const void *q,
                             const int32_t *context_lens, int32_t num_q_heads,
                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                             float scale, int32_t *error_flags, void *stream);
+
+/*
+ * pa_prefill_store_varlen -- pa_store_kv of the chunks' tokens and
+ * pa_prefill_varlen over them in one kernel ([EAS] "自写 Triton Kernel": the
+ * store through slot_mapping, here fused with the attention that follows).
+ * Token t of the packed chunks has K/V rows new_k / new_v + t *
+ * new_*_tok_stride + h * head_dim (heads contiguous, 16-byte aligned, token
+ * strides multiples of 8 elements) and pool slot slot_mapping[t] (< 0:
+ * padding, not stored).  Each chunk's own keys are read from these rows, the
+ * prefix keys from the pool; the rows are also stored, so the pools end as
+ * pa_store_kv leaves them and the output equals pa_store_kv followed by
+ * pa_prefill_varlen.  slot_mapping[t] must be the slot of token t's
+ * position under the block table (the attention reads the chunk from
+ * new_k / new_v); a slot past the pool sets PA_DEVERR_SLOT_INDEX and is
+ * skipped.  Other arguments as pa_prefill_varlen.
+ */
+PA_API pa_status pa_prefill_store_varlen(void *out, int32_t out_dtype, const void *q,
+                                         const void *new_k, const void *new_v,
+                                         int64_t new_k_tok_stride, int64_t new_v_tok_stride,
+                                         const int32_t *slot_mapping, const int32_t *cu_seqlens,
+                                         int32_t num_seqs, int32_t total_tokens,
+                                         int32_t max_q_len, void *k_cache, void *v_cache,
+                                         int64_t num_blocks, const int32_t *block_tables,
+                                         int32_t block_table_stride,
+                                         const int32_t *context_lens, int32_t num_q_heads,
+                                         int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, float scale, int32_t *error_flags,
+                                         void *stream);
 
 #ifdef __cplusplus
 }

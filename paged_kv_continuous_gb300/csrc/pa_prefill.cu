@@ -76,6 +76,18 @@ struct PrefillParams {
   int hq, hkv;
   float qk_scale_log2;
   int32_t *err;
+  // Fused store (new_k == nullptr: none).  The chunk rows of token t are
+  // new_k / new_v + t * new_*_tok + h * 128; they are stored at
+  // slot_mapping[t], and the chunk's keys are read from them (not from the
+  // pool, where other CTAs of the sequence may not have stored them yet).
+  const uint16_t *new_k;
+  const uint16_t *new_v;
+  long long new_k_tok, new_v_tok;
+  const int32_t *slot_mapping;
+  const uint16_t *k_cache;  // pools, for the page that straddles the prefix
+  const uint16_t *v_cache;
+  uint16_t *k_store;  // the same pools, written by the fused store
+  uint16_t *v_store;
 };
 
 // ---- tcgen05 helpers ----------------------------------------------------------
@@ -215,7 +227,9 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 template <int G>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tmap_v,
+                   const __grid_constant__ CUtensorMap tmap_nk,
+                   const __grid_constant__ CUtensorMap tmap_nv, const PrefillParams p) {
   constexpr int PT = kPfRows / G;  // query positions per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -304,12 +318,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     //      separate loaders halve the per-tile issue time (16 boxes each) ----
     const bool is_k = warp == 0;
     const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
+    // fused store: pages of the chunk come from the new rows
+    const bool fused = p.new_k != nullptr;
+    const CUtensorMap *nmap = is_k ? &tmap_nk : &tmap_nv;
+    const uint16_t *nrows = is_k ? p.new_k : p.new_v;
+    const long long ntok = is_k ? p.new_k_tok : p.new_v_tok;
+    const uint16_t *pool = is_k ? p.k_cache : p.v_cache;
     const uint32_t dst0 = base + (is_k ? kOffK : kOffV);
     const uint32_t b_full0 = is_k ? b_k_full0 : b_v_full0;
     const uint32_t b_empty0 = is_k ? b_k_empty0 : b_v_empty0;
     const int nst = is_k ? kKStages : kVStages;
-    if (lane == 0)
+    if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+      if (fused)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(nmap))
+                     : "memory");
+    }
     const int32_t *row = p.block_tables + (long long)s * p.bt_stride;
     // block-table entries of four tiles (32 pages) per round of loads, one per
     // lane: -1 = no key in the page (left as it is: masked), -2 = bad entry
@@ -327,23 +351,99 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(b_empty0 + 8 * st, (round - 1) & 1,
                                                            abort_flag, p.err)))
         break;
-      // lane L < 8 handles page L of the tile
+      // lane L < 8 handles page L of the tile; its kind: pool page (TMA
+      // from the pool), chunk page (fused: TMA from the new rows), the page
+      // that straddles the prefix (fused: assembled by the warp) or none
       const long long phys = __shfl_sync(0xffffffffu, ph_lane, (j & 3) * 8 + (lane & 7));
       const bool mine = lane < kPfKeys / kBlockSize;
-      const unsigned okm = __ballot_sync(0xffffffffu, mine && phys >= 0);
-      if (is_k && (__ballot_sync(0xffffffffu, mine && phys == -2) != 0u) && lane == 0)
+      const int kp0 = j * kPfKeys + (lane & 7) * kBlockSize;  // first key of the page
+      const bool in_chunk = fused && kp0 >= prefix;
+      const bool straddle = fused && kp0 < prefix && kp0 + kBlockSize > prefix;
+      const bool by_tma = phys != -1 && !straddle && (in_chunk || phys >= 0);
+      const unsigned okm = __ballot_sync(0xffffffffu, mine && by_tma);
+      if (is_k && (__ballot_sync(0xffffffffu, mine && phys == -2 && !in_chunk) != 0u) &&
+          lane == 0)
         report(p.err, PA_DEVERR_BLOCK_INDEX);
+      const unsigned mixm = __ballot_sync(0xffffffffu, mine && straddle && phys >= 0);
+      if (mixm) {
+        // rows 0 .. prefix - kp - 1 from the pool page, the rest from the new
+        // rows (rows past the sequence: zero), written in the layout the TMA
+        // uses (128-byte swizzle); then made visible to the tensor core
+        const int pg = __ffs(mixm) - 1;
+        const long long ph = __shfl_sync(0xffffffffu, phys, pg);
+        const int kp = j * kPfKeys + pg * kBlockSize;
+        // 16 rows x 16 chunks: 8 per lane, all loads issued before the stores
+        uint4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int i = lane + 32 * k, r = i >> 4, c = i & 15;
+          v[k] = make_uint4(0u, 0u, 0u, 0u);
+          if (kp + r < n) {
+            const uint16_t *src =
+                kp + r < prefix
+                    ? pool + ((ph * kBlockSize + r) * p.hkv + g) * kHeadDim + c * 8
+                    : nrows + (long long)(q0 + kp + r - prefix) * ntok + g * kHeadDim + c * 8;
+            v[k] = __ldg(reinterpret_cast<const uint4 *>(src));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int i = lane + 32 * k, r = i >> 4, c = i & 15;
+          const uint32_t a = dst + (c >> 3) * kHalfBytes + pg * kBlockSize * 128 + sw128(r, c & 7);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v[k].x),
+                       "r"(v[k].y), "r"(v[k].z), "r"(v[k].w)
+                       : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+      __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(b_full, __popc(okm) * 2u * kBlockSize * 64 * 2);
       __syncwarp();
       // one page at a time, its index broadcast to the whole warp
 #pragma unroll
       for (int pg = 0; pg < kPfKeys / kBlockSize; ++pg) {
+        if (!((okm >> pg) & 1u)) continue;
         const long long ph = __shfl_sync(0xffffffffu, phys, pg);
-        if (ph >= 0) {
-          const int z = (int)(ph * kBlockSize);
+        const int kp = j * kPfKeys + pg * kBlockSize;
+        const bool from_new = fused && kp >= prefix;
+        // pool page: token slots of block ph; chunk page: the new rows from
+        // token q0 + kp - prefix (rows past the last token are zero-filled)
+        const int z = from_new ? q0 + kp - prefix : (int)(ph * kBlockSize);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d(dst + h * kHalfBytes + pg * kBlockSize * 128, map, h * 64, g, z, b_full);
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(dst + h * kHalfBytes + pg * kBlockSize * 128, from_new ? nmap : map, h * 64,
+                      g, z, b_full);
+      }
+    }
+    if (fused && !*abort_flag) {
+      // the fused store: this CTA's positions pos0 .. pos0 + npos - 1, kv
+      // head g (warp 0: K rows, warp 2: V rows), 16-byte chunks over the lanes
+      uint16_t *dstp = is_k ? p.k_store : p.v_store;
+      const long long num_slots = p.num_blocks * kBlockSize;
+      // up to 21 positions x 16 chunks; four per lane per round, the loads of
+      // a round issued before its stores
+      for (int i0 = 0; i0 < npos * 16; i0 += 4 * 32) {
+        long long slot[4];
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = i0 + lane + 32 * k, r = i >> 4, c = i & 15;
+          slot[k] = -1;
+          if (i < npos * 16) {
+            const long long t = q0 + pos0 + r;
+            slot[k] = __ldg(p.slot_mapping + t);
+            v[k] = __ldg(reinterpret_cast<const uint4 *>(nrows + t * ntok + g * kHeadDim + c * 8));
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = (i0 + lane + 32 * k) & 15;
+          if (slot[k] < 0) continue;  // padding, or past this CTA's rows
+          if (slot[k] >= num_slots) {
+            if (c == 0) report(p.err, PA_DEVERR_SLOT_INDEX);
+            continue;
+          }
+          *reinterpret_cast<uint4 *>(dstp + (slot[k] * p.hkv + g) * kHeadDim + c * 8) = v[k];
         }
       }
     }
@@ -561,8 +661,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // MMAs; keys 2i and 2i + 1 share column i, the even key in the low
       // half; this half's 64 keys are columns 32 hf .. 32 hf + 31 of each
       // part).  hi is e with the low 16 mantissa bits cleared (exactly a
-      // bf16); lo = e - hi is exact in fp32 and likewise truncated to bf16,
-      // so hi + lo is e within 2^-14 relative.  Both are byte permutes.
+      // bf16); lo = e - hi is exact in fp32 and rounded to nearest bf16 by an
+      // integer add, so hi + lo is e within 2^-15 relative, without bias.
+      // Both parts are byte permutes (no conversion instruction).
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t hi[16], lo[16];
@@ -571,10 +672,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const uint32_t u0 = __float_as_uint(sv[cc][2 * i]);
           const uint32_t u1 = __float_as_uint(sv[cc][2 * i + 1]);
           hi[i] = __byte_perm(u0, u1, 0x7632);
-          lo[i] = __byte_perm(__float_as_uint(sv[cc][2 * i] - __uint_as_float(u0 & 0xFFFF0000u)),
-                              __float_as_uint(sv[cc][2 * i + 1] -
-                                              __uint_as_float(u1 & 0xFFFF0000u)),
-                              0x7632);
+          // lo >= 0; + 0x8000 rounds its top 16 bits to nearest (a carry
+          // into the exponent is the correct rounding)
+          lo[i] = __byte_perm(
+              __float_as_uint(sv[cc][2 * i] - __uint_as_float(u0 & 0xFFFF0000u)) + 0x8000u,
+              __float_as_uint(sv[cc][2 * i + 1] - __uint_as_float(u1 & 0xFFFF0000u)) + 0x8000u,
+              0x7632);
         }
         tmem_st16(tmem_p + trow + hf * 32 + cc * 16, hi);
         tmem_st16(tmem_p + trow + 64 + hf * 32 + cc * 16, lo);
@@ -679,8 +782,25 @@ bool pool_map(CUtensorMap *map, const void *pool, long long num_blocks, int hkv)
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// (dim 128, kv head, token) view of the new rows (token stride in elements,
+// a multiple of 8); the same box as pool_map: 64 dims x 1 head x 16 tokens.
+bool rows_map(CUtensorMap *map, const void *rows, long long num_tokens, int hkv,
+              long long tok_stride) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)num_tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)tok_stride * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kBlockSize};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(rows), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int G>
-cudaError_t launch_prefill(const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &pp,
+cudaError_t launch_prefill(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tnk,
+                           const CUtensorMap &tnv, const PrefillParams &pp,
                            int max_q_len, cudaStream_t s, int device) {
   static bool configured[64] = {};
   if (device < 0 || device >= 64 || !configured[device]) {
@@ -691,23 +811,24 @@ cudaError_t launch_prefill(const CUtensorMap &tk, const CUtensorMap &tv, const P
   }
   constexpr int PT = kPfRows / G;
   dim3 grid((max_q_len + PT - 1) / PT, pp.hkv, pp.num_seqs);
-  prefill_kernel<G><<<grid, kPfThreads, kPfSmem, s>>>(tk, tv, pp);
+  prefill_kernel<G><<<grid, kPfThreads, kPfSmem, s>>>(tk, tv, tnk, tnv, pp);
   return cudaGetLastError();
 }
 
 }  // namespace
 }  // namespace pa
 
-extern "C" pa_status pa_prefill_varlen(void *out, int32_t out_dtype, const void *q,
-                                       const int32_t *cu_seqlens, int32_t num_seqs,
-                                       int32_t total_tokens, int32_t max_q_len,
-                                       const void *k_cache, const void *v_cache,
-                                       int64_t num_blocks, const int32_t *block_tables,
-                                       int32_t block_table_stride, const int32_t *context_lens,
-                                       int32_t num_q_heads, int32_t num_kv_heads,
-                                       int32_t head_dim, int32_t block_size, float scale,
-                                       int32_t *error_flags, void *stream) {
-  using namespace pa;
+namespace pa {
+namespace {
+pa_status prefill_entry(void *out, int32_t out_dtype, const void *q, const int32_t *cu_seqlens,
+                        int32_t num_seqs, int32_t total_tokens, int32_t max_q_len,
+                        const void *k_cache, const void *v_cache, int64_t num_blocks,
+                        const int32_t *block_tables, int32_t block_table_stride,
+                        const int32_t *context_lens, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t block_size, float scale, int32_t *error_flags,
+                        void *stream, const void *new_k, const void *new_v,
+                        int64_t new_k_tok_stride, int64_t new_v_tok_stride,
+                        const int32_t *slot_mapping) {
   if (num_seqs < 0 || total_tokens < 0 || max_q_len < 0 || num_blocks < 0)
     return PA_ERR_INVALID_ARG;
   if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
@@ -727,13 +848,26 @@ extern "C" pa_status pa_prefill_varlen(void *out, int32_t out_dtype, const void 
   auto misaligned = [](const void *x) { return (reinterpret_cast<uintptr_t>(x) & 15) != 0; };
   if (misaligned(out) || misaligned(q) || misaligned(k_cache) || misaligned(v_cache))
     return PA_ERR_INVALID_ARG;
+  const bool fused = new_k != nullptr;
+  if (fused) {
+    if (!new_v || !slot_mapping || misaligned(new_k) || misaligned(new_v)) return PA_ERR_INVALID_ARG;
+    if (new_k_tok_stride < (int64_t)num_kv_heads * kHeadDim ||
+        new_v_tok_stride < (int64_t)num_kv_heads * kHeadDim || new_k_tok_stride % 8 ||
+        new_v_tok_stride % 8)
+      return PA_ERR_INVALID_ARG;
+  }
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_DEVICE;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tnk, tnv;
   memset(&tk, 0, sizeof tk);
   memset(&tv, 0, sizeof tv);
   if (!pool_map(&tk, k_cache, num_blocks, num_kv_heads) ||
       !pool_map(&tv, v_cache, num_blocks, num_kv_heads))
+    return PA_ERR_DEVICE;
+  tnk = tk;
+  tnv = tv;
+  if (fused && (!rows_map(&tnk, new_k, total_tokens, num_kv_heads, new_k_tok_stride) ||
+                !rows_map(&tnv, new_v, total_tokens, num_kv_heads, new_v_tok_stride)))
     return PA_ERR_DEVICE;
   PrefillParams pp;
   pp.out = out;
@@ -749,18 +883,61 @@ extern "C" pa_status pa_prefill_varlen(void *out, int32_t out_dtype, const void 
   pp.hkv = num_kv_heads;
   pp.qk_scale_log2 = scale * 1.4426950408889634f;
   pp.err = error_flags;
+  pp.new_k = static_cast<const uint16_t *>(new_k);
+  pp.new_v = static_cast<const uint16_t *>(new_v);
+  pp.new_k_tok = new_k_tok_stride;
+  pp.new_v_tok = new_v_tok_stride;
+  pp.slot_mapping = slot_mapping;
+  pp.k_cache = static_cast<const uint16_t *>(k_cache);
+  pp.v_cache = static_cast<const uint16_t *>(v_cache);
+  pp.k_store = static_cast<uint16_t *>(const_cast<void *>(k_cache));
+  pp.v_store = static_cast<uint16_t *>(const_cast<void *>(v_cache));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int G = num_q_heads / num_kv_heads;
   cudaError_t e;
   switch (G) {
-    case 1: e = launch_prefill<1>(tk, tv, pp, max_q_len, st, device); break;
-    case 2: e = launch_prefill<2>(tk, tv, pp, max_q_len, st, device); break;
-    case 3: e = launch_prefill<3>(tk, tv, pp, max_q_len, st, device); break;
-    case 4: e = launch_prefill<4>(tk, tv, pp, max_q_len, st, device); break;
-    case 5: e = launch_prefill<5>(tk, tv, pp, max_q_len, st, device); break;
-    case 6: e = launch_prefill<6>(tk, tv, pp, max_q_len, st, device); break;
-    case 7: e = launch_prefill<7>(tk, tv, pp, max_q_len, st, device); break;
-    default: e = launch_prefill<8>(tk, tv, pp, max_q_len, st, device); break;
+    case 1: e = launch_prefill<1>(tk, tv, tnk, tnv, pp, max_q_len, st, device); break;
+    case 2: e = launch_prefill<2>(tk, tv, tnk, tnv, pp, max_q_len, st, device); break;
+    case 3: e = launch_prefill<3>(tk, tv, tnk, tnv, pp, max_q_len, st, device); break;
+    case 4: e = launch_prefill<4>(tk, tv, tnk, tnv, pp, max_q_len, st, device); break;
+    case 5: e = launch_prefill<5>(tk, tv, tnk, tnv, pp, max_q_len, st, device); break;
+    case 6: e = launch_prefill<6>(tk, tv, tnk, tnv, pp, max_q_len, st, device); break;
+    case 7: e = launch_prefill<7>(tk, tv, tnk, tnv, pp, max_q_len, st, device); break;
+    default: e = launch_prefill<8>(tk, tv, tnk, tnv, pp, max_q_len, st, device); break;
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+}
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_prefill_varlen(void *out, int32_t out_dtype, const void *q,
+                                       const int32_t *cu_seqlens, int32_t num_seqs,
+                                       int32_t total_tokens, int32_t max_q_len,
+                                       const void *k_cache, const void *v_cache,
+                                       int64_t num_blocks, const int32_t *block_tables,
+                                       int32_t block_table_stride, const int32_t *context_lens,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t block_size, float scale,
+                                       int32_t *error_flags, void *stream) {
+  return pa::prefill_entry(out, out_dtype, q, cu_seqlens, num_seqs, total_tokens, max_q_len,
+                           k_cache, v_cache, num_blocks, block_tables, block_table_stride,
+                           context_lens, num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                           error_flags, stream, nullptr, nullptr, 0, 0, nullptr);
+}
+
+extern "C" pa_status pa_prefill_store_varlen(
+    void *out, int32_t out_dtype, const void *q, const void *new_k, const void *new_v,
+    int64_t new_k_tok_stride, int64_t new_v_tok_stride, const int32_t *slot_mapping,
+    const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t max_q_len,
+    void *k_cache, void *v_cache, int64_t num_blocks, const int32_t *block_tables,
+    int32_t block_table_stride, const int32_t *context_lens, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t block_size, float scale,
+    int32_t *error_flags, void *stream) {
+  if (total_tokens > 0 && num_seqs > 0 && max_q_len > 0 && (!new_k || !new_v || !slot_mapping))
+    return PA_ERR_INVALID_ARG;
+  return pa::prefill_entry(out, out_dtype, q, cu_seqlens, num_seqs, total_tokens, max_q_len,
+                           k_cache, v_cache, num_blocks, block_tables, block_table_stride,
+                           context_lens, num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                           error_flags, stream, new_k, new_v, new_k_tok_stride,
+                           new_v_tok_stride, slot_mapping);
 }

@@ -31,7 +31,7 @@ EXPORTED = (
     "pa_abi_version", "pa_status_string", "pa_store_kv", "pa_decode_workspace_size",
     "pa_decode_default_splits", "pa_decode", "pa_decode_merge", "pa_prefill_varlen",
     "pa_decode_noalloc", "pa_rope_store_kv", "pa_store_kv_fp8", "pa_decode_fp8",
-    "pa_store_decode", "pa_store_decode_fp8",
+    "pa_store_decode", "pa_store_decode_fp8", "pa_prefill_store_varlen",
 )
 
 
@@ -83,6 +83,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_prefill_varlen.restype = i32
     lib.pa_prefill_varlen.argtypes = [P, i32, P, P, i32, i32, i32, P, P, i64, P, i32, P, i32,
                                       i32, i32, i32, f32, P, P]
+    lib.pa_prefill_store_varlen.restype = i32
+    lib.pa_prefill_store_varlen.argtypes = [P, i32, P, P, P, i64, i64, P, P, i32, i32, i32, P,
+                                            P, i64, P, i32, P, i32, i32, i32, i32, f32, P, P]
     return lib
 
 
@@ -421,6 +424,40 @@ def prefill_varlen(q, cu_seqlens, k_cache, v_cache, block_tables, context_lens, 
                                  _ptr(v_cache), NB, _ptr(block_tables), block_tables.stride(0),
                                  _ptr(context_lens), Hq, Hkv, D, bs, float(scale),
                                  _ptr(error_flags), _stream(stream)), "pa_prefill_varlen")
+    return out
+
+
+def prefill_store_varlen(q, new_k, new_v, slot_mapping, cu_seqlens, k_cache, v_cache,
+                         block_tables, context_lens, scale, max_q_len, out=None,
+                         out_dtype=torch.bfloat16, error_flags=None, stream=None):
+    """pa_prefill_store_varlen: the chunks' K/V rows (new_k / new_v bf16
+    [T, Hkv, D], heads contiguous) stored at slot_mapping (int32 [T]) and
+    attended, in one kernel; otherwise as prefill_varlen."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(new_k, torch.bfloat16, "new_k", 3)
+    _need(new_v, torch.bfloat16, "new_v", 3)
+    _need(slot_mapping, torch.int32, "slot_mapping", 1)
+    _need(cu_seqlens, torch.int32, "cu_seqlens", 1)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    for t, n in ((new_k, "new_k"), (new_v, "new_v")):
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise PagedAttentionError(f"{n} needs contiguous heads")
+    T, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    if tuple(new_k.shape) != (T, Hkv, D) or new_v.shape != new_k.shape or \
+            slot_mapping.shape[0] != T:
+        raise PagedAttentionError("new_k / new_v / slot_mapping need one row per token")
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=out_dtype, device=q.device)
+    _check(lib.pa_prefill_store_varlen(_ptr(out), _out_code(out.dtype), _ptr(q), _ptr(new_k),
+                                       _ptr(new_v), new_k.stride(0), new_v.stride(0),
+                                       _ptr(slot_mapping), _ptr(cu_seqlens),
+                                       cu_seqlens.shape[0] - 1, T, int(max_q_len), _ptr(k_cache),
+                                       _ptr(v_cache), NB, _ptr(block_tables),
+                                       block_tables.stride(0), _ptr(context_lens), Hq, Hkv, D, bs,
+                                       float(scale), _ptr(error_flags), _stream(stream)),
+           "pa_prefill_store_varlen")
     return out
 
 

@@ -44,7 +44,7 @@ def test_binding_names_match_header():
 
 def test_version_and_status_strings(lib):
     lib.pa_abi_version.restype = ctypes.c_int32
-    assert lib.pa_abi_version() == 6
+    assert lib.pa_abi_version() == 7
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [ctypes.c_int32]
     assert lib.pa_status_string(0) == b"ok"

@@ -180,3 +180,67 @@ def test_prefill_shape_errors_are_reported(ops):
     err.zero_()
     gpu_prefill(ops, bad, err=err, store=False)
     assert int(err.item()) & ops.DEVERR_SHAPE
+
+
+# --------------------------------------------------------------------------
+# pa_prefill_store_varlen: the chunks' store fused into the prefill
+# --------------------------------------------------------------------------
+
+def fused_prefill(ops, w, out_dtype=torch.float32, err=None):
+    q = to_dev_bf16(w.q)
+    kc, vc = to_dev_bf16(w.k_cache), to_dev_bf16(w.v_cache)
+    out = ops.prefill_store_varlen(q, to_dev_bf16(w.new_k), to_dev_bf16(w.new_v),
+                                   to_dev_i32(w.slot_mapping), to_dev_i32(w.cu_seqlens), kc, vc,
+                                   to_dev_i32(w.block_tables), to_dev_i32(w.context_lens),
+                                   w.scale, int(w.q_lens.max()), out_dtype=out_dtype,
+                                   error_flags=err)
+    torch.cuda.synchronize()
+    return out, kc, vc
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("hq,hkv", [(12, 2), (32, 8), (8, 1), (16, 4)])
+def test_prefill_store_equals_store_then_prefill(ops, hq, hkv):
+    """Chunk pages read from the new rows, the page that straddles the
+    prefix assembled from both (prefixes 0, 1, 16, 129, 300): the output
+    equals pa_store_kv + pa_prefill_varlen bit for bit, the pools equal the
+    oracle's store, and the result matches the oracle."""
+    rng = np.random.default_rng(900 + hq * 10 + hkv)
+    q_lens = np.array([1, 17, 130, 5, 64])
+    prefix = np.array([0, 300, 1, 129, 16])
+    w = synth.make_paged(rng, "fused_shapes", prefix + q_lens, q_lens, num_blocks=200,
+                         num_q_heads=hq, num_kv_heads=hkv)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out_f, kc, vc = fused_prefill(ops, w, err=err)
+    assert int(err.item()) == 0
+    out_u = gpu_prefill(ops, w)
+    assert torch.equal(out_f, out_u)
+    kref, vref = w.stored_caches()
+    assert np.array_equal(_bits(kc), kref) and np.array_equal(_bits(vc), vref)
+    assert_attention_close(dev_to_f64(out_f), oracle_prefill(w), f"fused hq={hq} hkv={hkv}",
+                           strict=True)
+
+
+def test_prefill_store_full_workload(ops):
+    """The varlen_prefill workload (8 one-token rows + 8 chunks of 512):
+    fused equals store + prefill bit for bit; pools as the oracle's store."""
+    w = synth.varlen_prefill(keep_seq=False)
+    out_f, kc, vc = fused_prefill(ops, w, out_dtype=torch.bfloat16)
+    out_u = gpu_prefill(ops, w, out_dtype=torch.bfloat16)
+    assert torch.equal(out_f.view(torch.int16), out_u.view(torch.int16))
+    kref, vref = w.stored_caches()
+    assert np.array_equal(_bits(kc), kref) and np.array_equal(_bits(vc), vref)
+
+
+def test_prefill_store_bad_slot_reported(ops):
+    rng = np.random.default_rng(77)
+    q_lens = np.array([20, 3])
+    prefix = np.array([5, 40])
+    w = synth.make_paged(rng, "fused_bad", prefix + q_lens, q_lens, num_blocks=40)
+    w.slot_mapping[4] = w.num_blocks * 16 + 7
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fused_prefill(ops, w, err=err)
+    assert int(err.item()) & ops.DEVERR_SLOT_INDEX
