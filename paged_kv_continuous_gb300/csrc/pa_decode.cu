@@ -303,10 +303,10 @@ extern "C" pa_status pa_store_decode(void *out, int32_t out_dtype, const void *q
   r.new_k_tok = new_k_tok_stride;
   r.new_v_tok = new_v_tok_stride;
   r.slot_mapping = slot_mapping;
+  if (batch > 0 && (!new_k || !new_v || !slot_mapping)) return PA_ERR_INVALID_ARG;
   int device = -1;
   const pa_status st = check_decode_request(r, &device);
   if (st != PA_OK || batch == 0) return st;
-  if (!new_k || !new_v || !slot_mapping) return PA_ERR_INVALID_ARG;
   // the new rows are moved in 16-byte chunks
   if (!aligned16(new_k) || !aligned16(new_v) || new_k_tok_stride < num_kv_heads * head_dim ||
       new_v_tok_stride < num_kv_heads * head_dim || new_k_tok_stride % 8 ||
@@ -338,10 +338,11 @@ extern "C" pa_status pa_store_decode_fp8(
   r.new_k_tok = new_k_tok_stride;
   r.new_v_tok = new_v_tok_stride;
   r.slot_mapping = slot_mapping;
+  if (batch > 0 && (!k_scale || !v_scale || !new_k || !new_v || !slot_mapping))
+    return PA_ERR_INVALID_ARG;
   int device = -1;
   const pa_status st = check_decode_request(r, &device);
   if (st != PA_OK || batch == 0) return st;
-  if (!k_scale || !v_scale || !new_k || !new_v || !slot_mapping) return PA_ERR_INVALID_ARG;
   if (!aligned16(new_k) || !aligned16(new_v) || new_k_tok_stride < num_kv_heads * head_dim ||
       new_v_tok_stride < num_kv_heads * head_dim || new_k_tok_stride % 8 ||
       new_v_tok_stride % 8)
@@ -368,10 +369,10 @@ extern "C" pa_status pa_decode_fp8(void *out, int32_t out_dtype, const void *q,
   r.fp8 = true;
   r.k_scale = k_scale;
   r.v_scale = v_scale;
+  if (batch > 0 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
   int device = -1;
   const pa_status st = check_decode_request(r, &device);
   if (st != PA_OK || batch == 0) return st;
-  if (!k_scale || !v_scale) return PA_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < pa_decode_workspace_size(r.splits, num_q_heads, head_dim))
     return PA_ERR_WORKSPACE;

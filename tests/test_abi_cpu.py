@@ -128,3 +128,65 @@ def test_rope_store_kv_argument_checks(lib):
     assert call(Hkv=0) == 2
     assert call(flags=2) == 1
     assert call(tab=ctypes.c_void_p(0x10004)) == 1
+
+
+def _bind(lib, name, argtypes):
+    f = getattr(lib, name)
+    f.restype = ctypes.c_int32
+    f.argtypes = argtypes
+    return f
+
+
+def test_fused_and_fp8_entry_points_argument_checks(lib):
+    """pa_store_decode, pa_store_decode_fp8, pa_decode_fp8, pa_store_kv_fp8
+    and pa_prefill_store_varlen validate before any launch: empty batches are
+    no-ops, missing pointers are invalid, other shapes unsupported, unknown
+    flags rejected."""
+    P, i32, i64, u32, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                 ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t)
+    nul = None
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: every case fails before a launch
+    sd = _bind(lib, "pa_store_decode", [P, i32, P, P, P, i64, i64, P, P, P, i64, P, i32, P, i32,
+                                        i32, i32, i32, i32, f32, i32, P, sz, u32, P])
+
+    def store_decode(batch=4, new=fake, slots=fake, tok=256, hq=12, hkv=2, d=128, flags=0):
+        return sd(fake, 0, fake, new, new, tok, tok, slots, fake, fake, 64, fake, 8, fake, batch,
+                  hq, hkv, d, 16, 0.1, 0, nul, 0, flags, nul)
+    assert store_decode(batch=0, new=nul, slots=nul) == 0
+    assert store_decode(new=nul) == 1
+    assert store_decode(slots=nul) == 1
+    assert store_decode(d=64) == 2
+    assert store_decode(hq=12, hkv=3) == 2
+    assert store_decode(flags=2) == 1
+
+    df = _bind(lib, "pa_decode_fp8", [P, i32, P, P, P, P, P, i64, P, i32, P, i32, i32, i32, i32,
+                                      i32, f32, i32, P, sz, u32, P])
+
+    def decode_fp8(batch=4, scales=fake, d=128, flags=0):
+        return df(fake, 0, fake, fake, fake, scales, scales, 64, fake, 8, fake, batch, 12, 2, d,
+                  16, 0.1, 0, nul, 0, flags, nul)
+    assert decode_fp8(batch=0, scales=nul) == 0
+    assert decode_fp8(d=96) == 2
+    assert decode_fp8(flags=8) == 1
+
+    sf = _bind(lib, "pa_store_kv_fp8", [P, P, i64, i64, i64, i64, i64, P, P, P, P, i64, i32, i32,
+                                        i32, P, P, u32, P])
+
+    def store_fp8(T=4, scales=fake, d=128, flags=0):
+        return sf(fake, fake, T, 256, 128, 256, 128, fake, fake, scales, scales, 8, 16, 2, d,
+                  fake, nul, flags, nul)
+    assert store_fp8(T=0, scales=nul) == 0
+    assert store_fp8(scales=nul) == 1
+    assert store_fp8(d=64) == 2
+    assert store_fp8(flags=4) == 1
+
+    pf = _bind(lib, "pa_prefill_store_varlen", [P, i32, P, P, P, i64, i64, P, P, i32, i32, i32, P,
+                                                P, i64, P, i32, P, i32, i32, i32, i32, f32, P, P])
+
+    def prefill_store(T=10, new=fake, tok=256, d=128):
+        return pf(fake, 0, fake, new, new, tok, tok, fake, fake, 2, T, 8, fake, fake, 64, fake, 8,
+                  fake, 12, 2, d, 16, 0.1, nul, nul)
+    assert prefill_store(T=0, new=nul) == 0
+    assert prefill_store(new=nul) == 1
+    assert prefill_store(tok=257) == 1      # token stride not a multiple of 8 elements
+    assert prefill_store(d=64) == 2
