@@ -45,6 +45,15 @@
 // keeps ~16 bits of the fp32 weights.  K fragments come from ldmatrix on the
 // swizzled tiles, V fragments from ldmatrix.trans, P^T from movmatrix.trans
 // of the score fragment.
+//
+// Two variants share this code.  Fused store (pa_store_decode*): the CTA
+// that stages a sequence's last block patches the new token's K/V rows into
+// its tiles and writes them to the pool, so a decode step is one launch.
+// FP8 pools (F8): E4M3 codes with per-kv-head scales; K pages keep the
+// token-major layout, V pages are dim-major inside a block and come in one
+// bulk copy; codes widen exactly to f16 and the MMAs run in f16, with a
+// token order of the score rows that makes every V operand register one
+// 32-bit load (see the F8 branches).
 #pragma once
 
 #include <cuda.h>

@@ -25,6 +25,14 @@
 // and then each P into their TMEM lanes (both MMAs read their A operand from
 // tensor memory) and store the output.  QK of tile j + 1 is issued as soon
 // as the softmax has copied S_j to registers, so it runs under the softmax.
+//
+// pa_prefill_store_varlen (the store of the chunks' K/V fused in): other CTAs
+// of a sequence need chunk keys this CTA stores, so the chunk is never read
+// back from the pool.  Pages wholly before the prefix come from the pool,
+// pages wholly inside the chunk by TMA from the new rows, and the page that
+// straddles the prefix is assembled by the loader warp from both; after its
+// last tile each loader warp stores the CTA's own positions (K: warp 0, V:
+// warp 2) through slot_mapping.
 #include <cmath>
 #include <cstring>
 #include <mutex>
