@@ -6,13 +6,17 @@ lengths (median 1024, clipped to [1, 8192]), Qwen2.5-1.5B attention shapes
 (12 query heads, 2 KV heads, head_dim 128, 16-token blocks), a 40000-block
 shuffled pool per layer.  One step = the store of the 64 new tokens and the
 decode (balanced split-K + merge) of all sequences, for one layer, in one
-kernel (pa_store_decode; the two-launch form, pa_store_kv then pa_decode, is
-timed beside it as "unfused_step").
+kernel (pa_store_decode, launched with PA_LAUNCH_PDL | PA_LAUNCH_EARLY_KV: the
+kernel before it is the previous layer's, on other pools, so the first K/V
+pages may be requested during its tail; the two-launch form, pa_store_kv then
+pa_decode, is timed beside it as "unfused_step", and the fused step with PDL
+alone as "pdl_only_step").
 Steps cycle over L = 8 independent layer pools (same lengths and tables,
 different data), so every step reads its KV from HBM, not from L2 (8 x ~105
 MB of live KV >> the 126 MB L2).  Steps run as CUDA-graph replays (one graph
-= the L layers); external timing events inside the graphs give each
-kernel's duration on the launching stream.
+= the L layers) with nothing between the launches; after the timed region, a
+copy of the graph with external timing events around each launch gives the
+duration of an isolated launch (the events break the launch overlap).
 
 value  = algorithmic bytes of a step / device time of a step  (GB/s)
 e2e    = the same metric through the public Python API with the step's
@@ -284,7 +288,8 @@ def run_extras(ops, dev):
     def dec():
         kc, vc = pools[state["l"] % L]
         state["l"] += 1
-        ops.decode(q, kc, vc, tables, ctx, 128 ** -0.5, out=out, workspace=ws, pdl=True)
+        ops.decode(q, kc, vc, tables, ctx, 128 ** -0.5, out=out, workspace=ws, pdl=True,
+                   early_kv=True)
     ms = time_graph(dec, 4 * L)
     nbytes = decode_alg_bytes(np.full(B, ctxlen), hq, hkv)
     extra["long_decode_b4_ctx32768_h32_8"] = {
@@ -390,7 +395,7 @@ def run_extras(ops, dev):
         st8["l"] += 1
         ops.store_decode_fp8(x["q"], x["nk"], x["nv"], x["kp"], x["vp"], ks8, vs8, slots8,
                              tables8, ctx8, w.scale, out=x["out"], num_splits=splits8,
-                             workspace=ws8, pdl=True)
+                             workspace=ws8, pdl=True, early_kv=True)
 
     def fp8_step_unfused():
         x = fl[st8["l"] % L8]
@@ -405,7 +410,7 @@ def run_extras(ops, dev):
         "us_per_step": ms * 1e3, "alg_bytes": nbytes, "GB_per_s": nbytes / ms / 1e6,
         "frac_of_hbm": nbytes / ms / 1e6 / hbm, "seq_steps_per_s": B8 / (ms / 1e3),
         "step": "pa_store_decode_fp8 (64 new tokens quantised and stored, decode), one "
-                "kernel, PDL, 8 layer pools",
+                "kernel, PDL + early K/V, 8 layer pools",
         "unfused_us_per_step": ms_u * 1e3, "peak_kind": hbm_kind}
     del fl
     return extra
@@ -492,6 +497,9 @@ def run_ours(args):
 
     w = synth.cb_decode_b64(keep_seq=False)
     L = args.layers
+    # early K/V requests need the kernel before each call to be another
+    # layer's (other pools): true when the steps cycle over several pools
+    early = L > 1
     B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
 
     def dev16(a):
@@ -530,7 +538,8 @@ def run_ours(args):
         if timing:
             timing[0].record()
         ops.store_decode(x["q"], x["nk"], x["nv"], x["kc"], x["vc"], slots, tables, ctx,
-                         w.scale, out=x["out"], num_splits=splits, workspace=ws, pdl=True)
+                         w.scale, out=x["out"], num_splits=splits, workspace=ws, pdl=True,
+                         early_kv=early)
         if timing:
             timing[1].record()
 
@@ -557,16 +566,17 @@ def run_ours(args):
             for l in range(L):
                 step(l)
     torch.cuda.synchronize()
-    # Only the first copy carries event nodes (per-launch durations for the
-    # roofline); the other copies run the launches back to back, as a serving
-    # loop does, so the event nodes cost the step time little.
-    for c in range(NC):
+    # The timed copies run the launches back to back, as a serving loop does.
+    # A separate copy carries event nodes around each launch (which break the
+    # programmatic-launch overlap) and is replayed after the timed region for
+    # the per-launch duration of an isolated launch.
+    for c in range(NC + 1):
         g = torch.cuda.CUDAGraph()
         evs = []
         for l in range(L):
             try:
                 evs.append([torch.cuda.Event(enable_timing=True, external=True)
-                            for _ in range(2)] if c == 0 else None)
+                            for _ in range(2)] if c == NC else None)
             except TypeError:
                 ext_ok = False
                 evs.append(None)
@@ -575,6 +585,7 @@ def run_ours(args):
                 step(l, evs[l])
         graphs.append(g)
         events.append(evs)
+    ev_graph, ev_events = graphs.pop(), events.pop()
     rem = args.steps % L
     rem_graph = None
     if rem:
@@ -624,11 +635,16 @@ def run_ours(args):
     elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
     err_word = ops.read_error_word(ws)
 
-    # per-kernel durations from the last replay of each graph copy
+    # per-launch durations of isolated launches (untimed replays of the
+    # event-bracketed copy)
     decode_ms = []
-    if ext_ok and full >= 1:
+    if ext_ok:
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                ev_graph.replay()
+        torch.cuda.synchronize()
         for l in range(L):
-            e = events[0][l]
+            e = ev_events[l]
             if e is not None:
                 decode_ms.append(e[0].elapsed_time(e[1]))
     # the same step as two launches (pa_store_kv, then pa_decode), for comparison
@@ -638,6 +654,15 @@ def run_ours(args):
         step_unfused(st_u["l"] % L)
         st_u["l"] += 1
     unfused_ms = time_graph(unfused, 4 * L)
+    # the fused step launched with PDL only (no early K/V requests)
+    st_p = {"l": 0}
+
+    def pdl_only():
+        x = layers[st_p["l"] % L]
+        st_p["l"] += 1
+        ops.store_decode(x["q"], x["nk"], x["nv"], x["kc"], x["vc"], slots, tables, ctx,
+                         w.scale, out=x["out"], num_splits=splits, workspace=ws, pdl=True)
+    pdl_only_ms = time_graph(pdl_only, 4 * L)
 
     ms_per_step = elapsed_s * 1e3 / args.steps
     dec_bytes = decode_alg_bytes(w.context_lens, Hq, Hkv, D)
@@ -691,7 +716,8 @@ def run_ours(args):
         x = layers[l]
         d_pack.copy_(h_pack[l], non_blocking=True)
         ops.store_decode(d_q, d_nk, d_nv, x["kc"], x["vc"], d_slot, d_tab, d_ctx, w.scale,
-                         out=x["out"], num_splits=splits, workspace=ws, pdl=True)
+                         out=x["out"], num_splits=splits, workspace=ws, pdl=True,
+                         early_kv=early)
         h_out.copy_(x["out"], non_blocking=True)
 
     for i in range(min(args.warmup, 50)):
@@ -760,11 +786,17 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "step": "pa_store_decode: store of the 64 new tokens + decode (+merge) "
                            "in one kernel, one layer",
-                   "launch": "PA_LAUNCH_PDL (programmatic dependent launch)"},
+                   "launch": ("PA_LAUNCH_PDL | PA_LAUNCH_EARLY_KV (programmatic dependent "
+                              "launch; the first K/V pages requested during the previous "
+                              "layer's tail)") if early else
+                             "PA_LAUNCH_PDL (programmatic dependent launch)"},
         "seq_steps_per_s": world * B * args.steps / elapsed_s,
         "unfused_step": {"us_per_step": unfused_ms * 1e3,
                          "GB_per_s": step_bytes / unfused_ms / 1e6,
                          "step": "pa_store_kv + pa_decode, two launches, PDL"},
+        "pdl_only_step": {"us_per_step": pdl_only_ms * 1e3,
+                          "GB_per_s": step_bytes / pdl_only_ms / 1e6,
+                          "step": "pa_store_decode with PA_LAUNCH_PDL only"},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),

@@ -74,7 +74,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 7
+#define PA_ABI_VERSION 8
 
 #if defined(__GNUC__)
 #define PA_API __attribute__((visibility("default")))
@@ -120,9 +120,24 @@ typedef int32_t pa_status;
  * immediately before the call (host copies and earlier kernels are fine).
  * pa_store_kv and pa_rope_store_kv read nothing before that wait.
  * Every write and every other read happens after it, so the results are the
- * same with and without the flag.
+ * same with and without the flag.  The decode kernels let the kernel after
+ * them begin only once they have passed their own wait: when that next
+ * kernel starts, every kernel before them has completed.
+ *
+ * PA_LAUNCH_EARLY_KV (decode entry points only, together with
+ * PA_LAUNCH_PDL): the kernel also requests the K/V pages of its first ring
+ * round (up to 8 blocks per CTA) before the previous kernel completes, so
+ * that the copies overlap that kernel's tail.  q, the new rows, the
+ * workspace and every write still wait for it.  The caller guarantees that
+ * the kernel launched immediately before the call does not write k_cache /
+ * v_cache; in a layer-by-layer decode step with pa_store_decode this holds
+ * (the kernel before layer l's call writes layer l - 1's pools or
+ * activations), while a pa_store_kv or pa_rope_store_kv into the same pools
+ * just before the call rules the flag out.  Results are the same with and
+ * without it.  Without PA_LAUNCH_PDL it returns PA_ERR_INVALID_ARG.
  */
 #define PA_LAUNCH_PDL 1u
+#define PA_LAUNCH_EARLY_KV 2u
 
 /* ABI version of the loaded library (PA_ABI_VERSION it was built with). */
 PA_API int32_t pa_abi_version(void);

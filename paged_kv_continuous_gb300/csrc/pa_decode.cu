@@ -193,6 +193,7 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
   p.v_pool16 = r.fp8 ? nullptr : static_cast<uint16_t *>(const_cast<void *>(r.v_cache));
   p.k_pool8 = r.fp8 ? static_cast<uint8_t *>(const_cast<void *>(r.k_cache)) : nullptr;
   p.v_pool8 = r.fp8 ? static_cast<uint8_t *>(const_cast<void *>(r.v_cache)) : nullptr;
+  p.early_kv = (r.flags & PA_LAUNCH_EARLY_KV) != 0;
   cudaStream_t s = static_cast<cudaStream_t>(r.stream);
   if (clear_counters &&
       cudaMemsetAsync(p.counters, 0, (size_t)r.splits * sizeof(int32_t), s) != cudaSuccess)
@@ -220,7 +221,9 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
 
 pa_status check_decode_request(DecodeRequest &r, int *device_out) {
   if (r.batch < 0 || r.num_blocks < 0 || r.num_splits < 0) return PA_ERR_INVALID_ARG;
-  if (r.flags & ~static_cast<uint32_t>(PA_LAUNCH_PDL)) return PA_ERR_INVALID_ARG;
+  if (r.flags & ~static_cast<uint32_t>(PA_LAUNCH_PDL | PA_LAUNCH_EARLY_KV))
+    return PA_ERR_INVALID_ARG;
+  if ((r.flags & PA_LAUNCH_EARLY_KV) && !(r.flags & PA_LAUNCH_PDL)) return PA_ERR_INVALID_ARG;
   if (r.num_splits > PA_DECODE_MAX_SPLITS) return PA_ERR_UNSUPPORTED;
   if (r.out_dtype != PA_DTYPE_BF16 && r.out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
   if (r.head_dim != kHeadDim || r.block_size != kBlockSize) return PA_ERR_UNSUPPORTED;

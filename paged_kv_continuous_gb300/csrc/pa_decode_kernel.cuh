@@ -93,7 +93,19 @@ struct DecodeParams {
   uint16_t *v_pool16;
   uint8_t *k_pool8;  // FP8 pools, fused store
   uint8_t *v_pool8;
+  // Nonzero: the K/V pages of the first ring round are requested before the
+  // previous kernel in the stream completes (the caller guarantees that
+  // kernel does not write the pools).
+  int early_kv;
 };
+
+// Waits for the previous kernel in the stream to complete, then signals that
+// the next kernel may begin (programmatic dependent launch; both no-ops
+// without it).
+__device__ __forceinline__ void wait_prev_then_release() {
+  griddep_wait();
+  griddep_launch_dependents();
+}
 
 constexpr int kDecodeProducerWarps = 2;
 constexpr int kDecodeEpilogueWarp = 2;       // warp index of the epilogue warp
@@ -203,6 +215,9 @@ struct DecodeCtl {
   // piece start, off the epilogue's path)
   long long pc_cs0, pc_cs1;
   int pc_pieces;
+  // consumer thread 0 has decided how the final piece ends (the epilogue
+  // warp stops watching the counter)
+  int decided;
 };
 static_assert(sizeof(DecodeCtl) <= 256, "control words do not fit their 256 bytes");
 
@@ -392,6 +407,19 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *ptr) {
 
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// Arrival on a sequence's counter with release semantics at GPU scope: the
+// partial rows written before it (by this thread, or by the threads a CTA
+// or warp barrier ordered before it) are visible to whoever observes the new
+// count with an acquire.  Returns the old count.
+__device__ __forceinline__ int atom_add_release_gpu(int32_t *ptr, int v) {
+  int old;
+  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(ptr), "r"(v)
+               : "memory");
+  return old;
 }
 
 // ---- output writers ---------------------------------------------------------
@@ -693,9 +721,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
   // ---- 2b. Under a programmatic dependent launch the previous kernel in the
   //          stream may still be running.  Context lengths and block tables
-  //          may be read before griddep_wait(); q, the pools, the workspace
-  //          and every write come after it.
-  griddep_launch_dependents();
+  //          may be read before the wait for it; so may the K/V pages of the
+  //          first ring round when p.early_kv is set.  q, the new rows, the
+  //          workspace and every write come after it.  Each thread lets the
+  //          next kernel begin only once it has passed that wait
+  //          (wait_prev_then_release), so a kernel that starts early behind
+  //          this one finds every kernel before this one complete.
   // rows of empty sequences: sequence b is zeroed by CTA b mod S, by threads
   // t0, t0 + nt, ...
   auto zero_empty_rows = [&](int t0, int nt) {
@@ -707,7 +738,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (lo >= hi || ctl->first_b < 0) {
     // no block for this CTA (N < S), or inconsistent input (never walk from
     // b = -1): only the empty rows and the error bit remain
-    griddep_wait();
+    wait_prev_then_release();
     zero_empty_rows(tid, blockDim.x);
     if (lo < hi && tid == 0) report(p.err, PA_DEVERR_SHAPE);
     return;
@@ -732,6 +763,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     mbar_init(smem_addr(&ctl->seen_bar), 1);
     ctl->def_pending = 0;
     ctl->fin_valid = 0;
+    ctl->decided = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -750,6 +782,40 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
+    // The K and V pages of physical block ph into ring slot st, completing
+    // on the slot's full barrier (warp-uniform arguments; nothing for an
+    // entry outside the pool, which the caller reports).  arm: lane 0 first
+    // adds the pages' bytes to the barrier's expected count, without arriving.
+    auto issue_kv_stage = [&](int st, long long ph, bool arm) {
+      if (!(ph >= 0 && ph < p.num_blocks)) return;
+      const uint32_t dst = stage0 + st * S::STAGE_BYTES;
+      const uint32_t bar = full0 + 8 * st;
+      if (arm) {
+        if (lane == 0) mbar_expect_tx(bar, 2u * S::KV_BYTES);
+        __syncwarp();
+      }
+      const int z = (int)(ph * kBlockSize);
+      if constexpr (F8) {
+        // K: (128 dims, head, slot) box of each head pair, 128-byte
+        // swizzle; V: the block's dim-major page is one contiguous run
+        // (Hkv x 2 KB): one bulk copy (a tensor box would move 16-byte rows)
+#pragma unroll
+        for (int pr = 0; pr < S::NPAIR; ++pr)
+          tma_load_box(dst + pr * S::BOX_BYTES, &tmap_k, 0, pr * S::HB, z, bar, pol_kv);
+        bulk_load_elect(dst + S::KV_BYTES, p.v_pool + ph * S::KV_BYTES, S::KV_BYTES, bar,
+                        pol_kv);
+      } else {
+#pragma unroll
+        for (int pr = 0; pr < S::NPAIR; ++pr) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t off = (pr * 2 + h) * S::BOX_BYTES;
+            tma_load_box(dst + off, &tmap_k, h * 64, pr * S::HB, z, bar, pol_kv);
+            tma_load_box(dst + S::KV_BYTES + off, &tmap_v, h * 64, pr * S::HB, z, bar, pol_kv);
+          }
+        }
+      }
+    };
     int b = first_b;
     int ctx = __ldg(p.context_lens + b);
     int j = (int)(lo - first_prefix);
@@ -760,17 +826,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       int lb, lj, lctx;
       const int count = walk_chunk(p.context_lens, p.batch, b, ctx, j, hi - gb, lane, lb, lj, lctx);
       if (count == 0) {
-        griddep_wait();
+        wait_prev_then_release();
         if (lane == 0) report(p.err, PA_DEVERR_SHAPE);
         break;
       }
       // all block-table entries of the chunk in one round of loads
       const bool in_row = lane < count && lj < p.bt_stride;
       const long long phys = in_row ? __ldg(p.block_tables + (long long)lb * p.bt_stride + lj) : -1;
+      int n_early = 0;  // stages of this chunk whose K/V pages went out before the wait
       if (!waited) {
-        // the first chunk's descriptors are ready; the copies wait for the
-        // previous kernel (it may write the pools)
-        griddep_wait();
+        // the first chunk's descriptors are ready.  With p.early_kv the K/V
+        // pages of the first ring round go out now (issued == 0 here, so
+        // stage i of the chunk is ring slot i and needs no empty wait): lane
+        // 0 raises the slot's expected bytes without arriving, so the stage
+        // cannot complete before its arrival (with the q copy) below.  The
+        // rest waits for the previous kernel, which may write q, the new
+        // rows and the workspace.
+        if (p.early_kv) {
+          n_early = min(count, S::NST);
+          for (int i = pw; i < n_early; i += kDecodeProducerWarps)
+            issue_kv_stage(i, __shfl_sync(0xffffffffu, phys, i), true);
+        }
+        wait_prev_then_release();
         waited = true;
       }
       // the q rows go with the first NPH stages of every piece: each consumer
@@ -795,38 +872,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const bool ok = ph_i >= 0 && ph_i < p.num_blocks;
         const uint32_t dst = stage0 + st * S::STAGE_BYTES;
         const uint32_t bar = full0 + 8 * st;
+        const bool pre = i < n_early;  // K/V already requested and counted
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar, (ok ? 2u * S::KV_BYTES : 0u) + (q_i ? S::Q_BYTES : 0u));
+          mbar_arrive_expect_tx(bar, (ok && !pre ? 2u * S::KV_BYTES : 0u) +
+                                         (q_i ? S::Q_BYTES : 0u));
           // a context longer than the table row (caller error) or an entry
           // outside the pool: reported, not read
           if (!ok) report(p.err, row_i ? PA_DEVERR_BLOCK_INDEX : PA_DEVERR_SHAPE);
         }
         __syncwarp();
-        if (ok) {
-          const int z = (int)(ph_i * kBlockSize);
-          if constexpr (F8) {
-            // K: (128 dims, head, slot) box of each head pair, 128-byte
-            // swizzle; V: the block's dim-major page is one contiguous run
-            // (Hkv x 2 KB): one bulk copy (a tensor box would move 16-byte
-            // rows)
-#pragma unroll
-            for (int pr = 0; pr < S::NPAIR; ++pr)
-              tma_load_box(dst + pr * S::BOX_BYTES, &tmap_k, 0, pr * S::HB, z, bar, pol_kv);
-            bulk_load_elect(dst + S::KV_BYTES, p.v_pool + ph_i * S::KV_BYTES, S::KV_BYTES, bar,
-                            pol_kv);
-          } else {
-#pragma unroll
-            for (int pr = 0; pr < S::NPAIR; ++pr) {
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint32_t off = (pr * 2 + h) * S::BOX_BYTES;
-                tma_load_box(dst + off, &tmap_k, h * 64, pr * S::HB, z, bar, pol_kv);
-                tma_load_box(dst + S::KV_BYTES + off, &tmap_v, h * 64, pr * S::HB, z, bar,
-                             pol_kv);
-              }
-            }
-          }
-        }
+        if (!pre) issue_kv_stage(st, ph_i, false);
         if (q_i)
           bulk_load_elect(dst + 2 * S::KV_BYTES, p.q + (long long)b_i * S::HQ * kHeadDim,
                           S::Q_BYTES, bar, pol_q);
@@ -855,7 +910,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     //          For a cut piece it then publishes: fence, arrival, and the
     //          merge if the piece arrives last.  The consumers never wait for
     //          this, except to reuse a buffer two pieces later.
-    griddep_wait();
+    wait_prev_then_release();
     // While it waits for the next piece, lane 0 watches the arrival counter
     // of the CTA's final piece (once the consumers have named it): when every
     // other piece of that sequence has arrived it completes seen_bar, and the
@@ -899,7 +954,33 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const bool got = wait_full(smem_addr(&ctl->red_full[k]), (npe >> 1) & 1);
       const PieceDesc d = ctl->desc[k];
       if (!got || d.kind == kPieceEnd) {
+        // every piece handed to this warp is done, and a merge it left is
+        // recorded: the consumers need not wait for anything else from it
         if (lane == 0) mbar_arrive(smem_addr(&ctl->ew_done));
+        // The end mark comes when the final piece's blocks are done.  While
+        // the consumers combine that piece, lane 0 goes on watching its
+        // counter until they decide how the piece ends (bounded; giving up
+        // only loses the shortcut).
+        if (got && lane == 0) {
+          const long long t0 = clock64();
+          while (snoop < 2 && !*reinterpret_cast<volatile int *>(&ctl->decided) &&
+                 !*abort_flag && clock64() - t0 < kWaitTimeoutCycles) {
+            if (snoop == 0) {
+              // named before the end mark, or never: a whole final piece
+              if (!*reinterpret_cast<volatile int *>(&ctl->fin_valid)) break;
+              __threadfence_block();
+              fin_cs1 = ctl->fin_cs1;
+              fin_pieces = ctl->fin_pieces;
+              snoop = 1;
+            }
+            if (ld_acquire_gpu(p.counters + fin_cs1) == fin_pieces - 1) {
+              mbar_arrive(smem_addr(&ctl->seen_bar));
+              snoop = 2;
+            } else {
+              __nanosleep(64);
+            }
+          }
+        }
         return;
       }
       if constexpr (S::NPH > 1) {
@@ -955,8 +1036,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (lane == 0) {
           // release: the partial rows (this warp's, or the consumers' that
           // the red_full barrier ordered before) precede the arrival
-          __threadfence();
-          last = atomicAdd(p.counters + d.cs1, 1) == d.pieces - 1;
+          last = atom_add_release_gpu(p.counters + d.cs1, 1) == d.pieces - 1;
         }
         if (lane == 0 && last) {
           // arrived last: acquire the other pieces' partials and leave the
@@ -975,7 +1055,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   // ---- 5b. consumers ----------------------------------------------------------
   const int cw = warp - kDecodeFirstConsumerWarp;  // consumer warp 0..CW-1
-  griddep_wait();
+  wait_prev_then_release();
   zero_empty_rows(tid - 32 * kDecodeFirstConsumerWarp, S::CW * 32);
   const int g = cw % HKV;     // kv head of this warp
   const int ph = cw / HKV;    // stage phase of this warp
@@ -1009,6 +1089,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
 
   int npieces = 0;  // pieces ended so far (every consumer warp counts the same)
+  bool no_final = false;  // the block walk stopped early (inconsistent input)
   // consumer thread 0: the current piece's split words are in ctl
   bool pc_done = false;
   auto piece_splits = [&](long long gb, int j, int n) {
@@ -1046,7 +1127,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     int lb = 0, lj = 0, lctx = 0;
     const int count =
         walk_chunk(p.context_lens, p.batch, wb, wctx, wj, hi - gb0, lane, lb, lj, lctx);
-    if (count == 0) break;  // same decision in every consumer warp and the producer
+    if (count == 0) {
+      // same decision in every consumer warp and the producer; no final
+      // piece follows: the epilogue warp gets its end mark at the consumers'
+      // end
+      no_final = true;
+      break;
+    }
     // A warp visits only the blocks that concern it: its own stages (index
     // = ph mod NPH) and every piece end (all warps combine there).
     const bool in_chunk = lane < count;
@@ -1522,6 +1609,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
       }
 
+      if (final_piece) {
+        // no piece follows: the end mark goes to the epilogue warp now,
+        // before the final piece is published and merged, so that the
+        // epilogue warp is done before the consumers' end (buffer kbuf was
+        // released to the consumers above; they are done with it)
+        if (ct == 0) ctl->desc[kbuf].kind = kPieceEnd;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ctl->red_full[kbuf]));
+      }
       if (!final_piece) {
         // hand the piece to the epilogue warp (its rows are in rbuf, or
         // already written with one warp per kv head) and stream on
@@ -1546,13 +1642,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const long long cs0 = ctl->pc_cs0, cs1 = ctl->pc_cs1;
         const int pieces = ctl->pc_pieces;
         if (ct == 0) {
+          *reinterpret_cast<volatile int *>(&ctl->decided) = 1;
           if (mbar_test_wait(smem_addr(&ctl->seen_bar), 0)) {
             // every other piece had arrived (the epilogue warp acquired their
             // rows): this piece is the last, no arrival and no publication
             ctl->last = 1;
           } else {
-            __threadfence();  // release: the rows before the arrival
-            const bool last = atomicAdd(p.counters + cs1, 1) == pieces - 1;
+            // release: the rows before the arrival
+            const bool last = atom_add_release_gpu(p.counters + cs1, 1) == pieces - 1;
             if (last) fence_acq_rel_gpu();  // acquire the other pieces' rows
             ctl->last = last;
           }
@@ -1588,15 +1685,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
 consumers_done:
   {
-    // tell the epilogue warp that no piece follows, once it is done with the
-    // buffer it would look at next
-    const int kbuf = npieces & 1;
-    if (npieces >= 2)
-      __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->red_empty[kbuf]),
-                                        ((npieces >> 1) - 1) & 1, abort_flag, p.err));
-    if (ct == 0) ctl->desc[kbuf].kind = kPieceEnd;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&ctl->red_full[kbuf]));
+    if (no_final) {
+      // no final piece came (inconsistent input): tell the epilogue warp
+      // that no piece follows, once it is done with the buffer it would look
+      // at next
+      const int kbuf = npieces & 1;
+      if (npieces >= 2)
+        __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->red_empty[kbuf]),
+                                          ((npieces >> 1) - 1) & 1, abort_flag, p.err));
+      if (ct == 0) ctl->desc[kbuf].kind = kPieceEnd;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&ctl->red_full[kbuf]));
+    }
+    if (ct == 0) *reinterpret_cast<volatile int *>(&ctl->decided) = 1;
     // a merge the epilogue warp left (its piece arrived last)
     __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->ew_done), 0, abort_flag, p.err));
     if (ctl->def_pending) {

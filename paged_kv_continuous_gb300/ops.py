@@ -21,6 +21,7 @@ PA_OK = 0
 PA_DTYPE_BF16 = 0
 PA_DTYPE_F32 = 1
 PA_LAUNCH_PDL = 1  # programmatic dependent launch (see include/pa.h)
+PA_LAUNCH_EARLY_KV = 2  # decode: K/V pages requested before the previous kernel completes
 DEVERR_BLOCK_INDEX = 1
 DEVERR_SLOT_INDEX = 2
 DEVERR_WAIT_TIMEOUT = 4
@@ -219,11 +220,23 @@ def decode_workspace(num_q_heads: int, num_kv_heads: int, num_splits: int = 0,
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
+def _decode_flags(pdl, early_kv):
+    """Launch flags of the decode entry points.  early_kv (with pdl): the
+    kernel requests its first K/V pages before the kernel launched just
+    before it completes, so that kernel must not write the pools."""
+    if early_kv and not pdl:
+        raise PagedAttentionError("early_kv needs pdl")
+    return (PA_LAUNCH_PDL if pdl else 0) | (PA_LAUNCH_EARLY_KV if early_kv else 0)
+
+
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
-           out_dtype=torch.bfloat16, num_splits=0, workspace=None, stream=None, pdl=False):
+           out_dtype=torch.bfloat16, num_splits=0, workspace=None, stream=None, pdl=False,
+           early_kv=False):
     """pa_decode: q bf16 [B, Hq, D] over the paged pools; returns out [B, Hq, D].
     pdl: launch with PA_LAUNCH_PDL (context_lens and block_tables must then
-    not be written by the kernel launched just before)."""
+    not be written by the kernel launched just before).  early_kv (with pdl):
+    PA_LAUNCH_EARLY_KV, the first K/V pages are requested before that kernel
+    completes, so it must not write k_cache / v_cache either."""
     _need(q, torch.bfloat16, "q", 3)
     _need(k_cache, torch.bfloat16, "k_cache", 4)
     _need(v_cache, torch.bfloat16, "v_cache", 4)
@@ -243,13 +256,13 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
                          _ptr(v_cache), NB, _ptr(block_tables), block_tables.stride(0),
                          _ptr(context_lens), B, Hq, Hkv, D, bs, float(scale), int(num_splits),
                          _ptr(workspace), workspace.numel() * workspace.element_size(),
-                         PA_LAUNCH_PDL if pdl else 0, _stream(stream)), "pa_decode")
+                         _decode_flags(pdl, early_kv), _stream(stream)), "pa_decode")
     return out
 
 
 def store_decode(q, new_k, new_v, k_cache, v_cache, slot_mapping, block_tables, context_lens,
                  scale, out=None, out_dtype=torch.bfloat16, num_splits=0, workspace=None,
-                 stream=None, pdl=False):
+                 stream=None, pdl=False, early_kv=False):
     """pa_store_decode: one decode step in one kernel -- each sequence's new
     token (new_k / new_v bf16 [B, Hkv, D], heads contiguous) is stored at
     slot_mapping[b] and attended with the rest of the pool.  Returns out."""
@@ -283,7 +296,8 @@ def store_decode(q, new_k, new_v, k_cache, v_cache, slot_mapping, block_tables, 
                                block_tables.stride(0), _ptr(context_lens), B, Hq, Hkv, D, bs,
                                float(scale), int(num_splits), _ptr(workspace),
                                workspace.numel() * workspace.element_size(),
-                               PA_LAUNCH_PDL if pdl else 0, _stream(stream)), "pa_store_decode")
+                               _decode_flags(pdl, early_kv), _stream(stream)),
+           "pa_store_decode")
     return out
 
 
@@ -334,7 +348,7 @@ def store_kv_fp8(k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, error_f
 
 def decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale,
                out=None, out_dtype=torch.bfloat16, num_splits=0, workspace=None, stream=None,
-               pdl=False):
+               pdl=False, early_kv=False):
     """pa_decode_fp8: q bf16 [B, Hq, D] over the FP8 pools with per-kv-head
     scales; returns out [B, Hq, D]."""
     _need(q, torch.bfloat16, "q", 3)
@@ -355,13 +369,14 @@ def decode_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens
                              _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), B,
                              Hq, Hkv, D, bs, float(scale), int(num_splits), _ptr(workspace),
                              workspace.numel() * workspace.element_size(),
-                             PA_LAUNCH_PDL if pdl else 0, _stream(stream)), "pa_decode_fp8")
+                             _decode_flags(pdl, early_kv), _stream(stream)), "pa_decode_fp8")
     return out
 
 
 def store_decode_fp8(q, new_k, new_v, k_cache, v_cache, k_scale, v_scale, slot_mapping,
                      block_tables, context_lens, scale, out=None, out_dtype=torch.bfloat16,
-                     num_splits=0, workspace=None, stream=None, pdl=False):
+                     num_splits=0, workspace=None, stream=None, pdl=False,
+                     early_kv=False):
     """pa_store_decode_fp8: store_decode over FP8 pools (see fp8_pools)."""
     _need(q, torch.bfloat16, "q", 3)
     _need(new_k, torch.bfloat16, "new_k", 3)
@@ -392,7 +407,7 @@ def store_decode_fp8(q, new_k, new_v, k_cache, v_cache, k_scale, v_scale, slot_m
                                    block_tables.stride(0), _ptr(context_lens), B, Hq, Hkv, D, bs,
                                    float(scale), int(num_splits), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(),
-                                   PA_LAUNCH_PDL if pdl else 0, _stream(stream)),
+                                   _decode_flags(pdl, early_kv), _stream(stream)),
            "pa_store_decode_fp8")
     return out
 

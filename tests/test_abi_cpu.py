@@ -44,7 +44,7 @@ def test_binding_names_match_header():
 
 def test_version_and_status_strings(lib):
     lib.pa_abi_version.restype = ctypes.c_int32
-    assert lib.pa_abi_version() == 7
+    assert lib.pa_abi_version() == 8
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [ctypes.c_int32]
     assert lib.pa_status_string(0) == b"ok"
@@ -96,8 +96,9 @@ def test_argument_checks_before_any_launch():
     assert L.pa_store_kv(nul, nul, 0, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, 0, nul) == 0
     assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, 0, nul) == 1
     assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 96, nul, nul, 0, nul) == 2
-    # launch flags other than PA_LAUNCH_PDL are rejected
+    # store launch flags other than PA_LAUNCH_PDL are rejected (PA_LAUNCH_EARLY_KV is decode-only)
     assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, 2, nul) == 1
+    assert L.pa_store_kv(nul, nul, 4, 0, 0, 0, 0, nul, nul, 1, 16, 2, 128, nul, nul, 3, nul) == 1
     assert L.pa_decode(nul, 0, nul, nul, nul, 1, nul, 1, nul, 1, 12, 2, 128, 16, 0.1, 0, nul, 0,
                        4, nul) == 1
     assert L.pa_decode_merge(nul, 0, nul, 0, nul, 1, 12, 128, 16, 0, nul) == 1
@@ -157,7 +158,10 @@ def test_fused_and_fp8_entry_points_argument_checks(lib):
     assert store_decode(slots=nul) == 1
     assert store_decode(d=64) == 2
     assert store_decode(hq=12, hkv=3) == 2
-    assert store_decode(flags=2) == 1
+    assert store_decode(flags=2) == 1       # PA_LAUNCH_EARLY_KV needs PA_LAUNCH_PDL
+    assert store_decode(flags=2, d=64) == 1
+    assert store_decode(flags=3, d=64) == 2  # both flags accepted: the shape decides
+    assert store_decode(flags=7) == 1
 
     df = _bind(lib, "pa_decode_fp8", [P, i32, P, P, P, P, P, i64, P, i32, P, i32, i32, i32, i32,
                                       i32, f32, i32, P, sz, u32, P])
@@ -168,6 +172,7 @@ def test_fused_and_fp8_entry_points_argument_checks(lib):
     assert decode_fp8(batch=0, scales=nul) == 0
     assert decode_fp8(d=96) == 2
     assert decode_fp8(flags=8) == 1
+    assert decode_fp8(flags=3, d=96) == 2
 
     sf = _bind(lib, "pa_store_kv_fp8", [P, P, i64, i64, i64, i64, i64, P, P, P, P, i64, i32, i32,
                                         i32, P, P, u32, P])
