@@ -10,8 +10,11 @@ submitted at once.
 decode step -- ``pa_rope_store_kv`` (or ``pa_store_kv`` when no rotary
 tables are given) and then ``pa_decode`` -- both launched with
 ``PA_LAUNCH_PDL``, so each kernel's start-up overlaps the tail of the one
-before.  This module only records calls into the graph; every step of the
-computation runs in the library's kernels.
+before.  With ``fused=True`` (no rotary tables) a layer is one call,
+``pa_store_decode``, which also requests its first K/V pages early
+(``PA_LAUNCH_EARLY_KV``) whenever the call before it is another layer's, on
+other pools.  This module only records calls into the graph; every step of
+the computation runs in the library's kernels.
 
 Static state (fixed at capture): the batch size, the block-table width, the
 per-layer tensors (their addresses are baked into the graph), the split
@@ -40,14 +43,21 @@ class DecodeStepGraph:
     int32 [B]: the initial values of the static index buffers (copied).
     positions int32 [B] with cos_table / sin_table float32 [max_position,
     D/2]: rotary embedding of q and k fused into the store.
+    fused: one pa_store_decode per layer instead of a store and a decode
+    (without rotary tables only); slot_mapping[b] must then be the slot of
+    position context_lens[b] - 1 under the block table.
     """
 
     def __init__(self, layers, block_tables, context_lens, slot_mapping, scale,
-                 positions=None, cos_table=None, sin_table=None, num_splits=0, device=None):
+                 positions=None, cos_table=None, sin_table=None, num_splits=0, device=None,
+                 fused=False):
         if not layers:
             raise ops.PagedAttentionError("DecodeStepGraph needs at least one layer")
         if (cos_table is None) != (positions is None) or (cos_table is None) != (sin_table is None):
             raise ops.PagedAttentionError("positions, cos_table and sin_table go together")
+        if fused and cos_table is not None:
+            raise ops.PagedAttentionError("fused=True takes no rotary tables")
+        self.fused = bool(fused)
         dev = layers[0]["q"].device if device is None else torch.device(device)
         self.layers = layers
         self.scale = float(scale)
@@ -69,7 +79,16 @@ class DecodeStepGraph:
         self.graph = torch.cuda.CUDAGraph()
         self._capture()
 
-    def _layer_calls(self, x):
+    def _layer_calls(self, x, prev):
+        if self.fused:
+            # early K/V requests only behind another layer's call on other pools
+            early = prev is not None and prev["k_cache"].data_ptr() != x["k_cache"].data_ptr() \
+                and prev["v_cache"].data_ptr() != x["v_cache"].data_ptr()
+            ops.store_decode(x["q"], x["k"], x["v"], x["k_cache"], x["v_cache"],
+                             self.slot_mapping, self.block_tables, self.context_lens, self.scale,
+                             out=x["out"], num_splits=self.num_splits, workspace=self.workspace,
+                             pdl=True, early_kv=early)
+            return
         if self.rope:
             ops.rope_store_kv(x["q"], x["k"], x["v"], self.positions, self.cos_table,
                               self.sin_table, x["k_cache"], x["v_cache"], self.slot_mapping,
@@ -94,12 +113,14 @@ class DecodeStepGraph:
         torch.cuda.synchronize()
         self.stream.wait_stream(torch.cuda.current_stream())
         with torch.cuda.graph(self.graph, stream=self.stream):
+            prev = None
             for x in self.layers:
-                self._layer_calls(x)
+                self._layer_calls(x, prev)
+                prev = x
         torch.cuda.current_stream().wait_stream(self.stream)
 
     def launches_per_replay(self) -> int:
-        return 2 * len(self.layers)
+        return (1 if self.fused else 2) * len(self.layers)
 
     def update(self, block_tables=None, context_lens=None, slot_mapping=None, positions=None):
         """Write new values into the static index buffers (same shapes), in

@@ -195,3 +195,21 @@ def test_fused_and_fp8_entry_points_argument_checks(lib):
     assert prefill_store(new=nul) == 1
     assert prefill_store(tok=257) == 1      # token stride not a multiple of 8 elements
     assert prefill_store(d=64) == 2
+
+
+def test_launch_flag_values_match_header():
+    """The binding's launch-flag values are the header's, and early K/V
+    requests without PDL are refused before any call."""
+    from paged_kv_continuous_gb300 import build
+    build.build()
+    from paged_kv_continuous_gb300 import ops
+    hdr = open(os.path.join(ROOT, "include", "pa.h")).read()
+    vals = {m.group(1): int(m.group(2)) for m in
+            re.finditer(r"#define (PA_LAUNCH_\w+) (\d+)u", hdr)}
+    assert vals == {"PA_LAUNCH_PDL": ops.PA_LAUNCH_PDL,
+                    "PA_LAUNCH_EARLY_KV": ops.PA_LAUNCH_EARLY_KV}
+    assert ops._decode_flags(False, False) == 0
+    assert ops._decode_flags(True, False) == ops.PA_LAUNCH_PDL
+    assert ops._decode_flags(True, True) == ops.PA_LAUNCH_PDL | ops.PA_LAUNCH_EARLY_KV
+    with pytest.raises(ops.PagedAttentionError):
+        ops._decode_flags(False, True)

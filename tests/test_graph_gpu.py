@@ -64,8 +64,10 @@ def close(got_bits, ref):
     return np.all(np.abs(got.astype(np.float64) - ref) <= 2e-3 + 1e-2 * np.abs(ref))
 
 
-@pytest.mark.parametrize("use_rope", [False, True])
-def test_graph_replay_matches_eager_then_oracle_next_step(mods, use_rope):
+@pytest.mark.parametrize("use_rope,fused", [(False, False), (True, False), (False, True)])
+def test_graph_replay_matches_eager_then_oracle_next_step(mods, use_rope, fused):
+    """fused: one pa_store_decode per layer (early K/V requests behind the
+    previous layer), which must give the bits of the two-call form."""
     ops, graph = mods
     w = synth.qwen_decode_b8()
     rng = np.random.default_rng(77)
@@ -95,8 +97,9 @@ def test_graph_replay_matches_eager_then_oracle_next_step(mods, use_rope):
                    num_splits=splits, workspace=ws)
     # the graph over fresh copies
     layers = [to_dev(h) for h in host]
-    g = graph.DecodeStepGraph(layers, bt, cl, sm, w.scale, num_splits=splits, **extra)
-    assert g.launches_per_replay() == 2 * L
+    g = graph.DecodeStepGraph(layers, bt, cl, sm, w.scale, num_splits=splits, fused=fused,
+                              **extra)
+    assert g.launches_per_replay() == (1 if fused else 2) * L
     g.replay()
     torch.cuda.synchronize()
     assert g.read_error_word() == 0
@@ -153,3 +156,10 @@ def test_graph_update_rejects_shape_change(mods):
         g.update(context_lens=to_dev_i32(np.ones(w.batch + 1, np.int32)))
     with pytest.raises(ops.PagedAttentionError):
         g.update(positions=to_dev_i32(np.zeros(w.batch, np.int32)))
+    cos_t, sin_t = synth.rope_tables(64)
+    with pytest.raises(ops.PagedAttentionError):
+        graph.DecodeStepGraph(layers, to_dev_i32(w.block_tables), to_dev_i32(w.context_lens),
+                              to_dev_i32(w.slot_mapping), w.scale,
+                              positions=to_dev_i32(w.positions),
+                              cos_table=torch.from_numpy(cos_t).cuda(),
+                              sin_table=torch.from_numpy(sin_t).cuda(), fused=True)
