@@ -321,9 +321,10 @@ PA_API int32_t pa_decode_default_splits(int32_t device, int32_t num_q_heads,
  *                  0 = pa_decode_default_splits.
  *   workspace      device buffer of workspace_bytes >=
  *                  pa_decode_workspace_size(S, num_q_heads, head_dim).
- *   flags          0 or PA_LAUNCH_PDL (then context_lens and block_tables
+ *   flags          0, PA_LAUNCH_PDL (then context_lens and block_tables
  *                  must not be written by the kernel launched just before
- *                  this call).
+ *                  this call) or PA_LAUNCH_PDL | PA_LAUNCH_EARLY_KV (then
+ *                  not k_cache / v_cache either).
  * Results do not depend on how sequences are laid out in the pool; with a
  * fixed num_splits they are deterministic run to run.
  */
