@@ -74,7 +74,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 8
+#define PA_ABI_VERSION 9
 
 #if defined(__GNUC__)
 #define PA_API __attribute__((visibility("default")))
@@ -105,8 +105,8 @@ typedef int32_t pa_status;
 
 /*
  * Launch flags (the `flags` argument of pa_store_kv, pa_store_kv_fp8,
- * pa_rope_store_kv, pa_decode, pa_store_decode, pa_decode_fp8,
- * pa_store_decode_fp8 and pa_decode_noalloc).  Any other bit returns
+ * pa_rope_store_kv, pa_decode, pa_store_decode, pa_rope_store_decode,
+ * pa_decode_fp8, pa_store_decode_fp8 and pa_decode_noalloc).  Any other bit returns
  * PA_ERR_INVALID_ARG.
  *
  * PA_LAUNCH_PDL: programmatic dependent launch.  The call's kernel may begin
@@ -361,6 +361,36 @@ PA_API pa_status pa_store_decode(void *out, int32_t out_dtype, const void *q, co
                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                  float scale, int32_t num_splits, void *workspace,
                                  size_t workspace_bytes, uint32_t flags, void *stream);
+
+/*
+ * pa_rope_store_decode -- pa_rope_store_kv, pa_store_kv and pa_decode of one
+ * decode step in one kernel (bf16 pools): the rotary embedding of
+ * pa_rope_store_kv (koas-w, "errors and solutions", fused_rope_and_cache_store_kernel)
+ * applied inside pa_store_decode.  Sequence b's new token sits at position
+ * positions[b]; its q rows (q + b * num_q_heads * head_dim, as for
+ * pa_decode) and its new K row are rotated with row positions[b] of
+ * cos_table / sin_table (float32 [max_position][head_dim / 2], 16-byte
+ * aligned), rotate-half pairs (i, i + head_dim / 2), with the same arithmetic
+ * and rounding as pa_rope_store_kv: the output equals, bit for bit,
+ * pa_rope_store_kv (q rotated into q_out, K rotated and stored with V)
+ * followed by pa_decode on q_out, with the same split count; the pools
+ * after the call equal those pa_rope_store_kv leaves.  q itself is not
+ * written.  new_k / new_v / slot_mapping as for pa_store_decode.  A position
+ * outside [0, max_position) sets PA_DEVERR_POSITION in the workspace error
+ * word; that sequence's q is rotated with row 0 and its new row is neither
+ * stored nor patched.  Returns PA_ERR_INVALID_ARG for a missing pointer,
+ * max_position < 1 or unaligned tables (before any device query); other
+ * arguments, the workspace and the flags as for pa_decode.
+ */
+PA_API pa_status pa_rope_store_decode(
+    void *out, int32_t out_dtype, const void *q, const void *new_k, const void *new_v,
+    int64_t new_k_tok_stride, int64_t new_v_tok_stride, const int32_t *positions,
+    const float *cos_table, const float *sin_table, int64_t max_position,
+    const int32_t *slot_mapping, void *k_cache, void *v_cache, int64_t num_blocks,
+    const int32_t *block_tables, int32_t block_table_stride, const int32_t *context_lens,
+    int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, float scale, int32_t num_splits, void *workspace,
+    size_t workspace_bytes, uint32_t flags, void *stream);
 
 /*
  * pa_store_decode_fp8 -- pa_store_decode over FP8 pools: each sequence's new

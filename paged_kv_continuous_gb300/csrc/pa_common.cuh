@@ -180,6 +180,31 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Rotate-half RoPE of 8 bf16 pairs: a holds dims d .. d + 7 of a head row, b
+// their partners d + 64 .. d + 71; c0 / c1 and s0 / s1 the cos and sin table
+// entries of dims d .. d + 7.  ra = a c - b s, rb = b c + a s, each element
+// one fused multiply-add over a rounded product, then one rounding to bf16.
+// The store kernel with RoPE and the fused decode step both rotate with it,
+// so their rotated rows are the same bits.
+__device__ __forceinline__ void rope_rotate8(const uint4 &a, const uint4 &b, const float4 &c0,
+                                             const float4 &c1, const float4 &s0,
+                                             const float4 &s1, uint4 &ra, uint4 &rb) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  uint32_t ow[4], pw[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float2 x1 = bf16x2_to_float2(aw[w]), x2 = bf16x2_to_float2(bw[w]);
+    const float c_lo = cs[2 * w], c_hi = cs[2 * w + 1];
+    const float s_lo = sn[2 * w], s_hi = sn[2 * w + 1];
+    ow[w] = float2_to_bf16x2(fmaf(x1.x, c_lo, -(x2.x * s_lo)), fmaf(x1.y, c_hi, -(x2.y * s_hi)));
+    pw[w] = float2_to_bf16x2(fmaf(x2.x, c_lo, x1.x * s_lo), fmaf(x2.y, c_hi, x1.y * s_hi));
+  }
+  ra = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+  rb = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -194,6 +194,10 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
   p.k_pool8 = r.fp8 ? static_cast<uint8_t *>(const_cast<void *>(r.k_cache)) : nullptr;
   p.v_pool8 = r.fp8 ? static_cast<uint8_t *>(const_cast<void *>(r.v_cache)) : nullptr;
   p.early_kv = (r.flags & PA_LAUNCH_EARLY_KV) != 0;
+  p.positions = r.positions;
+  p.cos_table = r.cos_table;
+  p.sin_table = r.sin_table;
+  p.max_position = r.max_position;
   cudaStream_t s = static_cast<cudaStream_t>(r.stream);
   if (clear_counters &&
       cudaMemsetAsync(p.counters, 0, (size_t)r.splits * sizeof(int32_t), s) != cudaSuccess)
@@ -207,6 +211,13 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
       case 2: e = launch_decode<2, true>(G, tk, tv, p, s, device, pdl); break;
       case 4: e = launch_decode<4, true>(G, tk, tv, p, s, device, pdl); break;
       default: e = launch_decode<8, true>(G, tk, tv, p, s, device, pdl); break;
+    }
+  } else if (r.positions) {
+    switch (r.num_kv_heads) {
+      case 1: e = launch_decode<1, false, true>(G, tk, tv, p, s, device, pdl); break;
+      case 2: e = launch_decode<2, false, true>(G, tk, tv, p, s, device, pdl); break;
+      case 4: e = launch_decode<4, false, true>(G, tk, tv, p, s, device, pdl); break;
+      default: e = launch_decode<8, false, true>(G, tk, tv, p, s, device, pdl); break;
     }
   } else {
     switch (r.num_kv_heads) {
@@ -311,6 +322,47 @@ extern "C" pa_status pa_store_decode(void *out, int32_t out_dtype, const void *q
   const pa_status st = check_decode_request(r, &device);
   if (st != PA_OK || batch == 0) return st;
   // the new rows are moved in 16-byte chunks
+  if (!aligned16(new_k) || !aligned16(new_v) || new_k_tok_stride < num_kv_heads * head_dim ||
+      new_v_tok_stride < num_kv_heads * head_dim || new_k_tok_stride % 8 ||
+      new_v_tok_stride % 8)
+    return PA_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < pa_decode_workspace_size(r.splits, num_q_heads, head_dim))
+    return PA_ERR_WORKSPACE;
+  return run_decode(r, workspace, static_cast<int32_t *>(workspace), device, false);
+}
+
+extern "C" pa_status pa_rope_store_decode(
+    void *out, int32_t out_dtype, const void *q, const void *new_k, const void *new_v,
+    int64_t new_k_tok_stride, int64_t new_v_tok_stride, const int32_t *positions,
+    const float *cos_table, const float *sin_table, int64_t max_position,
+    const int32_t *slot_mapping, void *k_cache, void *v_cache, int64_t num_blocks,
+    const int32_t *block_tables, int32_t block_table_stride, const int32_t *context_lens,
+    int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, float scale, int32_t num_splits, void *workspace,
+    size_t workspace_bytes, uint32_t flags, void *stream) {
+  using namespace pa;
+  DecodeRequest r{out, out_dtype, q, k_cache, v_cache, num_blocks, block_tables,
+                  block_table_stride, context_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                  block_size, scale, num_splits, 0, flags, stream};
+  r.new_k = new_k;
+  r.new_v = new_v;
+  r.new_k_tok = new_k_tok_stride;
+  r.new_v_tok = new_v_tok_stride;
+  r.slot_mapping = slot_mapping;
+  r.positions = positions;
+  r.cos_table = cos_table;
+  r.sin_table = sin_table;
+  r.max_position = max_position;
+  if (batch > 0 &&
+      (!new_k || !new_v || !slot_mapping || !positions || !cos_table || !sin_table))
+    return PA_ERR_INVALID_ARG;
+  // table rows are brought by bulk copies: 16-byte aligned bases
+  if (batch > 0 && (max_position < 1 || !aligned16(cos_table) || !aligned16(sin_table)))
+    return PA_ERR_INVALID_ARG;
+  int device = -1;
+  const pa_status st = check_decode_request(r, &device);
+  if (st != PA_OK || batch == 0) return st;
   if (!aligned16(new_k) || !aligned16(new_v) || new_k_tok_stride < num_kv_heads * head_dim ||
       new_v_tok_stride < num_kv_heads * head_dim || new_k_tok_stride % 8 ||
       new_v_tok_stride % 8)

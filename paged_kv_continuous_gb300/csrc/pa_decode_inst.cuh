@@ -1,7 +1,8 @@
-// Instantiates decode_kernel<G, PA_HKV, PA_F8> for G = 1..8 and the launcher
-// the host ABI dispatches to.  Included once per kv-head count and pool type
-// by pa_decode_h{1,2,4,8}.cu (bf16 pools) and pa_decode_f8_h{1,2,4,8}.cu
-// (FP8 pools) so that the instantiations compile in parallel.
+// Instantiates decode_kernel<G, PA_HKV, PA_F8, PA_ROPE> for G = 1..8 and the
+// launcher the host ABI dispatches to.  Included once per kv-head count and
+// variant by pa_decode_h{1,2,4,8}.cu (bf16 pools), pa_decode_f8_h{1,2,4,8}.cu
+// (FP8 pools) and pa_decode_rope_h{1,2,4,8}.cu (bf16 pools, rotary embedding
+// in the fused store) so that the instantiations compile in parallel.
 #include "pa_decode_kernel.cuh"
 
 #ifndef PA_HKV
@@ -10,6 +11,9 @@
 #ifndef PA_F8
 #define PA_F8 false
 #endif
+#ifndef PA_ROPE
+#define PA_ROPE false
+#endif
 
 namespace pa {
 
@@ -17,21 +21,22 @@ namespace {
 template <int G>
 cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                      cudaStream_t s, int device, bool pdl) {
-  using Sh = DecodeShape<G, PA_HKV, PA_F8>;
+  using Sh = DecodeShape<G, PA_HKV, PA_F8, PA_ROPE>;
   static bool configured[64] = {};
   if (device < 0 || device >= 64 || !configured[device]) {
     const cudaError_t e = cudaFuncSetAttribute(
-        decode_kernel<G, PA_HKV, PA_F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM);
+        decode_kernel<G, PA_HKV, PA_F8, PA_ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        Sh::SMEM);
     if (e != cudaSuccess) return e;
     if (device >= 0 && device < 64) configured[device] = true;
   }
-  return launch_kernel(decode_kernel<G, PA_HKV, PA_F8>, dim3(p.num_splits), dim3(kDecodeThreads),
-                       Sh::SMEM, s, pdl, tk, tv, p);
+  return launch_kernel(decode_kernel<G, PA_HKV, PA_F8, PA_ROPE>, dim3(p.num_splits),
+                       dim3(kDecodeThreads), Sh::SMEM, s, pdl, tk, tv, p);
 }
 }  // namespace
 
 template <>
-cudaError_t launch_decode<PA_HKV, PA_F8>(int G, const CUtensorMap &tk, const CUtensorMap &tv,
+cudaError_t launch_decode<PA_HKV, PA_F8, PA_ROPE>(int G, const CUtensorMap &tk, const CUtensorMap &tv,
                                   const DecodeParams &p, cudaStream_t s, int device,
                                   bool pdl) {
   switch (G) {

@@ -47,6 +47,12 @@ struct DecodeRequest {
   const void *new_v = nullptr;
   int64_t new_k_tok = 0, new_v_tok = 0;
   const int32_t *slot_mapping = nullptr;
+  // rotary embedding of q and the new K rows inside the fused store (null:
+  // none): float32 tables [max_position][head_dim / 2]
+  const int32_t *positions = nullptr;
+  const float *cos_table = nullptr;
+  const float *sin_table = nullptr;
+  int64_t max_position = 0;
 };
 
 // Host checks shared by both decode entry points; resolves r.splits.

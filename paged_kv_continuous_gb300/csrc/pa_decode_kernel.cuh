@@ -97,6 +97,14 @@ struct DecodeParams {
   // previous kernel in the stream completes (the caller guarantees that
   // kernel does not write the pools).
   int early_kv;
+  // Rotary embedding inside the fused store (ROPE kernels): sequence b's new
+  // token sits at position positions[b]; its q rows and its new K row are
+  // rotated with row positions[b] of the float32 tables [max_position][64]
+  // before they are used or stored.
+  const int32_t *positions;
+  const float *cos_table;
+  const float *sin_table;
+  long long max_position;
 };
 
 // Waits for the previous kernel in the stream to complete, then signals that
@@ -121,7 +129,7 @@ __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / 
 // F8: the pools hold E4M3 codes (one byte per element) with per-kv-head
 // scales; K pages keep the token-major layout, V pages are dim-major inside a
 // block ([Hkv][128 dims][16 tokens]).
-template <int G, int HKV, bool F8 = false>
+template <int G, int HKV, bool F8 = false, bool ROPE = false>
 struct DecodeShape {
   static constexpr int HQ = G * HKV;
   static constexpr int CW = kDecodeConsumerWarps;
@@ -136,7 +144,9 @@ struct DecodeShape {
   static constexpr int BOX_BYTES = HB * kTileBytes;
   static constexpr int KV_BYTES = HKV * (F8 ? 1 : 2) * kTileBytes;  // one block of K (or V)
   static constexpr int Q_BYTES = HQ * kHeadDim * 2;
-  static constexpr int STAGE_BYTES = align_up(2 * KV_BYTES + Q_BYTES, 1024);
+  // ROPE: the cos and sin rows of the sequence's position follow the q rows
+  static constexpr int ROPE_BYTES = ROPE ? 2 * (kHeadDim / 2) * 4 : 0;
+  static constexpr int STAGE_BYTES = align_up(2 * KV_BYTES + Q_BYTES + ROPE_BYTES, 1024);
   // per consumer warp and query head of its group: o[128], m, l (rows of
   // 132 floats keep the o vectors 16-byte aligned)
   static constexpr int RED_FLOATS_PER_HEAD = kHeadDim + 4;
@@ -174,6 +184,7 @@ struct DecodeShape {
   // combine weights (NPH per query head) and lse live in the merge scratch
   static_assert((NPH + 1) * HQ <= MERGE_FLOATS, "combine weights do not fit");
   static_assert(CW * G * 4 <= EWW_BYTES, "epilogue warp weights do not fit");
+  static_assert(!(F8 && ROPE), "rotary embedding is fused for bf16 pools only");
 };
 
 // A piece handed to the epilogue warp (one per red buffer).
@@ -641,11 +652,11 @@ __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, 
   return true;
 }
 
-template <int G, int HKV, bool F8 = false>
+template <int G, int HKV, bool F8 = false, bool ROPE = false>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
-  using S = DecodeShape<G, HKV, F8>;
+  using S = DecodeShape<G, HKV, F8, ROPE>;
   extern __shared__ uint8_t smem_raw[];
   // realign to 1024 bytes: the 128-byte swizzle pattern repeats every 1 KB
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -875,16 +886,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const bool pre = i < n_early;  // K/V already requested and counted
         if (lane == 0) {
           mbar_arrive_expect_tx(bar, (ok && !pre ? 2u * S::KV_BYTES : 0u) +
-                                         (q_i ? S::Q_BYTES : 0u));
+                                         (q_i ? S::Q_BYTES + S::ROPE_BYTES : 0u));
           // a context longer than the table row (caller error) or an entry
           // outside the pool: reported, not read
           if (!ok) report(p.err, row_i ? PA_DEVERR_BLOCK_INDEX : PA_DEVERR_SHAPE);
         }
         __syncwarp();
         if (!pre) issue_kv_stage(st, ph_i, false);
-        if (q_i)
+        if (q_i) {
           bulk_load_elect(dst + 2 * S::KV_BYTES, p.q + (long long)b_i * S::HQ * kHeadDim,
                           S::Q_BYTES, bar, pol_q);
+          if constexpr (ROPE) {
+            // the cos and sin rows of the new token's position (row 0 for a
+            // position outside the tables: reported, and the new row is
+            // then neither stored nor patched)
+            long long pos = __ldg(p.positions + b_i);
+            if (pos < 0 || pos >= p.max_position) {
+              if (lane == 0) report(p.err, PA_DEVERR_POSITION);
+              pos = 0;
+            }
+            const uint32_t rd = dst + 2 * S::KV_BYTES + S::Q_BYTES;
+            bulk_load_elect(rd, p.cos_table + pos * (kHeadDim / 2), S::ROPE_BYTES / 2, bar, pol_q);
+            bulk_load_elect(rd + S::ROPE_BYTES / 2, p.sin_table + pos * (kHeadDim / 2),
+                            S::ROPE_BYTES / 2, bar, pol_q);
+          }
+        }
       }
       gb += count;
     }
@@ -1185,6 +1211,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               qf[ks][0] = x0;
               qf[ks][1] = x1;
             }
+            if constexpr (ROPE) {
+              // rotate-half: dims d < 64 (k-steps 0..3) pair with d + 64
+              // (k-steps 4..7) in the same fragment registers; the same
+              // products and one bf16 rounding as pa_rope_store_kv
+              const uint32_t crow = sbase + 2 * S::KV_BYTES + S::Q_BYTES;
+              const uint32_t srow = crow + S::ROPE_BYTES / 2;
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const int d = 16 * ks + 8 * h + 2 * qd;
+                  const float2 c2 = make_float2(__uint_as_float(lds32(crow + d * 4)),
+                                                __uint_as_float(lds32(crow + d * 4 + 4)));
+                  const float2 s2 = make_float2(__uint_as_float(lds32(srow + d * 4)),
+                                                __uint_as_float(lds32(srow + d * 4 + 4)));
+                  const float2 x1 = bf16x2_to_float2(qf[ks][h]);
+                  const float2 x2 = bf16x2_to_float2(qf[ks + 4][h]);
+                  if (gid < G) {
+                    qf[ks][h] = float2_to_bf16x2(fmaf(x1.x, c2.x, -(x2.x * s2.x)),
+                                                 fmaf(x1.y, c2.y, -(x2.y * s2.y)));
+                    qf[ks + 4][h] = float2_to_bf16x2(fmaf(x2.x, c2.x, x1.x * s2.x),
+                                                     fmaf(x2.y, c2.y, x1.y * s2.y));
+                  }
+                }
+              }
+            }
           }
         }
         const int valid = min(kBlockSize, ctx - j * kBlockSize);  // keys of this block (>= 1)
@@ -1209,15 +1261,45 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 // the slot must be the new position's, and inside the pool
                 // (a table entry outside it would make both agree on a slot
                 // past the pool)
+                long long pos = 0;
+                if constexpr (ROPE) pos = __ldg(p.positions + b);
                 if (slot != want || slot >= p.num_blocks * kBlockSize) {
                   if (lane == 0) report(p.err, PA_DEVERR_SLOT_INDEX);
+                } else if (ROPE && (pos < 0 || pos >= p.max_position)) {
+                  // reported by the producer: the row is neither stored nor patched
                 } else {
                   const int c = lane & 15;
                   const bool is_v = lane >= 16;
                   const uint16_t *src =
                       (is_v ? p.new_v + b * p.new_v_tok : p.new_k + b * p.new_k_tok) +
                       g * kHeadDim + c * 8;
-                  const uint4 val = *reinterpret_cast<const uint4 *>(src);
+                  uint4 val = *reinterpret_cast<const uint4 *>(src);
+                  if constexpr (ROPE) {
+                    // the K row rotated at its position: chunk c pairs with
+                    // chunk c ^ 8 (dims +- 64), held by lane ^ 8
+                    uint4 pv;
+                    pv.x = __shfl_xor_sync(0xffffffffu, val.x, 8);
+                    pv.y = __shfl_xor_sync(0xffffffffu, val.y, 8);
+                    pv.z = __shfl_xor_sync(0xffffffffu, val.z, 8);
+                    pv.w = __shfl_xor_sync(0xffffffffu, val.w, 8);
+                    if (!is_v) {
+                      const long long t0 = pos * (kHeadDim / 2) + (c & 7) * 8;
+                      const float4 c0 = __ldg(reinterpret_cast<const float4 *>(p.cos_table + t0));
+                      const float4 c1 =
+                          __ldg(reinterpret_cast<const float4 *>(p.cos_table + t0 + 4));
+                      const float4 s0 = __ldg(reinterpret_cast<const float4 *>(p.sin_table + t0));
+                      const float4 s1 =
+                          __ldg(reinterpret_cast<const float4 *>(p.sin_table + t0 + 4));
+                      uint4 ra, rb;
+                      if (c < 8) {
+                        rope_rotate8(val, pv, c0, c1, s0, s1, ra, rb);
+                        val = ra;
+                      } else {
+                        rope_rotate8(pv, val, c0, c1, s0, s1, ra, rb);
+                        val = rb;
+                      }
+                    }
+                  }
                   uint16_t *dstg = (is_v ? p.v_pool16 : p.k_pool) +
                                    (slot * HKV + g) * kHeadDim + c * 8;
                   *reinterpret_cast<uint4 *>(dstg) = val;
@@ -1716,9 +1798,9 @@ consumers_done:
   }
 }
 
-// Launches decode_kernel<G, HKV, F8> for one G (defined per HKV and F8 in
-// pa_decode_h*.cu and pa_decode_f8_h*.cu).
-template <int HKV, bool F8>
+// Launches decode_kernel<G, HKV, F8, ROPE> for one G (defined per HKV, F8
+// and ROPE in pa_decode_h*.cu, pa_decode_f8_h*.cu and pa_decode_rope_h*.cu).
+template <int HKV, bool F8, bool ROPE = false>
 cudaError_t launch_decode(int G, const CUtensorMap &tk, const CUtensorMap &tv,
                           const DecodeParams &p, cudaStream_t s, int device, bool pdl);
 

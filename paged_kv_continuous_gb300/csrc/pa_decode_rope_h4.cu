@@ -1,0 +1,5 @@
+// decode_kernel instantiations for bf16 pools with rotary embedding in the
+// fused store, 4 kv head(s) per sequence.
+#define PA_HKV 4
+#define PA_ROPE true
+#include "pa_decode_inst.cuh"

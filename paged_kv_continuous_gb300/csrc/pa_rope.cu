@@ -22,26 +22,6 @@ namespace pa {
 
 namespace {
 
-// rotate 8 bf16 pairs (a = first-half chunk, b = second-half chunk)
-__device__ __forceinline__ void rope8(const uint4 &a, const uint4 &b, const float4 &c0,
-                                      const float4 &c1, const float4 &s0, const float4 &s1,
-                                      uint4 &ra, uint4 &rb) {
-  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-  const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-  uint32_t ow[4], pw[4];
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const float2 x1 = bf16x2_to_float2(aw[w]), x2 = bf16x2_to_float2(bw[w]);
-    const float c_lo = cs[2 * w], c_hi = cs[2 * w + 1];
-    const float s_lo = sn[2 * w], s_hi = sn[2 * w + 1];
-    ow[w] = float2_to_bf16x2(fmaf(x1.x, c_lo, -(x2.x * s_lo)), fmaf(x1.y, c_hi, -(x2.y * s_hi)));
-    pw[w] = float2_to_bf16x2(fmaf(x2.x, c_lo, x1.x * s_lo), fmaf(x2.y, c_hi, x1.y * s_hi));
-  }
-  ra = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-  rb = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-}
-
 template <bool kVec>
 __device__ __forceinline__ uint4 load8(const uint16_t *p) {
   if constexpr (kVec) {
@@ -117,7 +97,7 @@ __global__ void __launch_bounds__(256) rope_store_kernel(const RopeParams p) {
     const uint4 a = load8<kVec>(src + d0), b = load8<kVec>(src + kHalf + d0);
     const float *cr = p.cos_t + pos * kHalf + d0, *sr = p.sin_t + pos * kHalf + d0;
     uint4 ra, rb;
-    rope8(a, b, __ldg(reinterpret_cast<const float4 *>(cr)),
+    rope_rotate8(a, b, __ldg(reinterpret_cast<const float4 *>(cr)),
           __ldg(reinterpret_cast<const float4 *>(cr + 4)),
           __ldg(reinterpret_cast<const float4 *>(sr)),
           __ldg(reinterpret_cast<const float4 *>(sr + 4)), ra, rb);
@@ -139,7 +119,7 @@ __global__ void __launch_bounds__(256) rope_store_kernel(const RopeParams p) {
     const uint4 a = load8<kVec>(src + d0), b = load8<kVec>(src + kHalf + d0);
     const float *cr = p.cos_t + pos * kHalf + d0, *sr = p.sin_t + pos * kHalf + d0;
     uint4 ra, rb;
-    rope8(a, b, __ldg(reinterpret_cast<const float4 *>(cr)),
+    rope_rotate8(a, b, __ldg(reinterpret_cast<const float4 *>(cr)),
           __ldg(reinterpret_cast<const float4 *>(cr + 4)),
           __ldg(reinterpret_cast<const float4 *>(sr)),
           __ldg(reinterpret_cast<const float4 *>(sr + 4)), ra, rb);

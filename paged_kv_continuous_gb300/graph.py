@@ -10,10 +10,10 @@ submitted at once.
 decode step -- ``pa_rope_store_kv`` (or ``pa_store_kv`` when no rotary
 tables are given) and then ``pa_decode`` -- both launched with
 ``PA_LAUNCH_PDL``, so each kernel's start-up overlaps the tail of the one
-before.  With ``fused=True`` (no rotary tables) a layer is one call,
-``pa_store_decode``, which also requests its first K/V pages early
-(``PA_LAUNCH_EARLY_KV``) whenever the call before it is another layer's, on
-other pools.  This module only records calls into the graph; every step of
+before.  With ``fused=True`` a layer is one call, ``pa_store_decode`` (or
+``pa_rope_store_decode`` with rotary tables, which leaves q as it is), which
+also requests its first K/V pages early (``PA_LAUNCH_EARLY_KV``) whenever
+the call before it is another layer's, on other pools.  This module only records calls into the graph; every step of
 the computation runs in the library's kernels.
 
 Static state (fixed at capture): the batch size, the block-table width, the
@@ -21,8 +21,9 @@ per-layer tensors (their addresses are baked into the graph), the split
 count and the decode workspace.  Values the caller changes between replays,
 in place: the index buffers, through :meth:`DecodeStepGraph.update`, and
 each layer's new q / k / v rows (written into the layer tensors given at
-construction; with rotary tables q is rotated in place, so it must be
-refilled before every replay).  The decode kernel partitions its work from
+construction; with rotary tables and two calls per layer q is rotated in
+place, so it must be refilled before every replay; the fused call leaves q
+as it is).  The decode kernel partitions its work from
 ``context_lens`` on the device, so a replay follows new lengths without a
 new capture.
 """
@@ -43,9 +44,9 @@ class DecodeStepGraph:
     int32 [B]: the initial values of the static index buffers (copied).
     positions int32 [B] with cos_table / sin_table float32 [max_position,
     D/2]: rotary embedding of q and k fused into the store.
-    fused: one pa_store_decode per layer instead of a store and a decode
-    (without rotary tables only); slot_mapping[b] must then be the slot of
-    position context_lens[b] - 1 under the block table.
+    fused: one pa_store_decode (pa_rope_store_decode with rotary tables)
+    per layer instead of a store and a decode; slot_mapping[b] must then be
+    the slot of position context_lens[b] - 1 under the block table.
     """
 
     def __init__(self, layers, block_tables, context_lens, slot_mapping, scale,
@@ -55,8 +56,6 @@ class DecodeStepGraph:
             raise ops.PagedAttentionError("DecodeStepGraph needs at least one layer")
         if (cos_table is None) != (positions is None) or (cos_table is None) != (sin_table is None):
             raise ops.PagedAttentionError("positions, cos_table and sin_table go together")
-        if fused and cos_table is not None:
-            raise ops.PagedAttentionError("fused=True takes no rotary tables")
         self.fused = bool(fused)
         dev = layers[0]["q"].device if device is None else torch.device(device)
         self.layers = layers
@@ -84,10 +83,17 @@ class DecodeStepGraph:
             # early K/V requests only behind another layer's call on other pools
             early = prev is not None and prev["k_cache"].data_ptr() != x["k_cache"].data_ptr() \
                 and prev["v_cache"].data_ptr() != x["v_cache"].data_ptr()
-            ops.store_decode(x["q"], x["k"], x["v"], x["k_cache"], x["v_cache"],
-                             self.slot_mapping, self.block_tables, self.context_lens, self.scale,
-                             out=x["out"], num_splits=self.num_splits, workspace=self.workspace,
-                             pdl=True, early_kv=early)
+            if self.rope:
+                ops.rope_store_decode(x["q"], x["k"], x["v"], x["k_cache"], x["v_cache"],
+                                      self.slot_mapping, self.block_tables, self.context_lens,
+                                      self.scale, self.positions, self.cos_table, self.sin_table,
+                                      out=x["out"], num_splits=self.num_splits,
+                                      workspace=self.workspace, pdl=True, early_kv=early)
+            else:
+                ops.store_decode(x["q"], x["k"], x["v"], x["k_cache"], x["v_cache"],
+                                 self.slot_mapping, self.block_tables, self.context_lens,
+                                 self.scale, out=x["out"], num_splits=self.num_splits,
+                                 workspace=self.workspace, pdl=True, early_kv=early)
             return
         if self.rope:
             ops.rope_store_kv(x["q"], x["k"], x["v"], self.positions, self.cos_table,

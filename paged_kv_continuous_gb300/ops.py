@@ -33,6 +33,7 @@ EXPORTED = (
     "pa_decode_default_splits", "pa_decode", "pa_decode_merge", "pa_prefill_varlen",
     "pa_decode_noalloc", "pa_rope_store_kv", "pa_store_kv_fp8", "pa_decode_fp8",
     "pa_store_decode", "pa_store_decode_fp8", "pa_prefill_store_varlen",
+    "pa_rope_store_decode",
 )
 
 
@@ -67,6 +68,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_store_decode.restype = i32
     lib.pa_store_decode.argtypes = [P, i32, P, P, P, i64, i64, P, P, P, i64, P, i32, P, i32,
                                     i32, i32, i32, i32, f32, i32, P, sz, u32, P]
+    lib.pa_rope_store_decode.restype = i32
+    lib.pa_rope_store_decode.argtypes = [P, i32, P, P, P, i64, i64, P, P, P, i64, P, P, P, i64,
+                                         P, i32, P, i32, i32, i32, i32, i32, f32, i32, P, sz,
+                                         u32, P]
     lib.pa_store_decode_fp8.restype = i32
     lib.pa_store_decode_fp8.argtypes = [P, i32, P, P, P, i64, i64, P, P, P, P, P, i64, P, i32,
                                         P, i32, i32, i32, i32, i32, f32, i32, P, sz, u32, P]
@@ -298,6 +303,57 @@ def store_decode(q, new_k, new_v, k_cache, v_cache, slot_mapping, block_tables, 
                                workspace.numel() * workspace.element_size(),
                                _decode_flags(pdl, early_kv), _stream(stream)),
            "pa_store_decode")
+    return out
+
+
+def rope_store_decode(q, new_k, new_v, k_cache, v_cache, slot_mapping, block_tables,
+                      context_lens, scale, positions, cos_table, sin_table, out=None,
+                      out_dtype=torch.bfloat16, num_splits=0, workspace=None, stream=None,
+                      pdl=False, early_kv=False):
+    """pa_rope_store_decode: store_decode with the rotary embedding of q and
+    the new K rows at positions (int32 [B]) from cos_table / sin_table
+    (float32 [max_position, D/2]).  q is not written.  Returns out."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(new_k, torch.bfloat16, "new_k", 3)
+    _need(new_v, torch.bfloat16, "new_v", 3)
+    _need(k_cache, torch.bfloat16, "k_cache", 4)
+    _need(v_cache, torch.bfloat16, "v_cache", 4)
+    _need(slot_mapping, torch.int32, "slot_mapping", 1)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    _need(positions, torch.int32, "positions", 1)
+    _need(cos_table, torch.float32, "cos_table", 2)
+    _need(sin_table, torch.float32, "sin_table", 2)
+    if not q.is_contiguous():
+        raise PagedAttentionError("q must be contiguous")
+    for t, n in ((new_k, "new_k"), (new_v, "new_v")):
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise PagedAttentionError(f"{n} needs contiguous heads")
+    if block_tables.stride(1) != 1:
+        raise PagedAttentionError("block_tables rows must be contiguous")
+    B, Hq, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    if tuple(new_k.shape) != (B, Hkv, D) or new_v.shape != new_k.shape or \
+            slot_mapping.shape[0] != B or positions.shape[0] != B:
+        raise PagedAttentionError(
+            "new_k / new_v / slot_mapping / positions need one row per sequence")
+    if cos_table.shape != sin_table.shape or cos_table.shape[1] != D // 2 or \
+            not cos_table.is_contiguous() or not sin_table.is_contiguous():
+        raise PagedAttentionError("cos_table / sin_table must be contiguous [max_position, D/2]")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(Hq, Hkv, num_splits, D, q.device)
+    _check(lib.pa_rope_store_decode(_ptr(out), _out_code(out.dtype), _ptr(q), _ptr(new_k),
+                                    _ptr(new_v), new_k.stride(0), new_v.stride(0),
+                                    _ptr(positions), _ptr(cos_table), _ptr(sin_table),
+                                    cos_table.shape[0], _ptr(slot_mapping), _ptr(k_cache),
+                                    _ptr(v_cache), NB, _ptr(block_tables),
+                                    block_tables.stride(0), _ptr(context_lens), B, Hq, Hkv, D, bs,
+                                    float(scale), int(num_splits), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _decode_flags(pdl, early_kv), _stream(stream)),
+           "pa_rope_store_decode")
     return out
 
 

@@ -44,7 +44,7 @@ def test_binding_names_match_header():
 
 def test_version_and_status_strings(lib):
     lib.pa_abi_version.restype = ctypes.c_int32
-    assert lib.pa_abi_version() == 8
+    assert lib.pa_abi_version() == 9
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [ctypes.c_int32]
     assert lib.pa_status_string(0) == b"ok"
@@ -213,3 +213,32 @@ def test_launch_flag_values_match_header():
     assert ops._decode_flags(True, True) == ops.PA_LAUNCH_PDL | ops.PA_LAUNCH_EARLY_KV
     with pytest.raises(ops.PagedAttentionError):
         ops._decode_flags(False, True)
+
+
+def test_rope_store_decode_argument_checks(lib):
+    """pa_rope_store_decode: empty batch is a no-op; a missing position or
+    table pointer, max_position < 1 and unaligned tables are invalid before
+    any device query; other shapes unsupported; store-only flags rejected."""
+    P, i32, i64, u32, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                 ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t)
+    nul = None
+    fake = ctypes.c_void_p(0x10000)    # never dereferenced: every case fails before a launch
+    odd = ctypes.c_void_p(0x10004)     # not 16-byte aligned
+    fn = _bind(lib, "pa_rope_store_decode",
+               [P, i32, P, P, P, i64, i64, P, P, P, i64, P, P, P, i64, P, i32, P, i32, i32, i32,
+                i32, i32, f32, i32, P, sz, u32, P])
+
+    def call(batch=4, pos=fake, cos=fake, sin=fake, maxp=64, d=128, hkv=2, flags=0):
+        return fn(fake, 0, fake, fake, fake, 256, 256, pos, cos, sin, maxp, fake, fake, fake, 64,
+                  fake, 8, fake, batch, 12, hkv, d, 16, 0.1, 0, nul, 0, flags, nul)
+    assert call(batch=0, pos=nul, cos=nul, sin=nul) == 0
+    assert call(pos=nul) == 1
+    assert call(cos=nul) == 1
+    assert call(sin=nul) == 1
+    assert call(maxp=0) == 1
+    assert call(cos=odd) == 1
+    assert call(sin=odd) == 1
+    assert call(d=64) == 2
+    assert call(hkv=3) == 2
+    assert call(flags=2) == 1
+    assert call(flags=3, d=64) == 2

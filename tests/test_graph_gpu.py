@@ -64,7 +64,8 @@ def close(got_bits, ref):
     return np.all(np.abs(got.astype(np.float64) - ref) <= 2e-3 + 1e-2 * np.abs(ref))
 
 
-@pytest.mark.parametrize("use_rope,fused", [(False, False), (True, False), (False, True)])
+@pytest.mark.parametrize("use_rope,fused", [(False, False), (True, False), (False, True),
+                                            (True, True)])
 def test_graph_replay_matches_eager_then_oracle_next_step(mods, use_rope, fused):
     """fused: one pa_store_decode per layer (early K/V requests behind the
     previous layer), which must give the bits of the two-call form."""
@@ -156,10 +157,3 @@ def test_graph_update_rejects_shape_change(mods):
         g.update(context_lens=to_dev_i32(np.ones(w.batch + 1, np.int32)))
     with pytest.raises(ops.PagedAttentionError):
         g.update(positions=to_dev_i32(np.zeros(w.batch, np.int32)))
-    cos_t, sin_t = synth.rope_tables(64)
-    with pytest.raises(ops.PagedAttentionError):
-        graph.DecodeStepGraph(layers, to_dev_i32(w.block_tables), to_dev_i32(w.context_lens),
-                              to_dev_i32(w.slot_mapping), w.scale,
-                              positions=to_dev_i32(w.positions),
-                              cos_table=torch.from_numpy(cos_t).cuda(),
-                              sin_table=torch.from_numpy(sin_t).cuda(), fused=True)
