@@ -663,6 +663,20 @@ def run_ours(args):
         ops.store_decode(x["q"], x["nk"], x["nv"], x["kc"], x["vc"], slots, tables, ctx,
                          w.scale, out=x["out"], num_splits=splits, workspace=ws, pdl=True)
     pdl_only_ms = time_graph(pdl_only, 4 * L)
+    # the same step with rotary embedding of q and the new K rows inside the
+    # kernel (pa_rope_store_decode), positions = context_lens - 1
+    cos_np, sin_np = synth.rope_tables(int(w.context_lens.max()) + 1)
+    cos_d, sin_d = torch.from_numpy(cos_np).to(dev), torch.from_numpy(sin_np).to(dev)
+    pos_d = torch.from_numpy(np.ascontiguousarray(w.positions, np.int32)).to(dev)
+    st_r = {"l": 0}
+
+    def rope_step():
+        x = layers[st_r["l"] % L]
+        st_r["l"] += 1
+        ops.rope_store_decode(x["q"], x["nk"], x["nv"], x["kc"], x["vc"], slots, tables, ctx,
+                              w.scale, pos_d, cos_d, sin_d, out=x["out"], num_splits=splits,
+                              workspace=ws, pdl=True, early_kv=early)
+    rope_ms = time_graph(rope_step, 4 * L)
 
     ms_per_step = elapsed_s * 1e3 / args.steps
     dec_bytes = decode_alg_bytes(w.context_lens, Hq, Hkv, D)
@@ -797,6 +811,10 @@ def run_ours(args):
         "pdl_only_step": {"us_per_step": pdl_only_ms * 1e3,
                           "GB_per_s": step_bytes / pdl_only_ms / 1e6,
                           "step": "pa_store_decode with PA_LAUNCH_PDL only"},
+        "rope_step": {"us_per_step": rope_ms * 1e3,
+                      "GB_per_s": (step_bytes + B * D * 4) / rope_ms / 1e6,
+                      "step": "pa_rope_store_decode (RoPE of q and the new K rows, store, "
+                              "decode: one kernel); bytes add each sequence's cos and sin rows"},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
