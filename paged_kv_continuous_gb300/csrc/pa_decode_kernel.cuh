@@ -46,14 +46,20 @@
 // swizzled tiles, V fragments from ldmatrix.trans, P^T from movmatrix.trans
 // of the score fragment.
 //
-// Two variants share this code.  Fused store (pa_store_decode*): the CTA
-// that stages a sequence's last block patches the new token's K/V rows into
-// its tiles and writes them to the pool, so a decode step is one launch.
+// Variants share this code.  Fused store (pa_store_decode*): the CTA that
+// stages a sequence's last block patches the new token's K/V rows into its
+// tiles and writes them to the pool, so a decode step is one launch.
+// Rotary embedding (ROPE, pa_rope_store_decode, with the fused store): the
+// cos and sin rows of each sequence's position travel with its q rows, the
+// consumers rotate their q fragments in registers and the patch rotates the
+// new K row, with the arithmetic of pa_rope_store_kv (rope_rotate8).
 // FP8 pools (F8): E4M3 codes with per-kv-head scales; K pages keep the
 // token-major layout, V pages are dim-major inside a block and come in one
 // bulk copy; codes widen exactly to f16 and the MMAs run in f16, with a
 // token order of the score rows that makes every V operand register one
-// 32-bit load (see the F8 branches).
+// 32-bit load (see the F8 branches).  Early K/V requests (p.early_kv, a
+// launch flag): the producers issue the first ring round's pages before the
+// wait for the previous kernel.
 #pragma once
 
 #include <cuda.h>
