@@ -479,10 +479,16 @@ def cpu_baseline_oracle(w, kc, vc, seconds=10.0):
         n += 1
     dt = (time.perf_counter() - t0) / n
     nbytes = decode_alg_bytes(w.context_lens, w.num_q_heads, w.num_kv_heads)
+    # the same call on one thread, once
+    t1 = time.perf_counter()
+    oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale, num_threads=1)
+    dt1 = time.perf_counter() - t1
     return ref, {"value": nbytes / dt / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
                  "sample": f"full cb_decode_b64 decode (64 sequences, "
                            f"{int(w.context_lens.sum())} keys), {n} call(s), "
-                           f"{dt * 1e3:.1f} ms per call"}
+                           f"{dt * 1e3:.1f} ms per call",
+                 "single_thread": {"value": nbytes / dt1 / 1e9, "unit": UNIT, "cores": 1,
+                                   "ms_per_call": dt1 * 1e3}}
 
 
 def run_ours(args):

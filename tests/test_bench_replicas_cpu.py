@@ -63,3 +63,22 @@ def test_reference_arm_nonzero_rank_exits_without_work():
                         "--gpus", "2", "--steps", "1", "--warmup", "0"],
                        env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_cpu_baseline_reports_all_cores_and_one_thread():
+    """The oracle leg of the bench times the full decode on every host core
+    and once on one thread; both figures are positive and the multi-thread
+    result is the oracle's decode of the same inputs."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import oracle
+    from paged_kv_continuous_gb300 import synth
+    w = synth.tiny_decode()
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.store_kv(w.new_k, w.new_v, kc, vc, w.slot_mapping)
+    ref, cpu = bench.cpu_baseline_oracle(w, kc, vc, seconds=0.05)
+    assert cpu["kind"] == "oracle" and cpu["value"] > 0 and cpu["cores"] >= 1
+    assert cpu["single_thread"]["cores"] == 1 and cpu["single_thread"]["value"] > 0
+    assert np.array_equal(ref, oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens,
+                                             w.scale))
