@@ -50,3 +50,47 @@ def test_pins_reject_mutant(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins accepted mutant {name}:\n{r.stdout[-2000:]}"
+
+
+# The FP8 functions of the oracle are NumPy code: a mutant is the function
+# rebuilt from its own source with one change, put in place of the original
+# for the duration of the test (monkeypatch restores it); the FP8 pins then
+# run in this process and at least one must fail.
+PY_MUTANTS = {
+    "e4m3_subnormal_scale": ("e4m3_values", "sign * m * 2.0 ** -9", "sign * m * 2.0 ** -10"),
+    "e4m3_exponent_bias": ("e4m3_values", "2.0 ** (e - 7)", "2.0 ** (e - 8)"),
+    "e4m3_ties_away_from_zero": ("e4m3_encode", "np.where(lo % 2 == 0, lo, hi)", "hi"),
+    "fp8_scale_multiplied": ("quantize_fp8", "y = xf / np.asarray(scale",
+                             "y = xf * np.asarray(scale"),
+    "fp8_v_widened_with_k_scale": ("dequantize_pools_fp8",
+                                   "vf = vals[v_pool] * np.asarray(v_scale",
+                                   "vf = vals[v_pool] * np.asarray(k_scale"),
+    "fp8_k_scale_of_other_head": ("dequantize_pools_fp8",
+                                  "np.asarray(k_scale, np.float32).astype(np.float64)[None",
+                                  "np.asarray(k_scale, np.float32).astype(np.float64)[::-1][None"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_fp8_pins_reject_mutant(name, monkeypatch):
+    import inspect
+    import textwrap
+    sys.path.insert(0, ROOT)
+    import oracle
+    from tests import test_oracle_pins as pins
+    fname, old, new = PY_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(getattr(oracle, fname)))
+    assert src.count(old) == 1, f"mutation site for {name} not found"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, fname, ns[fname])
+    failed = []
+    for test in (pins.test_e4m3_values_closed_forms_and_library,
+                 pins.test_e4m3_encode_round_trip_ties_and_saturation,
+                 pins.test_store_kv_fp8_layout_and_quantisation,
+                 pins.test_decode_fp8_equals_bf16_decode_on_exact_values):
+        try:
+            test()
+        except AssertionError:
+            failed.append(test.__name__)
+    assert failed, f"the FP8 pins accepted mutant {name}"

@@ -625,7 +625,16 @@ def test_decode_fp8_equals_bf16_decode_on_exact_values():
     finite = np.array([c for c in range(256) if not np.isnan(v[c])], np.uint8)
     kp = rng.choice(finite, size=(NB, bs, Hkv, D)).astype(np.uint8)
     vp = rng.choice(finite, size=(NB, Hkv, D, bs)).astype(np.uint8)
-    kf, vf = oracle.dequantize_pools_fp8(kp, vp, ks, vs)
+    # the widened pools written out from the definition, head by head and row
+    # by row (value of the code times its own kv head's scale; V dim-major)
+    kf = np.empty((NB, bs, Hkv, D))
+    vf = np.empty((NB, bs, Hkv, D))
+    for h in range(Hkv):
+        kf[:, :, h, :] = v[kp[:, :, h, :]] * float(ks[h])
+        for r in range(bs):
+            vf[:, r, h, :] = v[vp[:, h, :, r]] * float(vs[h])
+    got_k, got_v = oracle.dequantize_pools_fp8(kp, vp, ks, vs)
+    assert np.array_equal(got_k, kf) and np.array_equal(got_v, vf)
     kb, vb = bf16_bits(kf.astype(np.float32)), bf16_bits(vf.astype(np.float32))
     assert np.array_equal(bf16_to_f64(kb), kf) and np.array_equal(bf16_to_f64(vb), vf)
     q = normal_bits(rng, (len(ctx), Hq, D))
