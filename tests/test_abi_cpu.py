@@ -242,3 +242,21 @@ def test_rope_store_decode_argument_checks(lib):
     assert call(hkv=3) == 2
     assert call(flags=2) == 1
     assert call(flags=3, d=64) == 2
+
+
+def test_decode_step_graph_argument_checks_before_any_device_work():
+    """DecodeStepGraph rejects an empty layer list and rotary arguments given
+    only in part before it touches a device."""
+    from paged_kv_continuous_gb300 import build
+    build.build()
+    import torch
+    from paged_kv_continuous_gb300 import graph, ops
+    t = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ops.PagedAttentionError):
+        graph.DecodeStepGraph([], t, t, t, 0.1)
+    layer = {"q": torch.zeros((1, 12, 128), dtype=torch.bfloat16)}
+    with pytest.raises(ops.PagedAttentionError):
+        graph.DecodeStepGraph([layer], t, t, t, 0.1, positions=t)
+    with pytest.raises(ops.PagedAttentionError):
+        graph.DecodeStepGraph([layer], t, t, t, 0.1, positions=t,
+                              cos_table=torch.zeros((4, 64)))
