@@ -47,6 +47,16 @@ def brute_attention(q_bits, k_bits, v_bits, scale, n_keys):
     return (w @ V) / w.sum()
 
 
+def oracle_stored_caches(w):
+    """Copies of the workload's pools after the step's store, placed by the
+    oracle's store (every expected pool and every pool the oracle reads is
+    built here, from oracle/ alone)."""
+    import oracle
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.store_kv(w.new_k, w.new_v, kc, vc, w.slot_mapping)
+    return kc, vc
+
+
 def normal_bits(rng, shape):
     return bf16_bits(rng.standard_normal(shape, dtype=np.float32))
 

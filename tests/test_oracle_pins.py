@@ -12,8 +12,8 @@ import pytest
 import oracle
 from paged_kv_continuous_gb300 import synth
 from paged_kv_continuous_gb300.synth import BF16_NAN, bf16_bits, bf16_to_f64
-from tests.helpers import (brute_attention, const_bits, normal_bits, random_tables,
-                           scatter_pool)
+from tests.helpers import (brute_attention, const_bits, normal_bits, oracle_stored_caches,
+                           random_tables, scatter_pool)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 SCALE = 1.0 / math.sqrt(128.0)
@@ -317,7 +317,7 @@ def test_varlen_equals_per_sequence_bitwise():
     """The pages' equivalence: the flattened batch gives, row for row, what
     each sequence gives alone."""
     w = synth.varlen_prefill(chunk=24, n_decode=3, n_chunk=3, max_prefix=60)
-    kc, vc = w.stored_caches()
+    kc, vc = oracle_stored_caches(w)
     full = oracle.prefill_varlen(w.q, w.cu_seqlens, kc, vc, w.block_tables, w.context_lens,
                                  w.scale)
     for s in range(w.batch):
@@ -330,7 +330,7 @@ def test_varlen_equals_per_sequence_bitwise():
 
 def test_decode_equals_prefill_with_one_query_bitwise():
     w = synth.tiny_decode()
-    kc, vc = w.stored_caches()
+    kc, vc = oracle_stored_caches(w)
     dec = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
     pre = oracle.prefill_varlen(w.q, np.arange(w.batch + 1, dtype=np.int32), kc, vc,
                                 w.block_tables, w.context_lens, w.scale)
@@ -346,7 +346,7 @@ def test_merge_of_splits_equals_unsplit():
     attention over the whole range (the flash-decoding identity); an empty
     split (lse = -inf) carries no weight."""
     w = synth.qwen_decode_b8()
-    kc, vc = w.stored_caches()
+    kc, vc = oracle_stored_caches(w)
     full = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
     rng = np.random.default_rng(21)
     S = 5
@@ -376,7 +376,7 @@ def test_merge_single_split_is_identity_and_all_empty_is_zero():
 
 def test_decode_range_full_range_matches_decode_lse():
     w = synth.tiny_decode()
-    kc, vc = w.stored_caches()
+    kc, vc = oracle_stored_caches(w)
     o1, l1 = oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale,
                            with_lse=True)
     o2, l2 = oracle.decode_range(w.q, kc, vc, w.block_tables, np.zeros(w.batch, np.int32),

@@ -14,7 +14,8 @@ import torch
 import oracle
 from paged_kv_continuous_gb300 import synth
 from tests.helpers import (assert_attention_close, const_bits, dev_to_f64, normal_bits,
-                           random_tables, scatter_pool, to_dev_bf16, to_dev_i32)
+                           oracle_stored_caches, random_tables, scatter_pool, to_dev_bf16,
+                           to_dev_i32)
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -43,18 +44,19 @@ def gpu_prefill(ops, w, out_dtype=torch.float32, max_q_len=None, err=None, store
     return out
 
 
-def oracle_prefill(w, seqs=None):
-    kc, vc = w.stored_caches()
-    if seqs is None:
-        return oracle.prefill_varlen(w.q, w.cu_seqlens, kc, vc, w.block_tables, w.context_lens,
-                                     w.scale)
-    outs = {}
-    for s in seqs:
-        a, b = w.cu_seqlens[s], w.cu_seqlens[s + 1]
-        outs[s] = oracle.prefill_varlen(w.q[a:b], np.array([0, b - a], np.int32), kc, vc,
-                                        w.block_tables[s:s + 1], w.context_lens[s:s + 1],
-                                        w.scale)
-    return outs
+def oracle_prefill(w):
+    """The oracle over the whole launch, on pools placed by the oracle's store."""
+    kc, vc = oracle_stored_caches(w)
+    return oracle.prefill_varlen(w.q, w.cu_seqlens, kc, vc, w.block_tables, w.context_lens,
+                                 w.scale)
+
+
+@pytest.fixture(scope="module")
+def full_mix():
+    """The full 8 x 1 + 8 x 512 chunked-prefill mix (prefixes up to 2048) and
+    the oracle's answer for every one of its 4104 rows."""
+    w = synth.varlen_prefill(keep_seq=False)
+    return w, oracle_prefill(w)
 
 
 def test_prefill_reduced_mix_all_rows(ops):
@@ -69,20 +71,17 @@ def test_prefill_reduced_mix_all_rows(ops):
     assert_attention_close(dev_to_f64(gpu_prefill(ops, w, torch.bfloat16)), ref, "prefill bf16")
 
 
-def test_prefill_full_workload_sampled_sequences(ops):
-    """The full 8 x 1 + 8 x 512 mix (prefixes up to 2048), in the launch the
-    bench times; four sequences (two one-token rows, two 512-query chunks)
-    are recomputed by the oracle one by one."""
-    w = synth.varlen_prefill()
+def test_prefill_full_workload_all_sequences(ops, full_mix):
+    """The full mix in the launch the bench times: all 16 sequences (every
+    row, every head) against the oracle over the whole launch, fp32 output
+    held to the strict rule, bf16 output to the elementwise rule."""
+    w, ref = full_mix
     got = dev_to_f64(gpu_prefill(ops, w))
-    q_lens = w.q_lens
-    picks = [int(np.flatnonzero(q_lens == 1)[0]), int(np.flatnonzero(q_lens == 1)[-1]),
-             int(np.flatnonzero(q_lens == 512)[0]), int(np.flatnonzero(q_lens == 512)[-1])]
-    refs = oracle_prefill(w, picks)
-    for s in picks:
-        a, b = w.cu_seqlens[s], w.cu_seqlens[s + 1]
-        assert_attention_close(got[a:b], refs[s], f"sequence {s} (q_len {b - a})", strict=True)
-    assert np.all(np.isfinite(got))
+    for s in range(w.batch):
+        a, b = int(w.cu_seqlens[s]), int(w.cu_seqlens[s + 1])
+        assert_attention_close(got[a:b], ref[a:b], f"sequence {s} (q_len {b - a})", strict=True)
+    assert_attention_close(dev_to_f64(gpu_prefill(ops, w, torch.bfloat16)), ref,
+                           "full mix bf16")
 
 
 def test_prefill_cu_seqlens_example_from_the_pages(ops):
@@ -218,21 +217,26 @@ def test_prefill_store_equals_store_then_prefill(ops, hq, hkv):
     assert int(err.item()) == 0
     out_u = gpu_prefill(ops, w)
     assert torch.equal(out_f, out_u)
-    kref, vref = w.stored_caches()
+    kref, vref = oracle_stored_caches(w)
     assert np.array_equal(_bits(kc), kref) and np.array_equal(_bits(vc), vref)
     assert_attention_close(dev_to_f64(out_f), oracle_prefill(w), f"fused hq={hq} hkv={hkv}",
                            strict=True)
 
 
-def test_prefill_store_full_workload(ops):
+def test_prefill_store_full_workload(ops, full_mix):
     """The varlen_prefill workload (8 one-token rows + 8 chunks of 512):
-    fused equals store + prefill bit for bit; pools as the oracle's store."""
-    w = synth.varlen_prefill(keep_seq=False)
+    fused equals store + prefill bit for bit; pools as the oracle's store;
+    every row against the oracle (bf16 output: elementwise rule; fp32
+    output: strict)."""
+    w, ref = full_mix
     out_f, kc, vc = fused_prefill(ops, w, out_dtype=torch.bfloat16)
     out_u = gpu_prefill(ops, w, out_dtype=torch.bfloat16)
     assert torch.equal(out_f.view(torch.int16), out_u.view(torch.int16))
-    kref, vref = w.stored_caches()
+    kref, vref = oracle_stored_caches(w)
     assert np.array_equal(_bits(kc), kref) and np.array_equal(_bits(vc), vref)
+    assert_attention_close(dev_to_f64(out_f), ref, "fused full mix bf16")
+    out_f32, _, _ = fused_prefill(ops, w, out_dtype=torch.float32)
+    assert_attention_close(dev_to_f64(out_f32), ref, "fused full mix f32", strict=True)
 
 
 def test_prefill_store_bad_slot_reported(ops):

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from paged_kv_continuous_gb300 import synth
-from tests.helpers import bf16_dev_to_bits, to_dev_bf16, to_dev_i32
+from tests.helpers import bf16_dev_to_bits, oracle_stored_caches, to_dev_bf16, to_dev_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -23,7 +23,7 @@ def ops():
 
 def fused_vs_unfused(ops, w, slots=None, num_splits=0, pre_store=False):
     slots = w.slot_mapping if slots is None else slots
-    kc0, vc0 = (w.stored_caches() if pre_store else (w.k_cache, w.v_cache))
+    kc0, vc0 = (oracle_stored_caches(w) if pre_store else (w.k_cache, w.v_cache))
     q, nk, nv = to_dev_bf16(w.q), to_dev_bf16(w.new_k), to_dev_bf16(w.new_v)
     bt, cl, sm = to_dev_i32(w.block_tables), to_dev_i32(w.context_lens), to_dev_i32(slots)
     # fused
@@ -70,7 +70,7 @@ def test_store_decode_padding_and_wrong_slot(ops):
     slots = w.slot_mapping.copy()
     slots[1] = -1
     slots[4] = slots[4] + 1 if slots[4] % 16 != 15 else slots[4] - 1
-    kc0, vc0 = w.stored_caches()          # the pool already holds every new token
+    kc0, vc0 = oracle_stored_caches(w)    # the pool already holds every new token
     q, nk, nv = to_dev_bf16(w.q), to_dev_bf16(w.new_k), to_dev_bf16(w.new_v)
     kf, vf = to_dev_bf16(kc0), to_dev_bf16(vc0)
     ws = ops.decode_workspace(w.num_q_heads, w.num_kv_heads, 0, 128, "cuda")
