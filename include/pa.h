@@ -35,8 +35,13 @@
  *
  * Conventions shared by every entry point
  *   - All array arguments are DEVICE pointers into caller-owned memory; the
- *     library allocates nothing and keeps no state between calls.  Scalars
- *     are passed by value.  `stream` is a cudaStream_t (NULL = legacy default
+ *     library allocates nothing and keeps no data between calls (its only
+ *     host-side state: per-device flags recording that a kernel's shared
+ *     memory limit was raised, the driver entry points it looked up, and
+ *     pa_decode_noalloc's cached array address -- all set once, under
+ *     atomics or a lock, so the entry points may be called from several host
+ *     threads at once; two calls in flight must not share a workspace or an
+ *     output buffer).  Scalars are passed by value.  `stream` is a cudaStream_t (NULL = legacy default
  *     stream); all work is enqueued there and the call returns without
  *     synchronising.  PA_OK means "validated and launched", not "finished".
  *   - Element type of q, k, v and the pools is bf16.  Outputs are bf16
@@ -74,7 +79,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 9
+#define PA_ABI_VERSION 10
 
 #if defined(__GNUC__)
 #define PA_API __attribute__((visibility("default")))
@@ -144,6 +149,24 @@ PA_API int32_t pa_abi_version(void);
 
 /* Static, human-readable name of a pa_status value. */
 PA_API const char *pa_status_string(pa_status status);
+
+/*
+ * pa_get_device_error -- read back a device error word (host helper; the
+ * pages have no counterpart: it stands in for a debug-build error query).
+ *
+ * error_word is the caller's int32 word that a call ORs PA_DEVERR_* bits
+ * into: byte 0 of a decode workspace (pa_decode, pa_store_decode,
+ * pa_rope_store_decode, pa_decode_fp8, pa_store_decode_fp8), or the
+ * `error_flags` argument of the other entry points.  The helper enqueues a
+ * copy of the word to the host on `stream` (and, when `clear` is nonzero, a
+ * reset of the word to 0 after the copy), synchronises the stream, and
+ * stores the word in *out_flags.  It is the one entry point that blocks the
+ * calling thread; it allocates nothing.  Returns PA_ERR_INVALID_ARG for a
+ * null pointer (nothing enqueued) and PA_ERR_DEVICE when the copy, the reset
+ * or the synchronisation fails (*out_flags is then left untouched).
+ */
+PA_API pa_status pa_get_device_error(int32_t *error_word, int32_t *out_flags, int32_t clear,
+                                     void *stream);
 
 /*
  * pa_store_kv -- slot_mapping store ([EAS] "自写 Triton Kernel",
@@ -467,11 +490,18 @@ PA_API pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *works
  * query heads, S > 253 at 32) returns PA_ERR_WORKSPACE, launching nothing.  The
  * call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  * routine.  The first call on a device, with that device current, looks up
- * the array's device address and caches it; make that first call before
- * any stream capture.  All calls on a device share the array: calls that
- * overlap on the GPU race on it.  Each call clears the split arrival
- * counters in the array (an asynchronous memset on `stream`) before its
- * kernel; nothing else in it needs to start at zero.
+ * the array's device address and caches it with the current CUDA context;
+ * make that first call before any stream capture.  A call under another
+ * context on that device (after cudaDeviceReset, or after the primary
+ * context was released and created again) looks the address up again, so
+ * the first call after such a change must also come before any capture.
+ * All calls on a device share the array: calls that overlap on the GPU race
+ * on it.  Each call clears the split arrival counters in the array (an
+ * asynchronous memset on `stream`) before its kernel; nothing else in it
+ * needs to start at zero.  That memset sits between the previous kernel on
+ * the stream and the decode kernel, so PA_LAUNCH_PDL and PA_LAUNCH_EARLY_KV
+ * are accepted but give no overlap through this entry point (the kernel
+ * starts after the memset, as without the flags); results are the same.
  */
 PA_API pa_status pa_decode_noalloc(void *out, int32_t out_dtype, const void *q,
                                    const void *k_cache, const void *v_cache,

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/pa.h"
 
 namespace pa {
@@ -44,6 +46,20 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Raises `kernel`'s dynamic shared memory limit to `bytes` the first time it
+// is launched on `device` (one flag per device; devices past the table are
+// set every time).  The flags are atomic: several host threads may call on
+// one device at once, and setting the attribute twice is harmless.
+template <typename Kernel>
+cudaError_t set_smem_once(std::atomic<bool> (&done)[64], Kernel kernel, int device, int bytes) {
+  const bool tracked = device >= 0 && device < 64;
+  if (tracked && done[device].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && tracked) done[device].store(true, std::memory_order_release);
+  return e;
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

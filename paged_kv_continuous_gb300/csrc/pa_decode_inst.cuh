@@ -22,14 +22,10 @@ template <int G>
 cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                      cudaStream_t s, int device, bool pdl) {
   using Sh = DecodeShape<G, PA_HKV, PA_F8, PA_ROPE>;
-  static bool configured[64] = {};
-  if (device < 0 || device >= 64 || !configured[device]) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        decode_kernel<G, PA_HKV, PA_F8, PA_ROPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        Sh::SMEM);
-    if (e != cudaSuccess) return e;
-    if (device >= 0 && device < 64) configured[device] = true;
-  }
+  static std::atomic<bool> configured[64] = {};
+  const cudaError_t e =
+      set_smem_once(configured, decode_kernel<G, PA_HKV, PA_F8, PA_ROPE>, device, Sh::SMEM);
+  if (e != cudaSuccess) return e;
   return launch_kernel(decode_kernel<G, PA_HKV, PA_F8, PA_ROPE>, dim3(p.num_splits),
                        dim3(kDecodeThreads), Sh::SMEM, s, pdl, tk, tv, p);
 }

@@ -11,8 +11,12 @@
 // Set-up: the first call on each device, with that device current, resolves
 // the array's device address with cudaGetSymbolAddress (a host-side use of
 // the array's name is only a host stand-in, never a device address) and
-// caches it; make that first call before any stream capture.  Nothing here
-// calls cudaMalloc, cudaFree or any allocating routine.
+// caches it with the CUDA context it belongs to; make that first call before
+// any stream capture.  A later call under another context on that device
+// (after cudaDeviceReset, or a primary context released and made again)
+// looks the address up again, since the old one belonged to the old
+// context; that call, too, must come before any capture.  Nothing here calls
+// cudaMalloc, cudaFree or any allocating routine.
 //
 // Sharing: every call on a device uses the same array and leaves its
 // partials there.  The split-K arrival counters in it must start at zero:
@@ -22,6 +26,8 @@
 // streams, or two threads) race on the array and give wrong rows.
 #include <cmath>
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "pa_decode_internal.h"
 #include "pa_decode_kernel.cuh"
@@ -36,16 +42,42 @@ __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_decode_scratch on `device` (the current device).
+// The driver's cuCtxGetCurrent (the runtime has no call that names the
+// current context), looked up once.
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  return fn;
+}
+
+// Device address of g_decode_scratch on `device` (the current device), for
+// the current context: cached per device with the context it was looked up
+// in, and looked up again when the current context is another one.
 cudaError_t scratch_address(int device, void **ptr) {
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  PFN_cuCtxGetCurrent_v4000 get_ctx = ctx_get_current();
+  if (!get_ctx) return cudaErrorNotSupported;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_ptr[device]) {
+  CUcontext cur = nullptr;
+  if (get_ctx(&cur) != CUDA_SUCCESS) return cudaErrorUnknown;
+  if (!g_scratch_ptr[device] || cur == nullptr || cur != g_scratch_ctx[device]) {
     void *p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess) return e;
+    // the lookup made the runtime's context current if none was
+    if (get_ctx(&cur) != CUDA_SUCCESS || cur == nullptr) return cudaErrorUnknown;
     g_scratch_ptr[device] = p;
+    g_scratch_ctx[device] = cur;
   }
   *ptr = g_scratch_ptr[device];
   return cudaSuccess;

@@ -810,13 +810,9 @@ template <int G>
 cudaError_t launch_prefill(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tnk,
                            const CUtensorMap &tnv, const PrefillParams &pp,
                            int max_q_len, cudaStream_t s, int device) {
-  static bool configured[64] = {};
-  if (device < 0 || device >= 64 || !configured[device]) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        prefill_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
-    if (e != cudaSuccess) return e;
-    if (device >= 0 && device < 64) configured[device] = true;
-  }
+  static std::atomic<bool> configured[64] = {};
+  const cudaError_t e = set_smem_once(configured, prefill_kernel<G>, device, kPfSmem);
+  if (e != cudaSuccess) return e;
   constexpr int PT = kPfRows / G;
   dim3 grid((max_q_len + PT - 1) / PT, pp.hkv, pp.num_seqs);
   prefill_kernel<G><<<grid, kPfThreads, kPfSmem, s>>>(tk, tv, tnk, tnv, pp);

@@ -33,7 +33,7 @@ EXPORTED = (
     "pa_decode_default_splits", "pa_decode", "pa_decode_merge", "pa_prefill_varlen",
     "pa_decode_noalloc", "pa_rope_store_kv", "pa_store_kv_fp8", "pa_decode_fp8",
     "pa_store_decode", "pa_store_decode_fp8", "pa_prefill_store_varlen",
-    "pa_rope_store_decode",
+    "pa_rope_store_decode", "pa_get_device_error",
 )
 
 
@@ -52,6 +52,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_abi_version.argtypes = []
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [i32]
+    lib.pa_get_device_error.restype = i32
+    lib.pa_get_device_error.argtypes = [P, P, i32, P]
     lib.pa_store_kv.restype = i32
     lib.pa_store_kv.argtypes = [P, P, i64, i64, i64, i64, i64, P, P, i64, i32, i32, i32, P, P,
                                 u32, P]
@@ -532,7 +534,14 @@ def prefill_store_varlen(q, new_k, new_v, slot_mapping, cu_seqlens, k_cache, v_c
     return out
 
 
-def read_error_word(buf) -> int:
-    """Host copy of an int32 error word (first 4 bytes of ``buf``); syncs."""
-    return int(buf[:4].view(torch.int32).item()) if buf.dtype == torch.uint8 else int(
-        buf.reshape(-1)[0].item())
+def read_error_word(buf, clear=False, stream=None) -> int:
+    """The int32 error word at the start of ``buf`` (a decode workspace or an
+    error_flags tensor), read through pa_get_device_error: the copy is
+    enqueued on ``stream`` and the stream synchronised; ``clear`` resets the
+    word to 0 after the copy."""
+    if not buf.is_cuda or buf.numel() * buf.element_size() < 4:
+        raise PagedAttentionError("error word must be a CUDA tensor of at least 4 bytes")
+    flags = ctypes.c_int32(0)
+    _check(lib.pa_get_device_error(_ptr(buf), ctypes.byref(flags), 1 if clear else 0,
+                                   _stream(stream)), "pa_get_device_error")
+    return int(flags.value)

@@ -44,7 +44,7 @@ def test_binding_names_match_header():
 
 def test_version_and_status_strings(lib):
     lib.pa_abi_version.restype = ctypes.c_int32
-    assert lib.pa_abi_version() == 9
+    assert lib.pa_abi_version() == 10
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [ctypes.c_int32]
     assert lib.pa_status_string(0) == b"ok"
@@ -260,3 +260,15 @@ def test_decode_step_graph_argument_checks_before_any_device_work():
     with pytest.raises(ops.PagedAttentionError):
         graph.DecodeStepGraph([layer], t, t, t, 0.1, positions=t,
                               cos_table=torch.zeros((4, 64)))
+
+
+def test_device_error_readback_checks_pointers_first():
+    """pa_get_device_error rejects null pointers before it enqueues anything
+    (so it needs no device here)."""
+    from paged_kv_continuous_gb300 import build
+    build.build()
+    from paged_kv_continuous_gb300 import ops
+    L = ops.lib
+    word = ctypes.c_int32(0)
+    assert L.pa_get_device_error(None, ctypes.byref(word), 0, None) == 1
+    assert L.pa_get_device_error(ctypes.c_void_p(16), None, 1, None) == 1
