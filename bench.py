@@ -14,9 +14,12 @@ alone as "pdl_only_step").
 Steps cycle over L = 8 independent layer pools (same lengths and tables,
 different data), so every step reads its KV from HBM, not from L2 (8 x ~105
 MB of live KV >> the 126 MB L2).  Steps run as CUDA-graph replays (one graph
-= the L layers) with nothing between the launches; after the timed region, a
-copy of the graph with external timing events around each launch gives the
-duration of an isolated launch (the events break the launch overlap).
+of min(K, 512) launches, plus one for the remainder) with nothing between the
+launches.  The K timed steps are timed 7 times, each time bracketed by a
+barrier and a device synchronisation; the median is reported, the spread
+beside it.  After the timed region, a graph of the L layers with external
+timing events around each launch gives the duration of an isolated launch
+(the events break the launch overlap).
 
 value  = algorithmic bytes of a step / device time of a step  (GB/s)
 e2e    = the same metric through the public Python API with the step's
@@ -424,7 +427,8 @@ def run_reference(args):
     import oracle
     from paged_kv_continuous_gb300 import synth
     w = synth.cb_decode_b64()
-    kc, vc = w.stored_caches()
+    kc, vc = w.k_cache.copy(), w.v_cache.copy()
+    oracle.store_kv(w.new_k, w.new_v, kc, vc, w.slot_mapping)
     threads = oracle.max_threads()
     # size one step: a prefix of the sequences, so that W + K steps take ~2 min
     t = time.perf_counter()
@@ -561,44 +565,38 @@ def run_ours(args):
     torch.cuda.synchronize()
     got0 = layers[0]["out"].float().cpu().numpy().astype(np.float64)
 
-    # graphs: NC copies of "all L layers", each step bracketed by external events
+    # The timed steps run as replays of one graph of C = min(K, 512) launches
+    # (layer i % L for launch i; C is a multiple of L when K >= 512), plus one
+    # graph for the remaining K mod C launches: back to back, as a serving loop
+    # runs them, with a graph boundary (which the programmatic-launch overlap
+    # does not cross) once per C launches.  A separate graph of the L layers
+    # carries event nodes around each launch (which break that overlap); it is
+    # replayed after the timed region for the duration of an isolated launch.
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
-    NC = 8
-    graphs, events = [], []
-    ext_ok = True
     with torch.cuda.stream(s):
         for _ in range(3):
             for l in range(L):
                 step(l)
     torch.cuda.synchronize()
-    # The timed copies run the launches back to back, as a serving loop does.
-    # A separate copy carries event nodes around each launch (which break the
-    # programmatic-launch overlap) and is replayed after the timed region for
-    # the per-launch duration of an isolated launch.
-    for c in range(NC + 1):
+    C = min(args.steps, (512 // L) * L if args.steps >= 512 else args.steps)
+    n_full, rem = divmod(args.steps, C)
+
+    def capture(first, count, evs=None):
         g = torch.cuda.CUDAGraph()
-        evs = []
-        for l in range(L):
-            try:
-                evs.append([torch.cuda.Event(enable_timing=True, external=True)
-                            for _ in range(2)] if c == NC else None)
-            except TypeError:
-                ext_ok = False
-                evs.append(None)
         with torch.cuda.graph(g, stream=s):
-            for l in range(L):
-                step(l, evs[l])
-        graphs.append(g)
-        events.append(evs)
-    ev_graph, ev_events = graphs.pop(), events.pop()
-    rem = args.steps % L
-    rem_graph = None
-    if rem:
-        rem_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(rem_graph, stream=s):
-            for l in range(rem):
-                step(l)
+            for i in range(count):
+                step((first + i) % L, evs[i] if evs else None)
+        return g
+    main_graph = capture(0, C)
+    rem_graph = capture(n_full * C, rem) if rem else None
+    ext_ok = True
+    try:
+        ev_events = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+                     for _ in range(L)]
+    except TypeError:
+        ext_ok, ev_events = False, None
+    ev_graph = capture(0, L, ev_events) if ext_ok else None
     launches_per_step = 1  # decode_kernel: store, decode and merge in one launch
 
     def barrier():
@@ -609,6 +607,8 @@ def run_ours(args):
     # warm-up steps (untimed)
     for i in range(args.warmup):
         step(i % L)
+    torch.cuda.synchronize()
+    main_graph.replay()
     torch.cuda.synchronize()
 
     gpu_id = str(local)
@@ -621,24 +621,29 @@ def run_ours(args):
     sampler = ClockSampler(gpu_id)
     time.sleep(0.3)
 
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    full = args.steps // L
-    barrier()
-    torch.cuda.synchronize()
+    # REPEATS timed regions of exactly K steps each, every one bracketed by a
+    # barrier and a device synchronisation; the median is reported
+    REPEATS = 7
+    rep_s = []
     t_host0 = time.monotonic()
-    with torch.cuda.stream(s):
-        start.record()
-        for i in range(full):
-            graphs[i % NC].replay()
-        if rem_graph is not None:
-            rem_graph.replay()
-        end.record()
-    torch.cuda.synchronize()
+    for _ in range(REPEATS):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            start.record()
+            for _ in range(n_full):
+                main_graph.replay()
+            if rem_graph is not None:
+                rem_graph.replay()
+            end.record()
+        torch.cuda.synchronize()
+        barrier()
+        rep_s.append(max_over_ranks(start.elapsed_time(end) / 1e3, dev))
     t_host1 = time.monotonic()
-    barrier()
     sampler.stop()
-    elapsed_s = max_over_ranks(start.elapsed_time(end) / 1e3, dev)
+    elapsed_s = float(np.median(rep_s))
     err_word = ops.read_error_word(ws)
 
     # per-launch durations of isolated launches (untimed replays of the
@@ -649,10 +654,8 @@ def run_ours(args):
             for _ in range(3):
                 ev_graph.replay()
         torch.cuda.synchronize()
-        for l in range(L):
-            e = ev_events[l]
-            if e is not None:
-                decode_ms.append(e[0].elapsed_time(e[1]))
+        for e in ev_events:
+            decode_ms.append(e[0].elapsed_time(e[1]))
     # the same step as two launches (pa_store_kv, then pa_decode), for comparison
     st_u = {"l": 0}
 
@@ -764,7 +767,8 @@ def run_ours(args):
 
     # parity of the bench's own first step, and the CPU baseline (oracle)
     import oracle  # bench's cpu_baseline leg
-    kc_ref, vc_ref = w.stored_caches()
+    kc_ref, vc_ref = w.k_cache.copy(), w.v_cache.copy()
+    oracle.store_kv(w.new_k, w.new_v, kc_ref, vc_ref, w.slot_mapping)
     ref, cpu = cpu_baseline_oracle(w, kc_ref, vc_ref, seconds=args.cpu_seconds)
     abs_err = np.abs(got0 - ref)
     parity_ok = bool(np.all(abs_err <= 2e-3 + 1e-2 * np.abs(ref)))
@@ -811,6 +815,11 @@ def run_ours(args):
                               "layer's tail)") if early else
                              "PA_LAUNCH_PDL (programmatic dependent launch)"},
         "seq_steps_per_s": world * B * args.steps / elapsed_s,
+        "repeats": {"n": len(rep_s), "reported": "median",
+                    "ms_per_step": [r * 1e3 / args.steps for r in rep_s],
+                    "min_ms_per_step": min(rep_s) * 1e3 / args.steps,
+                    "max_ms_per_step": max(rep_s) * 1e3 / args.steps,
+                    "graph_launches_per_region": n_full + (1 if rem else 0)},
         "unfused_step": {"us_per_step": unfused_ms * 1e3,
                          "GB_per_s": step_bytes / unfused_ms / 1e6,
                          "step": "pa_store_kv + pa_decode, two launches, PDL"},
