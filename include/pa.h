@@ -282,14 +282,19 @@ PA_API pa_status pa_store_kv_fp8(const void *k, const void *v, int64_t num_token
  * n_b = ceil(context_lens[b] / block_size) blocks, the global block index of
  * its block j is P_b + j with P_b = n_0 + ... + n_{b-1}, and
  * N = n_0 + ... + n_{batch-1}.  With S = num_splits, split c in [0, S)
- * processes global blocks [floor(c N / S), floor((c + 1) N / S)).  Every
- * split therefore moves the same number of KV bytes (+-1 block), however
- * skewed the lengths are.
+ * processes global blocks [floor(N W(c) / W(S)), floor(N W(c + 1) / W(S))),
+ * where W(c) sums the weights of splits 0 .. c - 1: every split weighs 4,
+ * except that when S >= 32 and N >= 4 S the last four weigh 3, 3, 3 and 2
+ * (a grid's highest-indexed CTAs start last behind a previous kernel, on
+ * the SMs it frees last; their lighter shares let them end with the rest).
+ * Every split therefore moves the same number of KV bytes (+-1 block), the
+ * last four less, however skewed the lengths are.
  *
  * A sequence whose blocks all fall in one split is finished by that split,
  * which writes its output rows directly.  A sequence spread over splits
  * c0 < c1 leaves a partial result in every split it touches: split c0 in
- * slot (c0, 1) and every non-empty split c in (c0, c1] in slot (c, 0).  A
+ * slot 1, row block c0, and every non-empty split c in (c0, c1] in slot 0,
+ * row block c (so the slot-0 partials of one sequence are consecutive).  A
  * partial is the attention output over that split's keys only, normalised
  * over those keys, plus the natural-log sum-exp of its scaled scores.  The
  * split that completes a sequence's set of partials (counted in
@@ -303,8 +308,8 @@ PA_API pa_status pa_store_kv_fp8(const void *k, const void *v, int64_t num_token
  *                       only ORs bits in);
  *   [256, C)            int32 counters[PA_DECODE_MAX_SPLITS], zero between
  *                       calls, at the same place for every S;
- *   [C, ...)            float partial_o[S][2][H][D];
- *   C + R(8SHD)         float partial_lse[S][2][H].
+ *   [C, ...)            float partial_o[2][S][H][D]  (slot, split, head, dim);
+ *   C + R(8SHD)         float partial_lse[2][S][H].
  * Zero the whole workspace once when allocating it; every completed call
  * leaves the counters at zero again, so the workspace can be reused with
  * any split count.  After a call that reported PA_DEVERR_WAIT_TIMEOUT,

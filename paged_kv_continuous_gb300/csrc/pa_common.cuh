@@ -232,13 +232,38 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 
 __device__ __forceinline__ int ceil_div_blocks(int n) { return (n + kBlockSize - 1) / kBlockSize; }
 
-// Split c of S over N global blocks starts at floor(c N / S).
-__device__ __forceinline__ long long split_begin(long long c, long long S, long long N) {
-  return c * N / S;
+// Decode split partition.  Split c of S over N global blocks starts at
+// floor(N W(c) / W(S)), W(c) the summed weights of splits 0 .. c - 1.
+// Every split weighs 4, except that with S >= 32 and N >= 4 S the last four
+// weigh 3, 3, 3 and 2: in a chain of launches the hardware starts a grid's
+// CTAs in index order, so the highest-indexed ones land on the SMs the
+// previous kernel frees last and start up to a few microseconds after the
+// rest; a lighter share lets them end with the others (the rest take under
+// one percent more).  With N >= 4 S even the lightest split holds at least
+// two blocks, so N >= S still means that every split holds a block.
+__device__ __forceinline__ bool split_light_tail(long long S, long long N) {
+  return S >= 32 && N >= 4 * S;
 }
-// The split holding global block x: the largest c with split_begin(c) <= x.
+__device__ __forceinline__ long long split_weight_before(long long c, long long S) {
+  const long long base = S - 4;
+  if (c <= base) return 4 * c;
+  const long long t = c - base;  // 1 .. 4
+  return 4 * base + (t == 1 ? 3 : t == 2 ? 6 : t == 3 ? 9 : 11);
+}
+__device__ __forceinline__ long long split_begin(long long c, long long S, long long N) {
+  if (!split_light_tail(S, N)) return c * N / S;
+  return N * split_weight_before(c, S) / split_weight_before(S, S);
+}
+// The split holding global block x: the largest c with split_begin(c) <= x,
+// i.e. the largest c with W(c) <= floor(((x + 1) W(S) - 1) / N).
 __device__ __forceinline__ long long split_of_block(long long x, long long S, long long N) {
-  return ((x + 1) * S - 1) / N;
+  if (!split_light_tail(S, N)) return ((x + 1) * S - 1) / N;
+  const long long v = ((x + 1) * split_weight_before(S, S) - 1) / N;
+  const long long b4 = 4 * (S - 4);
+  if (v < b4 + 3) return v / 4 < S - 4 ? v / 4 : S - 4;
+  if (v < b4 + 6) return S - 3;
+  if (v < b4 + 9) return S - 2;
+  return S - 1;
 }
 
 }  // namespace pa

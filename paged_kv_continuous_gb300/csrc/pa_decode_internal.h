@@ -18,8 +18,8 @@ constexpr size_t kCounterBytes = size_t(PA_DECODE_MAX_SPLITS) * 4;
 // Byte offsets inside a decode workspace for `splits` splits.
 struct WorkspaceLayout {
   size_t counters;  // int32 [PA_DECODE_MAX_SPLITS], zero between calls
-  size_t part_o;    // float [splits][2][hq][128]
-  size_t part_lse;  // float [splits][2][hq]
+  size_t part_o;    // float [2][splits][hq][128]
+  size_t part_lse;  // float [2][splits][hq]
   size_t total;
 };
 WorkspaceLayout workspace_layout(long long splits, int hq);

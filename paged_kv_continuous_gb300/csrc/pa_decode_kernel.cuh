@@ -65,6 +65,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "pa_common.cuh"
 
 namespace pa {
@@ -80,8 +82,8 @@ struct DecodeParams {
   int batch;
   float qk_scale_log2;  // softmax scale * log2(e): exponentials are base 2
   int num_splits;
-  float *part_o;      // [S][2][HQ][128]
-  float *part_lse;    // [S][2][HQ], natural log
+  float *part_o;      // [2][S][HQ][128] (slot-major: a sequence's slot-0 rows are consecutive)
+  float *part_lse;    // [2][S][HQ], natural log
   int32_t *counters;  // [S] arrival counters, zero between calls
   int32_t *err;
   const float *k_scale;  // FP8 pools only: per kv head, value = code * scale
@@ -161,7 +163,17 @@ struct DecodeShape {
   // consumers already fill the other at the end of piece i + 1
   static constexpr int RED_ONE_FLOATS = align_up(CW * G * RED_FLOATS_PER_HEAD, 256);
   static constexpr int RED_BYTES = NPH > 1 ? 2 * RED_ONE_FLOATS * 4 : 0;
-  static constexpr int CTL_BYTES = 256;
+  static constexpr int CTL_BYTES = 512;
+  // Prefetched merges: while the consumers stream the CTA's final piece, the
+  // epilogue warp brings the other pieces' partials of its sequence into the
+  // red buffer nobody uses any more; up to PF_PIECES pieces' rows fit there.
+  // The prefetched lse values sit in the merge scratch at PF_W.  A merge the
+  // CTA owes besides its final one (a piece the epilogue warp published
+  // arrived last) runs beside it, with its weights at DEF_W.
+  static constexpr int PF_PIECES = NPH > 1 ? RED_ONE_FLOATS / (HQ * kHeadDim) : 0;
+  static constexpr bool PF_LSE_COPY = HQ % 4 == 0;  // lse rows are 16-byte runs
+  static constexpr int PF_W = 1024, DEF_W = 1536;
+  static constexpr int DEF_MAX_PIECES = 512 / HQ - 1;  // weights room of the owed merge
   // the epilogue warp's combine weights: NPH per query head (NPH * HQ = CW * G)
   static constexpr int EWW_BYTES = 256;
   // merge scratch: one weight per (piece, query head), up to MERGE_MAX_PIECES
@@ -191,6 +203,9 @@ struct DecodeShape {
   static_assert((NPH + 1) * HQ <= MERGE_FLOATS, "combine weights do not fit");
   static_assert(CW * G * 4 <= EWW_BYTES, "epilogue warp weights do not fit");
   static_assert(!(F8 && ROPE), "rotary embedding is fused for bf16 pools only");
+  static_assert(PF_W + (PF_PIECES + 1) * HQ <= DEF_W && DEF_W + 512 <= MERGE_FLOATS,
+                "prefetched lse and owed-merge weights do not fit the merge scratch");
+  static_assert(DEF_MAX_PIECES >= 1, "owed-merge weights do not fit");
 };
 
 // A piece handed to the epilogue warp (one per red buffer).
@@ -213,6 +228,8 @@ struct DecodeCtl {
   unsigned long long merge_bar2;    // mbarrier: the deferred merge's bulk copies
   unsigned long long ew_done;       // mbarrier: the epilogue warp has finished
   unsigned long long seen_bar;      // mbarrier: every other piece of the final one arrived
+  unsigned long long pf_bar;        // mbarrier: the final piece's prefetched partials
+  unsigned long long pub_done;      // mbarrier: the epilogue warp has published every piece
   PieceDesc desc[2];
   // a cut piece the epilogue warp published last: the consumers merge its
   // sequence at their end (def_pending = 1)
@@ -220,9 +237,14 @@ struct DecodeCtl {
   int def_b, def_pending;
   // the CTA's final piece, cut: its sequence's counter and piece count, for
   // the epilogue warp to watch (fin_valid = 1 once written)
-  long long fin_cs1;
+  long long fin_cs0, fin_cs1;
   int fin_pieces, fin_valid;
-  unsigned long long total;   // N, blocks of all sequences
+  int fin_npe;  // pieces handed to the epilogue warp before the final one
+  // the epilogue warp prefetched the final piece's other partials (written
+  // before it completes seen_bar); use_pf: the consumers' merge reads them
+  // (decided once, by consumer thread 0)
+  int pf_ready, use_pf;
+  int owed_now;  // an owed merge runs beside the final one (consumer thread 0 decides)
   long long first_prefix;    // global index of block 0 of first_b
   int first_b;               // sequence holding this CTA's first block
   int abort;                 // set by a wait that gave up
@@ -236,7 +258,7 @@ struct DecodeCtl {
   // warp stops watching the counter)
   int decided;
 };
-static_assert(sizeof(DecodeCtl) <= 256, "control words do not fit their 256 bytes");
+static_assert(sizeof(DecodeCtl) <= 512, "control words do not fit their 512 bytes");
 
 __device__ __forceinline__ int seq_blocks(const int32_t *ctx, int b) {
   const int n = __ldg(ctx + b);
@@ -426,10 +448,22 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
-// Arrival on a sequence's counter with release semantics at GPU scope: the
-// partial rows written before it (by this thread, or by the threads a CTA
-// or warp barrier ordered before it) are visible to whoever observes the new
-// count with an acquire.  Returns the old count.
+// A cut sequence's counter word holds two counts: the pieces that have
+// arrived (low 16 bits) and the pieces whose partial rows are published
+// (high 16 bits).  A piece arrives and publishes in one release add
+// (kArrivePublish) or, the CTA's final piece, arrives first with a relaxed
+// add (kArrive) and publishes afterwards (kPublish) unless it arrived last:
+// the last arrival merges, so it needs only to see every other piece
+// published and never publishes its own rows.  Piece counts stay below 2^16
+// (at most PA_DECODE_MAX_SPLITS).
+constexpr int kArrive = 1, kPublish = 1 << 16, kArrivePublish = kArrive | kPublish;
+__device__ __forceinline__ int arrived_count(int w) { return w & 0xFFFF; }
+__device__ __forceinline__ int published_count(int w) { return (int)((unsigned)w >> 16); }
+
+// Add with release semantics at GPU scope: the partial rows written before
+// it (by this thread, or by the threads a CTA or warp barrier ordered
+// before it) are visible to whoever observes the new word with an acquire.
+// Returns the old word.
 __device__ __forceinline__ int atom_add_release_gpu(int32_t *ptr, int v) {
   int old;
   asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;"
@@ -437,6 +471,36 @@ __device__ __forceinline__ int atom_add_release_gpu(int32_t *ptr, int v) {
                : "l"(ptr), "r"(v)
                : "memory");
   return old;
+}
+
+// Relaxed add (an arrival that publishes nothing); returns the old word.
+__device__ __forceinline__ int atom_add_relaxed_gpu(int32_t *ptr, int v) {
+  int old;
+  asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(ptr), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Waits (bounded) until `want` pieces are published on the counter word,
+// with acquire semantics: their partial rows are then visible to this
+// thread.  The pieces it waits for have arrived, so their CTAs are past
+// their blocks and publish without waiting for anything.  On timeout it sets
+// *abort, reports PA_DEVERR_WAIT_TIMEOUT and returns false.
+__device__ __forceinline__ bool wait_published(const int32_t *ptr, int want, volatile int *abort,
+                                               int32_t *err) {
+  const long long t0 = clock64();
+  while (published_count(ld_acquire_gpu(ptr)) < want) {
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitTimeoutCycles) {
+      *abort = 1;
+      report(err, PA_DEVERR_WAIT_TIMEOUT);
+      return false;
+    }
+    __nanosleep(32);
+  }
+  return true;
 }
 
 // ---- output writers ---------------------------------------------------------
@@ -468,7 +532,8 @@ __device__ __forceinline__ void store_out4(void *out, int out_f32, long long idx
 }
 
 // Log-sum-exp merge of one output row (sequence b, query head h) from the
-// split-K partials of splits c0..c1 (slot 1 of c0, slot 0 of the others),
+// split-K partials of splits c0..c1 (slot 1 of c0, slot 0 of the others;
+// partials are [slot][split][head][dim]),
 // by one warp; lane l owns dims 4l..4l+3.  Partials are read through L2
 // (written by other CTAs).  When N >= S every split holds at least one
 // block; otherwise empty splits are skipped.  Each lane walks the pieces in
@@ -484,7 +549,7 @@ __device__ __forceinline__ void merge_row(const float *part_o, const float *part
   auto piece = [&](long long cc) -> bool {
     return dense || cc == c0 || split_begin(cc, S, N) < split_begin(cc + 1, S, N);
   };
-  auto row_of = [&](long long cc) -> long long { return (cc * 2 + (cc == c0 ? 1 : 0)) * HQ + h; };
+  auto row_of = [&](long long cc) -> long long { return ((cc == c0 ? 1 : 0) * S + cc) * HQ + h; };
   float M = -INFINITY;
   for (long long base = c0; base <= c1; base += 32) {
     const long long cc = base + lane;
@@ -530,54 +595,97 @@ __device__ __forceinline__ void merge_row(const float *part_o, const float *part
              make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
 }
 
-// Log-sum-exp merge of all partials of sequence b by the NT consumer
-// threads of one CTA (needs every split of c0..c1 non-empty, N >= S, and
-// k = c1 - c0 + 1 <= MAXP; else returns false having done nothing).  One
-// round of loads brings every (piece, head) lse into `w`, where each head's
-// terms e_i = exp(lse_i - M) and the reciprocal of their sum are formed.
-// The pieces' partial rows come into shared memory (`buf`, 16-byte aligned,
-// `buf_bytes` long) by one bulk copy
-// per piece, as many pieces per batch as `buf` holds (all of them for the
-// common few-piece case: one round trip); each thread keeps the weighted
-// sums of its (head, 4 dims) items in registers across batches.  The piece
-// of split c_own is read from own_o / own_lse (c_own = -1: every piece comes
-// from the workspace).
+// Bulk copies of the partial rows of pieces i0 .. i1 - 1 of a sequence whose
+// first split is c0 (piece i at row block i - i0 of `buf`), skipping piece
+// own_i; with `lse`, also their lse values (piece i's HQ values at
+// lse + i * HQ, own piece included: its entries are overwritten after the
+// copies land).  One thread issues them; arms `mbar` with their bytes.
+// Pieces 1 .. k - 1 are slot-0 rows of consecutive splits, so a run of them
+// that skips the own piece is one copy (at most 32 KB each).
+template <int HQ>
+__device__ void issue_piece_copies(const DecodeParams &p, long long c0, long long S, int i0,
+                                   int i1, int own_i, float *buf, float *lse, uint32_t mbar) {
+  constexpr int ROW_FLOATS = HQ * kHeadDim;
+  constexpr int RUN = (32 * 1024) / (ROW_FLOATS * 4) > 0 ? (32 * 1024) / (ROW_FLOATS * 4) : 1;
+  auto row0 = [&](int i) -> long long { return ((i == 0 ? 1 : 0) * S + (c0 + i)) * HQ; };
+  const bool own_in = own_i >= i0 && own_i < i1;
+  uint32_t bytes = (uint32_t)((i1 - i0 - (own_in ? 1 : 0)) * ROW_FLOATS * 4);
+  if (lse) bytes += (uint32_t)((i1 - i0) * HQ * 4);
+  mbar_arrive_expect_tx(mbar, bytes);
+  const uint64_t pol = l2_policy_evict_first();
+  for (int i = i0; i < i1;) {
+    if (i == own_i) {
+      ++i;
+      continue;
+    }
+    int j = i + 1;
+    if (i > 0)
+      while (j < i1 && j != own_i && j - i < RUN) ++j;
+    bulk_load(smem_addr(buf + (long long)(i - i0) * ROW_FLOATS), p.part_o + row0(i) * kHeadDim,
+              (uint32_t)((j - i) * ROW_FLOATS * 4), mbar, pol);
+    i = j;
+  }
+  if (lse) {
+    // piece i0 (slot 1 when i0 = 0), then pieces i0 + 1 .. i1 - 1 (slot 0, consecutive)
+    bulk_load(smem_addr(lse + i0 * HQ), p.part_lse + row0(i0), HQ * 4, mbar, pol);
+    if (i1 > i0 + 1)
+      bulk_load(smem_addr(lse + (i0 + 1) * HQ), p.part_lse + row0(i0 + 1),
+                (uint32_t)((i1 - i0 - 1) * HQ * 4), mbar, pol);
+  }
+}
+
+// Log-sum-exp merge of all partials of sequence b by the NT threads
+// (thread index ct, named barrier bar_id) of one CTA (needs every split of
+// c0..c1 non-empty, N >= S, and k = c1 - c0 + 1 <= MAXP; else returns false
+// having done nothing).  One round of loads brings every (piece, head) lse
+// into `w`, where each head's terms e_i = exp(lse_i - M) and the reciprocal
+// of their sum are formed.  The pieces' partial rows come into shared
+// memory (`buf`, 16-byte aligned, `buf_bytes` long; piece i of a batch at
+// row block i - i0) by bulk copies, as many pieces per batch as `buf` holds
+// (all of them for the common few-piece case: one round trip).  Each thread
+// keeps the weighted sums of its (head, 4 dims) items in registers across
+// pieces and batches.  The piece of split c_own is read from own_o /
+// own_lse (c_own = -1: every piece comes from the workspace).  With
+// `prefetched`, every other piece's rows and all lse values were already
+// requested by issue_piece_copies into buf / w on `mbar` (phase 0, one
+// batch): the merge only waits for them.
 template <int HQ, int MAXP, int NT>
 __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, long long c1,
                                     long long S, long long N, float *w, int ct, int bar_id,
                                     long long c_own, const float *own_o, const float *own_lse,
                                     float *buf, long long buf_bytes, uint32_t mbar,
-                                    volatile int *abort_flag) {
+                                    volatile int *abort_flag, bool prefetched = false) {
   constexpr int ROW_FLOATS = HQ * kHeadDim;  // one piece: HQ rows of o
   constexpr int ITEMS = HQ * (kHeadDim / 4);
   constexpr int IPT = (ITEMS + NT - 1) / NT;  // items per thread
+  // many items per thread (a one-warp merge): items outer; when the pieces
+  // take several batches, the running sums wait in the last row block of buf
+  constexpr bool ITEMS_OUTER = IPT > 4;
   const long long k = c1 - c0 + 1;
-  const long long per_batch = buf_bytes / (ROW_FLOATS * 4);
-  if (N < S || k > MAXP || per_batch < 1) return false;
+  long long per_batch = buf_bytes / (ROW_FLOATS * 4);
+  if (ITEMS_OUTER && per_batch < k) --per_batch;  // one row block for the sums
+  if (N < S || k > MAXP || per_batch < 1 || (prefetched && per_batch < k)) return false;
   const int kk = (int)k, kb = (int)(per_batch < k ? per_batch : k);
-  auto row0 = [&](int i) -> long long {  // first workspace row of piece i
-    const long long cc = c0 + i;
-    return (cc * 2 + (i == 0 ? 1 : 0)) * HQ;
-  };
-  auto issue = [&](int i0) {
-    const int i1 = i0 + kb < kk ? i0 + kb : kk;
-    const bool own_in = c_own >= c0 + i0 && c_own < c0 + i1;
-    mbar_arrive_expect_tx(mbar, (uint32_t)((i1 - i0 - (own_in ? 1 : 0)) * ROW_FLOATS * 4));
-    const uint64_t pol = l2_policy_evict_first();
-    for (int i = i0; i < i1; ++i)
-      if (c0 + i != c_own)
-        bulk_load(smem_addr(buf + (long long)(i - i0) * ROW_FLOATS),
-                  p.part_o + row0(i) * kHeadDim, ROW_FLOATS * 4, mbar, pol);
-  };
-  if (ct == 0) {
-    // the ring was last read through the generic proxy, and the partials
-    // were acquired through it; the copies go through the async proxy
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    issue(0);
+  const int own_i = (int)(c_own - c0);  // outside [0, kk) when c_own = -1
+  if (prefetched) {
+    // the rows and lse values are (being) copied in; the own piece's lse
+    // entries are written once the copies have landed
+    __all_sync(0xffffffffu, mbar_wait(mbar, 0, abort_flag, p.err));
+    if (own_i >= 0 && own_i < kk)
+      for (int h = ct; h < HQ; h += NT) w[own_i * HQ + h] = own_lse[h];
+  } else {
+    if (ct == 0) {
+      // the ring was last read through the generic proxy, and the partials
+      // were acquired through it; the copies go through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      issue_piece_copies<HQ>(p, c0, S, 0, kb, own_i, buf, nullptr, mbar);
+    }
+    for (int e = ct; e < kk * HQ; e += NT)
+      w[e] = e / HQ == own_i ? own_lse[e % HQ]
+                             : __ldcg(p.part_lse + ((e < HQ ? 1 : 0) * S + c0 + e / HQ) * HQ +
+                                      e % HQ);
   }
-  for (int e = ct; e < kk * HQ; e += NT)
-    w[e] = c0 + e / HQ == c_own ? own_lse[e % HQ] : __ldcg(p.part_lse + row0(e / HQ) + e % HQ);
   named_barrier(bar_id, NT);
   // per head: e_i = exp(lse_i - M) in w (summed in split order) and the
   // reciprocal of the sum in winv; up to 16 pieces in registers
@@ -613,25 +721,71 @@ __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, 
     winv[h] = W > 0.f ? 1.f / W : 0.f;
   }
   named_barrier(bar_id, NT);
+  if constexpr (ITEMS_OUTER) {
+    // each thread's items in turn, the pieces of the batch in split order;
+    // between batches an item's running sum waits in `sums` (its own slot:
+    // no other thread reads it)
+    float4 *sums = reinterpret_cast<float4 *>(buf + (long long)kb * ROW_FLOATS);
+    for (int i0 = 0, batch = 0; i0 < kk; i0 += kb, ++batch) {
+      if (!prefetched) __all_sync(0xffffffffu, mbar_wait(mbar, batch & 1, abort_flag, p.err));
+      const int i1 = i0 + kb < kk ? i0 + kb : kk;
+      for (int item = ct; item < ITEMS; item += NT) {
+        const int h = item / (kHeadDim / 4), d = (item % (kHeadDim / 4)) * 4;
+        float4 a = i0 == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : sums[item];
+        for (int i = i0; i < i1; ++i) {
+          const float *rowp = i == own_i ? own_o : buf + (long long)(i - i0) * ROW_FLOATS;
+          const float wi = w[i * HQ + h];
+          const float4 v = *reinterpret_cast<const float4 *>(rowp + h * kHeadDim + d);
+          a.x = fmaf(wi, v.x, a.x);
+          a.y = fmaf(wi, v.y, a.y);
+          a.z = fmaf(wi, v.z, a.z);
+          a.w = fmaf(wi, v.w, a.w);
+        }
+        if (i1 < kk) {
+          sums[item] = a;
+        } else {
+          const float inv = winv[h];
+          store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d,
+                     make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv));
+        }
+      }
+      if (i1 < kk) {
+        // the next batch reuses the rows once every thread is done with them
+        named_barrier(bar_id, NT);
+        if (ct == 0) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          const int i2 = i1 + kb < kk ? i1 + kb : kk;
+          issue_piece_copies<HQ>(p, c0, S, i1, i2, own_i, buf, nullptr, mbar);
+        }
+      }
+    }
+    return true;
+  }
+  // this thread's items: head and dim offset of each
+  int hh[IPT], dd[IPT];
+#pragma unroll
+  for (int t = 0; t < IPT; ++t) {
+    const int item = ct + t * NT;
+    hh[t] = item < ITEMS ? item / (kHeadDim / 4) : 0;
+    dd[t] = (item % (kHeadDim / 4)) * 4;
+  }
   float4 acc[IPT];
 #pragma unroll
   for (int t = 0; t < IPT; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int own_i = (int)(c_own - c0);
   for (int i0 = 0, batch = 0; i0 < kk; i0 += kb, ++batch) {
-    // every consumer thread waits for the batch (warp-uniform; bounded)
-    __all_sync(0xffffffffu, mbar_wait(mbar, batch & 1, abort_flag, p.err));
+    // every thread waits for the batch (warp-uniform; bounded)
+    if (!prefetched) __all_sync(0xffffffffu, mbar_wait(mbar, batch & 1, abort_flag, p.err));
     const int i1 = i0 + kb < kk ? i0 + kb : kk;
+    // pieces in split order whichever CTA merges: the sums are the same
+    // bits run to run (merge_row keeps the same order and arithmetic)
+#pragma unroll 2
+    for (int i = i0; i < i1; ++i) {
+      const float *rowp = i == own_i ? own_o : buf + (long long)(i - i0) * ROW_FLOATS;
 #pragma unroll
-    for (int t = 0; t < IPT; ++t) {
-      const int item = ct + t * NT;
-      if (item < ITEMS) {
-        const int h = item / (kHeadDim / 4), d = (item % (kHeadDim / 4)) * 4;
-        // pieces in split order whichever CTA merges: the sums are the same
-        // bits run to run (merge_row keeps the same order and arithmetic)
-        for (int i = i0; i < i1; ++i) {
-          const float wi = w[i * HQ + h];
-          const float4 v = *reinterpret_cast<const float4 *>(
-              (i == own_i ? own_o : buf + (long long)(i - i0) * ROW_FLOATS) + h * kHeadDim + d);
+      for (int t = 0; t < IPT; ++t) {
+        if (ct + t * NT < ITEMS) {
+          const float wi = w[i * HQ + hh[t]];
+          const float4 v = *reinterpret_cast<const float4 *>(rowp + hh[t] * kHeadDim + dd[t]);
           acc[t].x = fmaf(wi, v.x, acc[t].x);
           acc[t].y = fmaf(wi, v.y, acc[t].y);
           acc[t].z = fmaf(wi, v.z, acc[t].z);
@@ -642,16 +796,18 @@ __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, 
     if (i1 < kk) {
       // the next batch reuses the buffer once every thread is done with it
       named_barrier(bar_id, NT);
-      if (ct == 0) issue(i1);
+      if (ct == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const int i2 = i1 + kb < kk ? i1 + kb : kk;
+        issue_piece_copies<HQ>(p, c0, S, i1, i2, own_i, buf, nullptr, mbar);
+      }
     }
   }
 #pragma unroll
   for (int t = 0; t < IPT; ++t) {
-    const int item = ct + t * NT;
-    if (item < ITEMS) {
-      const int h = item / (kHeadDim / 4), d = (item % (kHeadDim / 4)) * 4;
-      const float inv = winv[h];
-      store_out4(p.out, p.out_f32, ((long long)b * HQ + h) * kHeadDim + d,
+    if (ct + t * NT < ITEMS) {
+      const float inv = winv[hh[t]];
+      store_out4(p.out, p.out_f32, ((long long)b * HQ + hh[t]) * kHeadDim + dd[t],
                  make_float4(acc[t].x * inv, acc[t].y * inv, acc[t].z * inv, acc[t].w * inv));
     }
   }
@@ -684,31 +840,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const long long nsplit = p.num_splits;
   const long long c = blockIdx.x;
 
-  // ---- 1. total block count N and this CTA's block range --------------------
+  // ---- 1. block counts of all sequences: the total N, this CTA's block range
+  //         [lo, hi) and the sequence that holds block lo.  One block-wide
+  //         inclusive scan over the counts gives both when the batch fits one
+  //         pass (one round of context-length loads, two barriers); larger
+  //         batches take a pass for N, then a pass for the search.
+  __shared__ long long warp_tot[kDecodeWarps];
   if (tid == 0) {
-    ctl->total = 0;
     ctl->first_b = -1;
     ctl->first_prefix = 0;
     ctl->abort = 0;
     ctl->last = 0;
   }
-  __syncthreads();
+  long long N = 0;
   {
-    unsigned long long local = 0;
-    for (int b = tid; b < p.batch; b += blockDim.x) local += seq_blocks(p.context_lens, b);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) local += __shfl_xor_sync(0xffffffffu, local, off);
-    if (lane == 0 && local) atomicAdd(&ctl->total, local);
-  }
-  __syncthreads();
-  const long long N = (long long)ctl->total;
-  const long long lo = N ? split_begin(c, nsplit, N) : 0;
-  const long long hi = N ? split_begin(c + 1, nsplit, N) : 0;
-
-  // ---- 2. block-wide scan of sequence block counts: find the sequence that
-  //         holds block `lo`.
-  {
-    __shared__ long long warp_tot[kDecodeWarps];
+    const int nw = (int)(blockDim.x >> 5);
     long long running = 0;
     for (int base = 0; base < p.batch; base += blockDim.x) {
       const int b = base + tid;
@@ -721,16 +867,55 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       if (lane == 31) warp_tot[warp] = incl;
       __syncthreads();
-      long long before = running;
-      for (int w = 0; w < warp; ++w) before += warp_tot[w];
-      long long chunk_total = 0;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) chunk_total += warp_tot[w];
-      const long long prefix = before + incl - n;  // global index of block 0 of b
-      if (b < p.batch) {
-        if (n > 0 && prefix <= lo && lo < prefix + n && lo < hi) {
-          ctl->first_b = b;
-          ctl->first_prefix = prefix;
+      long long before = running, chunk_total = 0;
+      for (int w = 0; w < nw; ++w) {
+        const long long t = warp_tot[w];
+        if (w < warp) before += t;
+        chunk_total += t;
+      }
+      running += chunk_total;
+      if (base + (int)blockDim.x >= p.batch) {
+        // last pass: N is known, and (one-pass batches) so is this
+        // sequence's first block
+        N = running;
+        if (base == 0 && b < p.batch && n > 0) {
+          const long long lo1 = split_begin(c, nsplit, N), hi1 = split_begin(c + 1, nsplit, N);
+          const long long prefix = before + incl - n;
+          if (prefix <= lo1 && lo1 < prefix + n && lo1 < hi1) {
+            ctl->first_b = b;
+            ctl->first_prefix = prefix;
+          }
         }
+      }
+      __syncthreads();
+    }
+  }
+  const long long lo = N ? split_begin(c, nsplit, N) : 0;
+  const long long hi = N ? split_begin(c + 1, nsplit, N) : 0;
+  if (p.batch > (int)blockDim.x) {
+    // second pass over the prefix sums (batches larger than one pass)
+    long long running = 0;
+    for (int base = 0; base < p.batch; base += blockDim.x) {
+      const int b = base + tid;
+      const int n = b < p.batch ? seq_blocks(p.context_lens, b) : 0;
+      long long incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      if (lane == 31) warp_tot[warp] = incl;
+      __syncthreads();
+      long long before = running, chunk_total = 0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+        const long long t = warp_tot[w];
+        if (w < warp) before += t;
+        chunk_total += t;
+      }
+      const long long prefix = before + incl - n;  // global index of block 0 of b
+      if (b < p.batch && n > 0 && prefix <= lo && lo < prefix + n && lo < hi) {
+        ctl->first_b = b;
+        ctl->first_prefix = prefix;
       }
       running += chunk_total;
       __syncthreads();
@@ -778,8 +963,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     mbar_init(smem_addr(&ctl->merge_bar2), 1);
     mbar_init(smem_addr(&ctl->ew_done), 1);
     mbar_init(smem_addr(&ctl->seen_bar), 1);
+    mbar_init(smem_addr(&ctl->pf_bar), 1);
+    mbar_init(smem_addr(&ctl->pub_done), 1);
     ctl->def_pending = 0;
     ctl->fin_valid = 0;
+    ctl->pf_ready = 0;
     ctl->decided = 0;
     fence_barrier_init();
   }
@@ -799,6 +987,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
+    // the q base in a register before the wait (the copies after it are on
+    // the critical path of the first stage)
+    const uint16_t *q_base;
+    asm volatile("mov.b64 %0, %1;" : "=l"(q_base) : "l"(p.q));
     // The K and V pages of physical block ph into ring slot st, completing
     // on the slot's full barrier (warp-uniform arguments; nothing for an
     // entry outside the pool, which the caller reports).  arm: lane 0 first
@@ -900,7 +1092,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         __syncwarp();
         if (!pre) issue_kv_stage(st, ph_i, false);
         if (q_i) {
-          bulk_load_elect(dst + 2 * S::KV_BYTES, p.q + (long long)b_i * S::HQ * kHeadDim,
+          bulk_load_elect(dst + 2 * S::KV_BYTES, q_base + (long long)b_i * S::HQ * kHeadDim,
                           S::Q_BYTES, bar, pol_q);
           if constexpr (ROPE) {
             // the cos and sin rows of the new token's position (row 0 for a
@@ -943,29 +1135,62 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     //          merge if the piece arrives last.  The consumers never wait for
     //          this, except to reuse a buffer two pieces later.
     wait_prev_then_release();
+    zero_empty_rows(lane, 32);
     // While it waits for the next piece, lane 0 watches the arrival counter
     // of the CTA's final piece (once the consumers have named it): when every
     // other piece of that sequence has arrived it completes seen_bar, and the
-    // consumers merge at once, without publishing their own piece.
+    // consumers merge at once, without publishing their own piece.  Before
+    // it does, it requests the other pieces' partials (rows and lse) into the
+    // red buffer nobody uses any more, when they fit (pf_ready), so that the
+    // consumers' merge finds them in shared memory.
     int snoop = 0;  // 0: final piece not named yet, 1: watching, 2: done
-    long long fin_cs1 = 0;
+    long long fin_cs0 = 0, fin_cs1 = 0;
     int fin_pieces = 0;
-    auto wait_full = [&](uint32_t bar, int parity) -> bool {
+    bool pf_issued = false;
+    // lane 0: every other piece of the final one has arrived?  Then (with
+    // room) request their partials into free_buf, and complete seen_bar.
+    auto snoop_final = [&](float *free_buf) {
+      if (snoop == 0) {
+        if (!*reinterpret_cast<volatile int *>(&ctl->fin_valid)) return;
+        __threadfence_block();
+        fin_cs0 = ctl->fin_cs0;
+        fin_cs1 = ctl->fin_cs1;
+        fin_pieces = ctl->fin_pieces;
+        snoop = 1;
+      }
+      int cw_word = 0;
+      if (snoop == 1 && arrived_count(cw_word = ld_acquire_gpu(p.counters + fin_cs1)) ==
+                            fin_pieces - 1 &&
+          published_count(cw_word) == fin_pieces - 1) {
+        if constexpr (S::PF_PIECES > 0 && S::PF_LSE_COPY) {
+          if (free_buf != nullptr && fin_pieces <= S::PF_PIECES && N >= nsplit &&
+              !*reinterpret_cast<volatile int *>(&ctl->def_pending)) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            issue_piece_copies<S::HQ>(p, fin_cs0, nsplit, 0, fin_pieces, (int)(c - fin_cs0),
+                                      free_buf, mw + S::PF_W, smem_addr(&ctl->pf_bar));
+            *reinterpret_cast<volatile int *>(&ctl->pf_ready) = 1;
+            pf_issued = true;
+          }
+        }
+        mbar_arrive(smem_addr(&ctl->seen_bar));
+        snoop = 2;
+      }
+    };
+    auto wait_full = [&](uint32_t bar, int parity, float *free_buf, int npe) -> bool {
       const long long t0 = clock64();
       while (true) {
         int done = lane == 0 ? (int)mbar_test_wait(bar, parity) : 0;
-        if (lane == 0 && !done && snoop < 2) {
-          if (snoop == 0 && *reinterpret_cast<volatile int *>(&ctl->fin_valid)) {
-            __threadfence_block();
-            fin_cs1 = ctl->fin_cs1;
-            fin_pieces = ctl->fin_pieces;
-            snoop = 1;
-          }
-          if (snoop == 1 && ld_acquire_gpu(p.counters + fin_cs1) == fin_pieces - 1) {
-            mbar_arrive(smem_addr(&ctl->seen_bar));
-            snoop = 2;
-          }
+        // waiting for the final piece itself (named, and handed over after
+        // npe others): free_buf, the previous piece's buffer, is free for
+        // good (a non-final piece may still be in the consumers' hands when
+        // the final one is named)
+        int fin = 0;
+        if (lane == 0 && *reinterpret_cast<volatile int *>(&ctl->fin_valid)) {
+          __threadfence_block();
+          fin = ctl->fin_npe == npe;
         }
+        fin = __shfl_sync(0xffffffffu, fin, 0);
+        if (lane == 0 && !done && snoop < 2) snoop_final(fin ? free_buf : nullptr);
         if (__shfl_sync(0xffffffffu, done, 0)) {
           __syncwarp();  // the other lanes are ordered after lane 0's observation
           return true;
@@ -983,12 +1208,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     };
     for (int npe = 0;; ++npe) {
       const int k = npe & 1;
-      const bool got = wait_full(smem_addr(&ctl->red_full[k]), (npe >> 1) & 1);
+      // the buffer of the previous piece: once this warp waits for the final
+      // piece, nobody writes it again
+      float *const other_buf = S::NPH > 1 ? red + (k ^ 1) * S::RED_ONE_FLOATS : nullptr;
+      const bool got = wait_full(smem_addr(&ctl->red_full[k]), (npe >> 1) & 1, other_buf, npe);
       const PieceDesc d = ctl->desc[k];
       if (!got || d.kind == kPieceEnd) {
-        // every piece handed to this warp is done, and a merge it left is
-        // recorded: the consumers need not wait for anything else from it
-        if (lane == 0) mbar_arrive(smem_addr(&ctl->ew_done));
+        // every piece handed to this warp is published, and a merge it owes
+        // is recorded (def_pending)
+        if (lane == 0) mbar_arrive(smem_addr(&ctl->pub_done));
         // The end mark comes when the final piece's blocks are done.  While
         // the consumers combine that piece, lane 0 goes on watching its
         // counter until they decide how the piece ends (bounded; giving up
@@ -997,22 +1225,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const long long t0 = clock64();
           while (snoop < 2 && !*reinterpret_cast<volatile int *>(&ctl->decided) &&
                  !*abort_flag && clock64() - t0 < kWaitTimeoutCycles) {
-            if (snoop == 0) {
-              // named before the end mark, or never: a whole final piece
-              if (!*reinterpret_cast<volatile int *>(&ctl->fin_valid)) break;
-              __threadfence_block();
-              fin_cs1 = ctl->fin_cs1;
-              fin_pieces = ctl->fin_pieces;
-              snoop = 1;
-            }
-            if (ld_acquire_gpu(p.counters + fin_cs1) == fin_pieces - 1) {
-              mbar_arrive(smem_addr(&ctl->seen_bar));
-              snoop = 2;
-            } else {
-              __nanosleep(64);
-            }
+            // named before the end mark, or never: a whole final piece
+            if (snoop == 0 && !*reinterpret_cast<volatile int *>(&ctl->fin_valid)) break;
+            snoop_final(other_buf);
+            if (snoop < 2) __nanosleep(64);
           }
         }
+        // Copies this warp requested land before it signs off (bounded).
+        if (lane == 0 && pf_issued) {
+          volatile int never = 0;
+          mbar_wait(smem_addr(&ctl->pf_bar), 0, &never, nullptr);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ctl->ew_done));
         return;
       }
       if constexpr (S::NPH > 1) {
@@ -1067,14 +1292,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         int last = 0;
         if (lane == 0) {
           // release: the partial rows (this warp's, or the consumers' that
-          // the red_full barrier ordered before) precede the arrival
-          last = atom_add_release_gpu(p.counters + d.cs1, 1) == d.pieces - 1;
+          // the red_full barrier ordered before) precede the arrival, which
+          // publishes them too
+          last = arrived_count(atom_add_release_gpu(p.counters + d.cs1, kArrivePublish)) ==
+                 d.pieces - 1;
         }
         if (lane == 0 && last) {
-          // arrived last: acquire the other pieces' partials and leave the
-          // merge to the consumer warps, which merge with all their threads
-          // once the CTA's own blocks are done
-          fence_acq_rel_gpu();
+          // arrived last: wait (acquire) until every piece is published and
+          // leave the merge to the consumer warps, which merge with all
+          // their threads once the CTA's own blocks are done
+          wait_published(p.counters + d.cs1, d.pieces, abort_flag, p.err);
           ctl->def_b = d.b;
           ctl->def_cs0 = d.cs0;
           ctl->def_cs1 = d.cs1;
@@ -1087,20 +1314,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   // ---- 5b. consumers ----------------------------------------------------------
   const int cw = warp - kDecodeFirstConsumerWarp;  // consumer warp 0..CW-1
-  wait_prev_then_release();
-  zero_empty_rows(tid - 32 * kDecodeFirstConsumerWarp, S::CW * 32);
+  const int ct = tid - 32 * kDecodeFirstConsumerWarp;  // consumer thread index
+  // The first chunk's walk reads only context lengths, so it comes before
+  // the wait for the previous kernel (taken inside the loop, after the first
+  // walk): after the wait every global load misses the SM's caches, and the
+  // walk's loads would otherwise be dependent round trips between the wait
+  // and the first stage.  (The rows of empty sequences are the epilogue
+  // warp's.)
+  int wb = first_b;
+  int wctx = __ldg(p.context_lens + wb);
+  int wj = (int)(lo - first_prefix);
+  bool cons_waited = false;
   const int g = cw % HKV;     // kv head of this warp
   const int ph = cw / HKV;    // stage phase of this warp
   const int gid = lane >> 2;  // fragment row group
   const int qd = lane & 3;    // fragment column pair
-  const int ct = tid - 32 * kDecodeFirstConsumerWarp;  // consumer thread index
   // this warp's kv head inside the TMA boxes: box group, row offset
   const int gpair = g / S::HB, gsub = g % S::HB;
   // F8: the K scale of this kv head folds into the score scale, the V scale
   // into the rows at each piece end (codes widen exactly, so the products
   // equal those of the widened values)
-  const float cl2 = F8 ? p.qk_scale_log2 * __ldg(p.k_scale + g) : p.qk_scale_log2;
-  const float vsc = F8 ? __ldg(p.v_scale + g) : 1.f;
+  // (F8: the scales are read after the wait, below)
+  float cl2 = p.qk_scale_log2;
+  float vsc = 1.f;
   // F8: the 16 score rows of an MMA are the tokens tperm(r), so that a
   // thread's two token pairs of the PV operand are 4 consecutive bytes of
   // a dim-major V row: rows 2i, 2i + 1 -> tokens 4i, 4i + 1 and rows
@@ -1121,6 +1357,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
 
   int npieces = 0;  // pieces ended so far (every consumer warp counts the same)
+  bool def_done = false;  // an owed merge was handled with the final piece's
   bool no_final = false;  // the block walk stopped early (inconsistent input)
   // consumer thread 0: the current piece's split words are in ctl
   bool pc_done = false;
@@ -1143,22 +1380,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         pieces <= S::MERGE_MAX_PIECES) {
       // the CTA's final piece, cut (and mergeable from shared memory): the
       // epilogue warp watches its sequence's arrival counter meanwhile
+      ctl->fin_cs0 = cs0;
       ctl->fin_cs1 = cs1;
       ctl->fin_pieces = (int)pieces;
+      ctl->fin_npe = npieces;
       __threadfence_block();
       *reinterpret_cast<volatile int *>(&ctl->fin_valid) = 1;
     }
   };
   bool need_q = true;  // the q rows of the current piece are not loaded yet
-  int wb = first_b;
-  int wctx = __ldg(p.context_lens + wb);
-  int wj = (int)(lo - first_prefix);
   long long it0 = 0;  // stage index of the chunk's first block
   for (long long gb0 = lo; gb0 < hi;) {
     // the next (up to) 32 blocks: lane L describes block gb0 + L
     int lb = 0, lj = 0, lctx = 0;
     const int count =
         walk_chunk(p.context_lens, p.batch, wb, wctx, wj, hi - gb0, lane, lb, lj, lctx);
+    if (!cons_waited) {
+      // the first chunk is walked: now wait for the previous kernel, then
+      // read the FP8 scales
+      cons_waited = true;
+      wait_prev_then_release();
+      if constexpr (F8) {
+        cl2 *= __ldg(p.k_scale + g);
+        vsc = __ldg(p.v_scale + g);
+      }
+    }
     if (count == 0) {
       // same decision in every consumer warp and the producer; no final
       // piece follows: the epilogue warp gets its end mark at the consumers'
@@ -1559,7 +1805,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         L0 += __shfl_xor_sync(0xffffffffu, L0, off);
         L1 += __shfl_xor_sync(0xffffffffu, L1, off);
       }
-      const long long slot_row = (c * 2 + (head_cut ? 0 : 1)) * S::HQ;
+      const long long slot_row = ((head_cut ? 0 : 1) * nsplit + c) * S::HQ;
       const int ha = 2 * qd, hb = 2 * qd + 1;  // heads of this lane's fragment columns
       // red buffer of this piece; the epilogue warp must be done with its use
       // two pieces ago
@@ -1736,26 +1982,90 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             // rows): this piece is the last, no arrival and no publication
             ctl->last = 1;
           } else {
-            // release: the rows before the arrival
-            const bool last = atom_add_release_gpu(p.counters + cs1, 1) == pieces - 1;
-            if (last) fence_acq_rel_gpu();  // acquire the other pieces' rows
-            ctl->last = last;
+            // arrive first (relaxed: nothing of this piece is published yet).
+            // The last arrival merges and needs only every other piece
+            // published (acquire); any other publishes its rows (release).
+            const bool last =
+                arrived_count(atom_add_relaxed_gpu(p.counters + cs1, kArrive)) == pieces - 1;
+            if (last)
+              wait_published(p.counters + cs1, pieces - 1, abort_flag, p.err);
+            else
+              atom_add_release_gpu(p.counters + cs1, kPublish);
+            ctl->last = last && !*abort_flag;
           }
+          // the epilogue warp requested the other partials only once every
+          // other piece had arrived: when it has, they are this merge's
+          ctl->use_pf = ctl->last && *reinterpret_cast<volatile int *>(&ctl->pf_ready);
+          // The epilogue warp has published every earlier piece once it took
+          // the end mark: then whether the CTA owes a merge (a piece it
+          // published arrived last) is known, and an owed merge runs now,
+          // beside the final piece's (on the two halves of the consumer
+          // threads, with their own buffers, barriers and weights).  If the
+          // epilogue warp is not there yet, the owed merge waits for the end.
+          ctl->owed_now = mbar_test_wait(smem_addr(&ctl->pub_done), 0) &&
+                          *reinterpret_cast<volatile int *>(&ctl->def_pending);
         }
         named_barrier(1, S::CW * 32);
-        if (ctl->last) {
-          // consumer thread 0 acquired the partials before the last barrier
+        const bool fin_merge = ctl->last != 0;
+        const bool def_merge = ctl->owed_now != 0;
+        // the final piece's merge: threads [0, nt) of the consumers, named
+        // barrier bar; the rows of the other pieces come into the ring after
+        // the own rows, up to buf_end floats from the ring start
+        auto final_merge = [&](auto nt_tag, int t, int bar, long long buf_end) {
+          constexpr int NT = decltype(nt_tag)::value;
           float *mbuf = own_lse + ((S::HQ + 3) & ~3);
-          const long long mbuf_bytes =
-              (long long)S::NST * S::STAGE_BYTES - (long long)(mbuf - own_o) * 4;
-          if (!merge_sequence_bulk<S::HQ, S::MERGE_MAX_PIECES, S::CW * 32>(
-                  p, b, cs0, cs1, nsplit, N, mw, ct, 1, c, own_o, own_lse, mbuf, mbuf_bytes,
-                  smem_addr(&ctl->merge_bar), abort_flag))
-            for (int h = cw; h < S::HQ; h += S::CW)
+          const long long mbuf_bytes = (buf_end - (long long)(mbuf - own_o)) * 4;
+          const bool use_pf = ctl->use_pf != 0;
+          bool merged = false;
+          if constexpr (S::PF_PIECES > 0) {
+            if (use_pf)
+              merged = merge_sequence_bulk<S::HQ, S::PF_PIECES, NT>(
+                  p, b, cs0, cs1, nsplit, N, mw + S::PF_W, t, bar, c, own_o, own_lse,
+                  red + ((npieces & 1) ^ 1) * S::RED_ONE_FLOATS,
+                  (long long)S::RED_ONE_FLOATS * 4, smem_addr(&ctl->pf_bar), abort_flag, true);
+          }
+          // (beside an owed merge, the weights stay below DEF_W)
+          constexpr int MAXP = NT == S::CW * 32 ? S::MERGE_MAX_PIECES : S::DEF_W / S::HQ - 1;
+          if (!merged && !use_pf)
+            merged = merge_sequence_bulk<S::HQ, MAXP, NT>(
+                p, b, cs0, cs1, nsplit, N, mw, t, bar, c, own_o, own_lse, mbuf, mbuf_bytes,
+                smem_addr(&ctl->merge_bar), abort_flag);
+          if (!merged)
+            for (int h = t >> 5; h < S::HQ; h += NT / 32)
               merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * S::HQ + h, S::HQ, h,
                         cs0, cs1, nsplit, N, lane);
-          if (ct == 0) p.counters[cs1] = 0;
+          if (t == 0) p.counters[cs1] = 0;
+        };
+        // the owed merge: every piece from the workspace, rows into the ring
+        // from buf_begin floats on
+        auto owed_merge = [&](auto nt_tag, int t, int bar, long long buf_begin) {
+          constexpr int NT = decltype(nt_tag)::value;
+          const int db = ctl->def_b;
+          const long long d0 = ctl->def_cs0, d1 = ctl->def_cs1;
+          float *dbuf = own_o + buf_begin;
+          const long long dbuf_bytes = ((long long)S::NST * S::STAGE_BYTES / 4 - buf_begin) * 4;
+          if (!merge_sequence_bulk<S::HQ, S::DEF_MAX_PIECES, NT>(
+                  p, db, d0, d1, nsplit, N, mw + S::DEF_W, t, bar, -1, nullptr, nullptr, dbuf,
+                  dbuf_bytes, smem_addr(&ctl->merge_bar2), abort_flag))
+            for (int h = t >> 5; h < S::HQ; h += NT / 32)
+              merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)db * S::HQ + h, S::HQ,
+                        h, d0, d1, nsplit, N, lane);
+          if (t == 0) p.counters[d1] = 0;
+        };
+        constexpr int RING_FLOATS = S::NST * S::STAGE_BYTES / 4;
+        // the ring split in two (1 KB aligned) when both merges run
+        constexpr int HALF_FLOATS = RING_FLOATS / 2 / 256 * 256;
+        if (fin_merge && def_merge) {
+          if (ct < S::CW * 16)
+            final_merge(std::integral_constant<int, S::CW * 16>{}, ct, 3, HALF_FLOATS);
+          else
+            owed_merge(std::integral_constant<int, S::CW * 16>{}, ct - S::CW * 16, 4, HALF_FLOATS);
+        } else if (fin_merge) {
+          final_merge(std::integral_constant<int, S::CW * 32>{}, ct, 1, RING_FLOATS);
+        } else if (def_merge) {
+          owed_merge(std::integral_constant<int, S::CW * 32>{}, ct, 1, 0);
         }
+        def_done = def_merge;
         goto consumers_done;
       }
       // the next piece starts from nothing
@@ -1786,9 +2096,10 @@ consumers_done:
       if (lane == 0) mbar_arrive(smem_addr(&ctl->red_full[kbuf]));
     }
     if (ct == 0) *reinterpret_cast<volatile int *>(&ctl->decided) = 1;
-    // a merge the epilogue warp left (its piece arrived last)
+    // the epilogue warp has finished (copies it requested have landed); a
+    // merge it left, unless run beside the final one above
     __all_sync(0xffffffffu, mbar_wait(smem_addr(&ctl->ew_done), 0, abort_flag, p.err));
-    if (ctl->def_pending) {
+    if (!def_done && ctl->def_pending) {
       named_barrier(1, S::CW * 32);  // every consumer is done with the ring
       const int db = ctl->def_b;
       const long long d0 = ctl->def_cs0, d1 = ctl->def_cs1;

@@ -9,7 +9,8 @@ import torch
 import oracle
 from paged_kv_continuous_gb300 import synth
 from tests.helpers import (assert_attention_close, bf16_dev_to_bits, const_bits, dev_to_f64,
-                           normal_bits, random_tables, scatter_pool, to_dev_bf16, to_dev_i32)
+                           normal_bits, oracle_stored_caches, random_tables, scatter_pool,
+                           to_dev_bf16, to_dev_i32)
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +48,7 @@ class Dev:
 
 
 def oracle_decode(w):
-    kc, vc = w.stored_caches()
+    kc, vc = oracle_stored_caches(w)
     return oracle.decode(w.q, kc, vc, w.block_tables, w.context_lens, w.scale)
 
 
@@ -83,7 +84,7 @@ def test_decode_head_shapes_and_ragged_tails(ops, hq, hkv, ctx):
     # q rows exist for every sequence, also one with no key
     if w.q.shape[0] != len(ctx):
         w.q = normal_bits(rng, (len(ctx), hq, 128))
-    ref = oracle.decode(w.q, *w.stored_caches(), w.block_tables, w.context_lens, w.scale)
+    ref = oracle.decode(w.q, *oracle_stored_caches(w), w.block_tables, w.context_lens, w.scale)
     d = Dev(ops, w, store_on_gpu=False)
     for splits in (0, 3):
         got = dev_to_f64(d.decode(ops, torch.float32, splits))
@@ -255,29 +256,38 @@ def test_decode_bad_block_index_sets_error_without_fault(ops):
 
 
 def _partition(lens, S, bs=16):
-    """The documented split partition, restated: per sequence (c0, c1)."""
+    """The documented split partition, restated: split c starts at
+    floor(N W(c) / W(S)), every split weighing 4 except, with S >= 32 and
+    N >= 4 S, the last four (3, 3, 3, 2)."""
     n = [(c + bs - 1) // bs if c > 0 else 0 for c in lens]
     P = np.concatenate([[0], np.cumsum(n)]).astype(np.int64)
     N = int(P[-1])
+    tail = S >= 32 and N >= 4 * S
+    w = [4] * S
+    if tail:
+        w[-4:] = [3, 3, 3, 2]
+    W = np.concatenate([[0], np.cumsum(w)]).astype(np.int64)
 
     def begin(c):
-        return c * N // S
+        return int(N * W[c] // W[S])
 
     def split_of(x):
-        return ((x + 1) * S - 1) // N
+        # the largest c with begin(c) <= x, by search over the (few) splits
+        return int(np.searchsorted([begin(c) for c in range(S + 1)], x, side="right") - 1)
     return n, P, N, begin, split_of
 
 
-def test_merge_entry_point_against_oracle_partials(ops):
+@pytest.mark.parametrize("S", [29, 64])
+def test_merge_entry_point_against_oracle_partials(ops, S):
     """Fill the workspace with oracle partials laid out as the header
-    documents, run pa_decode_merge alone, compare with the oracle."""
+    documents, run pa_decode_merge alone, compare with the oracle (S = 64:
+    the lighter shares of the last four splits)."""
     w = synth.qwen_decode_b8()
-    kc, vc = w.stored_caches()
-    S = 29
+    kc, vc = oracle_stored_caches(w)
     n, P, N, begin, split_of = _partition(w.context_lens, S)
     Hq, D = w.num_q_heads, w.head_dim
-    part_o = np.zeros((S, 2, Hq, D), np.float32)
-    part_l = np.full((S, 2, Hq), np.nan, np.float32)   # unused slots are poison
+    part_o = np.zeros((2, S, Hq, D), np.float32)         # [slot][split][head][dim]
+    part_l = np.full((2, S, Hq), np.nan, np.float32)   # unused slots are poison
     cut = []
     for b in range(w.batch):
         c0, c1 = split_of(P[b]), split_of(P[b] + n[b] - 1)
@@ -295,8 +305,8 @@ def test_merge_entry_point_against_oracle_partials(ops):
             lo_arr[b], hi_arr[b] = klo, khi
             o, l = oracle.decode_range(w.q, kc, vc, w.block_tables, lo_arr, hi_arr, w.scale)
             slot = 1 if c == c0 else 0
-            part_o[c, slot] = o[b]
-            part_l[c, slot] = l[b]
+            part_o[slot, c] = o[b]
+            part_l[slot, c] = l[b]
     ws = ops.decode_workspace(Hq, w.num_kv_heads, S)
     hdr = 256 + 4 * 4096                      # error word + fixed counter area
     po_bytes = ((S * 2 * Hq * D * 4 + 255) // 256) * 256
