@@ -79,7 +79,7 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 10
+#define PA_ABI_VERSION 11
 
 #if defined(__GNUC__)
 #define PA_API __attribute__((visibility("default")))
@@ -131,7 +131,7 @@ typedef int32_t pa_status;
  *
  * PA_LAUNCH_EARLY_KV (decode entry points only, together with
  * PA_LAUNCH_PDL): the kernel also requests the K/V pages of its first ring
- * round (up to 8 blocks per CTA) before the previous kernel completes, so
+ * stages (up to 6 blocks per CTA) before the previous kernel completes, so
  * that the copies overlap that kernel's tail.  q, the new rows, the
  * workspace and every write still wait for it.  The caller guarantees that
  * the kernel launched immediately before the call does not write k_cache /
@@ -143,12 +143,39 @@ typedef int32_t pa_status;
  */
 #define PA_LAUNCH_PDL 1u
 #define PA_LAUNCH_EARLY_KV 2u
+#define PA_COPY_BEFORE_WAIT 4u
 
 /* ABI version of the loaded library (PA_ABI_VERSION it was built with). */
 PA_API int32_t pa_abi_version(void);
 
 /* Static, human-readable name of a pa_status value. */
 PA_API const char *pa_status_string(pa_status status);
+
+/*
+ * pa_copy -- a byte copy, as a kernel (host plumbing for a serving loop; the
+ * pages have no counterpart).
+ *
+ * Copies num_bytes from src to dst, two buffers the device can address:
+ * device memory, or pinned host memory (cudaHostAlloc / a pinned torch
+ * tensor), which the device reaches through the same address.  A
+ * cudaMemcpyAsync between two kernels of a stream ends their programmatic
+ * overlap; this copy keeps it.  flags: 0, PA_LAUNCH_PDL (the copy waits for
+ * the kernel launched just before it, then moves the bytes; the kernel after
+ * it begins once it has passed that wait), or PA_LAUNCH_PDL |
+ * PA_COPY_BEFORE_WAIT (it moves the bytes and lets the kernel after it begin
+ * while the kernel before it may still run, then waits for that one).  With
+ * PA_COPY_BEFORE_WAIT the caller guarantees that the kernel launched just
+ * before the copy neither writes src nor reads or writes dst, and that the
+ * kernel launched just after it reads dst only after its own wait (the
+ * decode entry points read context_lens and block_tables before theirs: stage
+ * those a launch earlier).  16-byte aligned
+ * addresses move in 16-byte chunks; otherwise at most 256 bytes may be
+ * copied (PA_ERR_UNSUPPORTED beyond).  Returns PA_ERR_INVALID_ARG for a
+ * null pointer, a negative size or a bad flag, before launching anything;
+ * num_bytes = 0 launches nothing.  Allocates nothing.
+ */
+PA_API pa_status pa_copy(void *dst, const void *src, int64_t num_bytes, uint32_t flags,
+                         void *stream);
 
 /*
  * pa_get_device_error -- read back a device error word (host helper; the

@@ -22,6 +22,7 @@ PA_DTYPE_BF16 = 0
 PA_DTYPE_F32 = 1
 PA_LAUNCH_PDL = 1  # programmatic dependent launch (see include/pa.h)
 PA_LAUNCH_EARLY_KV = 2  # decode: K/V pages requested before the previous kernel completes
+PA_COPY_BEFORE_WAIT = 4  # pa_copy: the bytes move before the previous kernel completes
 DEVERR_BLOCK_INDEX = 1
 DEVERR_SLOT_INDEX = 2
 DEVERR_WAIT_TIMEOUT = 4
@@ -33,7 +34,7 @@ EXPORTED = (
     "pa_decode_default_splits", "pa_decode", "pa_decode_merge", "pa_prefill_varlen",
     "pa_decode_noalloc", "pa_rope_store_kv", "pa_store_kv_fp8", "pa_decode_fp8",
     "pa_store_decode", "pa_store_decode_fp8", "pa_prefill_store_varlen",
-    "pa_rope_store_decode", "pa_get_device_error",
+    "pa_rope_store_decode", "pa_get_device_error", "pa_copy",
 )
 
 
@@ -54,6 +55,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_status_string.argtypes = [i32]
     lib.pa_get_device_error.restype = i32
     lib.pa_get_device_error.argtypes = [P, P, i32, P]
+    lib.pa_copy.restype = i32
+    lib.pa_copy.argtypes = [P, P, i64, u32, P]
     lib.pa_store_kv.restype = i32
     lib.pa_store_kv.argtypes = [P, P, i64, i64, i64, i64, i64, P, P, i64, i32, i32, i32, P, P,
                                 u32, P]
@@ -306,6 +309,103 @@ def store_decode(q, new_k, new_v, k_cache, v_cache, slot_mapping, block_tables, 
                                _decode_flags(pdl, early_kv), _stream(stream)),
            "pa_store_decode")
     return out
+
+
+class StoreDecodeCall:
+    """A prepared pa_store_decode: the tensors are checked once and the
+    marshalled arguments kept, so each call is one foreign call.  The caller
+    updates the tensors' contents in place between calls (as with the static
+    buffers of a captured step) and keeps them alive; ``call(stream)`` then
+    enqueues the step on ``stream`` (default: the current stream)."""
+
+    def __init__(self, q, new_k, new_v, k_cache, v_cache, slot_mapping, block_tables,
+                 context_lens, scale, out, num_splits=0, workspace=None, pdl=False,
+                 early_kv=False):
+        _need(q, torch.bfloat16, "q", 3)
+        _need(new_k, torch.bfloat16, "new_k", 3)
+        _need(new_v, torch.bfloat16, "new_v", 3)
+        _need(k_cache, torch.bfloat16, "k_cache", 4)
+        _need(v_cache, torch.bfloat16, "v_cache", 4)
+        _need(slot_mapping, torch.int32, "slot_mapping", 1)
+        _need(block_tables, torch.int32, "block_tables", 2)
+        _need(context_lens, torch.int32, "context_lens", 1)
+        if not q.is_contiguous():
+            raise PagedAttentionError("q must be contiguous")
+        for t, n in ((new_k, "new_k"), (new_v, "new_v")):
+            if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+                raise PagedAttentionError(f"{n} needs contiguous heads")
+        if block_tables.stride(1) != 1:
+            raise PagedAttentionError("block_tables rows must be contiguous")
+        B, Hq, D = q.shape
+        NB, bs, Hkv, _ = k_cache.shape
+        if tuple(new_k.shape) != (B, Hkv, D) or new_v.shape != new_k.shape or \
+                slot_mapping.shape[0] != B:
+            raise PagedAttentionError("new_k / new_v / slot_mapping need one row per sequence")
+        if out.shape != (B, Hq, D) or not out.is_contiguous():
+            raise PagedAttentionError("out must be a contiguous [B, Hq, D] tensor")
+        if workspace is None:
+            workspace = decode_workspace(Hq, Hkv, num_splits, D, q.device)
+        self._keep = (q, new_k, new_v, k_cache, v_cache, slot_mapping, block_tables,
+                      context_lens, out, workspace)
+        c = ctypes
+        self._args = (
+            c.c_void_p(out.data_ptr()), c.c_int32(_out_code(out.dtype)), c.c_void_p(q.data_ptr()),
+            c.c_void_p(new_k.data_ptr()), c.c_void_p(new_v.data_ptr()),
+            c.c_int64(new_k.stride(0)), c.c_int64(new_v.stride(0)),
+            c.c_void_p(slot_mapping.data_ptr()), c.c_void_p(k_cache.data_ptr()),
+            c.c_void_p(v_cache.data_ptr()), c.c_int64(NB), c.c_void_p(block_tables.data_ptr()),
+            c.c_int32(block_tables.stride(0)), c.c_void_p(context_lens.data_ptr()), c.c_int32(B),
+            c.c_int32(Hq), c.c_int32(Hkv), c.c_int32(D), c.c_int32(bs), c.c_float(scale),
+            c.c_int32(num_splits), c.c_void_p(workspace.data_ptr()),
+            c.c_size_t(workspace.numel() * workspace.element_size()),
+            c.c_uint32(_decode_flags(pdl, early_kv)))
+        self.out = out
+        self.workspace = workspace
+
+    def __call__(self, stream=None):
+        st = lib.pa_store_decode(*self._args, _stream(stream))
+        if st != PA_OK:
+            _check(st, "pa_store_decode")
+        return self.out
+
+
+class CopyCall:
+    """A prepared pa_copy (dst <- src, checked once, as ``copy`` checks)."""
+
+    def __init__(self, dst, src, pdl=False, before_wait=False):
+        nbytes, flags = _copy_check(dst, src, pdl, before_wait)
+        self._keep = (dst, src)
+        self._args = (ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()),
+                      ctypes.c_int64(nbytes), ctypes.c_uint32(flags))
+
+    def __call__(self, stream=None):
+        st = lib.pa_copy(*self._args, _stream(stream))
+        if st != PA_OK:
+            _check(st, "pa_copy")
+
+
+def _copy_check(dst, src, pdl, before_wait):
+    for t, n in ((dst, "dst"), (src, "src")):
+        if not (t.is_cuda or t.is_pinned()):
+            raise PagedAttentionError(f"{n} must be a CUDA tensor or pinned host memory")
+        if not t.is_contiguous():
+            raise PagedAttentionError(f"{n} must be contiguous")
+    nbytes = dst.numel() * dst.element_size()
+    if nbytes != src.numel() * src.element_size():
+        raise PagedAttentionError("dst and src differ in size")
+    if before_wait and not pdl:
+        raise PagedAttentionError("before_wait needs pdl")
+    return nbytes, (PA_LAUNCH_PDL if pdl else 0) | (PA_COPY_BEFORE_WAIT if before_wait else 0)
+
+
+def copy(dst, src, pdl=False, before_wait=False, stream=None):
+    """pa_copy: dst <- src (tensors of the same byte size, contiguous; each on
+    the GPU or in pinned host memory).  pdl: launch with PA_LAUNCH_PDL;
+    before_wait (with pdl): PA_COPY_BEFORE_WAIT, the bytes move before the
+    kernel launched just before completes (it must not write src nor touch
+    dst)."""
+    nbytes, flags = _copy_check(dst, src, pdl, before_wait)
+    _check(lib.pa_copy(_ptr(dst), _ptr(src), nbytes, flags, _stream(stream)), "pa_copy")
 
 
 def rope_store_decode(q, new_k, new_v, k_cache, v_cache, slot_mapping, block_tables,

@@ -44,7 +44,7 @@ def test_binding_names_match_header():
 
 def test_version_and_status_strings(lib):
     lib.pa_abi_version.restype = ctypes.c_int32
-    assert lib.pa_abi_version() == 10
+    assert lib.pa_abi_version() == 11
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_status_string.argtypes = [ctypes.c_int32]
     assert lib.pa_status_string(0) == b"ok"
@@ -272,3 +272,19 @@ def test_device_error_readback_checks_pointers_first():
     word = ctypes.c_int32(0)
     assert L.pa_get_device_error(None, ctypes.byref(word), 0, None) == 1
     assert L.pa_get_device_error(ctypes.c_void_p(16), None, 1, None) == 1
+
+
+def test_copy_checks_arguments_before_any_launch():
+    """pa_copy: bad flags, a negative size or a null pointer are rejected
+    before anything is launched; a zero-byte copy launches nothing."""
+    from paged_kv_continuous_gb300 import build
+    build.build()
+    from paged_kv_continuous_gb300 import ops
+    L = ops.lib
+    p = ctypes.c_void_p(16)
+    assert L.pa_copy(p, p, 16, 8, None) == 1              # unknown flag bit
+    assert L.pa_copy(p, p, 16, ops.PA_COPY_BEFORE_WAIT, None) == 1  # before-wait needs PDL
+    assert L.pa_copy(p, p, -1, 0, None) == 1
+    assert L.pa_copy(None, p, 16, 0, None) == 1
+    assert L.pa_copy(p, None, 16, 0, None) == 1
+    assert L.pa_copy(None, None, 0, 0, None) == 0
