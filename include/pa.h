@@ -34,7 +34,12 @@
  *         k_scale / v_scale kept beside the caches for FP8/INT8).
  *
  * Conventions shared by every entry point
- *   - All array arguments are DEVICE pointers into caller-owned memory; the
+ *   - All array arguments are DEVICE pointers into caller-owned memory, with
+ *     two exceptions: the `out` of the decode entry points and both buffers
+ *     of pa_copy may also be pinned host memory (cudaHostAlloc / a pinned
+ *     torch tensor), which the device reaches through the same address over
+ *     the CPU-GPU link -- a decode's `out` there delivers the result to the
+ *     host with no copy.  The
  *     library allocates nothing and keeps no data between calls (its only
  *     host-side state: per-device flags recording that a kernel's shared
  *     memory limit was raised, the driver entry points it looked up, and
@@ -168,7 +173,10 @@ PA_API const char *pa_status_string(pa_status status);
  * before the copy neither writes src nor reads or writes dst, and that the
  * kernel launched just after it reads dst only after its own wait (the
  * decode entry points read context_lens and block_tables before theirs: stage
- * those a launch earlier).  16-byte aligned
+ * those a launch earlier).  That next kernel may begin while the kernel
+ * before the copy still runs, so what it reads before its wait
+ * (context_lens, block_tables, and with PA_LAUNCH_EARLY_KV the pages) must
+ * not be written by that kernel either.  16-byte aligned
  * addresses move in 16-byte chunks; otherwise at most 256 bytes may be
  * copied (PA_ERR_UNSUPPORTED beyond).  Returns PA_ERR_INVALID_ARG for a
  * null pointer, a negative size or a bad flag, before launching anything;

@@ -43,38 +43,54 @@ def test_copy_unaligned_bytes(ops):
 
 
 def test_staged_step_chain_matches_oracle(ops):
-    """A serving loop's step as a programmatic-launch chain: the inputs copied
-    from pinned host memory by pa_copy before the wait, the prepared
-    pa_store_decode, the output copied back by pa_copy; three steps in a row
-    on two staging buffers, each output against the oracle."""
+    """A serving loop's step as a programmatic-launch chain of two kernels:
+    pa_copy stages the NEXT step's q, block tables and context lengths from
+    pinned host memory into one of three device buffers (bytes moved before
+    its wait, next launch released at once), then the prepared
+    pa_store_decode decodes this step's buffer and stores its output rows
+    straight into pinned host memory.  Steps alternate between q and -q;
+    five steps, each output against the oracle."""
     w = synth.qwen_decode_b8()
-    kc0, vc0 = w.k_cache, w.v_cache
     kref, vref = oracle_stored_caches(w)
-    ref = oracle.decode(w.q, kref, vref, w.block_tables, w.context_lens, w.scale)
-    host_q = torch.from_numpy(np.ascontiguousarray(w.q).view(np.int16)).view(
-        torch.bfloat16).pin_memory()
-    kc, vc = to_dev_bf16(kc0), to_dev_bf16(vc0)
+    qs = [w.q, w.q ^ np.uint16(0x8000)]  # bf16 bit patterns: q and -q
+    refs = [oracle.decode(q, kref, vref, w.block_tables, w.context_lens, w.scale) for q in qs]
+    B, Hq = w.batch, w.num_q_heads
+    qb, tb, cb = B * Hq * 128 * 2, w.block_tables.size * 4, B * 4
+    o_t, o_c = qb, qb + (tb + 15) // 16 * 16
+    pack = o_c + (cb + 15) // 16 * 16
+    host = []
+    for q in qs:
+        h = torch.zeros(pack, dtype=torch.uint8)
+        h[:qb] = torch.from_numpy(np.ascontiguousarray(q).view(np.uint8).reshape(-1))
+        h[o_t:o_t + tb] = torch.from_numpy(
+            np.ascontiguousarray(w.block_tables, np.int32).view(np.uint8).reshape(-1))
+        h[o_c:o_c + cb] = torch.from_numpy(
+            np.ascontiguousarray(w.context_lens, np.int32).view(np.uint8).reshape(-1))
+        host.append(h.pin_memory())
+    bufs = [torch.empty(pack, dtype=torch.uint8, device="cuda") for _ in range(3)]
+    kc, vc = to_dev_bf16(w.k_cache), to_dev_bf16(w.v_cache)
     nk, nv = to_dev_bf16(w.new_k), to_dev_bf16(w.new_v)
-    tables, ctx, slots = (to_dev_i32(w.block_tables), to_dev_i32(w.context_lens),
-                          to_dev_i32(w.slot_mapping))
-    qbuf = [torch.empty_like(host_q, device="cuda") for _ in range(2)]
-    outs = [torch.empty((w.batch, w.num_q_heads, 128), dtype=torch.float32, device="cuda")
-            for _ in range(2)]
-    ws = ops.decode_workspace(w.num_q_heads, w.num_kv_heads, 0, 128, "cuda")
-    calls = [ops.StoreDecodeCall(qbuf[i], nk, nv, kc, vc, slots, tables, ctx, w.scale, outs[i],
-                                 workspace=ws, pdl=True) for i in range(2)]
-    host_out = [torch.full((w.batch, w.num_q_heads, 128), float("nan")).pin_memory()
-                for _ in range(3)]
-    for step in range(3):
-        i = step % 2
-        ops.copy(qbuf[i], host_q, pdl=True, before_wait=step > 0)
-        calls[i]()
-        ops.copy(host_out[step], outs[i], pdl=True)
+    slots = to_dev_i32(w.slot_mapping)
+    ws = ops.decode_workspace(Hq, w.num_kv_heads, 0, 128, "cuda")
+    steps = 5
+    host_out = [torch.full((B, Hq, 128), float("nan")).pin_memory() for _ in range(steps)]
+    calls = []
+    for n in range(steps):
+        buf = bufs[n % 3]
+        calls.append(ops.StoreDecodeCall(
+            buf[:qb].view(torch.bfloat16).view(B, Hq, 128), nk, nv, kc, vc, slots,
+            buf[o_t:o_t + tb].view(torch.int32).view(w.block_tables.shape),
+            buf[o_c:o_c + cb].view(torch.int32), w.scale, host_out[n], workspace=ws,
+            pdl=True))
+    ops.copy(bufs[0], host[0])
+    for n in range(steps):
+        ops.copy(bufs[(n + 1) % 3], host[(n + 1) % 2], pdl=True, before_wait=True)
+        calls[n]()
     torch.cuda.synchronize()
     assert ops.read_error_word(ws) == 0
-    for step in range(3):
-        assert_attention_close(host_out[step].numpy().astype(np.float64), ref,
-                               f"step {step}", strict=True)
+    for n in range(steps):
+        assert_attention_close(host_out[n].numpy().astype(np.float64), refs[n % 2],
+                               f"step {n}", strict=True)
 
 
 def test_prepared_call_equals_store_decode(ops):
