@@ -300,6 +300,27 @@ def run_extras(ops, dev):
         "us_per_call": ms * 1e3, "alg_bytes": nbytes, "GB_per_s": nbytes / ms / 1e6,
         "frac_of_hbm": nbytes / ms / 1e6 / hbm, "peak_kind": hbm_kind}
     del pools
+    # the same long decode over E4M3 pools (per-kv-head scales), 4 layer pools
+    ks = torch.full((hkv,), 0.01, dtype=torch.float32, device=dev)
+    vs = torch.full((hkv,), 0.01, dtype=torch.float32, device=dev)
+    pools8 = []
+    for _ in range(L):
+        kp, vp = ops.fp8_pools(nb, hkv, device=dev)
+        kp.random_(0, 0x7F, generator=gen)     # finite positive codes
+        vp.random_(0, 0x7F, generator=gen)
+        pools8.append((kp, vp))
+
+    def dec8():
+        kp, vp = pools8[state["l"] % L]
+        state["l"] += 1
+        ops.decode_fp8(q, kp, vp, ks, vs, tables, ctx, 128 ** -0.5, out=out, workspace=ws,
+                       pdl=True, early_kv=True)
+    ms = time_graph(dec8, 4 * L)
+    nbytes = decode_alg_bytes(np.full(B, ctxlen), hq, hkv, kv_bytes=1)
+    extra["long_decode_b4_ctx32768_h32_8_fp8_e4m3"] = {
+        "us_per_call": ms * 1e3, "alg_bytes": nbytes, "GB_per_s": nbytes / ms / 1e6,
+        "frac_of_hbm": nbytes / ms / 1e6 / hbm, "peak_kind": hbm_kind}
+    del pools8
     # varlen prefill
     w = synth.varlen_prefill(keep_seq=False)
 
