@@ -8,23 +8,28 @@
 // One CTA computes a 128-row tile of one (sequence, kv head): rows are the
 // (query position, query head) pairs of PT = 128 / G consecutive positions
 // times the G query heads of the kv head, so every K/V tile read from the
-// pool serves the whole GQA group.  Per 128-key tile j:
-//   S   = Q K_j^T      tcgen05.mma (M 128, N 128, K 128), fp32 in TMEM
+// pool serves the whole GQA group.  Per 64-key tile j:
+//   S   = Q K_j^T      tcgen05.mma (M 128, N 64, K 128), fp32 in TMEM
 //   P   = exp2(S * c - m)  per row, with the causal and length masks (fp32)
-//   O  += P V_j        tcgen05.mma, O accumulated in TMEM.  A row's
-//                      exponentials use a reference max that moves only when
-//                      a tile's max exceeds it by more than 8 (base 2), so
-//                      O is rescaled in TMEM rarely; P stays <= 256.
-//                      P is split into bf16 hi + lo parts (two MMA passes)
-//                      so the product keeps ~16 bits of the fp32 weights.
-// Warps: 0 loads K tiles and 2 loads V tiles (TMA, 3 and 2 stages; the 8
-// block-table entries of a tile come in one round of lane loads); 1 issues
-// the MMAs (converged warp, one elected lane) and owns the TMEM allocation
-// (S, O, P and Q); 3..10 run the softmax, two warps per TMEM lane quarter,
-// each thread one half (64 keys, 64 output columns) of one row: they put Q
-// and then each P into their TMEM lanes (both MMAs read their A operand from
-// tensor memory) and store the output.  QK of tile j + 1 is issued as soon
-// as the softmax has copied S_j to registers, so it runs under the softmax.
+//   O  += P V_j        tcgen05.mma (M 128, N 128, K 64), O accumulated in
+//                      TMEM.  A row's exponentials use a reference max that
+//                      moves only when a tile's max exceeds it by more than 8
+//                      (base 2), so O is rescaled in TMEM rarely; P stays
+//                      <= 256.  P is split into bf16 hi + lo parts (two MMA
+//                      passes) so the product keeps ~16 bits of the fp32
+//                      weights.
+// Two CTAs share an SM (under half its shared memory, registers and tensor
+// memory each), so one CTA's softmax runs while the other's MMAs keep the
+// tensor pipe busy.  Warps: 0 loads K tiles and 2 loads V tiles (TMA, two
+// stages each; the block-table entries of eight tiles come in one round of
+// lane loads); 1 issues the MMAs (converged warp, one elected lane) and owns
+// the TMEM allocation (two score buffers and O); 3..6 run the softmax, one
+// warp per TMEM lane quarter and one row per thread: they write their Q rows
+// into shared memory, read each tile's scores, write P over them (the A
+// operand of the PV MMAs comes from tensor memory) and store the output.
+// Tile j's scores go to buffer j % 2 once the PV MMA of tile j - 2 that read
+// that buffer is done, so the score MMA of tile j + 1 runs under the softmax
+// of tile j.
 //
 // pa_prefill_store_varlen (the store of the chunks' K/V fused in): other CTAs
 // of a sequence need chunk keys this CTA stores, so the chunk is never read
@@ -45,31 +50,29 @@
 namespace pa {
 namespace {
 
-constexpr int kPfSoftWarps = 8;   // two per TMEM lane quarter: each takes half of a row
+constexpr int kPfSoftWarps = 4;   // one per TMEM lane quarter: a thread owns a row
 constexpr int kPfThreads = 32 * (3 + kPfSoftWarps);  // K loader, MMA, V loader, softmax
 constexpr int kPfRows = 128;      // M
-constexpr int kPfKeys = 128;      // keys per KV tile (N of the first MMA)
-constexpr int kHalfBytes = 128 * 128;  // 128 rows x 64 dims (bf16) with the 128-byte swizzle
-constexpr int kTileBytes2 = 2 * kHalfBytes;  // one 128 x 128 bf16 operand tile = 32 KB
-// shared memory (offsets from a 1024-aligned base)
-// K tiles are needed first (the score MMA of tile j + 1 is issued before
-// the PV MMA of tile j), so their ring is one stage deeper
-constexpr int kKStages = 3, kVStages = 2;
-constexpr int kOffK = 0;                                 // K tile j in stage j % 3
-constexpr int kOffV = kOffK + kKStages * kTileBytes2;    // V tile j in stage j % 2
+constexpr int kPfKeys = 64;       // keys per KV tile (N of the score MMA)
+constexpr int kPfPages = kPfKeys / kBlockSize;  // pages per KV tile
+constexpr int kHalfBytes = kPfKeys * 128;  // 64 keys x 64 dims (bf16) with the 128-byte swizzle
+constexpr int kTileBytes2 = 2 * kHalfBytes;  // one 64 x 128 bf16 K or V tile = 16 KB
+constexpr int kQHalf = kPfRows * 128;        // 128 rows x 64 dims of Q
+// Shared memory (offsets from a 1024-aligned base), under half an SM's so
+// that two CTAs share one: while one runs its softmax the other's MMAs keep
+// the tensor pipe busy.
+constexpr int kKStages = 2, kVStages = 2;
+constexpr int kOffQ = 0;                                  // Q tile, two 64-dim halves
+constexpr int kOffK = kOffQ + 2 * kQHalf;                 // K tile j in stage j % 2
+constexpr int kOffV = kOffK + kKStages * kTileBytes2;     // V tile j in stage j % 2
 constexpr int kOffBar = kOffV + kVStages * kTileBytes2;
-// partial row maxima / sums exchanged by the two halves of a row:
-// [tile parity][half][row] fp32
-constexpr int kOffX = kOffBar + 256;
-constexpr int kPfSmem = 1024 + kOffX + 2 * 2 * kPfRows * 4;
-// TMEM columns: S at 0..127 (fp32; the softmax copies it to registers at
-// once), O at 128..255 (fp32), P at 256..383 (bf16 hi parts in 256..319, lo
-// parts in 320..383, two keys per column), Q at 384..447 (bf16, two dims per
-// column).  Both MMAs take their A operand (Q, then P) from tensor memory, so
-// shared memory serves only the K and V tiles: its bandwidth is shared by the
-// B operands and the TMA writes alone.
-constexpr int kTmemCols = 512;
-constexpr int kTmemS = 0, kTmemO = 128, kTmemP = 256, kTmemQ = 384;
+constexpr int kPfSmem = 1024 + kOffBar + 256;
+// TMEM columns (256 of the SM's 512, two CTAs per SM): two score buffers
+// S_0, S_1 at 0..63 and 64..127 (fp32, tile j in buffer j % 2; the softmax
+// writes P over the scores it has read: bf16 hi parts in the buffer's
+// columns 0..31, lo parts in 32..63, two keys per column), O at 128..255.
+constexpr int kTmemCols = 256;
+constexpr int kTmemSCols = 64, kTmemO = 128;
 
 struct PrefillParams {
   void *out;
@@ -112,11 +115,11 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = 128,
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = n,
 // A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1).
-__host__ __device__ constexpr uint32_t umma_idesc(int b_mn) {
+__host__ __device__ constexpr uint32_t umma_idesc(int b_mn, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
-         ((uint32_t)(kPfKeys >> 3) << 17) | ((uint32_t)(kPfRows >> 4) << 24);
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kPfRows >> 4) << 24);
 }
 
 // The MMA, commit and TMA helpers below are executed by a whole converged
@@ -135,6 +138,18 @@ __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D (+)= A B with both operands described in shared memory.
+__device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -171,6 +186,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 64 consecutive fp32 columns of this thread's TMEM lane (two loads, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[2][32]) {
+  uint32_t r[64];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : "=r"(r[32 * h + 0]), "=r"(r[32 * h + 1]), "=r"(r[32 * h + 2]), "=r"(r[32 * h + 3]),
+          "=r"(r[32 * h + 4]), "=r"(r[32 * h + 5]), "=r"(r[32 * h + 6]), "=r"(r[32 * h + 7]),
+          "=r"(r[32 * h + 8]), "=r"(r[32 * h + 9]), "=r"(r[32 * h + 10]), "=r"(r[32 * h + 11]),
+          "=r"(r[32 * h + 12]), "=r"(r[32 * h + 13]), "=r"(r[32 * h + 14]),
+          "=r"(r[32 * h + 15]), "=r"(r[32 * h + 16]), "=r"(r[32 * h + 17]),
+          "=r"(r[32 * h + 18]), "=r"(r[32 * h + 19]), "=r"(r[32 * h + 20]),
+          "=r"(r[32 * h + 21]), "=r"(r[32 * h + 22]), "=r"(r[32 * h + 23]),
+          "=r"(r[32 * h + 24]), "=r"(r[32 * h + 25]), "=r"(r[32 * h + 26]),
+          "=r"(r[32 * h + 27]), "=r"(r[32 * h + 28]), "=r"(r[32 * h + 29]),
+          "=r"(r[32 * h + 30]), "=r"(r[32 * h + 31])
+        : "r"(taddr + 32 * h));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[h][i] = __uint_as_float(r[32 * h + i]);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
@@ -233,7 +275,7 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(kPfThreads, 1)
+__global__ void __launch_bounds__(kPfThreads, 2)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v,
                    const __grid_constant__ CUtensorMap tmap_nk,
@@ -246,19 +288,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
   // barrier slots ("0" slots: + 8 * stage, or + 8 * (tile & 1))
   const uint32_t b_k_full0 = smem_addr(bars + 0);
-  const uint32_t b_k_empty0 = smem_addr(bars + 3);
-  const uint32_t b_v_full0 = smem_addr(bars + 6);
-  const uint32_t b_v_empty0 = smem_addr(bars + 8);
-  const uint32_t b_q_ready = smem_addr(bars + 10);
-  const uint32_t b_s_full = smem_addr(bars + 11);
-  const uint32_t b_s_free = smem_addr(bars + 12);
-  const uint32_t b_p_full = smem_addr(bars + 13);
-  const uint32_t b_o_full0 = smem_addr(bars + 15);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 18);
-  // exchange barrier of lane quarter qq, tile parity t: bars + 19 + 2 qq + t
-  const uint32_t b_x0 = smem_addr(bars + 19);
-  float *xch = reinterpret_cast<float *>(smem + kOffX);
+  const uint32_t b_k_empty0 = smem_addr(bars + 2);
+  const uint32_t b_v_full0 = smem_addr(bars + 4);
+  const uint32_t b_v_empty0 = smem_addr(bars + 6);
+  const uint32_t b_q_ready = smem_addr(bars + 8);
+  const uint32_t b_s_full0 = smem_addr(bars + 9);   // scores of tile j in buffer j & 1
+  const uint32_t b_p_full0 = smem_addr(bars + 11);  // P of tile j written over them
+  const uint32_t b_o_full0 = smem_addr(bars + 13);  // PV of tile j done (j & 1)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 16);
 
   const int tid = threadIdx.x, lane = tid & 31;
   // broadcast from lane 0: the compiler then knows every role branch below
@@ -296,12 +334,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     constexpr int kSoft = 32 * kPfSoftWarps;
     mbar_init(b_q_ready, kSoft);
-    mbar_init(b_s_full, 1);
-    mbar_init(b_s_free, kSoft);
-    mbar_init(b_p_full, kSoft);
-    for (int i = 0; i < 8; ++i) mbar_init(b_x0 + 8 * i, 64);
-    mbar_init(b_o_full0, 1);
-    mbar_init(b_o_full0 + 8, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(b_s_full0 + 8 * i, 1);
+      mbar_init(b_p_full0 + 8 * i, kSoft);
+      mbar_init(b_o_full0 + 8 * i, 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -316,8 +353,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem + kTmemS, tmem_o = tmem + kTmemO, tmem_p = tmem + kTmemP;
-  const uint32_t tmem_q = tmem + kTmemQ;
+  const uint32_t tmem_o = tmem + kTmemO;
 
   if (warp == 0 || warp == 2) {
     // ---- TMA loaders: warp 0 brings the K tiles, warp 2 the V tiles, each
@@ -343,15 +379,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                      : "memory");
     }
     const int32_t *row = p.block_tables + (long long)s * p.bt_stride;
-    // block-table entries of four tiles (32 pages) per round of loads, one per
-    // lane: -1 = no key in the page (left as it is: masked), -2 = bad entry
+    // block-table entries of eight tiles (32 pages) per round of loads, one
+    // per lane: -1 = no key in the page (left as it is: masked), -2 = bad entry
     long long ph_lane = -1;
     int j = 0;
     for (; j < nkv; ++j) {
       const int st = j % nst, round = j / nst;
       const uint32_t dst = dst0 + st * kTileBytes2, b_full = b_full0 + 8 * st;
-      if ((j & 3) == 0) {
-        const int lb = j * (kPfKeys / kBlockSize) + lane;
+      if (j % (32 / kPfPages) == 0) {
+        const int lb = j * kPfPages + lane;
         const bool has = lb * kBlockSize < n;
         const long long ph = has && lb < p.bt_stride ? __ldg(row + lb) : -2;
         ph_lane = !has ? -1 : (ph >= 0 && ph < p.num_blocks) ? ph : -2;
@@ -359,12 +395,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(b_empty0 + 8 * st, (round - 1) & 1,
                                                            abort_flag, p.err)))
         break;
-      // lane L < 8 handles page L of the tile; its kind: pool page (TMA
+      // lane L < 4 handles page L of the tile; its kind: pool page (TMA
       // from the pool), chunk page (fused: TMA from the new rows), the page
       // that straddles the prefix (fused: assembled by the warp) or none
-      const long long phys = __shfl_sync(0xffffffffu, ph_lane, (j & 3) * 8 + (lane & 7));
-      const bool mine = lane < kPfKeys / kBlockSize;
-      const int kp0 = j * kPfKeys + (lane & 7) * kBlockSize;  // first key of the page
+      const long long phys =
+          __shfl_sync(0xffffffffu, ph_lane, (j % (32 / kPfPages)) * kPfPages + lane % kPfPages);
+      const bool mine = lane < kPfPages;
+      const int kp0 = j * kPfKeys + (lane % kPfPages) * kBlockSize;  // first key of the page
       const bool in_chunk = fused && kp0 >= prefix;
       const bool straddle = fused && kp0 < prefix && kp0 + kBlockSize > prefix;
       const bool by_tma = phys != -1 && !straddle && (in_chunk || phys >= 0);
@@ -409,7 +446,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       __syncwarp();
       // one page at a time, its index broadcast to the whole warp
 #pragma unroll
-      for (int pg = 0; pg < kPfKeys / kBlockSize; ++pg) {
+      for (int pg = 0; pg < kPfPages; ++pg) {
         if (!((okm >> pg) & 1u)) continue;
         const long long ph = __shfl_sync(0xffffffffu, phys, pg);
         const int kp = j * kPfKeys + pg * kBlockSize;
@@ -463,11 +500,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---- MMA issuer: QK of tile j + 1 goes out (once the softmax has copied
-    //      S_j to registers) before PV of tile j, so the score MMA of the next
-    //      tile overlaps the softmax of this one ----------------------------------
+    // ---- MMA issuer: S_j = Q K_j^T into buffer j & 1 (Q from shared
+    //      memory), then O += (P_hi + P_lo) V_j with P from that buffer.  The
+    //      scores of tile j + 2 go into the buffer once the PV of tile j that
+    //      read it is done, so the softmax of tile j + 1 runs with the scores
+    //      of tile j + 2 already on their way ------------------------------
     {  // the whole warp, converged (see umma_f16_ta)
-      constexpr uint32_t idesc_qk = umma_idesc(0), idesc_pv = umma_idesc(1);
+      constexpr uint32_t idesc_qk = umma_idesc(0, kPfKeys), idesc_pv = umma_idesc(1, kHeadDim);
       constexpr unsigned kAll = 0xffffffffu;
       bool ok = __all_sync(kAll, mbar_wait(b_q_ready, 0, abort_flag, p.err));
       tc_fence_after();
@@ -475,51 +514,58 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       int last_par = 0;
       // S_j = Q K_j^T: 8 k-steps of 16 dims (4 per 64-dim half)
       auto issue_qk = [&](int j) -> bool {
-        const int ks3 = j % kKStages;
-        if (!__all_sync(kAll, mbar_wait(b_k_full0 + 8 * ks3, (j / kKStages) & 1, abort_flag,
+        const int ks2 = j % kKStages;
+        if (!__all_sync(kAll, mbar_wait(b_k_full0 + 8 * ks2, (j / kKStages) & 1, abort_flag,
                                         p.err)))
           return false;
-        // the softmax has copied S_{j-1} to its registers
-        if (j >= 1 && !__all_sync(kAll, mbar_wait(b_s_free, (j - 1) & 1, abort_flag, p.err)))
+        // buffer j & 1 held P of tile j - 2: the PV that read it is done
+        if (j >= 2 && !__all_sync(kAll, mbar_wait(b_o_full0 + 8 * (j & 1), ((j - 2) >> 1) & 1,
+                                                  abort_flag, p.err)))
           return false;
         tc_fence_after();
+        const uint32_t sb = tmem + (j & 1) * kTmemSCols;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          umma_f16_ta(tmem_s, tmem_q + ks * 8,
-                      umma_desc(base + kOffK + ks3 * kTileBytes2 + off, 16, 1024), idesc_qk, ks > 0);
+          const uint32_t koff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+          const uint32_t qoff = (ks >> 2) * kQHalf + (ks & 3) * 32;
+          umma_f16_ss(sb, umma_desc(base + kOffQ + qoff, 16, 1024),
+                      umma_desc(base + kOffK + ks2 * kTileBytes2 + koff, 16, 1024), idesc_qk,
+                      ks > 0);
         }
-        umma_commit(b_s_full);
-        umma_commit(b_k_empty0 + 8 * ks3);  // the K stage may be refilled
-        last_bar = b_s_full;
-        last_par = j & 1;
+        umma_commit(b_s_full0 + 8 * (j & 1));
+        umma_commit(b_k_empty0 + 8 * ks2);  // the K stage may be refilled
+        last_bar = b_s_full0 + 8 * (j & 1);
+        last_par = (j >> 1) & 1;
         return true;
       };
       if (ok && nkv > 0) ok = issue_qk(0);
+      if (ok && nkv > 1) ok = issue_qk(1);
       int j = 0;
       for (; j < nkv && ok; ++j) {
-        if (j + 1 < nkv && !issue_qk(j + 1)) break;
-        // O += (P_hi + P_lo) V_j: 2 x 8 k-steps of 16 keys, P_j from TMEM
-        // buffer j & 1 (8 columns per step); V is MN-major (dims contiguous):
-        // LBO = distance between the two 64-dim halves, SBO = 8 keys
-        if (!__all_sync(kAll, mbar_wait(b_p_full, j & 1, abort_flag, p.err)))
+        // O += (P_hi + P_lo) V_j: 2 x 4 k-steps of 16 keys, P_j from buffer
+        // j & 1 (8 columns per step); V is MN-major (dims contiguous): LBO =
+        // distance between the two 64-dim halves, SBO = 8 keys
+        if (!__all_sync(kAll, mbar_wait(b_p_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.err)))
           break;
-        if (!__all_sync(kAll, mbar_wait(b_v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.err)))
+        if (!__all_sync(kAll, mbar_wait(b_v_full0 + 8 * (j % kVStages), (j / kVStages) & 1,
+                                        abort_flag, p.err)))
           break;
         tc_fence_after();
-        const uint32_t vb = base + kOffV + (j & 1) * kTileBytes2;
+        const uint32_t vb = base + kOffV + (j % kVStages) * kTileBytes2;
+        const uint32_t pb = tmem + (j & 1) * kTmemSCols;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_f16_ta(tmem_o, tmem_p + part * 64 + ks * 8,
+          for (int ks = 0; ks < kPfKeys / 16; ++ks)
+            umma_f16_ta(tmem_o, pb + part * (kTmemSCols / 2) + ks * 8,
                         umma_desc(vb + ks * 16 * 128, kHalfBytes, 1024), idesc_pv,
                         (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
         }
         umma_commit(b_o_full0 + 8 * (j & 1));
-        umma_commit(b_v_empty0 + 8 * (j & 1));  // the V stage may be refilled
+        umma_commit(b_v_empty0 + 8 * (j % kVStages));  // the V stage may be refilled
         last_bar = b_o_full0 + 8 * (j & 1);
         last_par = (j >> 1) & 1;
+        if (j + 2 < nkv && !issue_qk(j + 2)) break;
       }
       if (__any_sync(kAll, *abort_flag != 0) && last_bar) {
         // let issued MMAs finish before TMEM is released (bounded)
@@ -529,76 +575,59 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---- softmax / epilogue warps 3..10: warp w serves TMEM lane quarter
-    //      w % 4 (rows 32 (w % 4) .. + 31) and half hf of every row's keys
-    //      and output columns; the two warps of a quarter exchange partial
-    //      row maxima (and, at the end, sums) through shared memory ---------
+    // ---- softmax / epilogue warps 3..6: warp w serves TMEM lane quarter
+    //      w % 4 (rows 32 (w % 4) .. + 31); a thread owns its row's scores,
+    //      P and output columns ----------------------------------------------
     const int lb = 32 * (warp & 3);  // TMEM lanes this warp may access
-    const int hf = (warp - 3) >> 2;  // 0: keys / columns 0..63, 1: 64..127
     const int r = lb + lane;         // row of the tile
     const int rpos = r / G;          // query position in the tile
     const int hs = r % G;            // query head in the group
     const bool rvalid = r < rows;
     const int limit = rvalid ? prefix + pos0 + rpos : -1;  // last key this row sees
     const uint32_t trow = (uint32_t)lb << 16;
-    const uint32_t b_x = b_x0 + 8 * 2 * (warp & 3);  // + 8 * parity
-    // partial value v of this half for exchange t; returns the other half's
-    // (bounded wait: false on abort)
-    auto exchange = [&](int t, float v, float &other) -> bool {
-      xch[((t & 1) * 2 + hf) * kPfRows + r] = v;
-      mbar_arrive(b_x + 8 * (t & 1));
-      if (!__all_sync(0xffffffffu, mbar_wait(b_x + 8 * (t & 1), (t >> 1) & 1, abort_flag, p.err)))
-        return false;
-      other = xch[((t & 1) * 2 + (hf ^ 1)) * kPfRows + r];
-      return true;
-    };
 
-    // Q tile into this row's TMEM lane: row r = q[q0 + pos0 + rpos][g * G +
-    // hs][:], two dims per column in memory order (the even dim in the low
-    // half); this half brings dims 64 hf .. 64 hf + 63 (columns 32 hf ..)
+    // Q row r = q[q0 + pos0 + rpos][g * G + hs][:] into the Q tile in shared
+    // memory (K-major, two 64-dim halves, 128-byte swizzle, the layout the
+    // TMA gives the K tiles), then made visible to the tensor core
     {
       const uint4 *src = reinterpret_cast<const uint4 *>(
           p.q + ((long long)(q0 + pos0 + rpos) * p.hq + g * G + hs) * kHeadDim);
-      float qv[32];
+      uint4 qv[16];
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const uint4 v = rvalid ? __ldg(src + hf * 8 + c8) : make_uint4(0u, 0u, 0u, 0u);
-        qv[4 * c8] = __uint_as_float(v.x);
-        qv[4 * c8 + 1] = __uint_as_float(v.y);
-        qv[4 * c8 + 2] = __uint_as_float(v.z);
-        qv[4 * c8 + 3] = __uint_as_float(v.w);
+      for (int c16 = 0; c16 < 16; ++c16)
+        qv[c16] = rvalid ? __ldg(src + c16) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int c16 = 0; c16 < 16; ++c16) {
+        const uint32_t a = base + kOffQ + (c16 >> 3) * kQHalf + sw128(r, c16 & 7);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(qv[c16].x),
+                     "r"(qv[c16].y), "r"(qv[c16].z), "r"(qv[c16].w)
+                     : "memory");
       }
-      tmem_st32(tmem_q + trow + hf * 32, qv);
-      tc_fence_before();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(b_q_ready);
     }
 
-    // m: reference max (base-2 units) of this row's exponentials, the same
-    // in both halves (both combine the same two partial maxima).  It moves
+    // m: reference max (base-2 units) of this row's exponentials.  It moves
     // only when a tile's max exceeds it by more than 8 (a factor 256), so P
     // stays <= 256 and O needs rescaling (after the previous PV) rarely.
-    // l: this half's share of the row sum.
+    // l: the row sum.
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv && ok; ++j) {
       // warp-uniform: tcgen05.ld / st below are warp-collective
-      ok = __all_sync(0xffffffffu, mbar_wait(b_s_full, j & 1, abort_flag, p.err));
+      ok = __all_sync(0xffffffffu, mbar_wait(b_s_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag,
+                                            p.err));
       if (!ok) break;
       tc_fence_after();
-      const int key0 = j * kPfKeys + hf * 64;  // first key of this half
+      const uint32_t sb = tmem + (j & 1) * kTmemSCols;
+      const int key0 = j * kPfKeys;
       // every row of the tile sees every key of it: no masks
-      const bool tile_full = j * kPfKeys + kPfKeys - 1 <= prefix + pos0;
-      // this half of the S row into registers, read once; S is then free for
-      // QK of tile j + 1
+      const bool tile_full = key0 + kPfKeys - 1 <= prefix + pos0;
       float sv[2][32];
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) tmem_ld32(tmem_s + hf * 64 + trow + cc * 32, sv[cc]);
-      tc_fence_before();
-      mbar_arrive(b_s_free);
+      tmem_ld64(sb + trow, sv);
       // masked keys (diagonal and last tiles only) become -inf before the
       // max, so the max and the exponentials below have a single, unmasked
-      // body (selects, not branches; one copy of the code keeps the
-      // instruction cache warm)
+      // body (selects, not branches)
       if (!tile_full) {
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
@@ -606,7 +635,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int i = 0; i < 32; ++i)
             sv[cc][i] = key0 + cc * 32 + i <= limit ? sv[cc][i] : -INFINITY;
       }
-      // eight independent max chains, then the other half's partial max
+      // eight independent max chains
       float mx8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
@@ -614,23 +643,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
         for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[cc][i]);
-      const float mx_mine = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                  fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      float mx_other;
-      ok = exchange(j, mx_mine, mx_other);
-      if (!ok) break;
-      // the same operands in the same order in both halves: the same m
-      const float mx = hf == 0 ? fmaxf(mx_mine, mx_other) : fmaxf(mx_other, mx_mine);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float mxc = mx * c;
       const bool grow = mxc > m + 8.f;
       const float m_new = grow ? mxc : m;
       const float alpha = grow && m != -INFINITY ? exp2f(m - m_new) : 1.f;
       m = m_new;
-      // P = exp2(S c - m) in place, and this half's sum (eight chains),
-      // before waiting for the previous PV (this overlaps it).  A masked key
-      // has S = -inf, so its exponent is -inf and 2^x = +0; a row with no key
-      // yet (m = -inf: rows past the chunk) takes offset 0 instead of +inf,
-      // which keeps it -inf rather than NaN.
+      // P = exp2(S c - m) in place, and the row sum (eight chains).  A masked
+      // key has S = -inf, so its exponent is -inf and 2^x = +0; a row with no
+      // key yet (m = -inf: rows past the chunk) takes offset 0 instead of
+      // +inf, which keeps it -inf rather than NaN.
       const float neg_m = m == -INFINITY ? 0.f : -m;
       float ps8[8];
 #pragma unroll
@@ -645,30 +668,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
       const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) +
                          ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
-      // P and O are in use until the PV MMA of tile j - 1 is done
-      if (j >= 1) {
-        ok = __all_sync(0xffffffffu, mbar_wait(b_o_full0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1,
-                                              abort_flag, p.err));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      // rows whose reference max moved rescale this half of their O row
-      // (warp-wide: tcgen05.ld / st are collective)
+      // rows whose reference max moved rescale their O row, once the PV of
+      // tile j - 1 is done and before that of tile j (warp-wide: tcgen05.ld /
+      // st are collective)
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        if (j >= 1) {
+          ok = __all_sync(0xffffffffu, mbar_wait(b_o_full0 + 8 * ((j - 1) & 1),
+                                                ((j - 1) >> 1) & 1, abort_flag, p.err));
+          if (!ok) break;
+          tc_fence_after();
+        }
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < kHeadDim / 32; ++cc) {
           float ov[32];
-          tmem_ld32(tmem_o + hf * 64 + trow + cc * 32, ov);
+          tmem_ld32(tmem_o + trow + cc * 32, ov);
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-          tmem_st32(tmem_o + hf * 64 + trow + cc * 32, ov);
+          tmem_st32(tmem_o + trow + cc * 32, ov);
         }
       }
       l = l * alpha + psum;
-      // P as bf16 hi + lo into this row's TMEM lane (A operands of the PV
-      // MMAs; keys 2i and 2i + 1 share column i, the even key in the low
-      // half; this half's 64 keys are columns 32 hf .. 32 hf + 31 of each
-      // part).  hi is e with the low 16 mantissa bits cleared (exactly a
+      // P as bf16 hi + lo over the scores of this row's TMEM lane (A operands
+      // of the PV MMAs; keys 2i and 2i + 1 share column i, the even key in the
+      // low half; hi parts in the buffer's columns 0..31, lo parts in
+      // 32..63).  hi is e with the low 16 mantissa bits cleared (exactly a
       // bf16); lo = e - hi is exact in fp32 and rounded to nearest bf16 by an
       // integer add, so hi + lo is e within 2^-15 relative, without bias.
       // Both parts are byte permutes (no conversion instruction).
@@ -687,21 +710,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               __float_as_uint(sv[cc][2 * i + 1] - __uint_as_float(u1 & 0xFFFF0000u)) + 0x8000u,
               0x7632);
         }
-        tmem_st16(tmem_p + trow + hf * 32 + cc * 16, hi);
-        tmem_st16(tmem_p + trow + 64 + hf * 32 + cc * 16, lo);
+        tmem_st16(sb + trow + cc * 16, hi);
+        tmem_st16(sb + trow + kTmemSCols / 2 + cc * 16, lo);
       }
       tmem_wait_st();
       // keys past the end of the sequence: their V rows may hold anything;
       // zero them so that 0-weight rows add exactly 0 (last tile only, once
       // the V tile has landed)
-      if (j * kPfKeys + kPfKeys > n) {
-        ok = __all_sync(0xffffffffu, mbar_wait(b_v_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag,
-                                              p.err));
+      if (key0 + kPfKeys > n) {
+        ok = __all_sync(0xffffffffu, mbar_wait(b_v_full0 + 8 * (j % kVStages),
+                                              (j / kVStages) & 1, abort_flag, p.err));
         if (!ok) break;
-        const uint32_t vb = base + kOffV + (j & 1) * kTileBytes2;
-        for (int i = hf * kPfRows + r; i < kPfKeys * 16; i += 2 * kPfRows) {
+        const uint32_t vb = base + kOffV + (j % kVStages) * kTileBytes2;
+        for (int i = r; i < kPfKeys * 16; i += kPfRows) {
           const int key = i >> 4, ch = i & 15;
-          if (j * kPfKeys + key >= n) {
+          if (key0 + key >= n) {
             const uint32_t a = vb + (ch >> 3) * kHalfBytes + sw128(key, ch & 7);
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
           }
@@ -709,24 +732,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
       tc_fence_before();
-      mbar_arrive(b_p_full);
+      mbar_arrive(b_p_full0 + 8 * (j & 1));
     }
-    // epilogue: O / l -> out[q0 + pos0 + rpos][g * G + hs][64 hf .. 64 hf + 63]
-    float l_other = 0.f;
-    if (ok) ok = exchange(nkv, l, l_other);
-    if (ok)
+    // epilogue: O / l -> out[q0 + pos0 + rpos][g * G + hs][:]
+    if (ok && nkv > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(b_o_full0 + 8 * ((nkv - 1) & 1),
                                             ((nkv - 1) >> 1) & 1, abort_flag, p.err));
     tc_fence_after();
     if (ok) {
-      const float lt = hf == 0 ? l + l_other : l_other + l;
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      const long long orow =
-          ((long long)(q0 + pos0 + rpos) * p.hq + g * G + hs) * kHeadDim + hf * 64;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const long long orow = ((long long)(q0 + pos0 + rpos) * p.hq + g * G + hs) * kHeadDim;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < kHeadDim / 32; ++cc) {
         float ov[32];
-        tmem_ld32(tmem_o + hf * 64 + trow + cc * 32, ov);
+        tmem_ld32(tmem_o + trow + cc * 32, ov);
         if (rvalid) {
           if (p.out_f32) {
             float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + orow + cc * 32);
@@ -813,6 +832,9 @@ cudaError_t launch_prefill(const CUtensorMap &tk, const CUtensorMap &tv, const C
   static std::atomic<bool> configured[64] = {};
   const cudaError_t e = set_smem_once(configured, prefill_kernel<G>, device, kPfSmem);
   if (e != cudaSuccess) return e;
+  // two CTAs per SM: all of the unified L1 / shared memory as shared memory
+  // (a hint; setting it again is harmless)
+  cudaFuncSetAttribute(prefill_kernel<G>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   constexpr int PT = kPfRows / G;
   dim3 grid((max_q_len + PT - 1) / PT, pp.hkv, pp.num_seqs);
   prefill_kernel<G><<<grid, kPfThreads, kPfSmem, s>>>(tk, tv, tnk, tnv, pp);
