@@ -22,14 +22,15 @@
 // memory each), so one CTA's softmax runs while the other's MMAs keep the
 // tensor pipe busy.  Warps: 0 loads K tiles and 2 loads V tiles (TMA, two
 // stages each; the block-table entries of eight tiles come in one round of
-// lane loads); 1 issues the MMAs (converged warp, one elected lane) and owns
-// the TMEM allocation (two score buffers and O); 3..6 run the softmax, one
-// warp per TMEM lane quarter and one row per thread: they write their Q rows
-// into shared memory, read each tile's scores, write P over them (the A
-// operand of the PV MMAs comes from tensor memory) and store the output.
-// Tile j's scores go to buffer j % 2 once the PV MMA of tile j - 2 that read
-// that buffer is done, so the score MMA of tile j + 1 runs under the softmax
-// of tile j.
+// lane loads); 1 issues the score MMAs and owns the TMEM allocation (two
+// score buffers and O), 3 issues the PV MMAs (each a converged warp, one
+// elected lane, so neither chain waits behind the other); 4..7 run the
+// softmax, one warp per TMEM lane quarter and one row per thread: they write
+// their Q rows into shared memory, read each tile's scores, write P over them
+// (the A operand of the PV MMAs comes from tensor memory) and store the
+// output.  Tile j's scores go to buffer j % 2 once the PV MMA of tile j - 2
+// that read that buffer is done, so the score MMA of tile j + 1 runs under
+// the softmax of tile j.
 //
 // pa_prefill_store_varlen (the store of the chunks' K/V fused in): other CTAs
 // of a sequence need chunk keys this CTA stores, so the chunk is never read
@@ -51,7 +52,8 @@ namespace pa {
 namespace {
 
 constexpr int kPfSoftWarps = 4;   // one per TMEM lane quarter: a thread owns a row
-constexpr int kPfThreads = 32 * (3 + kPfSoftWarps);  // K loader, MMA, V loader, softmax
+constexpr int kPfThreads = 32 * (4 + kPfSoftWarps);  // K loader, QK, V loader, PV, softmax
+constexpr int kPfFirstSoftWarp = 4;
 constexpr int kPfRows = 128;      // M
 constexpr int kPfKeys = 64;       // keys per KV tile (N of the score MMA)
 constexpr int kPfPages = kPfKeys / kBlockSize;  // pages per KV tile
@@ -66,7 +68,16 @@ constexpr int kOffQ = 0;                                  // Q tile, two 64-dim 
 constexpr int kOffK = kOffQ + 2 * kQHalf;                 // K tile j in stage j % 2
 constexpr int kOffV = kOffK + kKStages * kTileBytes2;     // V tile j in stage j % 2
 constexpr int kOffBar = kOffV + kVStages * kTileBytes2;
-constexpr int kPfSmem = 1024 + kOffBar + 256;
+// 8-byte slots from kOffBar: K full / empty, V full / empty (one per stage),
+// Q ready, two score, two P and two PV barriers, the TMEM address, the abort flag
+constexpr int kBarKFull = 0, kBarKEmpty = kBarKFull + kKStages;
+constexpr int kBarVFull = kBarKEmpty + kKStages, kBarVEmpty = kBarVFull + kVStages;
+constexpr int kBarQ = kBarVEmpty + kVStages, kBarS = kBarQ + 1, kBarP = kBarS + 2;
+constexpr int kBarO = kBarP + 2, kBarTmem = kBarO + 2, kBarAbort = kBarTmem + 1;
+constexpr int kBarBytes = 256;
+static_assert((kBarAbort + 1) * 8 <= kBarBytes, "barrier slots do not fit");
+constexpr int kPfSmem = 1024 + kOffBar + kBarBytes;
+static_assert(kPfSmem <= 227 * 1024, "shared memory over the per-CTA limit");
 // TMEM columns (256 of the SM's 512, two CTAs per SM): two score buffers
 // S_0, S_1 at 0..63 and 64..127 (fp32, tile j in buffer j % 2; the softmax
 // writes P over the scores it has read: bf16 hi parts in the buffer's
@@ -286,17 +297,18 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t base = smem_addr(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-  // barrier slots ("0" slots: + 8 * stage, or + 8 * (tile & 1))
-  const uint32_t b_k_full0 = smem_addr(bars + 0);
-  const uint32_t b_k_empty0 = smem_addr(bars + 2);
-  const uint32_t b_v_full0 = smem_addr(bars + 4);
-  const uint32_t b_v_empty0 = smem_addr(bars + 6);
-  const uint32_t b_q_ready = smem_addr(bars + 8);
-  const uint32_t b_s_full0 = smem_addr(bars + 9);   // scores of tile j in buffer j & 1
-  const uint32_t b_p_full0 = smem_addr(bars + 11);  // P of tile j written over them
-  const uint32_t b_o_full0 = smem_addr(bars + 13);  // PV of tile j done (j & 1)
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 16);
+  // barrier slots ("0" slots: + 8 * stage, or + 8 * (tile & 1)), laid out
+  // from the stage counts: no two barriers share a slot
+  const uint32_t b_k_full0 = smem_addr(bars + kBarKFull);
+  const uint32_t b_k_empty0 = smem_addr(bars + kBarKEmpty);
+  const uint32_t b_v_full0 = smem_addr(bars + kBarVFull);
+  const uint32_t b_v_empty0 = smem_addr(bars + kBarVEmpty);
+  const uint32_t b_q_ready = smem_addr(bars + kBarQ);
+  const uint32_t b_s_full0 = smem_addr(bars + kBarS);  // scores of tile j in buffer j & 1
+  const uint32_t b_p_full0 = smem_addr(bars + kBarP);  // P of tile j written over them
+  const uint32_t b_o_full0 = smem_addr(bars + kBarO);  // PV of tile j done (j & 1)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kBarTmem);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + kBarAbort);
 
   const int tid = threadIdx.x, lane = tid & 31;
   // broadcast from lane 0: the compiler then knows every role branch below
@@ -499,31 +511,31 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         mbar_wait(b_full0 + 8 * (i % nst), (i / nst) & 1, &never, nullptr);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---- MMA issuer: S_j = Q K_j^T into buffer j & 1 (Q from shared
-    //      memory), then O += (P_hi + P_lo) V_j with P from that buffer.  The
-    //      scores of tile j + 2 go into the buffer once the PV of tile j that
-    //      read it is done, so the softmax of tile j + 1 runs with the scores
-    //      of tile j + 2 already on their way ------------------------------
-    {  // the whole warp, converged (see umma_f16_ta)
-      constexpr uint32_t idesc_qk = umma_idesc(0, kPfKeys), idesc_pv = umma_idesc(1, kHeadDim);
-      constexpr unsigned kAll = 0xffffffffu;
+  } else if (warp == 1 || warp == 3) {
+    // ---- MMA issuers, each a whole converged warp (see umma_f16_ta).  Warp
+    //      1 issues S_j = Q K_j^T into buffer j & 1 (Q from shared memory)
+    //      once the PV MMA of tile j - 2, which read that buffer, is done;
+    //      warp 3 issues O += (P_hi + P_lo) V_j with P from buffer j & 1.
+    //      Two issuers keep either chain from waiting behind the other ----
+    constexpr uint32_t idesc_qk = umma_idesc(0, kPfKeys), idesc_pv = umma_idesc(1, kHeadDim);
+    constexpr unsigned kAll = 0xffffffffu;
+    uint32_t last_bar = 0;  // barrier of this warp's latest commit (drained on abort)
+    int last_par = 0;
+    if (warp == 1) {
       bool ok = __all_sync(kAll, mbar_wait(b_q_ready, 0, abort_flag, p.err));
       tc_fence_after();
-      uint32_t last_bar = 0;  // barrier of the latest commit (drained on abort)
-      int last_par = 0;
-      // S_j = Q K_j^T: 8 k-steps of 16 dims (4 per 64-dim half)
-      auto issue_qk = [&](int j) -> bool {
+      for (int j = 0; j < nkv && ok; ++j) {
         const int ks2 = j % kKStages;
-        if (!__all_sync(kAll, mbar_wait(b_k_full0 + 8 * ks2, (j / kKStages) & 1, abort_flag,
-                                        p.err)))
-          return false;
+        ok = __all_sync(kAll, mbar_wait(b_k_full0 + 8 * ks2, (j / kKStages) & 1, abort_flag,
+                                        p.err));
         // buffer j & 1 held P of tile j - 2: the PV that read it is done
-        if (j >= 2 && !__all_sync(kAll, mbar_wait(b_o_full0 + 8 * (j & 1), ((j - 2) >> 1) & 1,
-                                                  abort_flag, p.err)))
-          return false;
+        if (ok && j >= 2)
+          ok = __all_sync(kAll, mbar_wait(b_o_full0 + 8 * (j & 1), ((j - 2) >> 1) & 1,
+                                          abort_flag, p.err));
+        if (!ok) break;
         tc_fence_after();
         const uint32_t sb = tmem + (j & 1) * kTmemSCols;
+        // 8 k-steps of 16 dims (4 per 64-dim half)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t koff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
@@ -536,15 +548,12 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         umma_commit(b_k_empty0 + 8 * ks2);  // the K stage may be refilled
         last_bar = b_s_full0 + 8 * (j & 1);
         last_par = (j >> 1) & 1;
-        return true;
-      };
-      if (ok && nkv > 0) ok = issue_qk(0);
-      if (ok && nkv > 1) ok = issue_qk(1);
-      int j = 0;
-      for (; j < nkv && ok; ++j) {
-        // O += (P_hi + P_lo) V_j: 2 x 4 k-steps of 16 keys, P_j from buffer
-        // j & 1 (8 columns per step); V is MN-major (dims contiguous): LBO =
-        // distance between the two 64-dim halves, SBO = 8 keys
+      }
+    } else {
+      for (int j = 0; j < nkv; ++j) {
+        // 2 x 4 k-steps of 16 keys, P_j from buffer j & 1 (8 columns per
+        // step); V is MN-major (dims contiguous): LBO = distance between the
+        // two 64-dim halves, SBO = 8 keys
         if (!__all_sync(kAll, mbar_wait(b_p_full0 + 8 * (j & 1), (j >> 1) & 1, abort_flag, p.err)))
           break;
         if (!__all_sync(kAll, mbar_wait(b_v_full0 + 8 * (j % kVStages), (j / kVStages) & 1,
@@ -565,17 +574,16 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         umma_commit(b_v_empty0 + 8 * (j % kVStages));  // the V stage may be refilled
         last_bar = b_o_full0 + 8 * (j & 1);
         last_par = (j >> 1) & 1;
-        if (j + 2 < nkv && !issue_qk(j + 2)) break;
       }
-      if (__any_sync(kAll, *abort_flag != 0) && last_bar) {
-        // let issued MMAs finish before TMEM is released (bounded)
-        volatile int never = 0;
-        mbar_wait(last_bar, last_par, &never, nullptr);
-      }
+    }
+    if (__any_sync(kAll, *abort_flag != 0) && last_bar) {
+      // let this warp's issued MMAs finish before TMEM is released (bounded)
+      volatile int never = 0;
+      mbar_wait(last_bar, last_par, &never, nullptr);
     }
     __syncwarp();
   } else {
-    // ---- softmax / epilogue warps 3..6: warp w serves TMEM lane quarter
+    // ---- softmax / epilogue warps 4..7: warp w serves TMEM lane quarter
     //      w % 4 (rows 32 (w % 4) .. + 31); a thread owns its row's scores,
     //      P and output columns ----------------------------------------------
     const int lb = 32 * (warp & 3);  // TMEM lanes this warp may access
