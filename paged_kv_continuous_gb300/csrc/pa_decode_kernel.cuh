@@ -455,13 +455,12 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 
 // A cut sequence's counter word holds two counts: the pieces that have
 // arrived (low 16 bits) and the pieces whose partial rows are published
-// (high 16 bits).  A piece arrives and publishes in one release add
-// (kArrivePublish) or, the CTA's final piece, arrives first with a relaxed
-// add (kArrive) and publishes afterwards (kPublish) unless it arrived last:
-// the last arrival merges, so it needs only to see every other piece
+// (high 16 bits).  A piece arrives first with a relaxed add (kArrive) and
+// publishes afterwards with a release add (kPublish) unless it arrived
+// last: the last arrival merges, so it needs only to see every other piece
 // published and never publishes its own rows.  Piece counts stay below 2^16
 // (at most PA_DECODE_MAX_SPLITS).
-constexpr int kArrive = 1, kPublish = 1 << 16, kArrivePublish = kArrive | kPublish;
+constexpr int kArrive = 1, kPublish = 1 << 16;
 __device__ __forceinline__ int arrived_count(int w) { return w & 0xFFFF; }
 __device__ __forceinline__ int published_count(int w) { return (int)((unsigned)w >> 16); }
 
@@ -1136,9 +1135,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     //          several warps per kv head it combines their rows and writes
     //          the output rows (whole sequence) or the partial (cut piece);
     //          with one warp per kv head the consumers wrote the rows already.
-    //          For a cut piece it then publishes: fence, arrival, and the
-    //          merge if the piece arrives last.  The consumers never wait for
-    //          this, except to reuse a buffer two pieces later.
+    //          A cut piece arrives on its sequence's counter when the warp
+    //          takes it, before the combine, and publishes its rows after
+    //          writing them, unless it arrived last: then its CTA owes the
+    //          merge.  The consumers never wait for this, except to reuse a
+    //          buffer two pieces later.
     wait_prev_then_release();
     zero_empty_rows(lane, 32);
     // While it waits for the next piece, lane 0 watches the arrival counter
@@ -1245,6 +1246,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (lane == 0) mbar_arrive(smem_addr(&ctl->ew_done));
         return;
       }
+      // a cut piece arrives now, before the combine (relaxed: it publishes
+      // its rows after writing them), so that its arrival is not late
+      int early_word = 0;
+      if (d.kind == kPieceCut && lane == 0)
+        early_word = atom_add_relaxed_gpu(p.counters + d.cs1, kArrive);
       if constexpr (S::NPH > 1) {
         const float *rk = red + k * S::RED_ONE_FLOATS;
         // per query head: the normalised weight of each of its NPH warps
@@ -1299,14 +1305,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           // release: the partial rows (this warp's, or the consumers' that
           // the red_full barrier ordered before) precede the arrival, which
           // publishes them too
-          last = arrived_count(atom_add_release_gpu(p.counters + d.cs1, kArrivePublish)) ==
-                 d.pieces - 1;
+          last = arrived_count(early_word) == d.pieces - 1;
+          if (!last) atom_add_release_gpu(p.counters + d.cs1, kPublish);
         }
         if (lane == 0 && last) {
-          // arrived last: wait (acquire) until every piece is published and
-          // leave the merge to the consumer warps, which merge with all
-          // their threads once the CTA's own blocks are done
-          wait_published(p.counters + d.cs1, d.pieces, abort_flag, p.err);
+          // arrived last: its own rows stay unpublished (this CTA merges);
+          // wait (acquire) until every other piece is published and leave
+          // the merge to the consumer warps
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          wait_published(p.counters + d.cs1, d.pieces - 1, abort_flag, p.err);
           ctl->def_b = d.b;
           ctl->def_cs0 = d.cs0;
           ctl->def_cs1 = d.cs1;
