@@ -132,7 +132,11 @@ typedef int32_t pa_status;
  * Every write and every other read happens after it, so the results are the
  * same with and without the flag.  The decode kernels let the kernel after
  * them begin only once they have passed their own wait: when that next
- * kernel starts, every kernel before them has completed.
+ * kernel starts, every kernel before them has completed.  A decode call that
+ * also launches the merge kernel (the partition below) lets the next call
+ * begin at once from that kernel, so its decode kernel may still run when
+ * the next call's first kernel begins: the "kernel launched immediately
+ * before" in the guarantees here and below is then that whole call.
  *
  * PA_LAUNCH_EARLY_KV (decode entry points only, together with
  * PA_LAUNCH_PDL): the kernel also requests the K/V pages of its first ring
@@ -334,7 +338,12 @@ PA_API pa_status pa_store_kv_fp8(const void *k, const void *v, int64_t num_token
  * over those keys, plus the natural-log sum-exp of its scaled scores.  The
  * split that completes a sequence's set of partials (counted in
  * counters[c1]) merges them into the output rows and sets the counter back
- * to zero, all inside the decode kernel.
+ * to zero, all inside the decode kernel.  Launches with num_kv_heads >= 4
+ * and S >= 8 * batch (few sequences, each cut into many pieces of many query
+ * heads) merge differently: the decode kernel only writes the partials, and
+ * the call's second kernel (the merge kernel, a programmatic dependent launch
+ * right behind it) merges every cut sequence once the decode kernel has
+ * completed; the counters are not used.
  *
  * Workspace layout (bytes from the workspace pointer; R(x) rounds x up to
  * a multiple of 256; H = num_q_heads, D = head_dim, C = 256 + 4 *
@@ -500,11 +509,12 @@ PA_API pa_status pa_decode_fp8(void *out, int32_t out_dtype, const void *q, cons
  * context_lens, block_size and num_splits) and every query head, with
  * partials (o_i, lse_i) read from the workspace slots listed above:
  *   M = max_i lse_i,  w_i = exp(lse_i - M),  out = sum_i w_i o_i / sum_i w_i.
- * Rows of sequences held by a single split are not touched.  pa_decode
- * performs the same merge inside its own kernel; this standalone kernel
- * combines partials that are already in a workspace (e.g. written by
- * another producer, or kept for inspection) and lets the merge be tested
- * and timed on its own.  Counters are neither read nor written.
+ * Rows of sequences held by a single split are not touched.  This is the
+ * merge kernel that pa_decode launches behind its decode kernel for launches
+ * with few long sequences (partition above); it also combines partials that
+ * are already in a workspace (e.g. written by another producer, or kept for
+ * inspection) and lets the merge be tested and timed on its own.  Counters
+ * are neither read nor written.
  */
 PA_API pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *workspace,
                           size_t workspace_bytes, const int32_t *context_lens,

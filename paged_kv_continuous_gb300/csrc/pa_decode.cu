@@ -27,47 +27,133 @@ struct MergeParams {
   int num_splits;
 };
 
-constexpr int kMergeSeqPerCta = 8;
+constexpr int kMergeWarps = 2;   // query heads per CTA, one warp each
+constexpr int kMergeChunk = 16;  // pieces whose loads are in flight together
 
-// grid (ceil(batch / 8), num_q_heads); warp w merges row (b0 + w, head).
-__global__ void __launch_bounds__(32 * kMergeSeqPerCta) merge_kernel(const MergeParams p) {
-  __shared__ unsigned long long tot[2];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b0 = blockIdx.x * kMergeSeqPerCta;
-  const int h = blockIdx.y;
-  if (tid < 2) tot[tid] = 0;
-  __syncthreads();
-  unsigned long long all = 0, before = 0;
-  for (int b = tid; b < p.batch; b += blockDim.x) {
-    const int n = seq_blocks(p.context_lens, b);
-    all += n;
-    if (b < b0) before += n;
-  }
+// Log-sum-exp merge of one output row (sequence b, query head h) from the
+// split-K partials of splits c0..c1 (slot 1 of c0, slot 0 of the others;
+// partials are [slot][split][head][dim]) by one warp; lane l owns dims
+// 4l..4l+3.  When N >= S every split holds at least one block; otherwise
+// empty splits are skipped.  Pieces go in split order, kMergeChunk at a
+// time with all their loads (lane i < kMergeChunk: the lse of piece i;
+// every lane: its four dims of each piece's row) in flight together, so a
+// sequence of up to kMergeChunk pieces costs one round trip.  With M the
+// running maximum of the lse values the weights are e_i = exp(lse_i - M); a
+// chunk that raises M rescales the sums so far by exp(M_old - M_new) (one
+// chunk: out = sum_i e_i o_i / sum_i e_i with M = max_i lse_i).
+__device__ __forceinline__ void merge_row_chunked(const float *part_o, const float *part_lse,
+                                                  void *out, int out_f32, long long out_row,
+                                                  int HQ, int h, long long c0, long long c1,
+                                                  long long S, long long N, int lane) {
+  const bool dense = N >= S;
+  auto piece = [&](long long cc) -> bool {
+    return cc <= c1 && (dense || cc == c0 || split_begin(cc, S, N) < split_begin(cc + 1, S, N));
+  };
+  auto row_of = [&](long long cc) -> long long { return ((cc == c0 ? 1 : 0) * S + cc) * HQ + h; };
+  float M = -INFINITY, W = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long base = c0; base <= c1; base += kMergeChunk) {
+    const long long mine = base + lane;
+    const float ls =
+        lane < kMergeChunk && piece(mine) ? __ldcg(part_lse + row_of(mine)) : -INFINITY;
+    float4 v[kMergeChunk];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    all += __shfl_xor_sync(0xffffffffu, all, off);
-    before += __shfl_xor_sync(0xffffffffu, before, off);
+    for (int u = 0; u < kMergeChunk; ++u)
+      v[u] = piece(base + u)
+                 ? __ldcg(reinterpret_cast<const float4 *>(part_o + row_of(base + u) * kHeadDim) +
+                          lane)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    float mc = ls;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
+    const float Mn = fmaxf(M, mc);
+    if (Mn == -INFINITY) continue;  // no piece with a key so far
+    const float sc = __expf(M - Mn);  // 0 for the first chunk (M = -inf)
+    W *= sc;
+    acc.x *= sc;
+    acc.y *= sc;
+    acc.z *= sc;
+    acc.w *= sc;
+#pragma unroll
+    for (int u = 0; u < kMergeChunk; ++u) {
+      const float lu = __shfl_sync(0xffffffffu, ls, u);
+      const float e = lu == -INFINITY ? 0.f : __expf(lu - Mn);
+      W += e;
+      acc.x = fmaf(e, v[u].x, acc.x);
+      acc.y = fmaf(e, v[u].y, acc.y);
+      acc.z = fmaf(e, v[u].z, acc.z);
+      acc.w = fmaf(e, v[u].w, acc.w);
+    }
+    M = Mn;
   }
-  if (lane == 0) {
-    if (all) atomicAdd(&tot[0], all);
-    if (before) atomicAdd(&tot[1], before);
-  }
-  __syncthreads();
-  const int b = b0 + warp;
-  if (b >= p.batch) return;
-  const long long N = (long long)tot[0];
-  long long P = (long long)tot[1];
-  for (int x = b0; x < b; ++x) P += seq_blocks(p.context_lens, x);
-  const int n = seq_blocks(p.context_lens, b);
-  if (n == 0) return;
-  const long long S = p.num_splits;
-  const long long c0 = split_of_block(P, S, N);
-  const long long c1 = split_of_block(P + n - 1, S, N);
-  if (c0 == c1) return;
-  merge_row(p.part_o, p.part_lse, p.out, p.out_f32, (long long)b * p.num_q_heads + h,
-            p.num_q_heads, h, c0, c1, S, N, lane);
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  store_out4(out, out_f32, out_row * kHeadDim + lane * 4,
+             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
 }
 
+// grid (S, ceil(num_q_heads / kMergeWarps)).  Every cut sequence ends in
+// exactly one split: the one that holds its last block, whose first block
+// lies inside the sequence.  CTA (c, y) merges the sequence holding split c's
+// first block when that sequence starts before it and ends inside split c,
+// for query heads kMergeWarps y + warp.  Block counts and the partition come
+// from context_lens alone, before the wait for the kernel before it (the
+// decode kernel, under a programmatic dependent launch); the partials after
+// it.  The next kernel in the stream may begin at once: its own wait covers
+// this one.
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergeParams p) {
+  griddep_launch_dependents();
+  __shared__ long long warp_tot[kMergeWarps];
+  __shared__ long long found[3];  // the sequence holding block lo: index, first block, blocks
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long S = p.num_splits, c = blockIdx.x;
+  if (tid == 0) found[0] = -1;
+  // block-wide inclusive scans of the block counts, 32 kMergeWarps at a
+  // time: pass 0 sums them (N), pass 1 finds the sequence holding block lo
+  long long N = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const long long lo = pass ? split_begin(c, S, N) : 0;
+    const long long hi = pass ? split_begin(c + 1, S, N) : 0;
+    if (pass && lo >= hi) return;  // no block in this split
+    long long running = 0;
+    for (int base = 0; base < p.batch; base += 32 * kMergeWarps) {
+      const int b = base + tid;
+      const int n = b < p.batch ? seq_blocks(p.context_lens, b) : 0;
+      long long incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      __syncthreads();  // the previous round's warp totals have been read
+      if (lane == 31) warp_tot[warp] = incl;
+      __syncthreads();
+      long long before = running;
+      for (int w = 0; w < kMergeWarps; ++w) {
+        if (w < warp) before += warp_tot[w];
+        running += warp_tot[w];
+      }
+      const long long prefix = before + incl - n;
+      if (pass && b < p.batch && n > 0 && prefix <= lo && lo < prefix + n) {
+        found[0] = b;
+        found[1] = prefix;
+        found[2] = n;
+      }
+    }
+    N = running;
+    if (N == 0) return;
+  }
+  __syncthreads();
+  const long long b = found[0];
+  if (b < 0) return;
+  const long long P = found[1], n = found[2];
+  const long long lo = split_begin(c, S, N), hi = split_begin(c + 1, S, N);
+  if (!(P < lo && P + n <= hi)) return;  // not a cut sequence ending in this split
+  const int h = blockIdx.y * kMergeWarps + warp;
+  if (h >= p.num_q_heads) return;
+  griddep_wait();
+  merge_row_chunked(p.part_o, p.part_lse, p.out, p.out_f32, b * p.num_q_heads + h,
+                    p.num_q_heads, h, split_of_block(P, S, N), c, S, N, lane);
+}
 
 namespace {
 
@@ -134,10 +220,10 @@ bool encode_pool_maps_fp8(CUtensorMap *mk, CUtensorMap *mv, const void *k_pool,
              CUDA_SUCCESS;
 }
 
-cudaError_t launch_merge(const MergeParams &m, cudaStream_t s) {
-  dim3 grid((m.batch + kMergeSeqPerCta - 1) / kMergeSeqPerCta, m.num_q_heads);
-  merge_kernel<<<grid, 32 * kMergeSeqPerCta, 0, s>>>(m);
-  return cudaGetLastError();
+cudaError_t launch_merge(const MergeParams &m, cudaStream_t s, bool pdl) {
+  const dim3 grid((unsigned)m.num_splits,
+                  (unsigned)((m.num_q_heads + kMergeWarps - 1) / kMergeWarps));
+  return launch_kernel(merge_kernel, grid, dim3(32 * kMergeWarps), 0, s, pdl, m);
 }
 
 }  // namespace
@@ -204,13 +290,25 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
     return PA_ERR_LAUNCH;
   const int G = r.num_q_heads / r.num_kv_heads;
   const bool pdl = (r.flags & PA_LAUNCH_PDL) != 0;
+  // Few sequences over many splits (at least 8 per sequence) with 4 or 8 kv
+  // heads: every cut sequence has many pieces of many query heads, and one
+  // CTA merging them at the end of the decode kernel sets its end; merge
+  // them in merge_kernel instead, spread over all splits and heads.
+  const bool split_merge = !r.positions && r.num_kv_heads >= 4 &&
+                           (long long)r.splits >= 8LL * r.batch;
   cudaError_t e;
   if (r.fp8) {
     switch (r.num_kv_heads) {
       case 1: e = launch_decode<1, true>(G, tk, tv, p, s, device, pdl); break;
       case 2: e = launch_decode<2, true>(G, tk, tv, p, s, device, pdl); break;
-      case 4: e = launch_decode<4, true>(G, tk, tv, p, s, device, pdl); break;
-      default: e = launch_decode<8, true>(G, tk, tv, p, s, device, pdl); break;
+      case 4:
+        e = split_merge ? launch_decode<4, true, false, true>(G, tk, tv, p, s, device, pdl)
+                        : launch_decode<4, true>(G, tk, tv, p, s, device, pdl);
+        break;
+      default:
+        e = split_merge ? launch_decode<8, true, false, true>(G, tk, tv, p, s, device, pdl)
+                        : launch_decode<8, true>(G, tk, tv, p, s, device, pdl);
+        break;
     }
   } else if (r.positions) {
     switch (r.num_kv_heads) {
@@ -223,11 +321,32 @@ pa_status run_decode(const DecodeRequest &r, void *workspace, int32_t *err, int 
     switch (r.num_kv_heads) {
       case 1: e = launch_decode<1, false>(G, tk, tv, p, s, device, pdl); break;
       case 2: e = launch_decode<2, false>(G, tk, tv, p, s, device, pdl); break;
-      case 4: e = launch_decode<4, false>(G, tk, tv, p, s, device, pdl); break;
-      default: e = launch_decode<8, false>(G, tk, tv, p, s, device, pdl); break;
+      case 4:
+        e = split_merge ? launch_decode<4, false, false, true>(G, tk, tv, p, s, device, pdl)
+                        : launch_decode<4, false>(G, tk, tv, p, s, device, pdl);
+        break;
+      default:
+        e = split_merge ? launch_decode<8, false, false, true>(G, tk, tv, p, s, device, pdl)
+                        : launch_decode<8, false>(G, tk, tv, p, s, device, pdl);
+        break;
     }
   }
-  return e == cudaSuccess ? PA_OK : PA_ERR_LAUNCH;
+  if (e != cudaSuccess) return PA_ERR_LAUNCH;
+  if (split_merge) {
+    // a programmatic dependent launch behind the decode kernel: it waits
+    // for the partials, and lets the next kernel in the stream begin at once
+    MergeParams m;
+    m.out = r.out;
+    m.out_f32 = p.out_f32;
+    m.part_o = p.part_o;
+    m.part_lse = p.part_lse;
+    m.context_lens = r.context_lens;
+    m.batch = r.batch;
+    m.num_q_heads = r.num_q_heads;
+    m.num_splits = r.splits;
+    if (launch_merge(m, s, true) != cudaSuccess) return PA_ERR_LAUNCH;
+  }
+  return PA_OK;
 }
 
 pa_status check_decode_request(DecodeRequest &r, int *device_out) {
@@ -459,6 +578,7 @@ extern "C" pa_status pa_decode_merge(void *out, int32_t out_dtype, const void *w
   m.batch = batch;
   m.num_q_heads = num_q_heads;
   m.num_splits = num_splits;
-  return launch_merge(m, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK
-                                                                           : PA_ERR_LAUNCH;
+  return launch_merge(m, static_cast<cudaStream_t>(stream), false) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_LAUNCH;
 }

@@ -1,8 +1,10 @@
-// Instantiates decode_kernel<G, PA_HKV, PA_F8, PA_ROPE> for G = 1..8 and the
-// launcher the host ABI dispatches to.  Included once per kv-head count and
-// variant by pa_decode_h{1,2,4,8}.cu (bf16 pools), pa_decode_f8_h{1,2,4,8}.cu
-// (FP8 pools) and pa_decode_rope_h{1,2,4,8}.cu (bf16 pools, rotary embedding
-// in the fused store) so that the instantiations compile in parallel.
+// Instantiates decode_kernel<G, PA_HKV, PA_F8, PA_ROPE, PA_SPLIT> for G = 1..8
+// and the launcher the host ABI dispatches to.  Included once per kv-head
+// count and variant by pa_decode_h{1,2,4,8}.cu (bf16 pools),
+// pa_decode_f8_h{1,2,4,8}.cu (FP8 pools), pa_decode_rope_h{1,2,4,8}.cu (bf16
+// pools, rotary embedding in the fused store), and pa_decode_sm_h{4,8}.cu /
+// pa_decode_f8_sm_h{4,8}.cu (merges left to merge_kernel) so that the
+// instantiations compile in parallel.
 #include "pa_decode_kernel.cuh"
 
 #ifndef PA_HKV
@@ -14,6 +16,9 @@
 #ifndef PA_ROPE
 #define PA_ROPE false
 #endif
+#ifndef PA_SPLIT
+#define PA_SPLIT false
+#endif
 
 namespace pa {
 
@@ -23,16 +28,16 @@ cudaError_t launch_g(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeP
                      cudaStream_t s, int device, bool pdl) {
   using Sh = DecodeShape<G, PA_HKV, PA_F8, PA_ROPE>;
   static std::atomic<bool> configured[64] = {};
-  const cudaError_t e =
-      set_smem_once(configured, decode_kernel<G, PA_HKV, PA_F8, PA_ROPE>, device, Sh::SMEM);
+  const cudaError_t e = set_smem_once(
+      configured, decode_kernel<G, PA_HKV, PA_F8, PA_ROPE, PA_SPLIT>, device, Sh::SMEM);
   if (e != cudaSuccess) return e;
-  return launch_kernel(decode_kernel<G, PA_HKV, PA_F8, PA_ROPE>, dim3(p.num_splits),
+  return launch_kernel(decode_kernel<G, PA_HKV, PA_F8, PA_ROPE, PA_SPLIT>, dim3(p.num_splits),
                        dim3(kDecodeThreads), Sh::SMEM, s, pdl, tk, tv, p);
 }
 }  // namespace
 
 template <>
-cudaError_t launch_decode<PA_HKV, PA_F8, PA_ROPE>(int G, const CUtensorMap &tk, const CUtensorMap &tv,
+cudaError_t launch_decode<PA_HKV, PA_F8, PA_ROPE, PA_SPLIT>(int G, const CUtensorMap &tk, const CUtensorMap &tv,
                                   const DecodeParams &p, cudaStream_t s, int device,
                                   bool pdl) {
   switch (G) {

@@ -818,7 +818,9 @@ __device__ bool merge_sequence_bulk(const DecodeParams &p, int b, long long c0, 
   return true;
 }
 
-template <int G, int HKV, bool F8 = false, bool ROPE = false>
+// SPLIT_MERGE: cut pieces only write their partials; merge_kernel, launched
+// behind this kernel, merges them (no counters, no merges in this kernel).
+template <int G, int HKV, bool F8 = false, bool ROPE = false, bool SPLIT_MERGE = false>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
@@ -1249,7 +1251,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       // a cut piece arrives now, before the combine (relaxed: it publishes
       // its rows after writing them), so that its arrival is not late
       int early_word = 0;
-      if (d.kind == kPieceCut && lane == 0)
+      if (!SPLIT_MERGE && d.kind == kPieceCut && lane == 0)
         early_word = atom_add_relaxed_gpu(p.counters + d.cs1, kArrive);
       if constexpr (S::NPH > 1) {
         const float *rk = red + k * S::RED_ONE_FLOATS;
@@ -1299,7 +1301,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         __syncwarp();
       }
       if (lane == 0) mbar_arrive(smem_addr(&ctl->red_empty[k]));  // buffer k is free again
-      if (d.kind == kPieceCut) {
+      if (!SPLIT_MERGE && d.kind == kPieceCut) {
         int last = 0;
         if (lane == 0) {
           // release: the partial rows (this warp's, or the consumers' that
@@ -1451,7 +1453,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (need_q) {
           // this warp's first stage of the piece: it carries the q rows
           need_q = false;
-          if (ct == 0 && !pc_done) piece_splits(gb, j, n);
+          if (!SPLIT_MERGE && ct == 0 && !pc_done) piece_splits(gb, j, n);
           if (have) {
             const uint32_t qrow = sbase + 2 * S::KV_BYTES + (g * G + gid) * kHeadDim * 2;
 #pragma unroll
@@ -1799,7 +1801,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) o[mt][i] *= vsc;
       }
-      if (ct == 0 && !pc_done) piece_splits(gb, j, n);  // warp 0 had no stage in the piece
+      // (warp 0 may have had no stage in the piece)
+      if (!SPLIT_MERGE && ct == 0 && !pc_done) piece_splits(gb, j, n);
       const bool head_cut = gb - j < lo;  // the sequence starts before this CTA's blocks
       const bool tail_cut = j < n - 1;
       const bool whole = !head_cut && !tail_cut;
@@ -1810,7 +1813,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       // the rest of the ring receives the other pieces' rows for the merge
       float *own_o = reinterpret_cast<float *>(smem);
       float *own_lse = own_o + S::HQ * kHeadDim;
-      const bool keep_own = !whole && final_piece;
+      const bool keep_own = !SPLIT_MERGE && !whole && final_piece;
       float L0 = l0, L1 = l1;
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
@@ -2127,9 +2130,10 @@ consumers_done:
   }
 }
 
-// Launches decode_kernel<G, HKV, F8, ROPE> for one G (defined per HKV, F8
-// and ROPE in pa_decode_h*.cu, pa_decode_f8_h*.cu and pa_decode_rope_h*.cu).
-template <int HKV, bool F8, bool ROPE = false>
+// Launches decode_kernel<G, HKV, F8, ROPE, SPLIT_MERGE> for one G (defined per
+// HKV and variant in pa_decode_h*.cu, pa_decode_f8_h*.cu, pa_decode_rope_h*.cu
+// and, with SPLIT_MERGE, pa_decode_sm_h{4,8}.cu and pa_decode_f8_sm_h{4,8}.cu).
+template <int HKV, bool F8, bool ROPE = false, bool SPLIT_MERGE = false>
 cudaError_t launch_decode(int G, const CUtensorMap &tk, const CUtensorMap &tv,
                           const DecodeParams &p, cudaStream_t s, int device, bool pdl);
 
