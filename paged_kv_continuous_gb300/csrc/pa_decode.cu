@@ -27,32 +27,34 @@ struct MergeParams {
   int num_splits;
 };
 
-constexpr int kMergeWarps = 2;   // query heads per CTA, one warp each
-constexpr int kMergeChunk = 16;  // pieces whose loads are in flight together
+constexpr int kMergeWarps = 4;   // warps per (sequence, head) row, a quarter of its pieces each
+constexpr int kMergeChunk = 16;  // pieces whose loads are in flight together in one warp
 
-// Log-sum-exp merge of one output row (sequence b, query head h) from the
-// split-K partials of splits c0..c1 (slot 1 of c0, slot 0 of the others;
-// partials are [slot][split][head][dim]) by one warp; lane l owns dims
-// 4l..4l+3.  When N >= S every split holds at least one block; otherwise
-// empty splits are skipped.  Pieces go in split order, kMergeChunk at a
-// time with all their loads (lane i < kMergeChunk: the lse of piece i;
-// every lane: its four dims of each piece's row) in flight together, so a
-// sequence of up to kMergeChunk pieces costs one round trip.  With M the
-// running maximum of the lse values the weights are e_i = exp(lse_i - M); a
-// chunk that raises M rescales the sums so far by exp(M_old - M_new) (one
-// chunk: out = sum_i e_i o_i / sum_i e_i with M = max_i lse_i).
-__device__ __forceinline__ void merge_row_chunked(const float *part_o, const float *part_lse,
-                                                  void *out, int out_f32, long long out_row,
-                                                  int HQ, int h, long long c0, long long c1,
-                                                  long long S, long long N, int lane) {
+// One warp's share of a log-sum-exp merge: the partials of splits ca..cb of
+// a sequence whose first split is c0 (slot 1 of c0, slot 0 of the others;
+// partials are [slot][split][head][dim]), row h; lane l owns dims 4l..4l+3.
+// When N >= S every split holds at least one block; otherwise empty splits
+// are skipped.  Pieces go in split order, kMergeChunk at a time with all
+// their loads (lane i < kMergeChunk: the lse of piece i; every lane: its
+// four dims of each piece's row) in flight together.  Returns M (the
+// largest lse), W = sum_i e_i and acc = sum_i e_i o_i with e_i =
+// exp(lse_i - M); a chunk that raises M rescales the sums so far by
+// exp(M_old - M_new).
+struct MergePart {
+  float M, W;
+  float4 acc;
+};
+__device__ __forceinline__ MergePart merge_part(const float *part_o, const float *part_lse,
+                                                int HQ, int h, long long c0, long long ca,
+                                                long long cb, long long S, long long N,
+                                                int lane) {
   const bool dense = N >= S;
   auto piece = [&](long long cc) -> bool {
-    return cc <= c1 && (dense || cc == c0 || split_begin(cc, S, N) < split_begin(cc + 1, S, N));
+    return cc <= cb && (dense || cc == c0 || split_begin(cc, S, N) < split_begin(cc + 1, S, N));
   };
   auto row_of = [&](long long cc) -> long long { return ((cc == c0 ? 1 : 0) * S + cc) * HQ + h; };
-  float M = -INFINITY, W = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (long long base = c0; base <= c1; base += kMergeChunk) {
+  MergePart r{-INFINITY, 0.f, make_float4(0.f, 0.f, 0.f, 0.f)};
+  for (long long base = ca; base <= cb; base += kMergeChunk) {
     const long long mine = base + lane;
     const float ls =
         lane < kMergeChunk && piece(mine) ? __ldcg(part_lse + row_of(mine)) : -INFINITY;
@@ -66,93 +68,103 @@ __device__ __forceinline__ void merge_row_chunked(const float *part_o, const flo
     float mc = ls;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
-    const float Mn = fmaxf(M, mc);
+    const float Mn = fmaxf(r.M, mc);
     if (Mn == -INFINITY) continue;  // no piece with a key so far
-    const float sc = __expf(M - Mn);  // 0 for the first chunk (M = -inf)
-    W *= sc;
-    acc.x *= sc;
-    acc.y *= sc;
-    acc.z *= sc;
-    acc.w *= sc;
+    const float sc = __expf(r.M - Mn);  // 0 for the first chunk (M = -inf)
+    r.W *= sc;
+    r.acc.x *= sc;
+    r.acc.y *= sc;
+    r.acc.z *= sc;
+    r.acc.w *= sc;
 #pragma unroll
     for (int u = 0; u < kMergeChunk; ++u) {
       const float lu = __shfl_sync(0xffffffffu, ls, u);
       const float e = lu == -INFINITY ? 0.f : __expf(lu - Mn);
-      W += e;
-      acc.x = fmaf(e, v[u].x, acc.x);
-      acc.y = fmaf(e, v[u].y, acc.y);
-      acc.z = fmaf(e, v[u].z, acc.z);
-      acc.w = fmaf(e, v[u].w, acc.w);
+      r.W += e;
+      r.acc.x = fmaf(e, v[u].x, r.acc.x);
+      r.acc.y = fmaf(e, v[u].y, r.acc.y);
+      r.acc.z = fmaf(e, v[u].z, r.acc.z);
+      r.acc.w = fmaf(e, v[u].w, r.acc.w);
     }
-    M = Mn;
+    r.M = Mn;
   }
-  const float inv = W > 0.f ? 1.f / W : 0.f;
-  store_out4(out, out_f32, out_row * kHeadDim + lane * 4,
-             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+  return r;
 }
 
-// grid (S, ceil(num_q_heads / kMergeWarps)).  Every cut sequence ends in
-// exactly one split: the one that holds its last block, whose first block
-// lies inside the sequence.  CTA (c, y) merges the sequence holding split c's
-// first block when that sequence starts before it and ends inside split c,
-// for query heads kMergeWarps y + warp.  Block counts and the partition come
-// from context_lens alone, before the wait for the kernel before it (the
-// decode kernel, under a programmatic dependent launch); the partials after
-// it.  The next kernel in the stream may begin at once: its own wait covers
-// this one.
+// grid (batch, num_q_heads): CTA (b, h) merges row h of sequence b when the
+// partition cut it (splits c0 < c1), its kMergeWarps warps taking a quarter
+// of the splits each (one round of loads for up to 64 pieces); warp 0 then
+// combines the four shares:
+//   M = max_w M_w,  s_w = exp(M_w - M),  out = sum_w s_w acc_w / sum_w s_w W_w.
+// The block counts and the partition come from context_lens alone, before
+// the wait for the kernel before it (the decode kernel, under a
+// programmatic dependent launch); the partials after it.  The next kernel in
+// the stream may begin at once: its own wait covers this one.
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const MergeParams p) {
   griddep_launch_dependents();
-  __shared__ long long warp_tot[kMergeWarps];
-  __shared__ long long found[3];  // the sequence holding block lo: index, first block, blocks
+  __shared__ long long red[2][kMergeWarps];
+  __shared__ float share_mw[kMergeWarps][2];
+  __shared__ float4 share_acc[kMergeWarps][32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long S = p.num_splits, c = blockIdx.x;
-  if (tid == 0) found[0] = -1;
-  // block-wide inclusive scans of the block counts, 32 kMergeWarps at a
-  // time: pass 0 sums them (N), pass 1 finds the sequence holding block lo
-  long long N = 0;
-  for (int pass = 0; pass < 2; ++pass) {
-    const long long lo = pass ? split_begin(c, S, N) : 0;
-    const long long hi = pass ? split_begin(c + 1, S, N) : 0;
-    if (pass && lo >= hi) return;  // no block in this split
-    long long running = 0;
-    for (int base = 0; base < p.batch; base += 32 * kMergeWarps) {
-      const int b = base + tid;
-      const int n = b < p.batch ? seq_blocks(p.context_lens, b) : 0;
-      long long incl = n;
+  const int b = blockIdx.x, h = blockIdx.y;
+  const long long S = p.num_splits;
+  // N and the blocks before sequence b
+  long long all = 0, before = 0;
+  for (int x = tid; x < p.batch; x += 32 * kMergeWarps) {
+    const int n = seq_blocks(p.context_lens, x);
+    all += n;
+    if (x < b) before += n;
+  }
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const long long y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      __syncthreads();  // the previous round's warp totals have been read
-      if (lane == 31) warp_tot[warp] = incl;
-      __syncthreads();
-      long long before = running;
-      for (int w = 0; w < kMergeWarps; ++w) {
-        if (w < warp) before += warp_tot[w];
-        running += warp_tot[w];
-      }
-      const long long prefix = before + incl - n;
-      if (pass && b < p.batch && n > 0 && prefix <= lo && lo < prefix + n) {
-        found[0] = b;
-        found[1] = prefix;
-        found[2] = n;
-      }
-    }
-    N = running;
-    if (N == 0) return;
+  for (int off = 16; off > 0; off >>= 1) {
+    all += __shfl_xor_sync(0xffffffffu, all, off);
+    before += __shfl_xor_sync(0xffffffffu, before, off);
+  }
+  if (lane == 0) {
+    red[0][warp] = all;
+    red[1][warp] = before;
   }
   __syncthreads();
-  const long long b = found[0];
-  if (b < 0) return;
-  const long long P = found[1], n = found[2];
-  const long long lo = split_begin(c, S, N), hi = split_begin(c + 1, S, N);
-  if (!(P < lo && P + n <= hi)) return;  // not a cut sequence ending in this split
-  const int h = blockIdx.y * kMergeWarps + warp;
-  if (h >= p.num_q_heads) return;
+  long long N = 0, P = 0;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) {
+    N += red[0][w];
+    P += red[1][w];
+  }
+  const int n = seq_blocks(p.context_lens, b);
+  if (n == 0) return;
+  const long long c0 = split_of_block(P, S, N), c1 = split_of_block(P + n - 1, S, N);
+  if (c0 == c1) return;  // held by one split: its rows are written already
   griddep_wait();
-  merge_row_chunked(p.part_o, p.part_lse, p.out, p.out_f32, b * p.num_q_heads + h,
-                    p.num_q_heads, h, split_of_block(P, S, N), c, S, N, lane);
+  const long long q = (c1 - c0 + kMergeWarps) / kMergeWarps;  // splits per warp
+  const long long ca = c0 + warp * q, cb = min(c1, ca + q - 1);
+  const MergePart r = merge_part(p.part_o, p.part_lse, p.num_q_heads, h, c0, ca, cb, S, N, lane);
+  share_acc[warp][lane] = r.acc;
+  if (lane == 0) {
+    share_mw[warp][0] = r.M;
+    share_mw[warp][1] = r.W;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) M = fmaxf(M, share_mw[w][0]);
+  float W = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) {
+    const float mw = share_mw[w][0];
+    const float sw = mw == -INFINITY ? 0.f : __expf(mw - M);
+    const float4 a = share_acc[w][lane];
+    W = fmaf(sw, share_mw[w][1], W);
+    acc.x = fmaf(sw, a.x, acc.x);
+    acc.y = fmaf(sw, a.y, acc.y);
+    acc.z = fmaf(sw, a.z, acc.z);
+    acc.w = fmaf(sw, a.w, acc.w);
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  store_out4(p.out, p.out_f32, ((long long)b * p.num_q_heads + h) * kHeadDim + lane * 4,
+             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
 }
 
 namespace {
@@ -221,8 +233,7 @@ bool encode_pool_maps_fp8(CUtensorMap *mk, CUtensorMap *mv, const void *k_pool,
 }
 
 cudaError_t launch_merge(const MergeParams &m, cudaStream_t s, bool pdl) {
-  const dim3 grid((unsigned)m.num_splits,
-                  (unsigned)((m.num_q_heads + kMergeWarps - 1) / kMergeWarps));
+  const dim3 grid((unsigned)m.batch, (unsigned)m.num_q_heads);
   return launch_kernel(merge_kernel, grid, dim3(32 * kMergeWarps), 0, s, pdl, m);
 }
 
