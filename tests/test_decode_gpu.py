@@ -95,6 +95,37 @@ def test_decode_head_shapes_and_ragged_tails(ops, hq, hkv, ctx):
                 assert np.all(got[b] == 0)
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (16, 4)])
+def test_decode_split_merge_path(ops, hq, hkv):
+    """Few long sequences over many splits (4 or 8 kv heads, S >= 8 * batch):
+    the decode kernel only writes the partials and a second kernel merges
+    them.  The same inputs through that path (default S = one per SM, and
+    S = 24), through the in-kernel merge (S = 23 < 8 * 3), and through
+    pa_store_decode on the merge-kernel path (the new rows stored and
+    attended in the decode kernel, the merge after it): every output against
+    the oracle, the pools bit for bit."""
+    rng = np.random.default_rng(4242 + hq)
+    ctx = [3000, 17, 1500]
+    w = synth.make_paged(rng, "split_merge", ctx, [1, 1, 1], num_blocks=512, num_q_heads=hq,
+                         num_kv_heads=hkv)
+    kref, vref = oracle_stored_caches(w)
+    ref = oracle.decode(w.q, kref, vref, w.block_tables, w.context_lens, w.scale)
+    d = Dev(ops, w, store_on_gpu=False)
+    for splits in (0, 24, 23):
+        assert_attention_close(dev_to_f64(d.decode(ops, torch.float32, splits)), ref,
+                               f"hq={hq} hkv={hkv} S={splits}", strict=True)
+    kc, vc = to_dev_bf16(w.k_cache), to_dev_bf16(w.v_cache)
+    ws = ops.decode_workspace(hq, hkv, 0)
+    out = ops.store_decode(to_dev_bf16(w.q), to_dev_bf16(w.new_k), to_dev_bf16(w.new_v), kc, vc,
+                           to_dev_i32(w.slot_mapping), d.tables, d.ctx, w.scale,
+                           out_dtype=torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    assert ops.read_error_word(ws) == 0
+    assert np.array_equal(bf16_dev_to_bits(kc), kref)
+    assert np.array_equal(bf16_dev_to_bits(vc), vref)
+    assert_attention_close(dev_to_f64(out), ref, f"store_decode hq={hq} hkv={hkv}", strict=True)
+
+
 def test_decode_deterministic_and_placement_invariant(ops):
     """Fixed split count: bit-identical across runs and across two physical
     placements of the same logical K/V."""
