@@ -445,7 +445,7 @@ def run_extras(ops, dev):
 # profiling mode: a few eager calls of one workload, for ncu captures
 # ---------------------------------------------------------------------------
 
-PROFILE_WORKLOADS = ("headline", "fp8_step", "long_decode", "prefill")
+PROFILE_WORKLOADS = ("headline", "fp8_step", "long_decode", "long_decode_fp8", "prefill")
 
 
 def run_profile(args):
@@ -456,6 +456,7 @@ def run_profile(args):
                    kernel before each call writes the same pools);
       fp8_step     pa_store_decode_fp8 on cb_decode_b64 over FP8 pools;
       long_decode  pa_decode on 4 x 32768 keys, Hq 32 / Hkv 8;
+      long_decode_fp8  pa_decode_fp8 on the same shape over FP8 pools;
       prefill      pa_prefill_varlen on the 8 x 1 + 8 x 512 chunked mix."""
     import torch
     from paged_kv_continuous_gb300 import ops, synth
@@ -494,19 +495,29 @@ def run_profile(args):
             for _ in range(calls):
                 ops.store_decode_fp8(q, nk, nv, kp, vp, ks, vs, slots, tables, ctx, w.scale,
                                      out=out, workspace=ws, pdl=True)
-    elif args.profile == "long_decode":
+    elif args.profile in ("long_decode", "long_decode_fp8"):
         rng = np.random.default_rng(synth.SEED_BASE + 3)
         B, ctxlen, hq, hkv, nb = 4, 32768, 32, 8, 10240
         perm = rng.permutation(nb).astype(np.int32)
         tables = torch.from_numpy(perm[:B * ctxlen // 16].reshape(B, -1).copy()).to(dev)
         ctx = torch.full((B,), ctxlen, dtype=torch.int32, device=dev)
-        kc = torch.randn((nb, 16, hkv, 128), generator=gen, device=dev, dtype=torch.bfloat16)
-        vc = torch.randn((nb, 16, hkv, 128), generator=gen, device=dev, dtype=torch.bfloat16)
         q = torch.randn((B, hq, 128), generator=gen, device=dev, dtype=torch.bfloat16)
         out = torch.empty((B, hq, 128), dtype=torch.bfloat16, device=dev)
         ws = ops.decode_workspace(hq, hkv, 0, 128, dev)
-        for _ in range(calls):
-            ops.decode(q, kc, vc, tables, ctx, 128 ** -0.5, out=out, workspace=ws, pdl=True)
+        if args.profile == "long_decode":
+            kc = torch.randn((nb, 16, hkv, 128), generator=gen, device=dev, dtype=torch.bfloat16)
+            vc = torch.randn((nb, 16, hkv, 128), generator=gen, device=dev, dtype=torch.bfloat16)
+            for _ in range(calls):
+                ops.decode(q, kc, vc, tables, ctx, 128 ** -0.5, out=out, workspace=ws, pdl=True)
+        else:
+            kp, vp = ops.fp8_pools(nb, hkv, device=dev)
+            kp.random_(0, 0x7F, generator=gen)
+            vp.random_(0, 0x7F, generator=gen)
+            ks = torch.full((hkv,), 0.01, dtype=torch.float32, device=dev)
+            vs = torch.full((hkv,), 0.01, dtype=torch.float32, device=dev)
+            for _ in range(calls):
+                ops.decode_fp8(q, kp, vp, ks, vs, tables, ctx, 128 ** -0.5, out=out, workspace=ws,
+                               pdl=True)
     else:
         w = synth.varlen_prefill(keep_seq=False)
         kc, vc = dev16(w.k_cache), dev16(w.v_cache)
