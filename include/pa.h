@@ -388,7 +388,9 @@ PA_API int32_t pa_decode_default_splits(int32_t device, int32_t num_q_heads,
  *   v_cache        bf16 pools (layout above), num_blocks blocks each.
  *   block_tables   int32 [batch][block_table_stride].
  *   context_lens   int32 [batch]; negative values are treated as 0.
- *   scale          softmax scale applied to q . k (e.g. 1/sqrt(head_dim)).
+ *   scale          softmax scale applied to q . k (e.g. 1/sqrt(head_dim));
+ *                  any finite value, of either sign (non-finite:
+ *                  PA_ERR_INVALID_ARG).
  *   num_splits     S of the partition, at most PA_DECODE_MAX_SPLITS;
  *                  0 = pa_decode_default_splits.
  *   workspace      device buffer of workspace_bytes >=

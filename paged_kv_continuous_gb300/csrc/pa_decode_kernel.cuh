@@ -39,7 +39,8 @@
 // bf16 in, fp32 accumulate), with the G query heads of the group as the
 // N = 8 dimension:
 //   S^T[16 tokens][8 heads] = K[16 x 128] . Q^T[128 x 8]      (8 MMAs)
-//   online softmax over the 16 tokens per head column (fp32, base 2)
+//   online softmax over the 16 tokens per head column (fp32, base 2; the
+//   reference max moves only by more than 8, so O is rescaled rarely)
 //   O^T[128][8]  += V^T[128 x 16] . P^T[16 x 8]                (8 MMAs x 2)
 // P is split into bf16 hi + lo parts (two MMAs per tile) so the product
 // keeps ~16 bits of the fp32 weights.  K fragments come from ldmatrix on the
@@ -1361,7 +1362,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   uint32_t qf[8][2];  // Q^T fragments of the group, per 16-dim k-step
   float o[8][4];      // O^T rows 16 mt + {gid, gid + 8}, head columns 2 qd, 2 qd + 1
-  float m0 = -INFINITY, m1 = -INFINITY;  // running max (raw score units), heads 2qd, 2qd+1
+  // m0, m1: reference max of the scaled scores (base 2), heads 2qd, 2qd + 1.
+  // It moves only when a block's max exceeds it by more than 8, so the
+  // exponentials stay <= 256 and o, l are rescaled rarely.
+  float m0 = -INFINITY, m1 = -INFINITY;
   float l0 = 0.f, l1 = 0.f;              // running sum over this lane's tokens
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) qf[ks][0] = qf[ks][1] = 0u;
@@ -1680,36 +1684,40 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 mma_bf16(sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
             }
           }
-          // scores: [0] (token tok0, head 2qd) [1] (tok0, 2qd+1) [2] (tok1, 2qd)
-          // [3] (tok1, 2qd+1)
+          // scaled scores (base 2): [0] (token tok0, head 2qd) [1] (tok0, 2qd+1)
+          // [2] (tok1, 2qd) [3] (tok1, 2qd+1); keys past the end are -inf
           const bool v0 = tok0 < valid, v1 = tok1 < valid;
-          const float s0 = v0 ? sa[0] + sb[0] : -INFINITY;
-          const float s1 = v0 ? sa[1] + sb[1] : -INFINITY;
-          const float s2 = v1 ? sa[2] + sb[2] : -INFINITY;
-          const float s3 = v1 ? sa[3] + sb[3] : -INFINITY;
+          const float s0 = v0 ? (sa[0] + sb[0]) * cl2 : -INFINITY;
+          const float s1 = v0 ? (sa[1] + sb[1]) * cl2 : -INFINITY;
+          const float s2 = v1 ? (sa[2] + sb[2]) * cl2 : -INFINITY;
+          const float s3 = v1 ? (sa[3] + sb[3]) * cl2 : -INFINITY;
           float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
 #pragma unroll
           for (int off = 4; off < 32; off <<= 1) {
             x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
             x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
           }
-          // token 0 of every block is a key, so x0, x1 are finite
-          const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-          const float al0 = exp2f((m0 - n0) * cl2), al1 = exp2f((m1 - n1) * cl2);
-          m0 = n0;
-          m1 = n1;
-          const float c0 = n0 * cl2, c1 = n1 * cl2;
-          const float p0 = exp2f(fmaf(s0, cl2, -c0)), p1 = exp2f(fmaf(s1, cl2, -c1));
-          const float p2 = exp2f(fmaf(s2, cl2, -c0)), p3 = exp2f(fmaf(s3, cl2, -c1));
-          l0 = fmaf(l0, al0, p0 + p2);
-          l1 = fmaf(l1, al1, p1 + p3);
+          // token 0 of every block is a key, so x0, x1 are finite (and the
+          // first block moves the reference: x - (-inf) = +inf)
+          const bool g0 = x0 - m0 > 8.f, g1 = x1 - m1 > 8.f;
+          if (__any_sync(0xffffffffu, g0 || g1)) {
+            const float al0 = g0 ? exp2f(m0 - x0) : 1.f, al1 = g1 ? exp2f(m1 - x1) : 1.f;
+            if (g0) m0 = x0;
+            if (g1) m1 = x1;
+            l0 *= al0;
+            l1 *= al1;
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
+            for (int mt = 0; mt < 8; ++mt) {
+              o[mt][0] *= al0;
+              o[mt][1] *= al1;
+              o[mt][2] *= al0;
+              o[mt][3] *= al1;
+            }
           }
+          const float p0 = exp2f(s0 - m0), p1 = exp2f(s1 - m1);
+          const float p2 = exp2f(s2 - m0), p3 = exp2f(s3 - m1);
+          l0 += p0 + p2;
+          l1 += p1 + p3;
           // P^T fragments, hi + lo split (bf16, or f16 with F8 pools)
           uint32_t hA, hB, lA, lB;
           if constexpr (F8) {
@@ -1861,8 +1869,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
         }
         if (!whole && gid == 0) {
-          const float lse_a = L0 > 0.f ? (m0 * cl2 + __log2f(L0)) * 0.69314718055994531f : -INFINITY;
-          const float lse_b = L1 > 0.f ? (m1 * cl2 + __log2f(L1)) * 0.69314718055994531f : -INFINITY;
+          const float lse_a = L0 > 0.f ? (m0 + __log2f(L0)) * 0.69314718055994531f : -INFINITY;
+          const float lse_b = L1 > 0.f ? (m1 + __log2f(L1)) * 0.69314718055994531f : -INFINITY;
           if (ha < G) {
             p.part_lse[slot_row + g * G + ha] = lse_a;
             if (keep_own) own_lse[g * G + ha] = lse_a;
@@ -1878,7 +1886,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (ha < G) {
           float *ra = rbuf + (cw * G + ha) * S::RED_FLOATS_PER_HEAD;
           if (gid == 0) {
-            ra[S::RED_M] = m0 == -INFINITY ? -INFINITY : m0 * cl2;
+            ra[S::RED_M] = m0;
             ra[S::RED_L] = L0;
           }
 #pragma unroll
@@ -1890,7 +1898,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (hb < G) {
           float *rb = rbuf + (cw * G + hb) * S::RED_FLOATS_PER_HEAD;
           if (gid == 0) {
-            rb[S::RED_M] = m1 == -INFINITY ? -INFINITY : m1 * cl2;
+            rb[S::RED_M] = m1;
             rb[S::RED_L] = L1;
           }
 #pragma unroll
