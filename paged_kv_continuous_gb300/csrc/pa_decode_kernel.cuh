@@ -58,7 +58,9 @@
 // token-major layout, V pages are dim-major inside a block and come in one
 // bulk copy; codes widen exactly to f16 and the MMAs run in f16, with a
 // token order of the score rows that makes every V operand register one
-// 32-bit load (see the F8 branches).  Early K/V requests (p.early_kv, a
+// 32-bit load, K rows read as 16-byte chunks (a dim order per fragment
+// column shared with q), and P as one f16 term (see the F8 branches).
+// Early K/V requests (p.early_kv, a
 // launch flag): the producers issue the first ring stages' pages before the
 // wait for the previous kernel.
 #pragma once
@@ -442,6 +444,18 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 // 128-byte swizzle: the chunk index is XORed with the row index mod 8.
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+// FP8 K rows: the 16-byte chunk (16 dims) that fragment column qd reads for
+// k-steps 4h .. 4h + 3.  The eight threads of a quarter warp read rows r and
+// r + HB (score rows gid and gid + 1), so the chunks of the four columns
+// must differ from their own set XOR HB for a conflict-free vector load:
+// {0, 1, 4, 5} then {2, 3, 6, 7} for HB = 2, {0, 2, 4, 6} then {1, 3, 5, 7}
+// for HB = 1.
+template <int HB>
+__device__ __forceinline__ int f8_k_chunk(int qd, int h) {
+  if constexpr (HB == 2) return ((qd & 1) | ((qd & 2) << 1)) + 2 * h;
+  else return 2 * qd + h;
 }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int *ptr) {
@@ -1466,10 +1480,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               if (gid < G) {
                 if constexpr (F8) {
                   // f16 operands; the k-step's dims in the order the K
-                  // fragments use: columns 2qd, 2qd + 1 = dims 4qd, 4qd + 1,
-                  // columns 2qd + 8, 2qd + 9 = dims 4qd + 2, 4qd + 3
-                  const uint32_t w0 = lds32(qrow + (16 * ks + 4 * qd) * 2);
-                  const uint32_t w1 = lds32(qrow + (16 * ks + 4 * qd + 2) * 2);
+                  // fragments use: columns 2qd, 2qd + 1 = dims dk, dk + 1,
+                  // columns 2qd + 8, 2qd + 9 = dims dk + 2, dk + 3
+                  const int dk = 16 * f8_k_chunk<S::HB>(qd, ks >> 2) + 4 * (ks & 3);
+                  const uint32_t w0 = lds32(qrow + dk * 2);
+                  const uint32_t w1 = lds32(qrow + (dk + 2) * 2);
                   const float2 f0 = bf16x2_to_float2(w0), f1 = bf16x2_to_float2(w1);
                   x0 = float2_to_f16x2(f0.x, f0.y);
                   x1 = float2_to_f16x2(f1.x, f1.y);
@@ -1655,13 +1670,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           // S^T = K . Q^T, two accumulation chains over the eight 16-dim k-steps
           float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
           if constexpr (F8) {
-            // 128-byte rows of E4M3 codes (token, head), 128-byte swizzle:
-            // four consecutive dims of rows tok0 and tok1 per k-step
+            // 128-byte rows of E4M3 codes (token, head), 128-byte swizzle.
+            // Thread qd reads 16-byte chunks kc0 and kc1 of rows tok0 and
+            // tok1 (one vector load each); k-step ks = 4 h + i takes word i
+            // of chunk kc_h: four consecutive dims per row.
             const int row0 = tok0 * S::HB + gsub, row1 = tok1 * S::HB + gsub;
+            const int kc0 = f8_k_chunk<S::HB>(qd, 0), kc1 = f8_k_chunk<S::HB>(qd, 1);
+            const uint4 r0a = lds128(kb + swz(row0, kc0)), r0b = lds128(kb + swz(row0, kc1));
+            const uint4 r1a = lds128(kb + swz(row1, kc0)), r1b = lds128(kb + swz(row1, kc1));
+            const uint32_t k0w[8] = {r0a.x, r0a.y, r0a.z, r0a.w, r0b.x, r0b.y, r0b.z, r0b.w};
+            const uint32_t k1w[8] = {r1a.x, r1a.y, r1a.z, r1a.w, r1b.x, r1b.y, r1b.z, r1b.w};
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-              const uint32_t w0 = lds32(kb + swz(row0, ks) + 4 * qd);
-              const uint32_t w1 = lds32(kb + swz(row1, ks) + 4 * qd);
+              const uint32_t w0 = k0w[ks];
+              const uint32_t w1 = k1w[ks];
               const uint32_t a0 = e4m3x2_to_f16x2(w0), a2 = e4m3x2_to_f16x2(w0 >> 16);
               const uint32_t a1 = e4m3x2_to_f16x2(w1), a3 = e4m3x2_to_f16x2(w1 >> 16);
               if (ks & 1)
@@ -1718,14 +1740,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const float p2 = exp2f(s2 - m0), p3 = exp2f(s3 - m1);
           l0 += p0 + p2;
           l1 += p1 + p3;
-          // P^T fragments, hi + lo split (bf16, or f16 with F8 pools)
-          uint32_t hA, hB, lA, lB;
+          // P^T fragments: bf16 hi + lo split, or with F8 pools one f16
+          // term (11-bit significand, far finer than the E4M3 values it
+          // weighs)
+          uint32_t hA, hB, lA = 0u, lB = 0u;
           if constexpr (F8) {
             hA = float2_to_f16x2(p0, p1);
             hB = float2_to_f16x2(p2, p3);
-            const float2 fA = f16x2_to_float2(hA), fB = f16x2_to_float2(hB);
-            lA = float2_to_f16x2(p0 - fA.x, p1 - fA.y);
-            lB = float2_to_f16x2(p2 - fB.x, p3 - fB.y);
           } else {
             hA = float2_to_bf16x2(p0, p1);
             hB = float2_to_bf16x2(p2, p3);
@@ -1776,7 +1797,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               const uint32_t a0 = e4m3x2_to_f16x2(w0), a2 = e4m3x2_to_f16x2(w0 >> 16);
               const uint32_t a1 = e4m3x2_to_f16x2(w1), a3 = e4m3x2_to_f16x2(w1 >> 16);
               mma_f16(o[mt], a0, a1, a2, a3, bh0, bh1);
-              mma_f16(o[mt], a0, a1, a2, a3, bl0, bl1);
             }
           } else {
             const int mi = lane >> 3, r = lane & 7;

@@ -96,7 +96,8 @@ struct PrefillParams {
   long long bt_stride;
   const int32_t *context_lens;
   int hq, hkv;
-  float qk_scale_log2;
+  float qk_scale_log2;  // > 0: a scale <= 0 is folded into q as staged
+  uint32_t q_and, q_xor;  // staged q pairs = (q & q_and) ^ q_xor
   int32_t *err;
   // Fused store (new_k == nullptr: none).  The chunk rows of token t are
   // new_k / new_v + t * new_*_tok + h * 128; they are stored at
@@ -606,6 +607,13 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         qv[c16] = rvalid ? __ldg(src + c16) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int c16 = 0; c16 < 16; ++c16) {
+        qv[c16].x = (qv[c16].x & p.q_and) ^ p.q_xor;
+        qv[c16].y = (qv[c16].y & p.q_and) ^ p.q_xor;
+        qv[c16].z = (qv[c16].z & p.q_and) ^ p.q_xor;
+        qv[c16].w = (qv[c16].w & p.q_and) ^ p.q_xor;
+      }
+#pragma unroll
+      for (int c16 = 0; c16 < 16; ++c16) {
         const uint32_t a = base + kOffQ + (c16 >> 3) * kQHalf + sw128(r, c16 & 7);
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(qv[c16].x),
                      "r"(qv[c16].y), "r"(qv[c16].z), "r"(qv[c16].w)
@@ -915,7 +923,13 @@ pa_status prefill_entry(void *out, int32_t out_dtype, const void *q, const int32
   pp.context_lens = context_lens;
   pp.hq = num_q_heads;
   pp.hkv = num_kv_heads;
-  pp.qk_scale_log2 = scale * 1.4426950408889634f;
+  // The softmax keeps its reference max in raw score units and masks keys
+  // with -inf before scaling, which needs a positive score scale: a negative
+  // scale is folded into q (its sign bits flipped, exact), a zero one makes
+  // q zero (every score 0, scale 1).
+  pp.qk_scale_log2 = (scale > 0.f ? scale : scale < 0.f ? -scale : 1.f) * 1.4426950408889634f;
+  pp.q_and = scale == 0.f ? 0u : 0xFFFFFFFFu;
+  pp.q_xor = scale < 0.f ? 0x80008000u : 0u;
   pp.err = error_flags;
   pp.new_k = static_cast<const uint16_t *>(new_k);
   pp.new_v = static_cast<const uint16_t *>(new_v);

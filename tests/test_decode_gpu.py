@@ -126,6 +126,25 @@ def test_decode_split_merge_path(ops, hq, hkv):
     assert_attention_close(dev_to_f64(out), ref, f"store_decode hq={hq} hkv={hkv}", strict=True)
 
 
+@pytest.mark.parametrize("scale", [-4.0, -0.09, 0.0, 2.5])
+@pytest.mark.parametrize("hq,hkv,splits", [(12, 2, 0), (12, 2, 7), (32, 8, 0)])
+def test_decode_scale_sign_and_size(ops, scale, hq, hkv, splits):
+    """Softmax scales of either sign, zero (every key weighs the same) and
+    large magnitudes (near one-hot weights, scaled scores spread over
+    hundreds of base-2 units, so the reference max moves many times):
+    against the oracle through the in-kernel merge, a small split count
+    and the merge-kernel path."""
+    rng = np.random.default_rng(900 + int(abs(scale) * 100) + hq + splits)
+    ctx = [2100, 1, 16, 333, 47]
+    w = synth.make_paged(rng, "scale", ctx, [1] * len(ctx), num_blocks=256, num_q_heads=hq,
+                         num_kv_heads=hkv, scale=scale)
+    kref, vref = oracle_stored_caches(w)
+    ref = oracle.decode(w.q, kref, vref, w.block_tables, w.context_lens, w.scale)
+    d = Dev(ops, w, store_on_gpu=False)
+    assert_attention_close(dev_to_f64(d.decode(ops, torch.float32, splits)), ref,
+                           f"scale={scale} hq={hq} hkv={hkv} S={splits}", strict=True)
+
+
 def test_decode_deterministic_and_placement_invariant(ops):
     """Fixed split count: bit-identical across runs and across two physical
     placements of the same logical K/V."""

@@ -108,6 +108,21 @@ def test_fp8_gqa_shapes_and_splits(ops, Hq, Hkv, num_splits):
     assert_close(got, ref)
 
 
+@pytest.mark.parametrize("scale", [-3.0, 0.0])
+@pytest.mark.parametrize("Hq,Hkv", [(12, 2), (32, 8)])
+def test_fp8_softmax_scale_sign(ops, scale, Hq, Hkv):
+    """A negative softmax scale (near one-hot weights at this size) and a zero
+    one (every key weighs the same), with the K scale folded into it."""
+    rng = np.random.default_rng(700 + Hq + int(abs(scale)))
+    ctx = np.array([900, 1, 37, 260])
+    w = synth.make_paged(rng, "fp8_scale", ctx, np.ones(4, np.int64), num_blocks=128,
+                         num_q_heads=Hq, num_kv_heads=Hkv, scale=scale)
+    ks = rng.uniform(0.008, 0.012, Hkv).astype(np.float32)
+    vs = rng.uniform(0.008, 0.012, Hkv).astype(np.float32)
+    got, ref = run_step(ops, w, ks, vs)
+    assert_close(got, ref)
+
+
 def test_fp8_saturating_scale_and_bf16_output(ops):
     """A scale small enough that many values saturate at +-448 codes, and a
     bf16 output (held to the elementwise rule)."""

@@ -117,6 +117,24 @@ def test_prefill_head_shapes_and_ragged_lengths(ops, hq, hkv):
     assert_attention_close(got, oracle_prefill(w), f"hq={hq} hkv={hkv}", strict=True)
 
 
+@pytest.mark.parametrize("scale", [-3.0, -0.088, 0.0])
+def test_prefill_scale_sign(ops, scale):
+    """Negative softmax scales (the larger one gives near one-hot weights)
+    and a zero one (every visible key weighs the same), on diagonal and
+    ragged tiles, with the fused store too."""
+    rng = np.random.default_rng(77 + int(abs(scale) * 1000))
+    q_lens = np.array([1, 17, 130, 5, 64])
+    prefix = np.array([0, 300, 1, 129, 16])
+    w = synth.make_paged(rng, "scale", prefix + q_lens, q_lens, num_blocks=200,
+                         num_q_heads=12, num_kv_heads=2, scale=scale)
+    ref = oracle_prefill(w)
+    assert_attention_close(dev_to_f64(gpu_prefill(ops, w)), ref, f"scale={scale}", strict=True)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _, _ = fused_prefill(ops, w, err=err)
+    assert int(err.item()) == 0
+    assert_attention_close(dev_to_f64(out), ref, f"fused store, scale={scale}", strict=True)
+
+
 def test_prefill_varlen_equals_per_sequence_bitwise(ops):
     """The pages' equivalence: each sequence's rows of the batched call are
     bit-identical to a call with that sequence alone."""
