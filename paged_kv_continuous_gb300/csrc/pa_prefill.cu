@@ -30,7 +30,8 @@
 // (the A operand of the PV MMAs comes from tensor memory) and store the
 // output.  Tile j's scores go to buffer j % 2 once the PV MMA of tile j - 2
 // that read that buffer is done, so the score MMA of tile j + 1 runs under
-// the softmax of tile j.
+// the softmax of tile j.  CTAs take their tiles longest first (the most KV
+// tiles to attend), so the long ones do not start at the end of the grid.
 //
 // pa_prefill_store_varlen (the store of the chunks' K/V fused in): other CTAs
 // of a sequence need chunk keys this CTA stores, so the chunk is never read
@@ -286,6 +287,159 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
   return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
+// ---- work order -------------------------------------------------------------
+// The work items are (sequence s, query tile mt, kv head g) with a query
+// tile of PT positions; an item costs one step per 64-key tile it attends,
+// nkv = (prefix + last position of the tile) / 64 + 1, which grows with mt.
+// CTAs start in block-index order, so the CTA of linear index r takes the
+// item of rank r in the order "most steps first" (ties: by s, then mt, then
+// g): long items start first and short ones fill the end of the grid.  Every
+// CTA finds its item from a histogram of the step counts (one thread per
+// run of sequences, counts clamped to kLptBins - 1, which only merges ties)
+// and two block scans.  Returns false when the CTA has no item.  Sequences
+// with rows beyond the grid's tiles or with context_lens < q_len are
+// reported (PA_DEVERR_SHAPE); the latter have no items.
+constexpr int kLptBins = 1024;
+static_assert((kLptBins + 32 + 5) * 4 <= kKStages * kTileBytes2,
+              "work-order scratch does not fit the K stages");
+__device__ __forceinline__ int lpt_bin(int prefix, int q_len, int mt, int PT) {
+  const int last = mt * PT + min(PT, q_len - mt * PT) - 1;  // last position of the tile
+  return min((prefix + last) / kPfKeys + 1, kLptBins - 1);
+}
+// exclusive block scan of one int per thread (kPfThreads threads)
+__device__ __forceinline__ int block_excl_scan(int v, int *wsum, int &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = lane < kPfThreads / 32 ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < kPfThreads / 32) wsum[lane] = t;  // inclusive warp prefix
+  }
+  __syncthreads();
+  total = wsum[kPfThreads / 32 - 1];
+  const int before = warp > 0 ? wsum[warp - 1] : 0;
+  __syncthreads();  // wsum is reused by the next scan
+  return before + x - v;
+}
+template <int PT>
+__device__ bool pick_work_item(const PrefillParams &p, int gx, int *sc, int &s_out, int &mt_out,
+                               int &g_out) {
+  int *hist = sc;                     // [kLptBins] items per step count
+  int *wsum = sc + kLptBins;          // [kPfThreads / 32] block-scan scratch
+  int *res = sc + kLptBins + 32;      // picked bin, items before it, s, mt, g
+  const int tid = threadIdx.x;
+  const int r = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+  for (int i = tid; i < kLptBins; i += kPfThreads) hist[i] = 0;
+  if (tid == 0) res[0] = -1;
+  __syncthreads();
+  const int ns = p.num_seqs, hkv = p.hkv;
+  const int spt = (ns + kPfThreads - 1) / kPfThreads;
+  const int s0 = min(ns, tid * spt), s1 = min(ns, s0 + spt);
+  // pass 1: the histogram (runs of equal counts added at once)
+  for (int s = s0; s < s1; ++s) {
+    const int q_len = __ldg(p.cu_seqlens + s + 1) - __ldg(p.cu_seqlens + s);
+    if (q_len <= 0) continue;
+    const int prefix = __ldg(p.context_lens + s) - q_len;
+    if (prefix < 0) {
+      report(p.err, PA_DEVERR_SHAPE);
+      continue;
+    }
+    if (q_len > gx * PT) report(p.err, PA_DEVERR_SHAPE);  // rows no CTA covers
+    const int T = min((q_len + PT - 1) / PT, gx);
+    int run_bin = lpt_bin(prefix, q_len, 0, PT), run = 0;
+    for (int mt = 0; mt < T; ++mt) {
+      const int b = lpt_bin(prefix, q_len, mt, PT);
+      if (b != run_bin) {
+        atomicAdd(hist + run_bin, run * hkv);
+        run_bin = b;
+        run = 0;
+      }
+      ++run;
+    }
+    if (T > 0) atomicAdd(hist + run_bin, run * hkv);
+  }
+  __syncthreads();
+  // pass 2 (warp 0): the bin of rank r, counting bins from the top
+  if (tid < 32) {
+    constexpr int kPer = kLptBins / 32;
+    int sum = 0;
+#pragma unroll 4
+    for (int k = 0; k < kPer; ++k) sum += hist[kLptBins - 1 - tid * kPer - k];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (tid >= o) incl += y;
+    }
+    const int excl = incl - sum;
+    if (r >= excl && r < incl) {
+      int acc = excl;
+      for (int k = 0; k < kPer; ++k) {
+        const int b = kLptBins - 1 - tid * kPer - k;
+        if (r < acc + hist[b]) {
+          res[0] = b;
+          res[1] = acc;
+          break;
+        }
+        acc += hist[b];
+      }
+    }
+  }
+  __syncthreads();
+  const int vb = res[0];
+  if (vb < 0) return false;  // rank past the last item
+  const int j = r - res[1];
+  // pass 3: the j-th item of bin vb in (s, mt, g) order
+  int cnt = 0;
+  for (int s = s0; s < s1; ++s) {
+    const int q_len = __ldg(p.cu_seqlens + s + 1) - __ldg(p.cu_seqlens + s);
+    const int prefix = __ldg(p.context_lens + s) - q_len;
+    if (q_len <= 0 || prefix < 0) continue;
+    const int T = min((q_len + PT - 1) / PT, gx);
+    for (int mt = 0; mt < T; ++mt) cnt += lpt_bin(prefix, q_len, mt, PT) == vb ? hkv : 0;
+  }
+  int total;
+  const int before = block_excl_scan(cnt, wsum, total);
+  if (j >= before && j < before + cnt) {
+    int k = j - before;
+    for (int s = s0; s < s1 && k >= 0; ++s) {
+      const int q_len = __ldg(p.cu_seqlens + s + 1) - __ldg(p.cu_seqlens + s);
+      const int prefix = __ldg(p.context_lens + s) - q_len;
+      if (q_len <= 0 || prefix < 0) continue;
+      const int T = min((q_len + PT - 1) / PT, gx);
+      for (int mt = 0; mt < T; ++mt) {
+        if (lpt_bin(prefix, q_len, mt, PT) != vb) continue;
+        if (k < hkv) {
+          res[2] = s;
+          res[3] = mt;
+          res[4] = k;
+          k = -1;
+          break;
+        }
+        k -= hkv;
+      }
+    }
+  }
+  __syncthreads();
+  s_out = res[2];
+  mt_out = res[3];
+  g_out = res[4];
+  // the scratch becomes a TMA destination: order these generic writes first
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  return true;
+}
+
 template <int G>
 __global__ void __launch_bounds__(kPfThreads, 2)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -315,21 +469,16 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   // broadcast from lane 0: the compiler then knows every role branch below
   // is warp-uniform
   const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
-  // the last tiles of a chunk see the most keys (causal): they start first
-  const int mt = (int)gridDim.x - 1 - (int)blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  // the work item of this CTA, longest first (pick_work_item); the scratch
+  // is the K stage region, which no TMA has written yet
+  int s, mt, g;
+  if (!pick_work_item<PT>(p, (int)gridDim.x, reinterpret_cast<int *>(smem + kOffK), s, mt, g))
+    return;
   const int q0 = __ldg(p.cu_seqlens + s);
   const int q_len = __ldg(p.cu_seqlens + s + 1) - q0;
   const int pos0 = mt * PT;
-  if (pos0 >= q_len) return;  // whole CTA: this tile has no query
   const int n = __ldg(p.context_lens + s);
   const int prefix = n - q_len;
-  if (prefix < 0) {
-    if (tid == 0) report(p.err, PA_DEVERR_SHAPE);
-    return;
-  }
-  // a chunk longer than max_q_len has rows no CTA covers: reported
-  if (mt == (int)gridDim.x - 1 && pos0 + PT < q_len && threadIdx.x == 0)
-    report(p.err, PA_DEVERR_SHAPE);
   const int npos = min(PT, q_len - pos0);
   const int rows = npos * G;
   const int kmax = prefix + pos0 + npos - 1;  // last key any row of the tile sees
