@@ -275,6 +275,34 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Packed pairs of floats (lo half first) and the f32x2 arithmetic on them:
+// each half is rounded as the scalar instruction would round it.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// max of three floats (exact; a NaN operand is ignored, as by fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x by the special-function unit (ex2.approx, relative error ~2^-22).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -800,16 +828,17 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           for (int i = 0; i < 32; ++i)
             sv[cc][i] = key0 + cc * 32 + i <= limit ? sv[cc][i] : -INFINITY;
       }
-      // eight independent max chains
+      // eight independent max chains, two keys per three-input max
       float mx8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[cc][i]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int i = 0; i < 32; i += 2)
+          mx8[(i >> 1) & 7] = fmax3(mx8[(i >> 1) & 7], sv[cc][i], sv[cc][i + 1]);
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
       const float mxc = mx * c;
       const bool grow = mxc > m + 8.f;
       const float m_new = grow ? mxc : m;
@@ -823,13 +852,19 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       float ps8[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
+      // (the exponents of a key pair in one packed f32x2 multiply-add)
+      const uint64_t c2 = pack_f32x2(c, c), nm2 = pack_f32x2(neg_m, neg_m);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float e = ex2_approx(fmaf(sv[cc][i], c, neg_m));
-          sv[cc][i] = e;
-          ps8[i & 7] += e;
+        for (int i = 0; i < 32; i += 2) {
+          float x0, x1;
+          unpack_f32x2(fma_f32x2(pack_f32x2(sv[cc][i], sv[cc][i + 1]), c2, nm2), x0, x1);
+          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+          sv[cc][i] = e0;
+          sv[cc][i + 1] = e1;
+          ps8[i & 7] += e0;
+          ps8[(i + 1) & 7] += e1;
         }
       const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) +
                          ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
@@ -857,9 +892,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       // of the PV MMAs; keys 2i and 2i + 1 share column i, the even key in the
       // low half; hi parts in the buffer's columns 0..31, lo parts in
       // 32..63).  hi is e with the low 16 mantissa bits cleared (exactly a
-      // bf16); lo = e - hi is exact in fp32 and rounded to nearest bf16 by an
-      // integer add, so hi + lo is e within 2^-15 relative, without bias.
-      // Both parts are byte permutes (no conversion instruction).
+      // bf16, one byte permute per key pair); lo = e - hi is exact in fp32
+      // (one packed subtraction per pair) and rounded to nearest even bf16
+      // (one packed conversion per pair), so hi + lo is e within 2^-15
+      // relative, without bias.
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t hi[16], lo[16];
@@ -868,12 +904,12 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           const uint32_t u0 = __float_as_uint(sv[cc][2 * i]);
           const uint32_t u1 = __float_as_uint(sv[cc][2 * i + 1]);
           hi[i] = __byte_perm(u0, u1, 0x7632);
-          // lo >= 0; + 0x8000 rounds its top 16 bits to nearest (a carry
-          // into the exponent is the correct rounding)
-          lo[i] = __byte_perm(
-              __float_as_uint(sv[cc][2 * i] - __uint_as_float(u0 & 0xFFFF0000u)) + 0x8000u,
-              __float_as_uint(sv[cc][2 * i + 1] - __uint_as_float(u1 & 0xFFFF0000u)) + 0x8000u,
-              0x7632);
+          float d0, d1;
+          unpack_f32x2(sub_f32x2(pack_f32x2(sv[cc][2 * i], sv[cc][2 * i + 1]),
+                                 pack_f32x2(__uint_as_float(u0 & 0xFFFF0000u),
+                                            __uint_as_float(u1 & 0xFFFF0000u))),
+                       d0, d1);
+          asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo[i]) : "f"(d1), "f"(d0));
         }
         tmem_st16(sb + trow + cc * 16, hi);
         tmem_st16(sb + trow + kTmemSCols / 2 + cc * 16, lo);
