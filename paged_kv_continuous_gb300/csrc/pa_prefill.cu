@@ -260,6 +260,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -288,6 +295,11 @@ __device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi) {
 __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t r;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
 __device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
@@ -844,14 +856,12 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       const float m_new = grow ? mxc : m;
       const float alpha = grow && m != -INFINITY ? exp2f(m - m_new) : 1.f;
       m = m_new;
-      // P = exp2(S c - m) in place, and the row sum (eight chains).  A masked
+      // P = exp2(S c - m) in place (its row sum is taken with the split of P
+      // below).  A masked
       // key has S = -inf, so its exponent is -inf and 2^x = +0; a row with no
       // key yet (m = -inf: rows past the chunk) takes offset 0 instead of
       // +inf, which keeps it -inf rather than NaN.
       const float neg_m = m == -INFINITY ? 0.f : -m;
-      float ps8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) ps8[u] = 0.f;
       // (the exponents of a key pair in one packed f32x2 multiply-add)
       const uint64_t c2 = pack_f32x2(c, c), nm2 = pack_f32x2(neg_m, neg_m);
 #pragma unroll
@@ -860,14 +870,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         for (int i = 0; i < 32; i += 2) {
           float x0, x1;
           unpack_f32x2(fma_f32x2(pack_f32x2(sv[cc][i], sv[cc][i + 1]), c2, nm2), x0, x1);
-          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-          sv[cc][i] = e0;
-          sv[cc][i + 1] = e1;
-          ps8[i & 7] += e0;
-          ps8[(i + 1) & 7] += e1;
+          sv[cc][i] = ex2_approx(x0);
+          sv[cc][i + 1] = ex2_approx(x1);
         }
-      const float psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) +
-                         ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       // rows whose reference max moved rescale their O row, once the PV of
       // tile j - 1 is done and before that of tile j (warp-wide: tcgen05.ld /
       // st are collective)
@@ -887,7 +892,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           tmem_st32(tmem_o + trow + cc * 32, ov);
         }
       }
-      l = l * alpha + psum;
+      const float l_scaled = l * alpha;
       // P as bf16 hi + lo over the scores of this row's TMEM lane (A operands
       // of the PV MMAs; keys 2i and 2i + 1 share column i, the even key in the
       // low half; hi parts in the buffer's columns 0..31, lo parts in
@@ -896,23 +901,36 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       // (one packed subtraction per pair) and rounded to nearest even bf16
       // (one packed conversion per pair), so hi + lo is e within 2^-15
       // relative, without bias.
+      // The row sum of the exponentials is taken here, on the key pairs the
+      // subtraction packs anyway (eight chains, two per packed add); 8-column
+      // stores keep the loop within the registers of two CTAs per SM.
+      uint64_t ps4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t hi[16], lo[16];
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t hi[8], lo[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t u0 = __float_as_uint(sv[cc][2 * i]);
-          const uint32_t u1 = __float_as_uint(sv[cc][2 * i + 1]);
+        for (int i = 0; i < 8; ++i) {
+          const float e0 = sv[cc >> 1][16 * (cc & 1) + 2 * i];
+          const float e1 = sv[cc >> 1][16 * (cc & 1) + 2 * i + 1];
+          const uint32_t u0 = __float_as_uint(e0), u1 = __float_as_uint(e1);
           hi[i] = __byte_perm(u0, u1, 0x7632);
+          const uint64_t e2 = pack_f32x2(e0, e1);
+          ps4[i & 3] = add_f32x2(ps4[i & 3], e2);
           float d0, d1;
-          unpack_f32x2(sub_f32x2(pack_f32x2(sv[cc][2 * i], sv[cc][2 * i + 1]),
-                                 pack_f32x2(__uint_as_float(u0 & 0xFFFF0000u),
-                                            __uint_as_float(u1 & 0xFFFF0000u))),
+          unpack_f32x2(sub_f32x2(e2, pack_f32x2(__uint_as_float(u0 & 0xFFFF0000u),
+                                                __uint_as_float(u1 & 0xFFFF0000u))),
                        d0, d1);
           asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo[i]) : "f"(d1), "f"(d0));
         }
-        tmem_st16(sb + trow + cc * 16, hi);
-        tmem_st16(sb + trow + kTmemSCols / 2 + cc * 16, lo);
+        tmem_st8(sb + trow + cc * 8, hi);
+        tmem_st8(sb + trow + kTmemSCols / 2 + cc * 8, lo);
+      }
+      {
+        float ps8[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) unpack_f32x2(ps4[u], ps8[2 * u], ps8[2 * u + 1]);
+        l = l_scaled + (((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) +
+                        ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7])));
       }
       tmem_wait_st();
       // keys past the end of the sequence: their V rows may hold anything;
