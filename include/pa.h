@@ -583,9 +583,13 @@ PA_API pa_status pa_decode_noalloc(void *out, int32_t out_dtype, const void *q,
  *   max_q_len      upper bound of every q_len_s (sizes the launch grid).
  *   context_lens   int32 [num_seqs]; q_len_s > n_s sets PA_DEVERR_SHAPE and
  *                  that sequence's rows are left unspecified.
+ *   scale          softmax scale applied to q . k; any finite value, of
+ *                  either sign (non-finite: PA_ERR_INVALID_ARG).
  *   error_flags    optional int32 word (may be NULL).
  * Rows of different sequences never attend to each other, so a sequence's
- * rows equal what the same call gives for that sequence alone.
+ * rows equal what the same call gives for that sequence alone.  The order
+ * in which the launch's tiles run (longest first) does not change any
+ * result.
  */
 PA_API pa_status pa_prefill_varlen(void *out, int32_t out_dtype, const void *q,
                             const int32_t *cu_seqlens, int32_t num_seqs,
