@@ -335,8 +335,9 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 // item of rank r in the order "most steps first" (ties: by s, then mt, then
 // g): long items start first and short ones fill the end of the grid.  Every
 // CTA finds its item from a histogram of the step counts (one thread per
-// run of sequences, counts clamped to kLptBins - 1, which only merges ties)
-// and two block scans.  Returns false when the CTA has no item.  Sequences
+// sequence, counts clamped to kLptBins - 1, which only merges ties) and two
+// block scans; the kernel uses it only while num_seqs <= kPfThreads, so
+// that this prologue stays one round of loads.  Returns false when the CTA has no item.  Sequences
 // with rows beyond the grid's tiles or with context_lens < q_len are
 // reported (PA_DEVERR_SHAPE); the latter have no items.
 constexpr int kLptBins = 1024;
@@ -509,11 +510,28 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   // broadcast from lane 0: the compiler then knows every role branch below
   // is warp-uniform
   const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
-  // the work item of this CTA, longest first (pick_work_item); the scratch
-  // is the K stage region, which no TMA has written yet
+  // the work item of this CTA: longest first (pick_work_item; the scratch
+  // is the K stage region, which no TMA has written yet) while one thread
+  // per sequence suffices, else in grid order with the last tiles of a
+  // chunk (the most keys, causal) first
   int s, mt, g;
-  if (!pick_work_item<PT>(p, (int)gridDim.x, reinterpret_cast<int *>(smem + kOffK), s, mt, g))
-    return;
+  if (p.num_seqs <= kPfThreads) {
+    if (!pick_work_item<PT>(p, (int)gridDim.x, reinterpret_cast<int *>(smem + kOffK), s, mt, g))
+      return;
+  } else {
+    mt = (int)gridDim.x - 1 - (int)blockIdx.x;
+    g = blockIdx.y;
+    s = blockIdx.z;
+    const int ql = __ldg(p.cu_seqlens + s + 1) - __ldg(p.cu_seqlens + s);
+    if (mt * PT >= ql) return;  // this tile has no query
+    if (__ldg(p.context_lens + s) < ql) {
+      if (tid == 0) report(p.err, PA_DEVERR_SHAPE);
+      return;
+    }
+    // a chunk longer than max_q_len has rows no CTA covers: reported
+    if (mt == (int)gridDim.x - 1 && mt * PT + PT < ql && tid == 0)
+      report(p.err, PA_DEVERR_SHAPE);
+  }
   const int q0 = __ldg(p.cu_seqlens + s);
   const int q_len = __ldg(p.cu_seqlens + s + 1) - q0;
   const int pos0 = mt * PT;

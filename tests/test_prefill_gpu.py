@@ -135,6 +135,20 @@ def test_prefill_scale_sign(ops, scale):
     assert_attention_close(dev_to_f64(out), ref, f"fused store, scale={scale}", strict=True)
 
 
+def test_prefill_many_sequences_grid_order(ops):
+    """More sequences than a CTA has threads (300 short chunks behind short
+    prefixes, some empty): the CTAs take their tiles in grid order instead
+    of the longest-first pick; every row against the oracle."""
+    rng = np.random.default_rng(300)
+    q_lens = rng.integers(0, 5, size=300)
+    q_lens[0] = 4
+    prefix = rng.integers(0, 40, size=300)
+    w = synth.make_paged(rng, "many_seqs", prefix + q_lens, q_lens, num_blocks=1000,
+                         num_q_heads=12, num_kv_heads=2)
+    got = dev_to_f64(gpu_prefill(ops, w))
+    assert_attention_close(got, oracle_prefill(w), "300 sequences", strict=True)
+
+
 def test_prefill_varlen_equals_per_sequence_bitwise(ops):
     """The pages' equivalence: each sequence's rows of the batched call are
     bit-identical to a call with that sequence alone."""
