@@ -97,6 +97,37 @@ def test_decode_brute_force_contiguous(ctx):
     assert np.all(np.isfinite(out))  # NaN-poisoned slots never reach the result
 
 
+@pytest.mark.parametrize("scale", [-4.0, -0.09, 0.0, 3.0])
+def test_decode_and_prefill_any_sign_of_scale(scale):
+    """Softmax scales of either sign and zero (the kernels accept any finite
+    scale): decode and prefill equal fp64 attention over the contiguous K/V,
+    and scale 0 gives the plain mean of the visible V rows (catches a scale
+    dropped, applied with the wrong sign or clamped to positive values)."""
+    rng = np.random.default_rng(700 + int(abs(scale) * 100))
+    lens = [45, 3]
+    ks = [normal_bits(rng, (n, 2, 128)) for n in lens]
+    vs = [normal_bits(rng, (n, 2, 128)) for n in lens]
+    t = random_tables(rng, lens, 16)
+    kc, vc = scatter_pool(ks, t, 16), scatter_pool(vs, t, 16)
+    q = normal_bits(rng, (2, 12, 128))
+    out = oracle.decode(q, kc, vc, t, np.array(lens, np.int32), scale)
+    for b, n in enumerate(lens):
+        for h in range(12):
+            ref = brute_attention(q[b, h], ks[b][:, h // 6], vs[b][:, h // 6], scale, n)
+            np.testing.assert_allclose(out[b, h], ref, rtol=1e-12, atol=1e-13)
+            if scale == 0.0:
+                mean = bf16_to_f64(vs[b][:n, h // 6]).mean(axis=0)
+                np.testing.assert_allclose(out[b, h], mean, rtol=1e-12, atol=1e-13)
+    # prefill: the last 5 positions of sequence 0 as a chunk behind a prefix of 40
+    qp = normal_bits(rng, (5, 12, 128))
+    cu = np.array([0, 5], np.int32)
+    outp = oracle.prefill_varlen(qp, cu, kc, vc, t[:1], np.array([45], np.int32), scale)
+    for i in range(5):
+        for h in range(12):
+            ref = brute_attention(qp[i, h], ks[0][:, h // 6], vs[0][:, h // 6], scale, 41 + i)
+            np.testing.assert_allclose(outp[i, h], ref, rtol=1e-12, atol=1e-13)
+
+
 def test_tiny_config_brute_force_after_store():
     """The 2-sequence workload: store the step's two tokens, then decode; the
     result equals brute force over the full contiguous sequences, so the
